@@ -1,0 +1,166 @@
+/*
+ * gemm_oracle.c -- plain CPU oracle for the half-precision GEMM with a fused
+ * ReLU epilogue, C = ReLU(A @ B).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product library links, loads or
+ * calls this file; it is used by the tests, by the smoke check and by the
+ * bench's CPU-baseline leg.  It shares no code, header, table or constant
+ * with the CUDA path.
+ *
+ * What it computes (written out from the definition, nothing reordered):
+ *
+ *   C[i,j] = f16_rne( R( sum_{k=0..K-1} (double)A[i,k] * (double)B[k,j] ) )
+ *
+ *   A (M,K), B (K,N), C (M,N): dense row-major IEEE binary16, leading
+ *   dimensions K, N and N.  R(x) = (x > 0) ? x : +0 when relu is set, else x.
+ *
+ * Sources, all on "Writing High-Performance Kernels in TileLang, from GEMM to
+ * MLA" (atlascloud.ai), section "Let's write a GEMM": the kernel computes
+ * C = ReLU(A @ B) with A (M,K), B (K,N) and C (M,N) in float16; the
+ * accumulator fragment is declared in float (fp32); ReLU is applied to the
+ * accumulator (max with 0) and the accumulator is then copied out to the
+ * float16 C, i.e. one cast at write-back.  The TileLang-MUSA lesson
+ * (7yue.com, section 3, "first TileLang kernel: GEMM") has the same
+ * contraction without ReLU and checks it against A.float() @ B.float().
+ *
+ * Readings where the pages leave a step open:
+ *   - accumulation: widened here to fp64 (every fp16 x fp16 product is exact
+ *     in fp64; the sum's own rounding is far below one fp16 ulp), summed in
+ *     ascending k for every output element;
+ *   - ReLU: applied to the accumulator before the cast; every x <= 0, -0 and
+ *     NaN give +0 (the "(x > 0) ? x : 0" reading of max(x, 0));
+ *   - cast: IEEE-754 round-to-nearest-even, overflow to +-inf, subnormals
+ *     kept (the rounding of the fp32 -> fp16 copy is not stated on the pages);
+ *   - K == 0: the empty sum is +0, so C = R(+0) = +0.
+ *
+ * Loop order: rows i in parallel (OpenMP), then k, then j with one fp64
+ * accumulator per output column of the row.  Each C[i,j] is still the sum
+ * over k in ascending order, exactly as the i-j-k loop would form it.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <omp.h>
+
+/* IEEE binary16 -> binary64 (exact).  Layout: 1 sign bit, 5 exponent bits
+ * (bias 15), 10 fraction bits. */
+double oracle_f16_to_f64(uint16_t h)
+{
+    const int sign = (h >> 15) & 1;
+    const int e = (h >> 10) & 0x1f;
+    const int m = h & 0x3ff;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)m, -24);              /* zero or subnormal: m * 2^-24 */
+    } else if (e == 31) {
+        v = (m == 0) ? INFINITY : NAN;          /* infinity or NaN */
+    } else {
+        v = ldexp((double)(m + 1024), e - 25);  /* (1 + m/2^10) * 2^(e-15) */
+    }
+    return sign ? -v : v;
+}
+
+/* IEEE binary64 -> binary16, round to nearest, ties to even.  Relies on the
+ * default floating-point environment (FE_TONEAREST) for nearbyint(). */
+uint16_t oracle_f64_to_f16(double x)
+{
+    const uint16_t sign = signbit(x) ? 0x8000u : 0u;
+    if (isnan(x)) return (uint16_t)(sign | 0x7e00u);
+    const double a = fabs(x);
+    if (isinf(a)) return (uint16_t)(sign | 0x7c00u);
+    if (a < ldexp(1.0, -14)) {
+        /* Subnormal range: the representable values are q * 2^-24 for
+         * integer q.  Scaling by 2^24 is exact; q == 1024 is the smallest
+         * normal number and its encoding is the same integer. */
+        const double q = nearbyint(ldexp(a, 24));
+        return (uint16_t)(sign | (uint16_t)q);
+    }
+    int e2;
+    (void)frexp(a, &e2);           /* a in [2^(e2-1), 2^e2) */
+    int E = e2 - 1;                /* unbiased exponent, E >= -14 here */
+    double q = nearbyint(ldexp(a, 10 - E));   /* significand * 2^10, in [1024, 2048] */
+    if (q == 2048.0) {             /* rounded up into the next binade */
+        q = 1024.0;
+        E += 1;
+    }
+    if (E > 15) return (uint16_t)(sign | 0x7c00u);   /* overflow -> infinity */
+    return (uint16_t)(sign | (uint16_t)((E + 15) << 10) | (uint16_t)(q - 1024.0));
+}
+
+/* Decoded value of every binary16 bit pattern, filled from
+ * oracle_f16_to_f64 before any row is computed. */
+static double g_f16_value[65536];
+static int g_f16_value_ready = 0;
+
+static void fill_f16_values(void)
+{
+    if (g_f16_value_ready) return;
+    for (int h = 0; h < 65536; ++h) g_f16_value[h] = oracle_f16_to_f64((uint16_t)h);
+    g_f16_value_ready = 1;
+}
+
+/*
+ * Computes the requested output rows.  rows[r] (0 <= rows[r] < M) names an
+ * output row; its N values are written to C_out[r*N .. r*N+N-1].  Passing
+ * rows = NULL means every row 0..M-1 in order (n_rows must then be M).
+ * Returns 0 on success, -1 on bad arguments or allocation failure.
+ */
+int oracle_gemm_f16_rows(const uint16_t *A, const uint16_t *B, uint16_t *C_out,
+                         int64_t M, int64_t N, int64_t K, int relu,
+                         const int64_t *rows, int64_t n_rows)
+{
+    if (M < 0 || N < 0 || K < 0 || n_rows < 0) return -1;
+    if (rows == NULL && n_rows != M) return -1;
+    for (int64_t r = 0; rows != NULL && r < n_rows; ++r)
+        if (rows[r] < 0 || rows[r] >= M) return -1;
+    if (n_rows == 0 || N == 0) return 0;
+    fill_f16_values();
+
+    int failed = 0;
+#pragma omp parallel
+    {
+        double *acc = (double *)malloc((size_t)N * sizeof(double));
+        if (acc == NULL) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t r = 0; r < n_rows; ++r) {
+            if (acc == NULL) continue;
+            const int64_t i = rows ? rows[r] : r;
+            for (int64_t j = 0; j < N; ++j) acc[j] = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                const double a = g_f16_value[A[i * K + k]];
+                const uint16_t *b_row = B + k * N;
+                for (int64_t j = 0; j < N; ++j) acc[j] += a * g_f16_value[b_row[j]];
+            }
+            uint16_t *c_row = C_out + r * N;
+            for (int64_t j = 0; j < N; ++j) {
+                double x = acc[j];
+                if (relu) x = (x > 0.0) ? x : 0.0;
+                c_row[j] = oracle_f64_to_f16(x);
+            }
+        }
+        free(acc);
+    }
+    return failed ? -1 : 0;
+}
+
+/* Whole matrix: C (M,N) row-major. */
+int oracle_gemm_f16(const uint16_t *A, const uint16_t *B, uint16_t *C,
+                    int64_t M, int64_t N, int64_t K, int relu)
+{
+    return oracle_gemm_f16_rows(A, B, C, M, N, K, relu, NULL, M);
+}
+
+/* Number of threads an OpenMP parallel region of this library uses. */
+int oracle_num_threads(void)
+{
+    int n = 1;
+#pragma omp parallel
+    {
+#pragma omp single
+        n = omp_get_num_threads();
+    }
+    return n;
+}
