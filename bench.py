@@ -1,0 +1,396 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused fp16 GEMM + ReLU on GB300.
+
+One "step" is one call of the hot path, C = ReLU(A @ B), on the headline
+workload (default ``relu_8192``: M = N = K = 8192, fp16 inputs N(0,1)/sqrt(K),
+seed 5).  The inputs (A, B: 256 MiB, C: 128 MiB) are larger than the 126 MB
+L2, so no flush is needed between steps.
+
+Prints ONE JSON line:
+  value        TFLOP/s, 2*M*N*K*steps*ranks / max-over-ranks device time
+               (CUDA events on the launching stream, inputs resident in HBM)
+  e2e          the same metric through the C ABI's host-buffer call
+               (gemm_f16_from_host: H2D copies of A and B, the GEMM, D2H of C
+               every step, pinned host memory)
+  roofline     tensor-core bound: achieved TFLOP/s per launch against the
+               measured bf16 matmul peak of this machine (fp16 has the same rate)
+  cpu_baseline the CPU oracle, as it stands, on a bounded sample of rows
+  clocks       SM clocks / throttle reasons sampled during the timed region
+
+``--impl reference`` times the CPU oracle instead (the reference arm: a
+deliberately slow, obviously correct program on the host cores).
+
+Multi-GPU: the method has no exchange step, so N GPUs run N independent
+replicas of the step (weak scaling); torch.distributed is used only for the
+barrier and the max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GEMM+ReLU TFLOP/s at 4096^3/8192^3 fp16 and % of GB300 dense FP16 peak"
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
+TENSOR_FLOP_PER_CLK_PER_SM = 8192   # dense fp16/bf16 tcgen05 rate per SM per clock
+
+
+# ---------------------------------------------------------------- helpers
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"bf16_tflops": FALLBACK_BF16_TFLOPS, "hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "dense_fp16_gemm_05_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    entry = rec.get(workload)
+    if not entry or entry.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.sw_power_cap,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown")
+
+    def __init__(self, device_index: int, interval_ms: int = 50):
+        self.device_index = device_index
+        self.interval_ms = interval_ms
+        self.proc = None
+        self.path = None
+
+    def _gpu_id(self):
+        try:
+            import torch
+            u = str(torch.cuda.get_device_properties(self.device_index).uuid)
+            return u if u.startswith("GPU-") else "GPU-" + u
+        except Exception:
+            return str(self.device_index)
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self._gpu_id(), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", str(self.interval_ms)],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 7:
+                    continue
+                try:
+                    rows.append((float(parts[0]), float(parts[1]), float(parts[2]), parts[3:7]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [r for r in rows if r[2] > 300.0] or rows   # samples under load (power draw)
+        names = ("sw_power_cap", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
+        reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "power_w_max": max(r[2] for r in rows), "samples": len(loaded), "reasons": reasons}
+
+
+def oracle_cpu_baseline(A, B, relu: bool, budget_s: float, workload_name: str, M: int):
+    """Times the CPU oracle on a bounded sample of full output rows."""
+    import oracle
+    N = B.shape[1]
+    K = A.shape[1]
+    rows_probe = max(1, min(M, 4))
+    _, t_probe = oracle.time_rows(A, B, relu, list(range(rows_probe)))
+    per_row = max(t_probe / rows_probe, 1e-6)
+    n_rows = int(max(1, min(M, budget_s / per_row)))
+    step = max(1, M // n_rows)
+    rows = list(range(0, M, step))[:n_rows]
+    _, secs = oracle.time_rows(A, B, relu, rows)
+    flops = 2.0 * len(rows) * N * K
+    return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{len(rows)} of {M} output rows (all {N} columns, full K={K}) of {workload_name}, "
+                      f"{secs:.1f} s"}, secs
+
+
+# ---------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    from dense_fp16_gemm_05_gb300.inputs import WORKLOADS, draw_workload
+    w = WORKLOADS[args.workload]
+    A, B = draw_workload(w)
+    # each step: a bounded sample of output rows, sized so the run ends within minutes
+    probe_rows = list(range(min(4, w.M)))
+    _, t_probe = oracle.time_rows(A, B, w.relu, probe_rows)
+    per_row = max(t_probe / len(probe_rows), 1e-6)
+    per_step_budget = max(0.5, min(10.0, 120.0 / max(1, args.steps + args.warmup)))
+    n_rows = int(max(1, min(w.M, per_step_budget / per_row)))
+    rng_rows = [(i * 7919) % w.M for i in range(n_rows)]
+    for _ in range(args.warmup):
+        oracle.time_rows(A, B, w.relu, rng_rows)
+    total = 0.0
+    for _ in range(args.steps):
+        _, s = oracle.time_rows(A, B, w.relu, rng_rows)
+        total += s
+    flops = 2.0 * n_rows * w.N * w.K * args.steps
+    value = flops / total / 1e12
+    cores = oracle.num_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "gpu_launches": 0,
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "relu": w.relu, "values": w.values,
+                   "seed": w.seed, "sample_rows_per_step": n_rows},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{n_rows} of {w.M} output rows per step (all {w.N} columns, full K)"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- our arm
+
+def time_device(g, A, B, C, relu, config, steps, warmup, stream):
+    """Returns (total_ms over the timed steps, list of per-launch ms)."""
+    import torch
+    for _ in range(warmup):
+        g.gemm_f16(A, B, C, relu=relu, stream=stream, config=config)
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(steps):
+        starts[i].record(stream)
+        g.gemm_f16(A, B, C, relu=relu, stream=stream, config=config)
+        ends[i].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1), [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend="nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from dense_fp16_gemm_05_gb300 import gemm_f16 as g
+    from dense_fp16_gemm_05_gb300.inputs import WORKLOADS, draw_workload
+    g.lib()   # fails loudly if the CUDA library is missing
+
+    w = WORKLOADS[args.workload]
+    A_cpu, B_cpu = draw_workload(w)
+    A = A_cpu.to(dev)
+    B = B_cpu.to(dev)
+    C = torch.empty((w.M, w.N), dtype=torch.float16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    config = args.config if args.config else g.auto_config(w.M, w.N, w.K)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(x: float) -> float:
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    # ---- device-resident timing
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier()
+    total_ms, per_launch = time_device(g, A, B, C, w.relu, config, args.steps, args.warmup, stream)
+    barrier()
+    clocks = sampler.stop()
+    st = g.check(stream)
+    if st != g.GEMM_OK:
+        raise RuntimeError(f"device status {st}: {g.strerror(st)}")
+    total_ms = max_over_ranks(total_ms)
+    ms_per_step = total_ms / args.steps
+    value = world * w.flops * args.steps / (total_ms * 1e-3) / 1e12
+
+    avg_launch_ms = statistics.mean(per_launch)
+    achieved = w.flops / (avg_launch_ms * 1e-3) / 1e12
+    peaks, peak_src = measured_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
+    sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
+    sm_max = float(peaks.get("sm_max_mhz", 2070.0))
+    theoretical = sm_count * TENSOR_FLOP_PER_CLK_PER_SM * sm_max * 1e6 / 1e12
+
+    # ---- secondary size of the metric: 4096^3 without ReLU
+    secondary = None
+    if args.workload == "relu_8192" and not args.no_secondary:
+        w2 = WORKLOADS["plain_4096"]
+        A2c, B2c = draw_workload(w2)
+        A2, B2 = A2c.to(dev), B2c.to(dev)
+        C2 = torch.empty((w2.M, w2.N), dtype=torch.float16, device=dev)
+        cfg2 = args.config if args.config else g.auto_config(w2.M, w2.N, w2.K)
+        # 96 MiB of inputs + 32 MiB output fit in L2: flush between launches
+        flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+        for _ in range(3):
+            g.gemm_f16(A2, B2, C2, relu=False, stream=stream, config=cfg2)
+        times = []
+        for _ in range(max(5, min(args.steps, 50))):
+            flush.zero_()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            g.gemm_f16(A2, B2, C2, relu=False, stream=stream, config=cfg2)
+            e.record(stream)
+            e.synchronize()
+            times.append(s.elapsed_time(e))
+        ms2 = statistics.median(times)
+        tf2 = w2.flops / (ms2 * 1e-3) / 1e12
+        secondary = {"workload": w2.name, "M": w2.M, "N": w2.N, "K": w2.K, "relu": False,
+                     "TFLOP_s": tf2, "ms": ms2, "frac_of_measured_peak": tf2 / peak,
+                     "frac_of_theoretical_peak": tf2 / theoretical, "kernel_config": g.config_name(cfg2),
+                     "l2": "256 MiB buffer written between launches (L2 flush); median of launches"}
+        del A2, B2, C2, flush
+
+    # ---- end to end through the host-buffer C call
+    A_h = A_cpu.pin_memory()
+    B_h = B_cpu.pin_memory()
+    C_h = torch.empty((w.M, w.N), dtype=torch.float16).pin_memory()
+    e2e_steps = max(3, min(args.steps, 30))
+    for _ in range(2):
+        g.gemm_f16_from_host(A_h, B_h, C_h, A, B, C, relu=w.relu, stream=stream)
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        g.gemm_f16_from_host(A_h, B_h, C_h, A, B, C, relu=w.relu, stream=stream)
+    e1.record(stream)
+    barrier()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1))
+    e2e_value = world * w.flops * e2e_steps / (e2e_ms * 1e-3) / 1e12
+
+    cpu_baseline = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu_baseline, _ = oracle_cpu_baseline(A_cpu, B_cpu, w.relu, args.cpu_budget, w.name, w.M)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "relu": w.relu,
+                       "values": "N(0,1)/sqrt(K) fp16" if w.values == "normal_scaled" else w.values,
+                       "seed": w.seed, "kernel_config": g.config_name(config), "accumulate": "f32",
+                       "l2": "inputs 384 MiB > 126 MB L2, no flush",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "frac_of_theoretical_peak": value / world / theoretical,
+            "theoretical_peak_tflops": theoretical,
+            "theoretical_peak_basis": f"{sm_count} SMs x {TENSOR_FLOP_PER_CLK_PER_SM} FLOP/clk x {sm_max:.0f} MHz",
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": recorded_traffic(w.name),
+                         "peak_source": f"{peak_src} bf16 matmul burst (fp16 has the same tensor rate)",
+                         "avg_launch_ms": avg_launch_ms},
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": int(A_h.numel() * 2 + B_h.numel() * 2),
+                    "d2h_bytes_per_step": int(C_h.numel() * 2), "steps": e2e_steps},
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+            "cpu_baseline": cpu_baseline,
+        }
+        if secondary is not None:
+            line["secondary"] = secondary
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=300)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="relu_8192")
+    p.add_argument("--config", type=int, default=0, help="kernel configuration id (0 = automatic)")
+    p.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-secondary", action="store_true")
+    args = p.parse_args(argv)
+    if args.warmup < 3:
+        p.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,377 @@
+// gemm_f16.cu -- host side of the GB300 fp16 GEMM + ReLU library: argument
+// checks, TMA tensor-map encoding, configuration choice, launch, and the
+// extern "C" entry points declared in include/gemm_f16.h.
+//
+// Nothing here computes the product on the host; every element of C is
+// written by the sm_103a kernel in gemm_kernel.cuh (or, for K == 0, by one
+// cudaMemsetAsync of +0, the value of the empty sum).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+
+#include "gemm_f16.h"
+#include "gemm_kernel.cuh"
+
+using namespace gemm_sm103;
+
+namespace {
+
+// ---------------------------------------------------------------- configurations
+
+struct ConfigInfo {
+    const char *name;
+    int tile_m;       // rows of C per tile (all CTAs of the tile together)
+    int tile_n;       // columns of C per tile
+};
+
+// id 1..kNumConfigs; index 0 is "auto".
+using Cfg256 = Cfg1Sm<256, 4>;
+using Cfg128 = Cfg1Sm<128, 6>;
+
+constexpr ConfigInfo kConfigs[] = {
+    {"auto", 0, 0},
+    {"1sm_128x256_s4", Cfg256::BM, Cfg256::BN},
+    {"1sm_128x128_s6", Cfg128::BM, Cfg128::BN},
+};
+constexpr int kNumConfigs = static_cast<int>(sizeof(kConfigs) / sizeof(kConfigs[0])) - 1;
+
+// ---------------------------------------------------------------- driver entry points
+
+struct DriverFns {
+    PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    PFN_cuMemGetAddressRange_v3020 range = nullptr;
+    bool ok = false;
+};
+
+const DriverFns &driver()
+{
+    static DriverFns fns;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q1 = cudaDriverEntryPointSymbolNotFound;
+        cudaDriverEntryPointQueryResult q2 = cudaDriverEntryPointSymbolNotFound;
+        void *f1 = nullptr, *f2 = nullptr;
+        cudaError_t e1 = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f1, 12000, cudaEnableDefault, &q1);
+        cudaError_t e2 = cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &f2, 3020, cudaEnableDefault, &q2);
+        if (e1 == cudaSuccess && q1 == cudaDriverEntryPointSuccess && f1 && e2 == cudaSuccess &&
+            q2 == cudaDriverEntryPointSuccess && f2) {
+            fns.encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f1);
+            fns.range = reinterpret_cast<PFN_cuMemGetAddressRange_v3020>(f2);
+            fns.ok = true;
+        }
+    });
+    return fns;
+}
+
+// ---------------------------------------------------------------- per-device facts
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    int checked = 0;        // 1 once filled
+    int supported = 0;      // compute capability 10.3
+    int sm_count = 0;
+};
+
+DeviceInfo g_devices[kMaxDevices];
+std::mutex g_device_mutex;
+
+int current_device_info(DeviceInfo *out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return GEMM_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> lock(g_device_mutex);
+    DeviceInfo &d = g_devices[dev];
+    if (!d.checked) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        d.supported = (major == 10 && minor == 3) ? 1 : 0;
+        d.sm_count = sms;
+        d.checked = 1;
+    }
+    *out = d;
+    return d.supported ? GEMM_OK : GEMM_ERR_UNSUPPORTED_DEVICE;
+}
+
+// ---------------------------------------------------------------- argument checks
+
+// A device buffer of `bytes` bytes starting at p: device (or managed) memory of
+// the current device, entirely inside one allocation.
+int check_device_buffer(const void *p, uint64_t bytes)
+{
+    if (p == nullptr) return GEMM_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(p) & 15u) != 0) return GEMM_ERR_ALIGNMENT;
+    cudaPointerAttributes attr{};
+    if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_INVALID_ARG;
+    }
+    if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged) return GEMM_ERR_INVALID_ARG;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (attr.type == cudaMemoryTypeDevice && attr.device != dev) return GEMM_ERR_INVALID_ARG;
+    const DriverFns &fns = driver();
+    if (!fns.ok) return GEMM_ERR_CUDA;
+    CUdeviceptr base = 0;
+    size_t size = 0;
+    if (fns.range(&base, &size, reinterpret_cast<CUdeviceptr>(p)) != CUDA_SUCCESS) return GEMM_ERR_INVALID_ARG;
+    const uint64_t off = static_cast<uint64_t>(reinterpret_cast<CUdeviceptr>(p) - base);
+    if (off > size || bytes > size - off) return GEMM_ERR_INVALID_ARG;
+    return GEMM_OK;
+}
+
+bool ranges_overlap(const void *a, uint64_t abytes, const void *b, uint64_t bbytes)
+{
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + bbytes && b0 < a0 + abytes;
+}
+
+int check_sizes(int64_t M, int64_t N, int64_t K, int relu)
+{
+    if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
+    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return GEMM_ERR_INVALID_ARG;
+    if (relu != 0 && relu != 1) return GEMM_ERR_INVALID_ARG;
+    return GEMM_OK;
+}
+
+// ---------------------------------------------------------------- tensor maps
+
+// Row-major fp16 matrix rows x cols (leading dimension cols), boxes of
+// box_cols x box_rows with 128-byte swizzle; out-of-range loads read zero.
+int encode_matrix(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t cols, uint32_t box_cols,
+                  uint32_t box_rows)
+{
+    const DriverFns &fns = driver();
+    if (!fns.ok) return GEMM_ERR_CUDA;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fns.encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
+                            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------- launch
+
+uint64_t timeout_cycles_for(int64_t K)
+{
+    // About a second of SM clocks plus a margin that grows with the K loop of
+    // one tile; a legitimate wait is at most one tile's mainloop.
+    return (1ull << 31) + 64ull * static_cast<uint64_t>(K);
+}
+
+int pick_config(int64_t M, int64_t N, int64_t K, int sm_count)
+{
+    (void)K;
+    const int64_t tiles256 = ((M + 127) / 128) * ((N + 255) / 256);
+    // Few tiles: narrower tiles put more SMs to work.
+    if (tiles256 < sm_count / 2) return 2;
+    return 1;
+}
+
+template <class Cfg, bool kRelu>
+int launch_1sm(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K, int sm_count,
+               cudaStream_t stream)
+{
+    CUtensorMap ta, tb, tc;
+    int st;
+    if ((st = encode_matrix(&ta, A, M, K, Cfg::BK, Cfg::BM)) != GEMM_OK) return st;
+    if ((st = encode_matrix(&tb, B, K, N, Cfg::B_BOX_N, Cfg::BK)) != GEMM_OK) return st;
+    if ((st = encode_matrix(&tc, C, M, N, Cfg::EPI_COLS, 32)) != GEMM_OK) return st;
+
+    GemmParams p{};
+    p.M = static_cast<int32_t>(M);
+    p.N = static_cast<int32_t>(N);
+    p.K = static_cast<int32_t>(K);
+    p.num_m_blocks = static_cast<int32_t>((M + Cfg::BM - 1) / Cfg::BM);
+    p.num_n_blocks = static_cast<int32_t>((N + Cfg::BN - 1) / Cfg::BN);
+    p.num_k_blocks = static_cast<int32_t>((K + Cfg::BK - 1) / Cfg::BK);
+    const int64_t tiles = static_cast<int64_t>(p.num_m_blocks) * p.num_n_blocks;
+    if (tiles > INT32_MAX) return GEMM_ERR_INVALID_ARG;
+    p.num_tiles = static_cast<int32_t>(tiles);
+    p.group_m = 16;
+    p.timeout_cycles = timeout_cycles_for(K);
+
+    auto kern = gemm_f16_relu_sm103a_1sm<Cfg, kRelu>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    const int grid = static_cast<int>(tiles < sm_count ? tiles : sm_count);
+    cudaLaunchConfig_t lc{};
+    lc.gridDim = dim3(grid, 1, 1);
+    lc.blockDim = dim3(Cfg::THREADS, 1, 1);
+    lc.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    lc.stream = stream;
+    cudaLaunchAttribute attrs[1];
+    attrs[0].id = cudaLaunchAttributeClusterDimension;
+    attrs[0].val.clusterDim.x = 1;
+    attrs[0].val.clusterDim.y = 1;
+    attrs[0].val.clusterDim.z = 1;
+    lc.attrs = attrs;
+    lc.numAttrs = 1;
+    if (cudaLaunchKernelEx(&lc, kern, ta, tb, tc, p) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    return GEMM_OK;
+}
+
+template <class Cfg>
+int launch_cfg(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K, int relu, int sm_count,
+               cudaStream_t stream)
+{
+    return relu ? launch_1sm<Cfg, true>(A, B, C, M, N, K, sm_count, stream)
+                : launch_1sm<Cfg, false>(A, B, C, M, N, K, sm_count, stream);
+}
+
+thread_local uint64_t t_last_timeout_record = 0;
+
+}  // namespace
+
+// ==================================================================== C ABI
+
+extern "C" int gemm_f16_ex(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K, int relu,
+                           int config, void *stream)
+{
+    int st = check_sizes(M, N, K, relu);
+    if (st != GEMM_OK) return st;
+    if (config < 0 || config > kNumConfigs) return GEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return GEMM_OK;
+
+    DeviceInfo dev;
+    if ((st = current_device_info(&dev)) != GEMM_OK) return st;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const uint64_t c_bytes = static_cast<uint64_t>(M) * static_cast<uint64_t>(N) * 2u;
+    if ((st = check_device_buffer(C, c_bytes)) != GEMM_OK) return st;
+
+    if (K == 0) {
+        // Empty sum: every output is R(+0) = +0.
+        if (cudaMemsetAsync(C, 0, c_bytes, s) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_CUDA;
+        }
+        return GEMM_OK;
+    }
+    if ((N % 8) != 0 || (K % 8) != 0) return GEMM_ERR_ALIGNMENT;
+    const uint64_t a_bytes = static_cast<uint64_t>(M) * static_cast<uint64_t>(K) * 2u;
+    const uint64_t b_bytes = static_cast<uint64_t>(K) * static_cast<uint64_t>(N) * 2u;
+    if ((st = check_device_buffer(A, a_bytes)) != GEMM_OK) return st;
+    if ((st = check_device_buffer(B, b_bytes)) != GEMM_OK) return st;
+    if (ranges_overlap(C, c_bytes, A, a_bytes) || ranges_overlap(C, c_bytes, B, b_bytes))
+        return GEMM_ERR_INVALID_ARG;
+
+    const int cfg = config == 0 ? pick_config(M, N, K, dev.sm_count) : config;
+    switch (cfg) {
+        case 1: return launch_cfg<Cfg256>(A, B, C, M, N, K, relu, dev.sm_count, s);
+        case 2: return launch_cfg<Cfg128>(A, B, C, M, N, K, relu, dev.sm_count, s);
+        default: return GEMM_ERR_INVALID_ARG;
+    }
+}
+
+extern "C" int gemm_f16(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K, int relu,
+                        void *stream)
+{
+    return gemm_f16_ex(A, B, C, M, N, K, relu, 0, stream);
+}
+
+extern "C" int gemm_f16_num_configs(void) { return kNumConfigs; }
+
+extern "C" const char *gemm_f16_config_name(int config)
+{
+    if (config < 0 || config > kNumConfigs) return nullptr;
+    return kConfigs[config].name;
+}
+
+extern "C" int gemm_f16_auto_config(int64_t M, int64_t N, int64_t K)
+{
+    int st = check_sizes(M, N, K, 0);
+    if (st != GEMM_OK) return st;
+    DeviceInfo dev;
+    if ((st = current_device_info(&dev)) != GEMM_OK) return st;
+    return pick_config(M, N, K, dev.sm_count);
+}
+
+extern "C" int gemm_f16_from_host(const void *A_host, const void *B_host, void *C_host, void *A_dev, void *B_dev,
+                                  void *C_dev, int64_t M, int64_t N, int64_t K, int relu, void *stream)
+{
+    int st = check_sizes(M, N, K, relu);
+    if (st != GEMM_OK) return st;
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (C_host == nullptr || (K > 0 && (A_host == nullptr || B_host == nullptr))) return GEMM_ERR_INVALID_ARG;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t a_bytes = static_cast<size_t>(M) * static_cast<size_t>(K) * 2u;
+    const size_t b_bytes = static_cast<size_t>(K) * static_cast<size_t>(N) * 2u;
+    const size_t c_bytes = static_cast<size_t>(M) * static_cast<size_t>(N) * 2u;
+    if (K > 0) {
+        // Validate the device side before any copy is enqueued.
+        DeviceInfo dev;
+        if ((st = current_device_info(&dev)) != GEMM_OK) return st;
+        if ((N % 8) != 0 || (K % 8) != 0) return GEMM_ERR_ALIGNMENT;
+        if ((st = check_device_buffer(A_dev, a_bytes)) != GEMM_OK) return st;
+        if ((st = check_device_buffer(B_dev, b_bytes)) != GEMM_OK) return st;
+        if ((st = check_device_buffer(C_dev, c_bytes)) != GEMM_OK) return st;
+        if (cudaMemcpyAsync(A_dev, A_host, a_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+            cudaMemcpyAsync(B_dev, B_host, b_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_CUDA;
+        }
+    }
+    if ((st = gemm_f16(A_dev, B_dev, C_dev, M, N, K, relu, stream)) != GEMM_OK) return st;
+    if (cudaMemcpyAsync(C_host, C_dev, c_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    return GEMM_OK;
+}
+
+extern "C" int gemm_f16_check(void *stream)
+{
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    unsigned long long v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_gemm_f16_status, sizeof(v)) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    if (v != 0) {
+        t_last_timeout_record = v;
+        const unsigned long long zero = 0;
+        if (cudaMemcpyToSymbol(g_gemm_f16_status, &zero, sizeof(zero)) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_CUDA;
+        }
+        return GEMM_ERR_TIMEOUT;
+    }
+    return GEMM_OK;
+}
+
+extern "C" uint64_t gemm_f16_last_timeout_record(void) { return t_last_timeout_record; }
+
+extern "C" const char *gemm_f16_strerror(int status)
+{
+    switch (status) {
+        case GEMM_OK: return "success";
+        case GEMM_ERR_INVALID_ARG: return "invalid argument";
+        case GEMM_ERR_ALIGNMENT: return "misaligned pointer, or N or K not a multiple of 8";
+        case GEMM_ERR_UNSUPPORTED_DEVICE: return "current device is not compute capability 10.3 (GB300)";
+        case GEMM_ERR_LAUNCH: return "kernel launch failed";
+        case GEMM_ERR_TIMEOUT: return "a kernel wait exceeded its limit; the output is incomplete";
+        case GEMM_ERR_CUDA: return "CUDA runtime or driver call failed";
+        default: return "unknown status";
+    }
+}
+
+extern "C" int gemm_f16_version(void) { return GEMM_F16_VERSION; }

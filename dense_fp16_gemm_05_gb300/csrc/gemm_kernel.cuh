@@ -1,0 +1,390 @@
+// gemm_kernel.cuh -- persistent, warp-specialised fp16 GEMM + fused ReLU for
+// sm_103a (GB300): TMA -> 128B-swizzled shared-memory ring -> tcgen05.mma with
+// the fp32 accumulator in tensor memory -> ReLU / fp16 cast -> TMA store.
+//
+// The method is the tiled GEMM of "Writing High-Performance Kernels in
+// TileLang, from GEMM to MLA" (atlascloud.ai), section "Let's write a GEMM":
+// shared-memory tiles of A and B, a software-pipelined K loop with several
+// stages in flight, a tile-level MMA into a float accumulator that is cleared
+// per output tile, ReLU on the accumulator, one cast on write-back, and an L2
+// rasterisation swizzle of the tile order.  Here each of those steps is a
+// Blackwell mechanism:
+//   * tile copies        -> TMA boxes with 128-byte swizzle (bank-conflict free
+//                            for both the copy and the MMA read)
+//   * K pipeline         -> a ring of STAGES shared-memory slots guarded by
+//                            "full" (TMA bytes landed) and "empty" (MMA done)
+//                            mbarriers
+//   * tile MMA           -> tcgen05.mma.kind::f16 issued by one thread,
+//                            accumulating in TMEM; the first MMA of a tile runs
+//                            with accumulate = 0 (the accumulator clear)
+//   * ReLU + cast + copy -> 4 epilogue warps: tcgen05.ld -> max(x,0) -> cvt.rn
+//                            f16x2 -> swizzled smem -> TMA store
+//   * L2 swizzle         -> grouped rasterisation in a persistent tile loop
+// Two TMEM accumulators let the epilogue of tile i overlap the MMAs of i+1.
+//
+// Ragged edges: TMA loads fill out-of-range elements with zeros, so partial
+// tiles in M, N and K contribute nothing; TMA stores do not write outside C.
+//
+// Every mbarrier wait is bounded (clock64 budget).  On expiry the waiting
+// thread records the site in a device status word, raises a CTA-wide abort
+// flag, and every role leaves its loop; the producer then waits (bounded) for
+// its own loads in flight, the MMA thread for its own MMAs, the epilogue for
+// its own stores, and the TMEM is freed before the CTA exits.
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include <cstdint>
+
+#include "sm103_ptx.cuh"
+
+namespace gemm_sm103 {
+
+// Problem description passed by value to the kernel.
+struct GemmParams {
+    int32_t M, N, K;
+    int32_t num_m_blocks;   // ceil(M / tile rows)
+    int32_t num_n_blocks;   // ceil(N / tile cols)
+    int32_t num_k_blocks;   // ceil(K / BK)
+    int32_t num_tiles;      // num_m_blocks * num_n_blocks
+    int32_t group_m;        // rasterisation panel height, in tiles
+    uint64_t timeout_cycles;
+};
+
+// Where a bounded wait expired (bits 0-7 of the status word).
+enum WaitSite : uint32_t {
+    kSiteProducerEmpty = 1,
+    kSiteMmaTmemEmpty = 2,
+    kSiteMmaFull = 3,
+    kSiteEpilogueTmemFull = 4,
+    kSiteDrainLoads = 5,
+    kSiteDrainMma = 6,
+};
+
+// Tile shapes and shared-memory budget of one kernel configuration.
+//   kBN      columns of C per tile
+//   kStages  depth of the shared-memory K ring
+template <int kBN, int kStages>
+struct Cfg1Sm {
+    static constexpr int kCtaGroup = 1;
+    static constexpr int BM = 128;            // rows of C per tile = TMEM lanes
+    static constexpr int BN = kBN;
+    static constexpr int BK = 64;             // 64 fp16 = 128 bytes = one swizzle row
+    static constexpr int UMMA_K = 16;         // K of one tcgen05.mma.kind::f16
+    static constexpr int STAGES = kStages;
+    static constexpr int THREADS = 192;       // producer, MMA, 4 epilogue warps
+    static constexpr int B_BOX_N = 64;        // N extent of one B box (128 bytes)
+    static constexpr int B_BOXES = BN / B_BOX_N;
+    static constexpr int A_STAGE_BYTES = BM * BK * 2;
+    static constexpr int B_BOX_BYTES = B_BOX_N * BK * 2;
+    static constexpr int B_STAGE_BYTES = B_BOXES * B_BOX_BYTES;
+    static constexpr int STAGE_TX_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+    static constexpr int ACC_COLS = BN;       // fp32 TMEM columns of one accumulator
+    static constexpr int TMEM_COLS = 2 * ACC_COLS;
+    static constexpr int EPI_COLS = 64;       // columns per epilogue chunk (128 bytes of fp16)
+    static constexpr int C_BUF_BYTES = 32 * EPI_COLS * 2;
+    static constexpr int SMEM_A_OFF = 0;
+    static constexpr int SMEM_B_OFF = SMEM_A_OFF + STAGES * A_STAGE_BYTES;
+    static constexpr int SMEM_C_OFF = SMEM_B_OFF + STAGES * B_STAGE_BYTES;
+    static constexpr int SMEM_CTL_OFF = SMEM_C_OFF + 4 * 2 * C_BUF_BYTES;
+    static constexpr int SMEM_CTL_BYTES = 256;
+    static constexpr int SMEM_BYTES = 1024 /* alignment slack */ + SMEM_CTL_OFF + SMEM_CTL_BYTES;
+    static constexpr uint32_t IDESC = idesc_f16_f32(BM, BN, /*A MN-major*/ false, /*B MN-major*/ true);
+
+    static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "UMMA N for M=128 is a multiple of 16 up to 256");
+    static_assert(TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation is a power of 2");
+    static_assert((2 * STAGES + 5) * 8 + 8 <= SMEM_CTL_BYTES, "control block");
+    static_assert(SMEM_BYTES <= 232448, "shared memory per block on sm_103");
+};
+
+// Device status word: 0 = fine; otherwise the first timeout record.
+__device__ unsigned long long g_gemm_f16_status;
+
+// Bounded wait on an mbarrier phase.  Fast path: one probe.  Slow path: probe
+// until the phase completes, the CTA's abort flag is raised, or the clock64
+// budget is spent (then record the site and raise the abort flag).
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int *abort_flag, uint64_t limit,
+                                           uint32_t site)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (static_cast<uint64_t>(clock64() - t0) > limit) {
+            *abort_flag = 1;
+            atomicCAS(&g_gemm_f16_status, 0ull,
+                      static_cast<unsigned long long>(site) | (static_cast<unsigned long long>(blockIdx.x) << 8));
+            return false;
+        }
+    }
+}
+
+// Bounded wait used while tearing down after an abort: ignores the abort flag.
+__device__ __forceinline__ bool wait_phase_drain(uint32_t bar, uint32_t parity, uint64_t limit, uint32_t site)
+{
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (static_cast<uint64_t>(clock64() - t0) > limit) {
+            atomicCAS(&g_gemm_f16_status, 0ull,
+                      static_cast<unsigned long long>(site) | (static_cast<unsigned long long>(blockIdx.x) << 8));
+            return false;
+        }
+    }
+    return true;
+}
+
+// Grouped rasterisation: tiles are visited in panels of group_m tile rows; inside
+// a panel the row index runs fastest, so CTAs that run at the same time share
+// the same few A row-panels and B column-panels in L2.
+__device__ __forceinline__ void tile_coords(int t, const GemmParams &p, int &mb, int &nb)
+{
+    const int per_group = p.group_m * p.num_n_blocks;
+    const int g = t / per_group;
+    const int first_m = g * p.group_m;
+    const int rows = min(p.num_m_blocks - first_m, p.group_m);
+    const int r = t - g * per_group;
+    mb = first_m + r % rows;
+    nb = r / rows;
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+template <bool kRelu>
+__device__ __forceinline__ float epilogue_value(uint32_t bits)
+{
+    const float x = __uint_as_float(bits);
+    if constexpr (kRelu) return x > 0.0f ? x : 0.0f;  // -0, NaN and negatives give +0
+    else return x;
+}
+
+template <bool kRelu>
+__device__ __forceinline__ uint32_t pack_f16x2(uint32_t lo_bits, uint32_t hi_bits)
+{
+    const __half2 h = __floats2half2_rn(epilogue_value<kRelu>(lo_bits), epilogue_value<kRelu>(hi_bits));
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+template <class Cfg, bool kRelu>
+__global__ void __launch_bounds__(Cfg::THREADS, 1)
+    gemm_f16_relu_sm103a_1sm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                             const __grid_constant__ CUtensorMap tmap_c, const GemmParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;   // SW128 atoms need 1024-byte alignment
+    uint8_t *base_ptr = smem_raw + (base - raw);
+
+    const uint32_t sA = base + Cfg::SMEM_A_OFF;
+    const uint32_t sB = base + Cfg::SMEM_B_OFF;
+    const uint32_t sC = base + Cfg::SMEM_C_OFF;
+    const uint32_t ctl = base + Cfg::SMEM_CTL_OFF;
+    auto full_bar = [&](int s) { return ctl + 8u * s; };
+    auto empty_bar = [&](int s) { return ctl + 8u * (Cfg::STAGES + s); };
+    auto tfull_bar = [&](int b) { return ctl + 8u * (2 * Cfg::STAGES + b); };
+    auto tempty_bar = [&](int b) { return ctl + 8u * (2 * Cfg::STAGES + 2 + b); };
+    const uint32_t drain_bar = ctl + 8u * (2 * Cfg::STAGES + 4);
+    const uint32_t tmem_slot = ctl + 8u * (2 * Cfg::STAGES + 5);
+    volatile int *abort_flag =
+        reinterpret_cast<volatile int *>(base_ptr + Cfg::SMEM_CTL_OFF + 8 * (2 * Cfg::STAGES + 5) + 4);
+    volatile uint32_t *tmem_slot_ptr =
+        reinterpret_cast<volatile uint32_t *>(base_ptr + Cfg::SMEM_CTL_OFF + 8 * (2 * Cfg::STAGES + 5));
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < Cfg::STAGES; ++s) {
+            mbar_init(full_bar(s), 1);    // producer's arrive.expect_tx
+            mbar_init(empty_bar(s), 1);   // MMA thread's commit
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull_bar(b), 1);   // MMA thread's commit after the tile's last MMA
+            mbar_init(tempty_bar(b), 4);  // one arrive per epilogue warp
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&tmap_a);
+        prefetch_tensormap(&tmap_b);
+        prefetch_tensormap(&tmap_c);
+    }
+    if (warp == 1) {
+        tmem_alloc<1>(tmem_slot, Cfg::TMEM_COLS);
+        tmem_relinquish<1>();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot_ptr;
+    const uint64_t limit = p.timeout_cycles;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t issued_mask = 0, issued_parity = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+                int mb, nb;
+                tile_coords(t, p, mb, nb);
+                const int m0 = mb * Cfg::BM;
+                const int n0 = nb * Cfg::BN;
+                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                    if (!wait_phase(empty_bar(s), ph ^ 1u, abort_flag, limit, kSiteProducerEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full_bar(s), Cfg::STAGE_TX_BYTES);
+                    const int k0 = kb * Cfg::BK;
+                    tma_load_2d(sA + s * Cfg::A_STAGE_BYTES, &tmap_a, full_bar(s), k0, m0);
+#pragma unroll
+                    for (int j = 0; j < Cfg::B_BOXES; ++j)
+                        tma_load_2d(sB + s * Cfg::B_STAGE_BYTES + j * Cfg::B_BOX_BYTES, &tmap_b, full_bar(s),
+                                    n0 + j * Cfg::B_BOX_N, k0);
+                    issued_mask |= 1u << s;
+                    issued_parity = (issued_parity & ~(1u << s)) | (ph << s);
+                    if (++s == Cfg::STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // Abort: let this thread's loads in flight land before the CTA exits.
+                for (int i = 0; i < Cfg::STAGES; ++i)
+                    if (issued_mask & (1u << i))
+                        wait_phase_drain(full_bar(i), (issued_parity >> i) & 1u, limit, kSiteDrainLoads);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            int it = 0;
+            bool ok = true, issued_any = false;
+            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++it) {
+                const int b = it & 1;
+                const uint32_t acc_ph = (it >> 1) & 1;
+                if (!wait_phase(tempty_bar(b), acc_ph ^ 1u, abort_flag, limit, kSiteMmaTmemEmpty)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + b * Cfg::ACC_COLS;
+                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                    if (!wait_phase(full_bar(s), ph, abort_flag, limit, kSiteMmaFull)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t a0 = sA + s * Cfg::A_STAGE_BYTES;
+                    const uint32_t b0 = sB + s * Cfg::B_STAGE_BYTES;
+#pragma unroll
+                    for (int ks = 0; ks < Cfg::BK / Cfg::UMMA_K; ++ks) {
+                        // A: K-major, 8-row groups 1024 B apart; a K step of 16
+                        // elements is 32 B inside the 128-byte swizzle row.
+                        const uint64_t a_desc = smem_desc_sw128(a0 + ks * (Cfg::UMMA_K * 2), 16, 1024);
+                        // B: N-major; 64-column boxes B_BOX_BYTES apart (LBO),
+                        // 8-row K groups 1024 B apart (SBO); a K step of 16 rows
+                        // is 16 * 128 B.
+                        const uint64_t b_desc =
+                            smem_desc_sw128(b0 + ks * (Cfg::UMMA_K * 128), Cfg::B_BOX_BYTES, 1024);
+                        mma_f16_ss<1>(d_tmem, a_desc, b_desc, Cfg::IDESC, (kb | ks) != 0 ? 1u : 0u);
+                    }
+                    mma_commit(empty_bar(s));   // frees the slot once these MMAs have read it
+                    issued_any = true;
+                    if (++s == Cfg::STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                mma_commit(tfull_bar(b));   // accumulator b complete
+            }
+            if (!ok && issued_any) {
+                // Abort: wait for this thread's MMAs before the TMEM is freed.
+                mma_commit(drain_bar);
+                wait_phase_drain(drain_bar, 0, limit, kSiteDrainMma);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue (warps 2..5)
+        const int ew = warp - 2;        // owner of smem staging buffers
+        const int q = warp & 3;         // TMEM lane quarter this warp may access
+        const uint32_t row_off = static_cast<uint32_t>(lane) * 128u;
+        const uint32_t sw = static_cast<uint32_t>(lane & 7);
+        int it = 0;
+        uint32_t chunk = 0;
+        for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++it) {
+            int mb, nb;
+            tile_coords(t, p, mb, nb);
+            const int b = it & 1;
+            const uint32_t acc_ph = (it >> 1) & 1;
+            int ok = 1;
+            if (lane == 0) ok = wait_phase(tfull_bar(b), acc_ph, abort_flag, limit, kSiteEpilogueTmemFull) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after_sync();
+            const int row0 = mb * Cfg::BM + q * 32;
+#pragma unroll 1
+            for (int c = 0; c < Cfg::BN / Cfg::EPI_COLS; ++c) {
+                uint32_t r[64];
+                tmem_load_32x32b_x64(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * Cfg::ACC_COLS +
+                                         c * Cfg::EPI_COLS,
+                                     r);
+                if (c == Cfg::BN / Cfg::EPI_COLS - 1) {
+                    // All TMEM reads of accumulator b by this warp are done.
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(tempty_bar(b));
+                }
+                const int col0 = nb * Cfg::BN + c * Cfg::EPI_COLS;
+                const bool in_range = row0 < p.M && col0 < p.N;
+                const uint32_t cbuf = sC + (ew * 2 + (chunk & 1u)) * Cfg::C_BUF_BYTES;
+                ++chunk;
+                if (lane == 0) bulk_wait_group_read<1>();   // the store that used cbuf has read it
+                __syncwarp();
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t w0 = pack_f16x2<kRelu>(r[8 * j + 0], r[8 * j + 1]);
+                    const uint32_t w1 = pack_f16x2<kRelu>(r[8 * j + 2], r[8 * j + 3]);
+                    const uint32_t w2 = pack_f16x2<kRelu>(r[8 * j + 4], r[8 * j + 5]);
+                    const uint32_t w3 = pack_f16x2<kRelu>(r[8 * j + 6], r[8 * j + 7]);
+                    // 16-byte chunk j of this row goes to chunk j ^ (row % 8): the
+                    // layout a SWIZZLE_128B tensor-map store expects.
+                    st_shared_v4(cbuf + row_off + ((static_cast<uint32_t>(j) ^ sw) << 4), w0, w1, w2, w3);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    if (in_range) tma_store_2d(&tmap_c, cbuf, col0, row0);
+                    // One group per chunk, empty or not, so that "at most one group
+                    // pending" above always means the other buffer's store.
+                    bulk_commit_group();
+                }
+            }
+        }
+        if (lane == 0) bulk_wait_group<0>();
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after_sync();
+        tmem_dealloc<1>(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
+}  // namespace gemm_sm103

@@ -1,0 +1,186 @@
+"""ctypes binding over the C ABI of ``libgemm_f16.so`` (``include/gemm_f16.h``).
+
+Argument marshalling only: tensors become device pointers and sizes, the
+current torch stream becomes a ``cudaStream_t``, and status codes become
+exceptions.  Every element of C is computed by the library's sm_103a kernel;
+there is no fallback of any kind.  If the library has not been built, every
+call raises :class:`LibraryNotBuilt`.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+from . import build as _build
+
+GEMM_OK = 0
+GEMM_ERR_INVALID_ARG = -1
+GEMM_ERR_ALIGNMENT = -2
+GEMM_ERR_UNSUPPORTED_DEVICE = -3
+GEMM_ERR_LAUNCH = -4
+GEMM_ERR_TIMEOUT = -5
+GEMM_ERR_CUDA = -6
+
+HEADER = os.path.join(_build.INCLUDE, "gemm_f16.h")
+
+
+class LibraryNotBuilt(RuntimeError):
+    pass
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: status {status} ({strerror(status)})")
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (raises LibraryNotBuilt if it is missing)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_build.LIB):
+        raise LibraryNotBuilt(f"{_build.LIB} is missing; build it with __graft_entry__.build() "
+                              "or python -m dense_fp16_gemm_05_gb300.build")
+    L = ctypes.CDLL(_build.LIB)
+    vp, i64, ci = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    L.gemm_f16.argtypes = [vp, vp, vp, i64, i64, i64, ci, vp]
+    L.gemm_f16.restype = ci
+    L.gemm_f16_ex.argtypes = [vp, vp, vp, i64, i64, i64, ci, ci, vp]
+    L.gemm_f16_ex.restype = ci
+    L.gemm_f16_from_host.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, ci, vp]
+    L.gemm_f16_from_host.restype = ci
+    L.gemm_f16_check.argtypes = [vp]
+    L.gemm_f16_check.restype = ci
+    L.gemm_f16_last_timeout_record.argtypes = []
+    L.gemm_f16_last_timeout_record.restype = ctypes.c_uint64
+    L.gemm_f16_strerror.argtypes = [ci]
+    L.gemm_f16_strerror.restype = ctypes.c_char_p
+    L.gemm_f16_version.argtypes = []
+    L.gemm_f16_version.restype = ci
+    L.gemm_f16_num_configs.argtypes = []
+    L.gemm_f16_num_configs.restype = ci
+    L.gemm_f16_config_name.argtypes = [ci]
+    L.gemm_f16_config_name.restype = ctypes.c_char_p
+    L.gemm_f16_auto_config.argtypes = [i64, i64, i64]
+    L.gemm_f16_auto_config.restype = ci
+    _lib = L
+    return L
+
+
+def header_functions() -> list[str]:
+    """Names of the functions declared in include/gemm_f16.h."""
+    with open(HEADER) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gemm_f16\w*)\s*\(", text)))
+
+
+def strerror(status: int) -> str:
+    try:
+        return lib().gemm_f16_strerror(int(status)).decode()
+    except LibraryNotBuilt:
+        return "library not built"
+
+
+def version() -> int:
+    return int(lib().gemm_f16_version())
+
+
+def num_configs() -> int:
+    return int(lib().gemm_f16_num_configs())
+
+
+def config_name(config: int) -> str | None:
+    r = lib().gemm_f16_config_name(int(config))
+    return None if r is None else r.decode()
+
+
+def _stream_handle(stream, device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    if isinstance(stream, torch.cuda.Stream):
+        return int(stream.cuda_stream)
+    return int(stream)
+
+
+def _check_operand(t: torch.Tensor, name: str):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != torch.float16 or t.dim() != 2 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous 2-D float16 tensor, got {t.dtype} {tuple(t.shape)}")
+
+
+def gemm_f16(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None, relu: bool = True,
+             stream=None, config: int = 0) -> torch.Tensor:
+    """C = ReLU(A @ B) (relu=True) or A @ B, fp16 in and out, fp32 accumulation.
+
+    A (M,K), B (K,N), C (M,N): contiguous float16 CUDA tensors on one device.
+    C is allocated (torch.empty) when not given.  The call is asynchronous on
+    ``stream`` (default: torch's current stream); errors in the arguments raise
+    :class:`GemmError` immediately.
+    """
+    _check_operand(A, "A")
+    _check_operand(B, "B")
+    M, K = A.shape
+    K2, N = B.shape
+    if K != K2:
+        raise ValueError(f"inner sizes differ: A {tuple(A.shape)}, B {tuple(B.shape)}")
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.float16, device=A.device)
+    _check_operand(C, "C")
+    if tuple(C.shape) != (M, N):
+        raise ValueError(f"C must be {(M, N)}, got {tuple(C.shape)}")
+    L = lib()
+    with torch.cuda.device(A.device):
+        st = L.gemm_f16_ex(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, int(bool(relu)), int(config),
+                           _stream_handle(stream, A.device))
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_f16")
+    return C
+
+
+def gemm_f16_raw(A_ptr: int, B_ptr: int, C_ptr: int, M: int, N: int, K: int, relu: int, stream: int = 0,
+                 config: int = 0) -> int:
+    """The C call with raw pointers; returns the status code (no exception)."""
+    return int(lib().gemm_f16_ex(A_ptr, B_ptr, C_ptr, M, N, K, relu, config, stream))
+
+
+def gemm_f16_from_host(A_host: torch.Tensor, B_host: torch.Tensor, C_host: torch.Tensor,
+                       A_dev: torch.Tensor, B_dev: torch.Tensor, C_dev: torch.Tensor,
+                       relu: bool = True, stream=None) -> None:
+    """End-to-end call: host A, B -> device, GEMM, device C -> host, all on ``stream``.
+
+    The host tensors should be pinned (``pin_memory()``) for asynchronous
+    copies.  Returns after enqueueing; synchronise the stream before reading
+    C_host.
+    """
+    for t, n in ((A_host, "A_host"), (B_host, "B_host"), (C_host, "C_host"),
+                 (A_dev, "A_dev"), (B_dev, "B_dev"), (C_dev, "C_dev")):
+        _check_operand(t, n)
+    M, K = A_host.shape
+    N = B_host.shape[1]
+    L = lib()
+    with torch.cuda.device(A_dev.device):
+        st = L.gemm_f16_from_host(A_host.data_ptr(), B_host.data_ptr(), C_host.data_ptr(), A_dev.data_ptr(),
+                                  B_dev.data_ptr(), C_dev.data_ptr(), M, N, K, int(bool(relu)),
+                                  _stream_handle(stream, A_dev.device))
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_f16_from_host")
+
+
+def check(stream=None, device=None) -> int:
+    """Synchronises the stream and returns the device status (GEMM_OK or an error code)."""
+    dev = device if device is not None else torch.cuda.current_device()
+    with torch.cuda.device(dev):
+        return int(lib().gemm_f16_check(_stream_handle(stream, dev)))
+
+
+def auto_config(M: int, N: int, K: int) -> int:
+    return int(lib().gemm_f16_auto_config(M, N, K))

@@ -1,0 +1,143 @@
+/*
+ * gemm_f16.h -- C ABI of the GB300 (sm_103a) half-precision GEMM with a fused
+ * ReLU epilogue.
+ *
+ * Operation.  C = R(A @ B) for dense row-major IEEE binary16 matrices
+ * A (M,K), B (K,N) and C (M,N), products accumulated in fp32, R(x) = max(x, 0)
+ * when relu = 1 (every x <= 0, -0 and NaN give +0) and R(x) = x when relu = 0,
+ * then one round-to-nearest-even cast to binary16.  This is the kernel of
+ * "Writing High-Performance Kernels in TileLang, from GEMM to MLA"
+ * (atlascloud.ai), section "Let's write a GEMM": float16 A, B and C, a float
+ * accumulator cleared per output tile, ReLU on the accumulator, one copy back
+ * to float16.  relu = 0 is the plain GEMM of the TileLang-MUSA lesson
+ * (7yue.com, section 3) and of the nxmr.cn A100 benchmark (section 2.2).
+ *
+ * Layout.  Leading dimensions are implied: K for A, N for B and N for C (no
+ * stride arguments, as in the pages' T.Tensor((M,K)) ... declarations).
+ *
+ * Ownership.  The caller owns every buffer.  The library allocates nothing per
+ * call; its only device state is one status word per GPU (a __device__
+ * variable of the library's module) that the kernels set when a bounded wait
+ * expires.  C must not overlap A or B.
+ *
+ * Asynchrony.  gemm_f16 and gemm_f16_ex only enqueue work on `stream` (a
+ * cudaStream_t; NULL is the legacy default stream) and return without
+ * synchronising.  Argument errors are reported synchronously by the return
+ * value and launch nothing.  A device-side timeout is reported later, by
+ * gemm_f16_check.
+ *
+ * Thread safety.  All entry points may be called from several host threads.
+ * Tensor-map descriptors are built on the host per call and passed by value
+ * as kernel parameters; there is no cache to race on.
+ *
+ * Device.  Requires a compute capability 10.3 GPU (GB300) as the current
+ * device; any other device gives GEMM_ERR_UNSUPPORTED_DEVICE.
+ */
+#ifndef GEMM_F16_H_
+#define GEMM_F16_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GEMM_F16_VERSION 1
+
+/* Return codes.  0 is success; every error is negative. */
+enum gemm_f16_status {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = -1,        /* negative size, size > INT32_MAX, relu not 0/1,
+                                         NULL or non-device pointer, buffer smaller than
+                                         its matrix, C overlapping A or B, bad config id */
+    GEMM_ERR_ALIGNMENT = -2,          /* a pointer not 16-byte aligned, or N or K not a
+                                         multiple of 8 (the 16-byte row-pitch rule of the
+                                         tensor-memory-access unit) */
+    GEMM_ERR_UNSUPPORTED_DEVICE = -3, /* current device is not compute capability 10.3 */
+    GEMM_ERR_LAUNCH = -4,             /* the CUDA launch itself failed */
+    GEMM_ERR_TIMEOUT = -5,            /* a kernel's bounded wait expired (gemm_f16_check) */
+    GEMM_ERR_CUDA = -6                /* another CUDA runtime/driver call failed */
+};
+
+/*
+ * gemm_f16 -- C = R(A @ B) on the current device, enqueued on `stream`.
+ *
+ *   A       device pointer, M*K binary16 values, row-major (leading dim K)
+ *   B       device pointer, K*N binary16 values, row-major (leading dim N)
+ *   C       device pointer, M*N binary16 values, row-major (leading dim N), written
+ *   M,N,K   sizes, 0 <= M,N,K <= INT32_MAX
+ *   relu    1: fused ReLU epilogue; 0: plain product
+ *   stream  cudaStream_t (NULL: legacy default stream)
+ *
+ * Degenerate sizes: M == 0 or N == 0 is a no-op returning GEMM_OK (no pointer
+ * is touched or checked).  K == 0 fills C with +0 (the empty sum; R(+0) = +0).
+ * Alignment: A, B, C 16-byte aligned and N % 8 == 0, K % 8 == 0, else
+ * GEMM_ERR_ALIGNMENT.  M is unrestricted; ragged edges in M, N and K are
+ * handled in the kernel (out-of-range operand elements read as zero,
+ * out-of-range C elements are never written).
+ */
+int gemm_f16(const void *A, const void *B, void *C,
+             int64_t M, int64_t N, int64_t K, int relu, void *stream);
+
+/*
+ * gemm_f16_ex -- gemm_f16 with an explicit kernel configuration.
+ *
+ *   config  0: automatic choice (what gemm_f16 uses); 1..gemm_f16_num_configs():
+ *           a fixed tiling, see gemm_f16_config_name().  Every configuration
+ *           computes the same function; they differ in tile shape and in the
+ *           number of SMs that cooperate on one tile.  Unknown id:
+ *           GEMM_ERR_INVALID_ARG.
+ */
+int gemm_f16_ex(const void *A, const void *B, void *C,
+                int64_t M, int64_t N, int64_t K, int relu, int config, void *stream);
+
+/* Number of fixed configurations accepted by gemm_f16_ex (ids 1..n). */
+int gemm_f16_num_configs(void);
+
+/* Short name of a configuration id ("auto" for 0), or NULL for an unknown id.
+ * The string is static; the caller must not free it. */
+const char *gemm_f16_config_name(int config);
+
+/* Configuration id that gemm_f16 picks for this problem size on the current
+ * device (never 0), or a negative status for invalid sizes. */
+int gemm_f16_auto_config(int64_t M, int64_t N, int64_t K);
+
+/*
+ * gemm_f16_from_host -- end-to-end call on host buffers.
+ *
+ * Enqueues on `stream`: a copy of A_host into A_dev and of B_host into B_dev,
+ * gemm_f16(A_dev, B_dev, C_dev, ...), and a copy of C_dev into C_host.  All
+ * six buffers belong to the caller (host ones ideally page-locked, so that
+ * the copies are asynchronous; device ones sized as for gemm_f16).  Returns
+ * after enqueueing; the caller synchronises `stream` before reading C_host.
+ * Errors as gemm_f16, plus GEMM_ERR_INVALID_ARG for a NULL host pointer and
+ * GEMM_ERR_CUDA when a copy cannot be enqueued.
+ */
+int gemm_f16_from_host(const void *A_host, const void *B_host, void *C_host,
+                       void *A_dev, void *B_dev, void *C_dev,
+                       int64_t M, int64_t N, int64_t K, int relu, void *stream);
+
+/*
+ * gemm_f16_check -- synchronises `stream`, then reads and clears the device
+ * status word of the current device.  Returns GEMM_OK, GEMM_ERR_TIMEOUT if any
+ * kernel launched on this device since the last check hit its wait limit (its
+ * output is then incomplete), or GEMM_ERR_CUDA if the stream reported an
+ * error.  The status word is shared by all launches on the device.
+ */
+int gemm_f16_check(void *stream);
+
+/* Raw value of the last timeout record read by gemm_f16_check on this thread
+ * (0 if none): bits 0-7 the wait site, bits 8-31 the block index. */
+uint64_t gemm_f16_last_timeout_record(void);
+
+/* Human-readable text for a status code (static storage). */
+const char *gemm_f16_strerror(int status);
+
+/* GEMM_F16_VERSION of the built library. */
+int gemm_f16_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_F16_H_ */

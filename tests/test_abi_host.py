@@ -1,0 +1,94 @@
+"""Host-only checks of the C ABI (no GPU needed, no kernel launched).
+
+The library must load on a machine without a GPU driver, export every
+function that include/gemm_f16.h declares, and reject bad arguments before
+touching the GPU.
+"""
+from __future__ import annotations
+
+import ctypes
+import re
+
+import pytest
+
+from dense_fp16_gemm_05_gb300 import build as gbuild
+
+
+@pytest.fixture(scope="module")
+def g():
+    gbuild.build()
+    from dense_fp16_gemm_05_gb300 import gemm_f16
+    gemm_f16.lib()
+    return gemm_f16
+
+
+def test_library_exports_every_declared_function(g):
+    names = g.header_functions()
+    assert "gemm_f16" in names and "gemm_f16_check" in names
+    raw = ctypes.CDLL(gbuild.LIB)
+    missing = [n for n in names if not hasattr(raw, n)]
+    assert not missing, missing
+
+
+def test_header_declarations_are_extern_c_and_plain_types():
+    with open(gbuild.os.path.join(gbuild.INCLUDE, "gemm_f16.h")) as f:
+        text = f.read()
+    assert 'extern "C"' in text
+    assert "torch" not in re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+
+
+def test_version_matches_header(g):
+    with open(g.HEADER) as f:
+        m = re.search(r"#define GEMM_F16_VERSION (\d+)", f.read())
+    assert g.version() == int(m.group(1))
+
+
+def test_strerror_covers_all_codes(g):
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        s = g.strerror(code)
+        assert s and s != "unknown status"
+    assert g.strerror(-99) == "unknown status"
+
+
+def test_configs_are_named(g):
+    n = g.num_configs()
+    assert n >= 1
+    assert g.config_name(0) == "auto"
+    for i in range(1, n + 1):
+        assert g.config_name(i)
+    assert g.config_name(n + 1) is None and g.config_name(-1) is None
+
+
+@pytest.mark.parametrize("M,N,K", [(-1, 8, 8), (8, -1, 8), (8, 8, -1), (2**31, 8, 8), (8, 2**31, 8),
+                                   (8, 8, 2**31)])
+def test_bad_sizes_rejected_before_any_cuda_call(g, M, N, K):
+    assert g.gemm_f16_raw(0, 0, 0, M, N, K, 1) == g.GEMM_ERR_INVALID_ARG
+
+
+def test_bad_relu_and_config_rejected(g):
+    assert g.gemm_f16_raw(0, 0, 0, 8, 8, 8, 2) == g.GEMM_ERR_INVALID_ARG
+    assert g.gemm_f16_raw(0, 0, 0, 8, 8, 8, -1) == g.GEMM_ERR_INVALID_ARG
+    assert g.gemm_f16_raw(0, 0, 0, 8, 8, 8, 1, config=g.num_configs() + 1) == g.GEMM_ERR_INVALID_ARG
+    assert g.gemm_f16_raw(0, 0, 0, 8, 8, 8, 1, config=-1) == g.GEMM_ERR_INVALID_ARG
+
+
+def test_empty_problem_is_a_no_op(g):
+    # M == 0 or N == 0 touches nothing, so even NULL pointers are fine
+    assert g.gemm_f16_raw(0, 0, 0, 0, 8, 8, 1) == g.GEMM_OK
+    assert g.gemm_f16_raw(0, 0, 0, 8, 0, 8, 1) == g.GEMM_OK
+
+
+def test_no_gpu_gives_a_status_not_a_crash(g):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    st = g.gemm_f16_raw(16, 16, 16, 8, 8, 8, 1)
+    assert st in (g.GEMM_ERR_CUDA, g.GEMM_ERR_UNSUPPORTED_DEVICE)
+
+
+def test_binding_fails_loudly_without_library(monkeypatch):
+    from dense_fp16_gemm_05_gb300 import gemm_f16 as mod
+    monkeypatch.setattr(mod, "_lib", None)
+    monkeypatch.setattr(mod._build, "LIB", "/nonexistent/libgemm_f16.so")
+    with pytest.raises(mod.LibraryNotBuilt):
+        mod.lib()
