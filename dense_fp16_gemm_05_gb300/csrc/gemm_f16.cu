@@ -11,6 +11,7 @@
 
 #include <cstdint>
 #include <cstdio>
+#include <cstdlib>
 #include <mutex>
 
 #include "gemm_f16.h"
@@ -29,13 +30,15 @@ struct ConfigInfo {
 };
 
 // id 1..kNumConfigs; index 0 is "auto".
-using Cfg256 = Cfg1Sm<256, 4>;
-using Cfg128 = Cfg1Sm<128, 6>;
+using Cfg1x256 = GemmCfg<1, 256, 4>;
+using Cfg1x128 = GemmCfg<1, 128, 6>;
+using Cfg2x256 = GemmCfg<2, 256, 6>;
 
 constexpr ConfigInfo kConfigs[] = {
     {"auto", 0, 0},
-    {"1sm_128x256_s4", Cfg256::BM, Cfg256::BN},
-    {"1sm_128x128_s6", Cfg128::BM, Cfg128::BN},
+    {"1sm_128x256_s4", Cfg1x256::TILE_M, Cfg1x256::BN},
+    {"1sm_128x128_s6", Cfg1x128::TILE_M, Cfg1x128::BN},
+    {"2sm_256x256_s6", Cfg2x256::TILE_M, Cfg2x256::BN},
 };
 constexpr int kNumConfigs = static_cast<int>(sizeof(kConfigs) / sizeof(kConfigs[0])) - 1;
 
@@ -173,15 +176,71 @@ uint64_t timeout_cycles_for(int64_t K)
 int pick_config(int64_t M, int64_t N, int64_t K, int sm_count)
 {
     (void)K;
+    const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
+    // Enough 256x256 tiles to keep every SM pair busy: the CTA-pair kernel.
+    if (pair_tiles >= sm_count / 2) return 3;
     const int64_t tiles256 = ((M + 127) / 128) * ((N + 255) / 256);
+    if (tiles256 >= sm_count / 2) return 1;
     // Few tiles: narrower tiles put more SMs to work.
-    if (tiles256 < sm_count / 2) return 2;
-    return 1;
+    return 2;
+}
+
+int group_m_override()
+{
+    static int v = [] {
+        const char *e = std::getenv("GEMM_F16_GROUP_M");
+        const int x = e ? std::atoi(e) : 0;
+        return x > 0 && x <= 4096 ? x : 0;
+    }();
+    return v;
+}
+
+// Persistent grid size in tiles-at-once: one CTA (or CTA pair) per SM (pair
+// of SMs) that can be co-resident, never more than there are tiles.
+template <class Cfg, bool kRelu>
+int64_t persistent_units(int64_t tiles, int sm_count)
+{
+    int slots = sm_count / Cfg::CTA_GROUP;
+    if (Cfg::CTA_GROUP > 1) {
+        auto kern = gemm_f16_relu_sm103a<Cfg, kRelu>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        cudaLaunchConfig_t lc{};
+        lc.blockDim = dim3(Cfg::THREADS, 1, 1);
+        lc.dynamicSmemBytes = Cfg::SMEM_BYTES;
+        lc.gridDim = dim3(Cfg::CTA_GROUP * slots, 1, 1);
+        cudaLaunchAttribute attrs[1];
+        attrs[0].id = cudaLaunchAttributeClusterDimension;
+        attrs[0].val.clusterDim.x = Cfg::CTA_GROUP;
+        attrs[0].val.clusterDim.y = 1;
+        attrs[0].val.clusterDim.z = 1;
+        lc.attrs = attrs;
+        lc.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, kern, &lc) == cudaSuccess && clusters > 0)
+            slots = clusters < slots ? clusters : slots;
+        else
+            cudaGetLastError();
+    }
+    return tiles < slots ? tiles : slots;
+}
+
+template <class Cfg>
+int fill_launch_info(int64_t M, int64_t N, int sm_count, int *grid_ctas, int *cluster_size, int *tiles)
+{
+    const int64_t t = ((M + Cfg::TILE_M - 1) / Cfg::TILE_M) * ((N + Cfg::BN - 1) / Cfg::BN);
+    if (tiles) *tiles = static_cast<int>(t < INT32_MAX ? t : INT32_MAX);
+    if (cluster_size) *cluster_size = Cfg::CTA_GROUP;
+    if (grid_ctas) *grid_ctas = static_cast<int>(persistent_units<Cfg, true>(t, sm_count) * Cfg::CTA_GROUP);
+    return GEMM_OK;
 }
 
 template <class Cfg, bool kRelu>
-int launch_1sm(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K, int sm_count,
-               cudaStream_t stream)
+int launch(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K, int sm_count,
+           cudaStream_t stream)
 {
     CUtensorMap ta, tb, tc;
     int st;
@@ -193,33 +252,34 @@ int launch_1sm(const void *A, const void *B, void *C, int64_t M, int64_t N, int6
     p.M = static_cast<int32_t>(M);
     p.N = static_cast<int32_t>(N);
     p.K = static_cast<int32_t>(K);
-    p.num_m_blocks = static_cast<int32_t>((M + Cfg::BM - 1) / Cfg::BM);
+    p.num_m_blocks = static_cast<int32_t>((M + Cfg::TILE_M - 1) / Cfg::TILE_M);
     p.num_n_blocks = static_cast<int32_t>((N + Cfg::BN - 1) / Cfg::BN);
     p.num_k_blocks = static_cast<int32_t>((K + Cfg::BK - 1) / Cfg::BK);
     const int64_t tiles = static_cast<int64_t>(p.num_m_blocks) * p.num_n_blocks;
-    if (tiles > INT32_MAX) return GEMM_ERR_INVALID_ARG;
+    if (tiles > INT32_MAX / 2) return GEMM_ERR_INVALID_ARG;
     p.num_tiles = static_cast<int32_t>(tiles);
-    p.group_m = 16;
+    p.group_m = group_m_override() ? group_m_override() : (Cfg::CTA_GROUP == 2 ? 8 : 16);
     p.timeout_cycles = timeout_cycles_for(K);
 
-    auto kern = gemm_f16_relu_sm103a_1sm<Cfg, kRelu>;
+    auto kern = gemm_f16_relu_sm103a<Cfg, kRelu>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;
     }
-    const int grid = static_cast<int>(tiles < sm_count ? tiles : sm_count);
     cudaLaunchConfig_t lc{};
-    lc.gridDim = dim3(grid, 1, 1);
     lc.blockDim = dim3(Cfg::THREADS, 1, 1);
     lc.dynamicSmemBytes = Cfg::SMEM_BYTES;
     lc.stream = stream;
     cudaLaunchAttribute attrs[1];
     attrs[0].id = cudaLaunchAttributeClusterDimension;
-    attrs[0].val.clusterDim.x = 1;
+    attrs[0].val.clusterDim.x = Cfg::CTA_GROUP;
     attrs[0].val.clusterDim.y = 1;
     attrs[0].val.clusterDim.z = 1;
     lc.attrs = attrs;
     lc.numAttrs = 1;
+
+    const int64_t units = persistent_units<Cfg, kRelu>(tiles, sm_count);
+    lc.gridDim = dim3(static_cast<unsigned>(units * Cfg::CTA_GROUP), 1, 1);
     if (cudaLaunchKernelEx(&lc, kern, ta, tb, tc, p) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;
@@ -231,8 +291,8 @@ template <class Cfg>
 int launch_cfg(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K, int relu, int sm_count,
                cudaStream_t stream)
 {
-    return relu ? launch_1sm<Cfg, true>(A, B, C, M, N, K, sm_count, stream)
-                : launch_1sm<Cfg, false>(A, B, C, M, N, K, sm_count, stream);
+    return relu ? launch<Cfg, true>(A, B, C, M, N, K, sm_count, stream)
+                : launch<Cfg, false>(A, B, C, M, N, K, sm_count, stream);
 }
 
 thread_local uint64_t t_last_timeout_record = 0;
@@ -273,8 +333,9 @@ extern "C" int gemm_f16_ex(const void *A, const void *B, void *C, int64_t M, int
 
     const int cfg = config == 0 ? pick_config(M, N, K, dev.sm_count) : config;
     switch (cfg) {
-        case 1: return launch_cfg<Cfg256>(A, B, C, M, N, K, relu, dev.sm_count, s);
-        case 2: return launch_cfg<Cfg128>(A, B, C, M, N, K, relu, dev.sm_count, s);
+        case 1: return launch_cfg<Cfg1x256>(A, B, C, M, N, K, relu, dev.sm_count, s);
+        case 2: return launch_cfg<Cfg1x128>(A, B, C, M, N, K, relu, dev.sm_count, s);
+        case 3: return launch_cfg<Cfg2x256>(A, B, C, M, N, K, relu, dev.sm_count, s);
         default: return GEMM_ERR_INVALID_ARG;
     }
 }
@@ -300,6 +361,23 @@ extern "C" int gemm_f16_auto_config(int64_t M, int64_t N, int64_t K)
     DeviceInfo dev;
     if ((st = current_device_info(&dev)) != GEMM_OK) return st;
     return pick_config(M, N, K, dev.sm_count);
+}
+
+extern "C" int gemm_f16_launch_info(int64_t M, int64_t N, int64_t K, int config, int *grid_ctas,
+                                    int *cluster_size, int *tiles)
+{
+    int st = check_sizes(M, N, K, 0);
+    if (st != GEMM_OK) return st;
+    if (config < 0 || config > kNumConfigs) return GEMM_ERR_INVALID_ARG;
+    DeviceInfo dev;
+    if ((st = current_device_info(&dev)) != GEMM_OK) return st;
+    const int cfg = config == 0 ? pick_config(M, N, K, dev.sm_count) : config;
+    switch (cfg) {
+        case 1: return fill_launch_info<Cfg1x256>(M, N, dev.sm_count, grid_ctas, cluster_size, tiles);
+        case 2: return fill_launch_info<Cfg1x128>(M, N, dev.sm_count, grid_ctas, cluster_size, tiles);
+        case 3: return fill_launch_info<Cfg2x256>(M, N, dev.sm_count, grid_ctas, cluster_size, tiles);
+        default: return GEMM_ERR_INVALID_ARG;
+    }
 }
 
 extern "C" int gemm_f16_from_host(const void *A_host, const void *B_host, void *C_host, void *A_dev, void *B_dev,

@@ -22,14 +22,24 @@
 //   * L2 swizzle         -> grouped rasterisation in a persistent tile loop
 // Two TMEM accumulators let the epilogue of tile i overlap the MMAs of i+1.
 //
+// CTA-pair mode (CTA_GROUP == 2, a cluster of two CTAs on two SMs): one
+// tcgen05.mma.cta_group::2 computes a 256 x BN tile.  Each CTA loads its own
+// 128 rows of A and its own BN/2 columns of B into its own shared memory; the
+// pair's tensor cores read both halves, and each CTA's TMEM receives its 128
+// rows of the accumulator.  Only the even CTA (the leader) issues MMAs: both
+// CTAs' loads complete on the leader's "full" barrier, the leader's commits
+// arrive on both CTAs' "empty" and "tmem full" barriers, and both CTAs'
+// epilogue warps arrive on the leader's "tmem empty" barrier.
+//
 // Ragged edges: TMA loads fill out-of-range elements with zeros, so partial
 // tiles in M, N and K contribute nothing; TMA stores do not write outside C.
 //
 // Every mbarrier wait is bounded (clock64 budget).  On expiry the waiting
-// thread records the site in a device status word, raises a CTA-wide abort
-// flag, and every role leaves its loop; the producer then waits (bounded) for
-// its own loads in flight, the MMA thread for its own MMAs, the epilogue for
-// its own stores, and the TMEM is freed before the CTA exits.
+// thread records the site in a device status word, raises the abort flag of
+// its CTA (and of the peer CTA in pair mode), and every role leaves its loop;
+// the producer then waits (bounded) for its own loads in flight, the MMA thread
+// for its own MMAs, the epilogue for its own stores, and the TMEM is freed
+// before the CTA exits.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -62,26 +72,29 @@ enum WaitSite : uint32_t {
 };
 
 // Tile shapes and shared-memory budget of one kernel configuration.
-//   kBN      columns of C per tile
-//   kStages  depth of the shared-memory K ring
-template <int kBN, int kStages>
-struct Cfg1Sm {
-    static constexpr int kCtaGroup = 1;
-    static constexpr int BM = 128;            // rows of C per tile = TMEM lanes
+//   kCtaGroup  1: one CTA per tile; 2: a CTA pair per tile (cta_group::2)
+//   kBN        columns of C per tile (the MMA's N)
+//   kStages    depth of the shared-memory K ring
+template <int kCtaGroup, int kBN, int kStages>
+struct GemmCfg {
+    static constexpr int CTA_GROUP = kCtaGroup;
+    static constexpr int BM = 128;                    // rows of C per CTA = TMEM lanes
+    static constexpr int TILE_M = BM * CTA_GROUP;     // rows of C per tile (the MMA's M)
     static constexpr int BN = kBN;
-    static constexpr int BK = 64;             // 64 fp16 = 128 bytes = one swizzle row
-    static constexpr int UMMA_K = 16;         // K of one tcgen05.mma.kind::f16
+    static constexpr int BN_CTA = BN / CTA_GROUP;     // columns of B each CTA loads
+    static constexpr int BK = 64;                     // 64 fp16 = 128 bytes = one swizzle row
+    static constexpr int UMMA_K = 16;                 // K of one tcgen05.mma.kind::f16
     static constexpr int STAGES = kStages;
-    static constexpr int THREADS = 192;       // producer, MMA, 4 epilogue warps
-    static constexpr int B_BOX_N = 64;        // N extent of one B box (128 bytes)
-    static constexpr int B_BOXES = BN / B_BOX_N;
+    static constexpr int THREADS = 192;               // producer, MMA, 4 epilogue warps
+    static constexpr int B_BOX_N = 64;                // N extent of one B box (128 bytes)
+    static constexpr int B_BOXES = BN_CTA / B_BOX_N;
     static constexpr int A_STAGE_BYTES = BM * BK * 2;
     static constexpr int B_BOX_BYTES = B_BOX_N * BK * 2;
     static constexpr int B_STAGE_BYTES = B_BOXES * B_BOX_BYTES;
-    static constexpr int STAGE_TX_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
-    static constexpr int ACC_COLS = BN;       // fp32 TMEM columns of one accumulator
-    static constexpr int TMEM_COLS = 2 * ACC_COLS;
-    static constexpr int EPI_COLS = 64;       // columns per epilogue chunk (128 bytes of fp16)
+    static constexpr int STAGE_TX_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;   // loaded per CTA per stage
+    static constexpr int ACC_COLS = BN;               // fp32 TMEM columns of one accumulator
+    static constexpr int TMEM_COLS = 2 * ACC_COLS;    // two accumulators
+    static constexpr int EPI_COLS = 64;               // columns per epilogue chunk (128 bytes of fp16)
     static constexpr int C_BUF_BYTES = 32 * EPI_COLS * 2;
     static constexpr int SMEM_A_OFF = 0;
     static constexpr int SMEM_B_OFF = SMEM_A_OFF + STAGES * A_STAGE_BYTES;
@@ -89,9 +102,10 @@ struct Cfg1Sm {
     static constexpr int SMEM_CTL_OFF = SMEM_C_OFF + 4 * 2 * C_BUF_BYTES;
     static constexpr int SMEM_CTL_BYTES = 256;
     static constexpr int SMEM_BYTES = 1024 /* alignment slack */ + SMEM_CTL_OFF + SMEM_CTL_BYTES;
-    static constexpr uint32_t IDESC = idesc_f16_f32(BM, BN, /*A MN-major*/ false, /*B MN-major*/ true);
+    static constexpr uint32_t IDESC = idesc_f16_f32(TILE_M, BN, /*A MN-major*/ false, /*B MN-major*/ true);
 
-    static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "UMMA N for M=128 is a multiple of 16 up to 256");
+    static_assert(CTA_GROUP == 1 || CTA_GROUP == 2, "one CTA or a CTA pair");
+    static_assert(BN_CTA % 64 == 0 && BN >= 64 && BN <= 256, "UMMA N: multiple of 16 up to 256");
     static_assert(TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation is a power of 2");
     static_assert((2 * STAGES + 5) * 8 + 8 <= SMEM_CTL_BYTES, "control block");
     static_assert(SMEM_BYTES <= 232448, "shared memory per block on sm_103");
@@ -100,21 +114,39 @@ struct Cfg1Sm {
 // Device status word: 0 = fine; otherwise the first timeout record.
 __device__ unsigned long long g_gemm_f16_status;
 
+// Abort flag of this CTA, and (pair mode) the shared::cluster address of the
+// peer CTA's flag.
+struct AbortFlag {
+    volatile int *local;
+    uint32_t peer_addr;
+    bool pair;
+
+    __device__ __forceinline__ bool raised() const { return *local != 0; }
+    __device__ __forceinline__ void raise(uint32_t site) const
+    {
+        *local = 1;
+        if (pair) st_shared_cluster_u32(peer_addr, 1u);
+        atomicCAS(&g_gemm_f16_status, 0ull,
+                  static_cast<unsigned long long>(site) | (static_cast<unsigned long long>(blockIdx.x) << 8));
+    }
+};
+
 // Bounded wait on an mbarrier phase.  Fast path: one probe.  Slow path: probe
-// until the phase completes, the CTA's abort flag is raised, or the clock64
-// budget is spent (then record the site and raise the abort flag).
-__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int *abort_flag, uint64_t limit,
+// until the phase completes, the abort flag is raised, or the clock64 budget
+// is spent (then record the site and raise the abort flag).  The probe is the
+// default (CTA-scope) form also for barriers another CTA arrives on: TMA bytes
+// become visible through the barrier's transaction count, and TMEM hand-offs
+// are ordered by the tcgen05 fences around the waits.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const AbortFlag &abort, uint64_t limit,
                                            uint32_t site)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
+        if (abort.raised()) return false;
         if (static_cast<uint64_t>(clock64() - t0) > limit) {
-            *abort_flag = 1;
-            atomicCAS(&g_gemm_f16_status, 0ull,
-                      static_cast<unsigned long long>(site) | (static_cast<unsigned long long>(blockIdx.x) << 8));
+            abort.raise(site);
             return false;
         }
     }
@@ -135,7 +167,7 @@ __device__ __forceinline__ bool wait_phase_drain(uint32_t bar, uint32_t parity, 
 }
 
 // Grouped rasterisation: tiles are visited in panels of group_m tile rows; inside
-// a panel the row index runs fastest, so CTAs that run at the same time share
+// a panel the row index runs fastest, so tiles that run at the same time share
 // the same few A row-panels and B column-panels in L2.
 __device__ __forceinline__ void tile_coords(int t, const GemmParams &p, int &mb, int &nb)
 {
@@ -171,9 +203,11 @@ __device__ __forceinline__ uint32_t pack_f16x2(uint32_t lo_bits, uint32_t hi_bit
 
 template <class Cfg, bool kRelu>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
-    gemm_f16_relu_sm103a_1sm(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                             const __grid_constant__ CUtensorMap tmap_c, const GemmParams p)
+    gemm_f16_relu_sm103a(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                         const __grid_constant__ CUtensorMap tmap_c, const GemmParams p)
 {
+    constexpr bool kPair = Cfg::CTA_GROUP == 2;
+
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;   // SW128 atoms need 1024-byte alignment
@@ -189,25 +223,33 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     auto tempty_bar = [&](int b) { return ctl + 8u * (2 * Cfg::STAGES + 2 + b); };
     const uint32_t drain_bar = ctl + 8u * (2 * Cfg::STAGES + 4);
     const uint32_t tmem_slot = ctl + 8u * (2 * Cfg::STAGES + 5);
-    volatile int *abort_flag =
-        reinterpret_cast<volatile int *>(base_ptr + Cfg::SMEM_CTL_OFF + 8 * (2 * Cfg::STAGES + 5) + 4);
+    const uint32_t abort_addr = tmem_slot + 4;
     volatile uint32_t *tmem_slot_ptr =
         reinterpret_cast<volatile uint32_t *>(base_ptr + Cfg::SMEM_CTL_OFF + 8 * (2 * Cfg::STAGES + 5));
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = kPair ? cluster_ctarank() : 0u;   // 0 = leader
+    const bool leader = rank == 0;
+    const int cluster_id = static_cast<int>(blockIdx.x) / Cfg::CTA_GROUP;
+    const int num_clusters = static_cast<int>(gridDim.x) / Cfg::CTA_GROUP;
+
+    AbortFlag abort;
+    abort.local = reinterpret_cast<volatile int *>(tmem_slot_ptr + 1);
+    abort.pair = kPair;
+    abort.peer_addr = kPair ? mapa_shared(abort_addr, rank ^ 1u) : 0u;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < Cfg::STAGES; ++s) {
-            mbar_init(full_bar(s), 1);    // producer's arrive.expect_tx
-            mbar_init(empty_bar(s), 1);   // MMA thread's commit
+            mbar_init(full_bar(s), Cfg::CTA_GROUP);   // each CTA's producer: arrive.expect_tx
+            mbar_init(empty_bar(s), 1);               // the leader's MMA commit
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(tfull_bar(b), 1);   // MMA thread's commit after the tile's last MMA
-            mbar_init(tempty_bar(b), 4);  // one arrive per epilogue warp
+            mbar_init(tfull_bar(b), 1);                       // commit after a tile's last MMA
+            mbar_init(tempty_bar(b), 4 * Cfg::CTA_GROUP);     // one arrive per epilogue warp
         }
         mbar_init(drain_bar, 1);
-        *abort_flag = 0;
+        *abort.local = 0;
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -216,14 +258,21 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         prefetch_tensormap(&tmap_c);
     }
     if (warp == 1) {
-        tmem_alloc<1>(tmem_slot, Cfg::TMEM_COLS);
-        tmem_relinquish<1>();
+        tmem_alloc<Cfg::CTA_GROUP>(tmem_slot, Cfg::TMEM_COLS);
+        tmem_relinquish<Cfg::CTA_GROUP>();
     }
     tc_fence_before_sync();
     __syncthreads();
+    if constexpr (kPair) {
+        // Both CTAs' barriers are initialised and both TMEMs allocated before
+        // either CTA signals the other.
+        cluster_arrive();
+        cluster_wait();
+    }
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot_ptr;
     const uint64_t limit = p.timeout_cycles;
+    bool aborted = false;
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -232,23 +281,36 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             uint32_t ph = 0;
             uint32_t issued_mask = 0, issued_parity = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+            for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
                 int mb, nb;
                 tile_coords(t, p, mb, nb);
-                const int m0 = mb * Cfg::BM;
-                const int n0 = nb * Cfg::BN;
+                const int m0 = mb * Cfg::TILE_M + static_cast<int>(rank) * Cfg::BM;
+                const int n0 = nb * Cfg::BN + static_cast<int>(rank) * Cfg::BN_CTA;
                 for (int kb = 0; kb < p.num_k_blocks; ++kb) {
-                    if (!wait_phase(empty_bar(s), ph ^ 1u, abort_flag, limit, kSiteProducerEmpty)) {
+                    if (!wait_phase(empty_bar(s), ph ^ 1u, abort, limit, kSiteProducerEmpty)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(full_bar(s), Cfg::STAGE_TX_BYTES);
                     const int k0 = kb * Cfg::BK;
-                    tma_load_2d(sA + s * Cfg::A_STAGE_BYTES, &tmap_a, full_bar(s), k0, m0);
+                    const uint32_t a_dst = sA + s * Cfg::A_STAGE_BYTES;
+                    const uint32_t b_dst = sB + s * Cfg::B_STAGE_BYTES;
+                    if constexpr (!kPair) {
+                        mbar_arrive_expect_tx(full_bar(s), Cfg::STAGE_TX_BYTES);
+                        tma_load_2d(a_dst, &tmap_a, full_bar(s), k0, m0);
 #pragma unroll
-                    for (int j = 0; j < Cfg::B_BOXES; ++j)
-                        tma_load_2d(sB + s * Cfg::B_STAGE_BYTES + j * Cfg::B_BOX_BYTES, &tmap_b, full_bar(s),
-                                    n0 + j * Cfg::B_BOX_N, k0);
+                        for (int j = 0; j < Cfg::B_BOXES; ++j)
+                            tma_load_2d(b_dst + j * Cfg::B_BOX_BYTES, &tmap_b, full_bar(s), n0 + j * Cfg::B_BOX_N,
+                                        k0);
+                    } else {
+                        // Both CTAs' bytes land on the leader's barrier.
+                        const uint32_t fb = leader ? full_bar(s) : mapa_shared(full_bar(s), 0);
+                        if (leader) mbar_arrive_expect_tx(fb, Cfg::STAGE_TX_BYTES);
+                        else mbar_arrive_expect_tx_cluster(fb, Cfg::STAGE_TX_BYTES);
+                        tma_load_2d_pair(a_dst, &tmap_a, fb, k0, m0);
+#pragma unroll
+                        for (int j = 0; j < Cfg::B_BOXES; ++j)
+                            tma_load_2d_pair(b_dst + j * Cfg::B_BOX_BYTES, &tmap_b, fb, n0 + j * Cfg::B_BOX_N, k0);
+                    }
                     issued_mask |= 1u << s;
                     issued_parity = (issued_parity & ~(1u << s)) | (ph << s);
                     if (++s == Cfg::STAGES) {
@@ -258,31 +320,40 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 }
             }
             if (!ok) {
-                // Abort: let this thread's loads in flight land before the CTA exits.
-                for (int i = 0; i < Cfg::STAGES; ++i)
-                    if (issued_mask & (1u << i))
-                        wait_phase_drain(full_bar(i), (issued_parity >> i) & 1u, limit, kSiteDrainLoads);
+                aborted = true;
+                if (leader) {
+                    // Let the loads in flight land before the CTA exits.
+                    for (int i = 0; i < Cfg::STAGES; ++i)
+                        if (issued_mask & (1u << i))
+                            wait_phase_drain(full_bar(i), (issued_parity >> i) & 1u, limit, kSiteDrainLoads);
+                } else {
+                    // This CTA's loads complete on the leader's barrier, which it
+                    // cannot probe: give them a bounded time (~1e6 cycles) to land.
+                    const long long t0 = clock64();
+                    while (clock64() - t0 < 1000000) {
+                    }
+                }
             }
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // ------------------------------------------------------------ MMA issuer (leader CTA)
+        if (lane == 0 && leader) {
             int s = 0;
             uint32_t ph = 0;
             int it = 0;
             bool ok = true, issued_any = false;
-            for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++it) {
+            for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters, ++it) {
                 const int b = it & 1;
                 const uint32_t acc_ph = (it >> 1) & 1;
-                if (!wait_phase(tempty_bar(b), acc_ph ^ 1u, abort_flag, limit, kSiteMmaTmemEmpty)) {
+                if (!wait_phase(tempty_bar(b), acc_ph ^ 1u, abort, limit, kSiteMmaTmemEmpty)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + b * Cfg::ACC_COLS;
                 for (int kb = 0; kb < p.num_k_blocks; ++kb) {
-                    if (!wait_phase(full_bar(s), ph, abort_flag, limit, kSiteMmaFull)) {
+                    if (!wait_phase(full_bar(s), ph, abort, limit, kSiteMmaFull)) {
                         ok = false;
                         break;
                     }
@@ -299,9 +370,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         // is 16 * 128 B.
                         const uint64_t b_desc =
                             smem_desc_sw128(b0 + ks * (Cfg::UMMA_K * 128), Cfg::B_BOX_BYTES, 1024);
-                        mma_f16_ss<1>(d_tmem, a_desc, b_desc, Cfg::IDESC, (kb | ks) != 0 ? 1u : 0u);
+                        mma_f16_ss<Cfg::CTA_GROUP>(d_tmem, a_desc, b_desc, Cfg::IDESC, (kb | ks) != 0 ? 1u : 0u);
                     }
-                    mma_commit(empty_bar(s));   // frees the slot once these MMAs have read it
+                    // Frees the slot (in both CTAs) once these MMAs have read it.
+                    if constexpr (kPair) mma_commit_pair_mc(empty_bar(s), 0x3);
+                    else mma_commit(empty_bar(s));
                     issued_any = true;
                     if (++s == Cfg::STAGES) {
                         s = 0;
@@ -309,12 +382,18 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     }
                 }
                 if (!ok) break;
-                mma_commit(tfull_bar(b));   // accumulator b complete
+                // Accumulator b complete (in both CTAs' TMEM).
+                if constexpr (kPair) mma_commit_pair_mc(tfull_bar(b), 0x3);
+                else mma_commit(tfull_bar(b));
             }
-            if (!ok && issued_any) {
-                // Abort: wait for this thread's MMAs before the TMEM is freed.
-                mma_commit(drain_bar);
-                wait_phase_drain(drain_bar, 0, limit, kSiteDrainMma);
+            if (!ok) {
+                aborted = true;
+                if (issued_any) {
+                    // Wait for this thread's MMAs before the TMEM is freed.
+                    if constexpr (kPair) mma_commit_pair_mc(drain_bar, 0x1);
+                    else mma_commit(drain_bar);
+                    wait_phase_drain(drain_bar, 0, limit, kSiteDrainMma);
+                }
             }
         }
         __syncwarp();
@@ -324,19 +403,23 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         const int q = warp & 3;         // TMEM lane quarter this warp may access
         const uint32_t row_off = static_cast<uint32_t>(lane) * 128u;
         const uint32_t sw = static_cast<uint32_t>(lane & 7);
+        const uint32_t tempty_leader0 = kPair && !leader ? mapa_shared(tempty_bar(0), 0) : tempty_bar(0);
         int it = 0;
         uint32_t chunk = 0;
-        for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++it) {
+        for (int t = cluster_id; t < p.num_tiles; t += num_clusters, ++it) {
             int mb, nb;
             tile_coords(t, p, mb, nb);
             const int b = it & 1;
             const uint32_t acc_ph = (it >> 1) & 1;
             int ok = 1;
-            if (lane == 0) ok = wait_phase(tfull_bar(b), acc_ph, abort_flag, limit, kSiteEpilogueTmemFull) ? 1 : 0;
+            if (lane == 0) ok = wait_phase(tfull_bar(b), acc_ph, abort, limit, kSiteEpilogueTmemFull) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
+            if (!ok) {
+                aborted = true;
+                break;
+            }
             tc_fence_after_sync();
-            const int row0 = mb * Cfg::BM + q * 32;
+            const int row0 = mb * Cfg::TILE_M + static_cast<int>(rank) * Cfg::BM + q * 32;
 #pragma unroll 1
             for (int c = 0; c < Cfg::BN / Cfg::EPI_COLS; ++c) {
                 uint32_t r[64];
@@ -347,7 +430,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     // All TMEM reads of accumulator b by this warp are done.
                     tc_fence_before_sync();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(tempty_bar(b));
+                    if (lane == 0) {
+                        if (kPair && !leader) mbar_arrive_cluster(tempty_leader0 + 8u * b);
+                        else mbar_arrive(tempty_bar(b));
+                    }
                 }
                 const int col0 = nb * Cfg::BN + c * Cfg::EPI_COLS;
                 const bool in_range = row0 < p.M && col0 < p.N;
@@ -377,13 +463,20 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         }
         if (lane == 0) bulk_wait_group<0>();
     }
+    (void)aborted;
 
     tc_fence_before_sync();
     __syncthreads();
+    if constexpr (kPair) {
+        // No CTA of the pair exits while the other may still signal its
+        // barriers or read its shared memory.
+        cluster_arrive();
+        cluster_wait();
+    }
     if (warp == 1) {
         __syncwarp();
         tc_fence_after_sync();
-        tmem_dealloc<1>(tmem_base, Cfg::TMEM_COLS);
+        tmem_dealloc<Cfg::CTA_GROUP>(tmem_base, Cfg::TMEM_COLS);
     }
 }
 

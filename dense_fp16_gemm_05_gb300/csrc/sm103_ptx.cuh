@@ -37,7 +37,17 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar)
 // Arrive on a barrier of another CTA of the cluster (address from mapa).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster_addr)
 {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster_addr)
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster_addr)
+                 : "memory");
+}
+
+// Arrive with an expected transaction count on a barrier of another CTA of
+// the cluster (address from mapa).
+__device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t bar_cluster_addr, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cluster.b64 _, [%0], %1;" ::"r"(
+                     bar_cluster_addr),
+                 "r"(bytes)
                  : "memory");
 }
 
@@ -63,20 +73,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
-// Same probe with cluster-scope acquire (a barrier another CTA arrives on).
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
 // ---------------------------------------------------------------- cluster
 
 __device__ __forceinline__ uint32_t cluster_ctarank()
@@ -92,6 +88,12 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank)
     uint32_t out;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(addr), "r"(rank));
     return out;
+}
+
+// 32-bit store to shared memory of another CTA of the cluster.
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t addr, uint32_t v)
+{
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ void cluster_arrive()

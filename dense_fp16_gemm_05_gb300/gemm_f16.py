@@ -70,6 +70,9 @@ def lib() -> ctypes.CDLL:
     L.gemm_f16_config_name.restype = ctypes.c_char_p
     L.gemm_f16_auto_config.argtypes = [i64, i64, i64]
     L.gemm_f16_auto_config.restype = ci
+    pi = ctypes.POINTER(ctypes.c_int)
+    L.gemm_f16_launch_info.argtypes = [i64, i64, i64, ci, pi, pi, pi]
+    L.gemm_f16_launch_info.restype = ci
     _lib = L
     return L
 
@@ -184,3 +187,12 @@ def check(stream=None, device=None) -> int:
 
 def auto_config(M: int, N: int, K: int) -> int:
     return int(lib().gemm_f16_auto_config(M, N, K))
+
+
+def launch_info(M: int, N: int, K: int, config: int = 0) -> dict:
+    """Grid CTAs, cluster size and tile count that a call would launch with."""
+    g, c, t = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    st = lib().gemm_f16_launch_info(M, N, K, int(config), ctypes.byref(g), ctypes.byref(c), ctypes.byref(t))
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_f16_launch_info")
+    return {"grid_ctas": g.value, "cluster_size": c.value, "tiles": t.value}

@@ -103,6 +103,16 @@ const char *gemm_f16_config_name(int config);
 int gemm_f16_auto_config(int64_t M, int64_t N, int64_t K);
 
 /*
+ * gemm_f16_launch_info -- launch geometry gemm_f16_ex would use on the current
+ * device for this problem and configuration (0 = automatic): the persistent
+ * grid in CTAs (a multiple of the cluster size, at most one CTA per SM), the
+ * CTAs per cluster (2 for the CTA-pair configurations), and the number of
+ * output tiles.  Any output pointer may be NULL.  Launches nothing.
+ */
+int gemm_f16_launch_info(int64_t M, int64_t N, int64_t K, int config, int *grid_ctas, int *cluster_size,
+                         int *tiles);
+
+/*
  * gemm_f16_from_host -- end-to-end call on host buffers.
  *
  * Enqueues on `stream`: a copy of A_host into A_dev and of B_host into B_dev,
