@@ -33,12 +33,16 @@ struct ConfigInfo {
 using Cfg1x256 = GemmCfg<1, 256, 4>;
 using Cfg1x128 = GemmCfg<1, 128, 6>;
 using Cfg2x256 = GemmCfg<2, 256, 6>;
+using Cfg2x256d = GemmCfg<2, 256, 7, /*stage C in smem*/ false>;
+using Cfg2x512 = GemmCfg<2, 512, 4>;
 
 constexpr ConfigInfo kConfigs[] = {
     {"auto", 0, 0},
     {"1sm_128x256_s4", Cfg1x256::TILE_M, Cfg1x256::BN},
     {"1sm_128x128_s6", Cfg1x128::TILE_M, Cfg1x128::BN},
     {"2sm_256x256_s6", Cfg2x256::TILE_M, Cfg2x256::BN},
+    {"2sm_256x256_s7_direct", Cfg2x256d::TILE_M, Cfg2x256d::BN},
+    {"2sm_256x512_s4", Cfg2x512::TILE_M, Cfg2x512::BN},
 };
 constexpr int kNumConfigs = static_cast<int>(sizeof(kConfigs) / sizeof(kConfigs[0])) - 1;
 
@@ -195,10 +199,10 @@ int group_m_override()
     return v;
 }
 
-// Persistent grid size in tiles-at-once: one CTA (or CTA pair) per SM (pair
-// of SMs) that can be co-resident, never more than there are tiles.
+// Number of CTAs (or CTA pairs) of this configuration that can be resident
+// at once: one per SM (pair of SMs), as the occupancy API reports for clusters.
 template <class Cfg, bool kRelu>
-int64_t persistent_units(int64_t tiles, int sm_count)
+int64_t resident_slots(int sm_count)
 {
     int slots = sm_count / Cfg::CTA_GROUP;
     if (Cfg::CTA_GROUP > 1) {
@@ -225,16 +229,55 @@ int64_t persistent_units(int64_t tiles, int sm_count)
         else
             cudaGetLastError();
     }
-    return tiles < slots ? tiles : slots;
+    return slots;
+}
+
+// Persistent schedule: full waves of tiles, then the tiles of a partly filled
+// last wave split along N into 2^shift units while the split units still fit
+// in one wave (the tail then costs 1/2^shift of a tile time).
+struct Schedule {
+    int64_t tiles = 0, units = 0, split_start = 0, grid_units = 0;
+    int shift = 0;
+};
+
+template <class Cfg>
+Schedule make_schedule(int64_t M, int64_t N, int64_t slots)
+{
+    Schedule sc;
+    sc.tiles = ((M + Cfg::TILE_M - 1) / Cfg::TILE_M) * ((N + Cfg::BN - 1) / Cfg::BN);
+    sc.units = sc.tiles;
+    sc.split_start = sc.tiles;
+    if (slots <= 0) return sc;
+    const int64_t full = (sc.tiles / slots) * slots;
+    const int64_t rest = sc.tiles - full;
+    // Split shift with the shortest tail: ceil(rest * 2^s / slots) / 2^s tile
+    // times (ties go to the coarser split).
+    int shift = 0;
+    double best = 1e30;
+    for (int s = 0; rest > 0 && s <= Cfg::MAX_SPLIT_LOG2; ++s) {
+        const int64_t waves = ((rest << s) + slots - 1) / slots;
+        const double t = static_cast<double>(waves) / static_cast<double>(1 << s);
+        if (t < best - 1e-9) {
+            best = t;
+            shift = s;
+        }
+    }
+    if (shift > 0) {
+        sc.shift = shift;
+        sc.split_start = full;
+        sc.units = full + (rest << shift);
+    }
+    sc.grid_units = sc.units < slots ? sc.units : slots;
+    return sc;
 }
 
 template <class Cfg>
 int fill_launch_info(int64_t M, int64_t N, int sm_count, int *grid_ctas, int *cluster_size, int *tiles)
 {
-    const int64_t t = ((M + Cfg::TILE_M - 1) / Cfg::TILE_M) * ((N + Cfg::BN - 1) / Cfg::BN);
-    if (tiles) *tiles = static_cast<int>(t < INT32_MAX ? t : INT32_MAX);
+    const Schedule sc = make_schedule<Cfg>(M, N, resident_slots<Cfg, true>(sm_count));
+    if (tiles) *tiles = static_cast<int>(sc.tiles < INT32_MAX ? sc.tiles : INT32_MAX);
     if (cluster_size) *cluster_size = Cfg::CTA_GROUP;
-    if (grid_ctas) *grid_ctas = static_cast<int>(persistent_units<Cfg, true>(t, sm_count) * Cfg::CTA_GROUP);
+    if (grid_ctas) *grid_ctas = static_cast<int>(sc.grid_units * Cfg::CTA_GROUP);
     return GEMM_OK;
 }
 
@@ -255,11 +298,17 @@ int launch(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t 
     p.num_m_blocks = static_cast<int32_t>((M + Cfg::TILE_M - 1) / Cfg::TILE_M);
     p.num_n_blocks = static_cast<int32_t>((N + Cfg::BN - 1) / Cfg::BN);
     p.num_k_blocks = static_cast<int32_t>((K + Cfg::BK - 1) / Cfg::BK);
-    const int64_t tiles = static_cast<int64_t>(p.num_m_blocks) * p.num_n_blocks;
-    if (tiles > INT32_MAX / 2) return GEMM_ERR_INVALID_ARG;
-    p.num_tiles = static_cast<int32_t>(tiles);
+    const int64_t slots = resident_slots<Cfg, kRelu>(sm_count);
+    if (slots <= 0) return GEMM_ERR_LAUNCH;
+    const Schedule sc = make_schedule<Cfg>(M, N, slots);
+    if (sc.units > INT32_MAX / 2) return GEMM_ERR_INVALID_ARG;
+    p.num_tiles = static_cast<int32_t>(sc.tiles);
+    p.num_units = static_cast<int32_t>(sc.units);
+    p.split_start = static_cast<int32_t>(sc.split_start);
+    p.split_log2 = sc.shift;
     p.group_m = group_m_override() ? group_m_override() : (Cfg::CTA_GROUP == 2 ? 8 : 16);
     p.timeout_cycles = timeout_cycles_for(K);
+    p.C = static_cast<__half *>(C);
 
     auto kern = gemm_f16_relu_sm103a<Cfg, kRelu>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess) {
@@ -278,8 +327,7 @@ int launch(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t 
     lc.attrs = attrs;
     lc.numAttrs = 1;
 
-    const int64_t units = persistent_units<Cfg, kRelu>(tiles, sm_count);
-    lc.gridDim = dim3(static_cast<unsigned>(units * Cfg::CTA_GROUP), 1, 1);
+    lc.gridDim = dim3(static_cast<unsigned>(sc.grid_units * Cfg::CTA_GROUP), 1, 1);
     if (cudaLaunchKernelEx(&lc, kern, ta, tb, tc, p) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;
@@ -336,6 +384,8 @@ extern "C" int gemm_f16_ex(const void *A, const void *B, void *C, int64_t M, int
         case 1: return launch_cfg<Cfg1x256>(A, B, C, M, N, K, relu, dev.sm_count, s);
         case 2: return launch_cfg<Cfg1x128>(A, B, C, M, N, K, relu, dev.sm_count, s);
         case 3: return launch_cfg<Cfg2x256>(A, B, C, M, N, K, relu, dev.sm_count, s);
+        case 4: return launch_cfg<Cfg2x256d>(A, B, C, M, N, K, relu, dev.sm_count, s);
+        case 5: return launch_cfg<Cfg2x512>(A, B, C, M, N, K, relu, dev.sm_count, s);
         default: return GEMM_ERR_INVALID_ARG;
     }
 }
@@ -376,6 +426,8 @@ extern "C" int gemm_f16_launch_info(int64_t M, int64_t N, int64_t K, int config,
         case 1: return fill_launch_info<Cfg1x256>(M, N, dev.sm_count, grid_ctas, cluster_size, tiles);
         case 2: return fill_launch_info<Cfg1x128>(M, N, dev.sm_count, grid_ctas, cluster_size, tiles);
         case 3: return fill_launch_info<Cfg2x256>(M, N, dev.sm_count, grid_ctas, cluster_size, tiles);
+        case 4: return fill_launch_info<Cfg2x256d>(M, N, dev.sm_count, grid_ctas, cluster_size, tiles);
+        case 5: return fill_launch_info<Cfg2x512>(M, N, dev.sm_count, grid_ctas, cluster_size, tiles);
         default: return GEMM_ERR_INVALID_ARG;
     }
 }

@@ -51,6 +51,9 @@
 namespace gemm_sm103 {
 
 // Problem description passed by value to the kernel.
+// Work units: tiles in rasterised order, except that the tiles of a last,
+// partly filled wave may be split along N into 2^split_log2 narrower units
+// (so that the tail costs a fraction of a tile time instead of a whole one).
 struct GemmParams {
     int32_t M, N, K;
     int32_t num_m_blocks;   // ceil(M / tile rows)
@@ -58,7 +61,11 @@ struct GemmParams {
     int32_t num_k_blocks;   // ceil(K / BK)
     int32_t num_tiles;      // num_m_blocks * num_n_blocks
     int32_t group_m;        // rasterisation panel height, in tiles
+    int32_t num_units;      // split_start + (num_tiles - split_start) << split_log2
+    int32_t split_start;    // first split tile (== num_tiles: no split)
+    int32_t split_log2;     // each tile from split_start on is 2^split_log2 units
     uint64_t timeout_cycles;
+    __half *C;              // output base (used by the direct-store epilogue)
 };
 
 // Where a bounded wait expired (bits 0-7 of the status word).
@@ -71,16 +78,24 @@ enum WaitSite : uint32_t {
     kSiteDrainMma = 6,
 };
 
+constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
+
 // Tile shapes and shared-memory budget of one kernel configuration.
 //   kCtaGroup  1: one CTA per tile; 2: a CTA pair per tile (cta_group::2)
-//   kBN        columns of C per tile (the MMA's N)
+//   kBN        columns of C per tile; tiles wider than 256 (the largest MMA N)
+//              issue BN/256 MMAs per K step into adjacent TMEM columns
 //   kStages    depth of the shared-memory K ring
-template <int kCtaGroup, int kBN, int kStages>
+//   kEpiSmem   true: stage C tiles in shared memory and store them with TMA;
+//              false: store C from registers (frees shared memory for a deeper ring)
+template <int kCtaGroup, int kBN, int kStages, bool kEpiSmem = true>
 struct GemmCfg {
     static constexpr int CTA_GROUP = kCtaGroup;
+    static constexpr bool EPI_SMEM = kEpiSmem;
     static constexpr int BM = 128;                    // rows of C per CTA = TMEM lanes
     static constexpr int TILE_M = BM * CTA_GROUP;     // rows of C per tile (the MMA's M)
     static constexpr int BN = kBN;
+    static constexpr int UMMA_N = BN < 256 ? BN : 256;   // N of one MMA instruction
+    static constexpr int N_MMAS = BN / UMMA_N;        // MMAs per K step
     static constexpr int BN_CTA = BN / CTA_GROUP;     // columns of B each CTA loads
     static constexpr int BK = 64;                     // 64 fp16 = 128 bytes = one swizzle row
     static constexpr int UMMA_K = 16;                 // K of one tcgen05.mma.kind::f16
@@ -93,19 +108,23 @@ struct GemmCfg {
     static constexpr int B_STAGE_BYTES = B_BOXES * B_BOX_BYTES;
     static constexpr int STAGE_TX_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;   // loaded per CTA per stage
     static constexpr int ACC_COLS = BN;               // fp32 TMEM columns of one accumulator
-    static constexpr int TMEM_COLS = 2 * ACC_COLS;    // two accumulators
+    static constexpr int ACC_STAGES = 2 * BN <= 512 ? 2 : 1;   // double-buffer when TMEM allows
+    static constexpr int TMEM_COLS = ACC_STAGES * ACC_COLS;
     static constexpr int EPI_COLS = 64;               // columns per epilogue chunk (128 bytes of fp16)
     static constexpr int C_BUF_BYTES = 32 * EPI_COLS * 2;
     static constexpr int SMEM_A_OFF = 0;
     static constexpr int SMEM_B_OFF = SMEM_A_OFF + STAGES * A_STAGE_BYTES;
     static constexpr int SMEM_C_OFF = SMEM_B_OFF + STAGES * B_STAGE_BYTES;
-    static constexpr int SMEM_CTL_OFF = SMEM_C_OFF + 4 * 2 * C_BUF_BYTES;
+    static constexpr int SMEM_CTL_OFF = SMEM_C_OFF + (kEpiSmem ? 4 * 2 * C_BUF_BYTES : 0);
+    // Narrowest split unit: one B box per CTA per MMA.
+    static constexpr int MAX_SPLIT_LOG2 = ilog2(BN / (B_BOX_N * CTA_GROUP));
     static constexpr int SMEM_CTL_BYTES = 256;
     static constexpr int SMEM_BYTES = 1024 /* alignment slack */ + SMEM_CTL_OFF + SMEM_CTL_BYTES;
-    static constexpr uint32_t IDESC = idesc_f16_f32(TILE_M, BN, /*A MN-major*/ false, /*B MN-major*/ true);
+    static constexpr uint32_t IDESC = idesc_f16_f32(TILE_M, UMMA_N, /*A MN-major*/ false, /*B MN-major*/ true);
 
     static_assert(CTA_GROUP == 1 || CTA_GROUP == 2, "one CTA or a CTA pair");
-    static_assert(BN_CTA % 64 == 0 && BN >= 64 && BN <= 256, "UMMA N: multiple of 16 up to 256");
+    static_assert(BN % (B_BOX_N * CTA_GROUP) == 0 && BN <= 512, "whole B boxes per CTA; at most 512 TMEM columns");
+    static_assert(UMMA_N % 16 == 0 && UMMA_N <= 256, "UMMA N: multiple of 16 up to 256");
     static_assert(TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation is a power of 2");
     static_assert((2 * STAGES + 5) * 8 + 8 <= SMEM_CTL_BYTES, "control block");
     static_assert(SMEM_BYTES <= 232448, "shared memory per block on sm_103");
@@ -137,12 +156,17 @@ struct AbortFlag {
 // default (CTA-scope) form also for barriers another CTA arrives on: TMA bytes
 // become visible through the barrier's transaction count, and TMEM hand-offs
 // are ordered by the tcgen05 fences around the waits.
+// kSleepNs > 0 adds a short sleep to each slow-path probe: for waits off the
+// critical path (the epilogue waiting for a whole tile), it spends fewer issue
+// slots, and so less power, on polling.
+template <int kSleepNs = 0>
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const AbortFlag &abort, uint64_t limit,
                                            uint32_t site)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
+        if constexpr (kSleepNs > 0) __nanosleep(kSleepNs);
         if (mbar_try_wait(bar, parity)) return true;
         if (abort.raised()) return false;
         if (static_cast<uint64_t>(clock64() - t0) > limit) {
@@ -178,6 +202,30 @@ __device__ __forceinline__ void tile_coords(int t, const GemmParams &p, int &mb,
     const int r = t - g * per_group;
     mb = first_m + r % rows;
     nb = r / rows;
+}
+
+// Work unit u -> tile row block mb, first output column col0 of the unit, and
+// the split shift (the unit is BN >> shift columns wide).
+template <int kBN>
+__device__ __forceinline__ void unit_coords(int u, const GemmParams &p, int &mb, int &col0, int &shift)
+{
+    int t = u, sub = 0;
+    shift = 0;
+    if (u >= p.split_start) {
+        shift = p.split_log2;
+        const int d = u - p.split_start;
+        t = p.split_start + (d >> shift);
+        sub = d & ((1 << shift) - 1);
+    }
+    int nb;
+    tile_coords(t, p, mb, nb);
+    col0 = nb * kBN + sub * (kBN >> shift);
+}
+
+__device__ __forceinline__ void st_global_v4(void *ptr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(ptr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
@@ -281,11 +329,19 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             uint32_t ph = 0;
             uint32_t issued_mask = 0, issued_parity = 0;
             bool ok = true;
-            for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
-                int mb, nb;
-                tile_coords(t, p, mb, nb);
+            for (int u = cluster_id; ok && u < p.num_units; u += num_clusters) {
+                int mb, col0, shift;
+                unit_coords<Cfg::BN>(u, p, mb, col0, shift);
                 const int m0 = mb * Cfg::TILE_M + static_cast<int>(rank) * Cfg::BM;
-                const int n0 = nb * Cfg::BN + static_cast<int>(rank) * Cfg::BN_CTA;
+                // Unit width W = BN >> shift, issued as W / umma_n MMAs of N = umma_n.
+                // For MMA h, this CTA supplies umma_n / CTA_GROUP columns (bpm boxes),
+                // starting at tile column h * umma_n + rank * umma_n / CTA_GROUP.
+                const int width = Cfg::BN >> shift;
+                const int umma_n = width < Cfg::UMMA_N ? width : Cfg::UMMA_N;
+                const int bpm = umma_n / (Cfg::CTA_GROUP * Cfg::B_BOX_N);
+                const int boxes = Cfg::B_BOXES >> shift;
+                const int n_cta = col0 + static_cast<int>(rank) * (umma_n / Cfg::CTA_GROUP);
+                const uint32_t tx = Cfg::A_STAGE_BYTES + boxes * Cfg::B_BOX_BYTES;
                 for (int kb = 0; kb < p.num_k_blocks; ++kb) {
                     if (!wait_phase(empty_bar(s), ph ^ 1u, abort, limit, kSiteProducerEmpty)) {
                         ok = false;
@@ -295,21 +351,20 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     const uint32_t a_dst = sA + s * Cfg::A_STAGE_BYTES;
                     const uint32_t b_dst = sB + s * Cfg::B_STAGE_BYTES;
                     if constexpr (!kPair) {
-                        mbar_arrive_expect_tx(full_bar(s), Cfg::STAGE_TX_BYTES);
+                        mbar_arrive_expect_tx(full_bar(s), tx);
                         tma_load_2d(a_dst, &tmap_a, full_bar(s), k0, m0);
-#pragma unroll
-                        for (int j = 0; j < Cfg::B_BOXES; ++j)
-                            tma_load_2d(b_dst + j * Cfg::B_BOX_BYTES, &tmap_b, full_bar(s), n0 + j * Cfg::B_BOX_N,
-                                        k0);
+                        for (int j = 0; j < boxes; ++j)
+                            tma_load_2d(b_dst + j * Cfg::B_BOX_BYTES, &tmap_b, full_bar(s),
+                                        n_cta + (j / bpm) * umma_n + (j % bpm) * Cfg::B_BOX_N, k0);
                     } else {
                         // Both CTAs' bytes land on the leader's barrier.
                         const uint32_t fb = leader ? full_bar(s) : mapa_shared(full_bar(s), 0);
-                        if (leader) mbar_arrive_expect_tx(fb, Cfg::STAGE_TX_BYTES);
-                        else mbar_arrive_expect_tx_cluster(fb, Cfg::STAGE_TX_BYTES);
+                        if (leader) mbar_arrive_expect_tx(fb, tx);
+                        else mbar_arrive_expect_tx_cluster(fb, tx);
                         tma_load_2d_pair(a_dst, &tmap_a, fb, k0, m0);
-#pragma unroll
-                        for (int j = 0; j < Cfg::B_BOXES; ++j)
-                            tma_load_2d_pair(b_dst + j * Cfg::B_BOX_BYTES, &tmap_b, fb, n0 + j * Cfg::B_BOX_N, k0);
+                        for (int j = 0; j < boxes; ++j)
+                            tma_load_2d_pair(b_dst + j * Cfg::B_BOX_BYTES, &tmap_b, fb,
+                                             n_cta + (j / bpm) * umma_n + (j % bpm) * Cfg::B_BOX_N, k0);
                     }
                     issued_mask |= 1u << s;
                     issued_parity = (issued_parity & ~(1u << s)) | (ph << s);
@@ -343,9 +398,18 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             uint32_t ph = 0;
             int it = 0;
             bool ok = true, issued_any = false;
-            for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters, ++it) {
-                const int b = it & 1;
-                const uint32_t acc_ph = (it >> 1) & 1;
+            for (int u = cluster_id; ok && u < p.num_units; u += num_clusters, ++it) {
+                const int b = it % Cfg::ACC_STAGES;
+                const uint32_t acc_ph = (it / Cfg::ACC_STAGES) & 1;
+                const int shift = u >= p.split_start ? p.split_log2 : 0;
+                const int width = Cfg::BN >> shift;
+                const int umma_n = width < Cfg::UMMA_N ? width : Cfg::UMMA_N;
+                const int n_mmas = width / umma_n;
+                const uint32_t bpm_bytes = static_cast<uint32_t>(umma_n / (Cfg::CTA_GROUP * Cfg::B_BOX_N)) *
+                                           Cfg::B_BOX_BYTES;
+                // The MMA's N field (bits 17-22, N >> 3) for this unit's width.
+                const uint32_t idesc =
+                    (Cfg::IDESC & ~(0x3Fu << 17)) | (static_cast<uint32_t>(umma_n >> 3) << 17);
                 if (!wait_phase(tempty_bar(b), acc_ph ^ 1u, abort, limit, kSiteMmaTmemEmpty)) {
                     ok = false;
                     break;
@@ -365,12 +429,17 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         // A: K-major, 8-row groups 1024 B apart; a K step of 16
                         // elements is 32 B inside the 128-byte swizzle row.
                         const uint64_t a_desc = smem_desc_sw128(a0 + ks * (Cfg::UMMA_K * 2), 16, 1024);
-                        // B: N-major; 64-column boxes B_BOX_BYTES apart (LBO),
-                        // 8-row K groups 1024 B apart (SBO); a K step of 16 rows
-                        // is 16 * 128 B.
-                        const uint64_t b_desc =
-                            smem_desc_sw128(b0 + ks * (Cfg::UMMA_K * 128), Cfg::B_BOX_BYTES, 1024);
-                        mma_f16_ss<Cfg::CTA_GROUP>(d_tmem, a_desc, b_desc, Cfg::IDESC, (kb | ks) != 0 ? 1u : 0u);
+#pragma unroll
+                        for (int h = 0; h < Cfg::N_MMAS; ++h) {
+                            if (h >= n_mmas) break;
+                            // B: N-major; 64-column boxes B_BOX_BYTES apart (LBO),
+                            // 8-row K groups 1024 B apart (SBO); a K step of 16 rows
+                            // is 16 * 128 B; MMA h starts at its own boxes.
+                            const uint64_t b_desc = smem_desc_sw128(
+                                b0 + h * bpm_bytes + ks * (Cfg::UMMA_K * 128), Cfg::B_BOX_BYTES, 1024);
+                            mma_f16_ss<Cfg::CTA_GROUP>(d_tmem + h * umma_n, a_desc, b_desc, idesc,
+                                                       (kb | ks) != 0 ? 1u : 0u);
+                        }
                     }
                     // Frees the slot (in both CTAs) once these MMAs have read it.
                     if constexpr (kPair) mma_commit_pair_mc(empty_bar(s), 0x3);
@@ -406,13 +475,15 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         const uint32_t tempty_leader0 = kPair && !leader ? mapa_shared(tempty_bar(0), 0) : tempty_bar(0);
         int it = 0;
         uint32_t chunk = 0;
-        for (int t = cluster_id; t < p.num_tiles; t += num_clusters, ++it) {
-            int mb, nb;
-            tile_coords(t, p, mb, nb);
-            const int b = it & 1;
-            const uint32_t acc_ph = (it >> 1) & 1;
+        for (int u = cluster_id; u < p.num_units; u += num_clusters, ++it) {
+            int mb, col0_unit, shift;
+            unit_coords<Cfg::BN>(u, p, mb, col0_unit, shift);
+            const int chunks = (Cfg::BN >> shift) / Cfg::EPI_COLS;
+            const int b = it % Cfg::ACC_STAGES;
+            const uint32_t acc_ph = (it / Cfg::ACC_STAGES) & 1;
             int ok = 1;
-            if (lane == 0) ok = wait_phase(tfull_bar(b), acc_ph, abort, limit, kSiteEpilogueTmemFull) ? 1 : 0;
+            if (lane == 0)
+                ok = wait_phase<256>(tfull_bar(b), acc_ph, abort, limit, kSiteEpilogueTmemFull) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) {
                 aborted = true;
@@ -421,12 +492,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             tc_fence_after_sync();
             const int row0 = mb * Cfg::TILE_M + static_cast<int>(rank) * Cfg::BM + q * 32;
 #pragma unroll 1
-            for (int c = 0; c < Cfg::BN / Cfg::EPI_COLS; ++c) {
+            for (int c = 0; c < chunks; ++c) {
                 uint32_t r[64];
                 tmem_load_32x32b_x64(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * Cfg::ACC_COLS +
                                          c * Cfg::EPI_COLS,
                                      r);
-                if (c == Cfg::BN / Cfg::EPI_COLS - 1) {
+                if (c == chunks - 1) {
                     // All TMEM reads of accumulator b by this warp are done.
                     tc_fence_before_sync();
                     __syncwarp();
@@ -435,35 +506,55 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         else mbar_arrive(tempty_bar(b));
                     }
                 }
-                const int col0 = nb * Cfg::BN + c * Cfg::EPI_COLS;
-                const bool in_range = row0 < p.M && col0 < p.N;
-                const uint32_t cbuf = sC + (ew * 2 + (chunk & 1u)) * Cfg::C_BUF_BYTES;
-                ++chunk;
-                if (lane == 0) bulk_wait_group_read<1>();   // the store that used cbuf has read it
-                __syncwarp();
+                const int col0 = col0_unit + c * Cfg::EPI_COLS;
+                if constexpr (Cfg::EPI_SMEM) {
+                    const bool in_range = row0 < p.M && col0 < p.N;
+                    const uint32_t cbuf = sC + (ew * 2 + (chunk & 1u)) * Cfg::C_BUF_BYTES;
+                    ++chunk;
+                    if (lane == 0) bulk_wait_group_read<1>();   // the store that used cbuf has read it
+                    __syncwarp();
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const uint32_t w0 = pack_f16x2<kRelu>(r[8 * j + 0], r[8 * j + 1]);
-                    const uint32_t w1 = pack_f16x2<kRelu>(r[8 * j + 2], r[8 * j + 3]);
-                    const uint32_t w2 = pack_f16x2<kRelu>(r[8 * j + 4], r[8 * j + 5]);
-                    const uint32_t w3 = pack_f16x2<kRelu>(r[8 * j + 6], r[8 * j + 7]);
-                    // 16-byte chunk j of this row goes to chunk j ^ (row % 8): the
-                    // layout a SWIZZLE_128B tensor-map store expects.
-                    st_shared_v4(cbuf + row_off + ((static_cast<uint32_t>(j) ^ sw) << 4), w0, w1, w2, w3);
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    if (in_range) tma_store_2d(&tmap_c, cbuf, col0, row0);
-                    // One group per chunk, empty or not, so that "at most one group
-                    // pending" above always means the other buffer's store.
-                    bulk_commit_group();
+                    for (int j = 0; j < 8; ++j) {
+                        const uint32_t w0 = pack_f16x2<kRelu>(r[8 * j + 0], r[8 * j + 1]);
+                        const uint32_t w1 = pack_f16x2<kRelu>(r[8 * j + 2], r[8 * j + 3]);
+                        const uint32_t w2 = pack_f16x2<kRelu>(r[8 * j + 4], r[8 * j + 5]);
+                        const uint32_t w3 = pack_f16x2<kRelu>(r[8 * j + 6], r[8 * j + 7]);
+                        // 16-byte chunk j of this row goes to chunk j ^ (row % 8): the
+                        // layout a SWIZZLE_128B tensor-map store expects.
+                        st_shared_v4(cbuf + row_off + ((static_cast<uint32_t>(j) ^ sw) << 4), w0, w1, w2, w3);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (in_range) tma_store_2d(&tmap_c, cbuf, col0, row0);
+                        // One group per chunk, empty or not, so that "at most one group
+                        // pending" above always means the other buffer's store.
+                        bulk_commit_group();
+                    }
+                } else {
+                    // Each thread owns one row: 64 fp16 = 128 contiguous bytes.  N is
+                    // a multiple of 8, so every 16-byte piece is wholly in or out.
+                    const int row = row0 + lane;
+                    if (row < p.M) {
+                        __half *crow = p.C + static_cast<int64_t>(row) * p.N + col0;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            if (col0 + 8 * j < p.N)
+                                st_global_v4(crow + 8 * j, pack_f16x2<kRelu>(r[8 * j + 0], r[8 * j + 1]),
+                                             pack_f16x2<kRelu>(r[8 * j + 2], r[8 * j + 3]),
+                                             pack_f16x2<kRelu>(r[8 * j + 4], r[8 * j + 5]),
+                                             pack_f16x2<kRelu>(r[8 * j + 6], r[8 * j + 7]));
+                        }
+                    }
                 }
             }
         }
-        if (lane == 0) bulk_wait_group<0>();
+        if constexpr (Cfg::EPI_SMEM) {
+            if (lane == 0) bulk_wait_group<0>();
+        }
     }
     (void)aborted;
+    (void)sC;
 
     tc_fence_before_sync();
     __syncthreads();
