@@ -12,6 +12,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
+#include <atomic>
 #include <mutex>
 
 #include "gemm_f16.h"
@@ -35,14 +36,16 @@ using Cfg1x128 = GemmCfg<1, 128, 6>;
 using Cfg2x256 = GemmCfg<2, 256, 6>;
 using Cfg2x256d = GemmCfg<2, 256, 7, /*stage C in smem*/ false>;
 using Cfg2x512 = GemmCfg<2, 512, 4>;
+using Cfg4x256mc = GemmCfg<2, 256, 6, /*stage C in smem*/ true, /*pairs sharing B*/ 2>;
 
 constexpr ConfigInfo kConfigs[] = {
     {"auto", 0, 0},
-    {"1sm_128x256_s4", Cfg1x256::TILE_M, Cfg1x256::BN},
-    {"1sm_128x128_s6", Cfg1x128::TILE_M, Cfg1x128::BN},
-    {"2sm_256x256_s6", Cfg2x256::TILE_M, Cfg2x256::BN},
-    {"2sm_256x256_s7_direct", Cfg2x256d::TILE_M, Cfg2x256d::BN},
-    {"2sm_256x512_s4", Cfg2x512::TILE_M, Cfg2x512::BN},
+    {"1sm_128x256_s4", Cfg1x256::SUPER_M, Cfg1x256::BN},
+    {"1sm_128x128_s6", Cfg1x128::SUPER_M, Cfg1x128::BN},
+    {"2sm_256x256_s6", Cfg2x256::SUPER_M, Cfg2x256::BN},
+    {"2sm_256x256_s7_direct", Cfg2x256d::SUPER_M, Cfg2x256d::BN},
+    {"2sm_256x512_s4", Cfg2x512::SUPER_M, Cfg2x512::BN},
+    {"4sm_512x256_mc_s6", Cfg4x256mc::SUPER_M, Cfg4x256mc::BN},
 };
 constexpr int kNumConfigs = static_cast<int>(sizeof(kConfigs) / sizeof(kConfigs[0])) - 1;
 
@@ -79,40 +82,47 @@ const DriverFns &driver()
 constexpr int kMaxDevices = 64;
 
 struct DeviceInfo {
-    int checked = 0;        // 1 once filled
+    int device = 0;
     int supported = 0;      // compute capability 10.3
     int sm_count = 0;
 };
 
-DeviceInfo g_devices[kMaxDevices];
-std::mutex g_device_mutex;
+// Filled once per device; read without locking afterwards.
+std::atomic<int> g_device_state[kMaxDevices];   // 0 unknown, 1 supported, 2 unsupported
+int g_device_sms[kMaxDevices];
 
 int current_device_info(DeviceInfo *out)
 {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
     if (dev < 0 || dev >= kMaxDevices) return GEMM_ERR_UNSUPPORTED_DEVICE;
-    std::lock_guard<std::mutex> lock(g_device_mutex);
-    DeviceInfo &d = g_devices[dev];
-    if (!d.checked) {
+    int state = g_device_state[dev].load(std::memory_order_acquire);
+    if (state == 0) {
         int major = 0, minor = 0, sms = 0;
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
             return GEMM_ERR_CUDA;
-        d.supported = (major == 10 && minor == 3) ? 1 : 0;
-        d.sm_count = sms;
-        d.checked = 1;
+        }
+        g_device_sms[dev] = sms;
+        state = (major == 10 && minor == 3) ? 1 : 2;
+        g_device_state[dev].store(state, std::memory_order_release);
     }
-    *out = d;
-    return d.supported ? GEMM_OK : GEMM_ERR_UNSUPPORTED_DEVICE;
+    out->device = dev;
+    out->sm_count = g_device_sms[dev];
+    out->supported = state == 1;
+    return state == 1 ? GEMM_OK : GEMM_ERR_UNSUPPORTED_DEVICE;
 }
 
 // ---------------------------------------------------------------- argument checks
 
 // A device buffer of `bytes` bytes starting at p: device (or managed) memory of
 // the current device, entirely inside one allocation.
-int check_device_buffer(const void *p, uint64_t bytes)
+int check_device_buffer(const void *p, uint64_t bytes, int dev)
 {
     if (p == nullptr) return GEMM_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(p) & 15u) != 0) return GEMM_ERR_ALIGNMENT;
@@ -122,8 +132,6 @@ int check_device_buffer(const void *p, uint64_t bytes)
         return GEMM_ERR_INVALID_ARG;
     }
     if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged) return GEMM_ERR_INVALID_ARG;
-    int dev = 0;
-    cudaGetDevice(&dev);
     if (attr.type == cudaMemoryTypeDevice && attr.device != dev) return GEMM_ERR_INVALID_ARG;
     const DriverFns &fns = driver();
     if (!fns.ok) return GEMM_ERR_CUDA;
@@ -180,9 +188,15 @@ uint64_t timeout_cycles_for(int64_t K)
 int pick_config(int64_t M, int64_t N, int64_t K, int sm_count)
 {
     (void)K;
+    const int64_t pairs = sm_count / 2;
+    const int64_t tiles_256x512 = ((M + 255) / 256) * ((N + 511) / 512);
+    // Many 256x512 tiles (about 13 or more waves): the wide pair tile needs the
+    // fewest operand bytes per flop; its single accumulator costs little
+    // when tiles are long and the tail is a small share.
+    if (tiles_256x512 >= 13 * pairs) return 5;
     const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
     // Enough 256x256 tiles to keep every SM pair busy: the CTA-pair kernel.
-    if (pair_tiles >= sm_count / 2) return 3;
+    if (pair_tiles >= pairs) return 3;
     const int64_t tiles256 = ((M + 127) / 128) * ((N + 255) / 256);
     if (tiles256 >= sm_count / 2) return 1;
     // Few tiles: narrower tiles put more SMs to work.
@@ -199,38 +213,53 @@ int group_m_override()
     return v;
 }
 
-// Number of CTAs (or CTA pairs) of this configuration that can be resident
-// at once: one per SM (pair of SMs), as the occupancy API reports for clusters.
+// Per device and kernel instance, prepared once: the dynamic shared-memory
+// attribute is set, and the number of CTAs (or CTA clusters) of this
+// configuration that can be resident at once -- one per SM, or per group of
+// SMs as the occupancy API reports for clusters -- is cached.  forget()
+// drops the entry (after a failed launch, e.g. once the context was reset).
 template <class Cfg, bool kRelu>
-int64_t resident_slots(int sm_count)
-{
-    int slots = sm_count / Cfg::CTA_GROUP;
-    if (Cfg::CTA_GROUP > 1) {
+struct Prepared {
+    static std::atomic<int> slots[kMaxDevices];   // 0: not prepared
+
+    static int64_t get(int dev, int sm_count)
+    {
+        int v = slots[dev].load(std::memory_order_acquire);
+        if (v > 0) return v;
         auto kern = gemm_f16_relu_sm103a<Cfg, kRelu>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) !=
             cudaSuccess) {
             cudaGetLastError();
             return 0;
         }
-        cudaLaunchConfig_t lc{};
-        lc.blockDim = dim3(Cfg::THREADS, 1, 1);
-        lc.dynamicSmemBytes = Cfg::SMEM_BYTES;
-        lc.gridDim = dim3(Cfg::CTA_GROUP * slots, 1, 1);
-        cudaLaunchAttribute attrs[1];
-        attrs[0].id = cudaLaunchAttributeClusterDimension;
-        attrs[0].val.clusterDim.x = Cfg::CTA_GROUP;
-        attrs[0].val.clusterDim.y = 1;
-        attrs[0].val.clusterDim.z = 1;
-        lc.attrs = attrs;
-        lc.numAttrs = 1;
-        int clusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&clusters, kern, &lc) == cudaSuccess && clusters > 0)
-            slots = clusters < slots ? clusters : slots;
-        else
-            cudaGetLastError();
+        v = sm_count / Cfg::CLUSTER;
+        if (Cfg::CLUSTER > 1) {
+            cudaLaunchConfig_t lc{};
+            lc.blockDim = dim3(Cfg::THREADS, 1, 1);
+            lc.dynamicSmemBytes = Cfg::SMEM_BYTES;
+            lc.gridDim = dim3(Cfg::CLUSTER * v, 1, 1);
+            cudaLaunchAttribute attrs[1];
+            attrs[0].id = cudaLaunchAttributeClusterDimension;
+            attrs[0].val.clusterDim.x = Cfg::CLUSTER;
+            attrs[0].val.clusterDim.y = 1;
+            attrs[0].val.clusterDim.z = 1;
+            lc.attrs = attrs;
+            lc.numAttrs = 1;
+            int clusters = 0;
+            if (cudaOccupancyMaxActiveClusters(&clusters, kern, &lc) == cudaSuccess && clusters > 0)
+                v = clusters < v ? clusters : v;
+            else
+                cudaGetLastError();
+        }
+        if (v > 0) slots[dev].store(v, std::memory_order_release);
+        return v;
     }
-    return slots;
-}
+
+    static void forget(int dev) { slots[dev].store(0, std::memory_order_release); }
+};
+
+template <class Cfg, bool kRelu>
+std::atomic<int> Prepared<Cfg, kRelu>::slots[kMaxDevices];
 
 // Persistent schedule: full waves of tiles, then the tiles of a partly filled
 // last wave split along N into 2^shift units while the split units still fit
@@ -244,7 +273,7 @@ template <class Cfg>
 Schedule make_schedule(int64_t M, int64_t N, int64_t slots)
 {
     Schedule sc;
-    sc.tiles = ((M + Cfg::TILE_M - 1) / Cfg::TILE_M) * ((N + Cfg::BN - 1) / Cfg::BN);
+    sc.tiles = ((M + Cfg::SUPER_M - 1) / Cfg::SUPER_M) * ((N + Cfg::BN - 1) / Cfg::BN);
     sc.units = sc.tiles;
     sc.split_start = sc.tiles;
     if (slots <= 0) return sc;
@@ -272,17 +301,17 @@ Schedule make_schedule(int64_t M, int64_t N, int64_t slots)
 }
 
 template <class Cfg>
-int fill_launch_info(int64_t M, int64_t N, int sm_count, int *grid_ctas, int *cluster_size, int *tiles)
+int fill_launch_info(int64_t M, int64_t N, const DeviceInfo &dev, int *grid_ctas, int *cluster_size, int *tiles)
 {
-    const Schedule sc = make_schedule<Cfg>(M, N, resident_slots<Cfg, true>(sm_count));
+    const Schedule sc = make_schedule<Cfg>(M, N, Prepared<Cfg, true>::get(dev.device, dev.sm_count));
     if (tiles) *tiles = static_cast<int>(sc.tiles < INT32_MAX ? sc.tiles : INT32_MAX);
-    if (cluster_size) *cluster_size = Cfg::CTA_GROUP;
-    if (grid_ctas) *grid_ctas = static_cast<int>(sc.grid_units * Cfg::CTA_GROUP);
+    if (cluster_size) *cluster_size = Cfg::CLUSTER;
+    if (grid_ctas) *grid_ctas = static_cast<int>(sc.grid_units * Cfg::CLUSTER);
     return GEMM_OK;
 }
 
 template <class Cfg, bool kRelu>
-int launch(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K, int sm_count,
+int launch(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K, const DeviceInfo &dev,
            cudaStream_t stream)
 {
     CUtensorMap ta, tb, tc;
@@ -295,10 +324,10 @@ int launch(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t 
     p.M = static_cast<int32_t>(M);
     p.N = static_cast<int32_t>(N);
     p.K = static_cast<int32_t>(K);
-    p.num_m_blocks = static_cast<int32_t>((M + Cfg::TILE_M - 1) / Cfg::TILE_M);
+    p.num_m_blocks = static_cast<int32_t>((M + Cfg::SUPER_M - 1) / Cfg::SUPER_M);
     p.num_n_blocks = static_cast<int32_t>((N + Cfg::BN - 1) / Cfg::BN);
     p.num_k_blocks = static_cast<int32_t>((K + Cfg::BK - 1) / Cfg::BK);
-    const int64_t slots = resident_slots<Cfg, kRelu>(sm_count);
+    const int64_t slots = Prepared<Cfg, kRelu>::get(dev.device, dev.sm_count);
     if (slots <= 0) return GEMM_ERR_LAUNCH;
     const Schedule sc = make_schedule<Cfg>(M, N, slots);
     if (sc.units > INT32_MAX / 2) return GEMM_ERR_INVALID_ARG;
@@ -306,41 +335,44 @@ int launch(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t 
     p.num_units = static_cast<int32_t>(sc.units);
     p.split_start = static_cast<int32_t>(sc.split_start);
     p.split_log2 = sc.shift;
-    p.group_m = group_m_override() ? group_m_override() : (Cfg::CTA_GROUP == 2 ? 8 : 16);
+    // Rasterisation panels 2048 rows high whatever the tile height.
+    p.group_m = group_m_override() ? group_m_override() : (Cfg::SUPER_M >= 2048 ? 1 : 2048 / Cfg::SUPER_M);
     p.timeout_cycles = timeout_cycles_for(K);
     p.C = static_cast<__half *>(C);
 
     auto kern = gemm_f16_relu_sm103a<Cfg, kRelu>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess) {
-        cudaGetLastError();
-        return GEMM_ERR_LAUNCH;
-    }
     cudaLaunchConfig_t lc{};
     lc.blockDim = dim3(Cfg::THREADS, 1, 1);
     lc.dynamicSmemBytes = Cfg::SMEM_BYTES;
     lc.stream = stream;
     cudaLaunchAttribute attrs[1];
     attrs[0].id = cudaLaunchAttributeClusterDimension;
-    attrs[0].val.clusterDim.x = Cfg::CTA_GROUP;
+    attrs[0].val.clusterDim.x = Cfg::CLUSTER;
     attrs[0].val.clusterDim.y = 1;
     attrs[0].val.clusterDim.z = 1;
     lc.attrs = attrs;
     lc.numAttrs = 1;
 
-    lc.gridDim = dim3(static_cast<unsigned>(sc.grid_units * Cfg::CTA_GROUP), 1, 1);
+    lc.gridDim = dim3(static_cast<unsigned>(sc.grid_units * Cfg::CLUSTER), 1, 1);
     if (cudaLaunchKernelEx(&lc, kern, ta, tb, tc, p) != cudaSuccess) {
         cudaGetLastError();
-        return GEMM_ERR_LAUNCH;
+        // Prepare again (the attribute may have been lost) and retry once.
+        Prepared<Cfg, kRelu>::forget(dev.device);
+        if (Prepared<Cfg, kRelu>::get(dev.device, dev.sm_count) <= 0 ||
+            cudaLaunchKernelEx(&lc, kern, ta, tb, tc, p) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_LAUNCH;
+        }
     }
     return GEMM_OK;
 }
 
 template <class Cfg>
-int launch_cfg(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K, int relu, int sm_count,
-               cudaStream_t stream)
+int launch_cfg(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K, int relu,
+               const DeviceInfo &dev, cudaStream_t stream)
 {
-    return relu ? launch<Cfg, true>(A, B, C, M, N, K, sm_count, stream)
-                : launch<Cfg, false>(A, B, C, M, N, K, sm_count, stream);
+    return relu ? launch<Cfg, true>(A, B, C, M, N, K, dev, stream)
+                : launch<Cfg, false>(A, B, C, M, N, K, dev, stream);
 }
 
 thread_local uint64_t t_last_timeout_record = 0;
@@ -361,7 +393,7 @@ extern "C" int gemm_f16_ex(const void *A, const void *B, void *C, int64_t M, int
     if ((st = current_device_info(&dev)) != GEMM_OK) return st;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     const uint64_t c_bytes = static_cast<uint64_t>(M) * static_cast<uint64_t>(N) * 2u;
-    if ((st = check_device_buffer(C, c_bytes)) != GEMM_OK) return st;
+    if ((st = check_device_buffer(C, c_bytes, dev.device)) != GEMM_OK) return st;
 
     if (K == 0) {
         // Empty sum: every output is R(+0) = +0.
@@ -374,18 +406,19 @@ extern "C" int gemm_f16_ex(const void *A, const void *B, void *C, int64_t M, int
     if ((N % 8) != 0 || (K % 8) != 0) return GEMM_ERR_ALIGNMENT;
     const uint64_t a_bytes = static_cast<uint64_t>(M) * static_cast<uint64_t>(K) * 2u;
     const uint64_t b_bytes = static_cast<uint64_t>(K) * static_cast<uint64_t>(N) * 2u;
-    if ((st = check_device_buffer(A, a_bytes)) != GEMM_OK) return st;
-    if ((st = check_device_buffer(B, b_bytes)) != GEMM_OK) return st;
+    if ((st = check_device_buffer(A, a_bytes, dev.device)) != GEMM_OK) return st;
+    if ((st = check_device_buffer(B, b_bytes, dev.device)) != GEMM_OK) return st;
     if (ranges_overlap(C, c_bytes, A, a_bytes) || ranges_overlap(C, c_bytes, B, b_bytes))
         return GEMM_ERR_INVALID_ARG;
 
     const int cfg = config == 0 ? pick_config(M, N, K, dev.sm_count) : config;
     switch (cfg) {
-        case 1: return launch_cfg<Cfg1x256>(A, B, C, M, N, K, relu, dev.sm_count, s);
-        case 2: return launch_cfg<Cfg1x128>(A, B, C, M, N, K, relu, dev.sm_count, s);
-        case 3: return launch_cfg<Cfg2x256>(A, B, C, M, N, K, relu, dev.sm_count, s);
-        case 4: return launch_cfg<Cfg2x256d>(A, B, C, M, N, K, relu, dev.sm_count, s);
-        case 5: return launch_cfg<Cfg2x512>(A, B, C, M, N, K, relu, dev.sm_count, s);
+        case 1: return launch_cfg<Cfg1x256>(A, B, C, M, N, K, relu, dev, s);
+        case 2: return launch_cfg<Cfg1x128>(A, B, C, M, N, K, relu, dev, s);
+        case 3: return launch_cfg<Cfg2x256>(A, B, C, M, N, K, relu, dev, s);
+        case 4: return launch_cfg<Cfg2x256d>(A, B, C, M, N, K, relu, dev, s);
+        case 5: return launch_cfg<Cfg2x512>(A, B, C, M, N, K, relu, dev, s);
+        case 6: return launch_cfg<Cfg4x256mc>(A, B, C, M, N, K, relu, dev, s);
         default: return GEMM_ERR_INVALID_ARG;
     }
 }
@@ -423,11 +456,12 @@ extern "C" int gemm_f16_launch_info(int64_t M, int64_t N, int64_t K, int config,
     if ((st = current_device_info(&dev)) != GEMM_OK) return st;
     const int cfg = config == 0 ? pick_config(M, N, K, dev.sm_count) : config;
     switch (cfg) {
-        case 1: return fill_launch_info<Cfg1x256>(M, N, dev.sm_count, grid_ctas, cluster_size, tiles);
-        case 2: return fill_launch_info<Cfg1x128>(M, N, dev.sm_count, grid_ctas, cluster_size, tiles);
-        case 3: return fill_launch_info<Cfg2x256>(M, N, dev.sm_count, grid_ctas, cluster_size, tiles);
-        case 4: return fill_launch_info<Cfg2x256d>(M, N, dev.sm_count, grid_ctas, cluster_size, tiles);
-        case 5: return fill_launch_info<Cfg2x512>(M, N, dev.sm_count, grid_ctas, cluster_size, tiles);
+        case 1: return fill_launch_info<Cfg1x256>(M, N, dev, grid_ctas, cluster_size, tiles);
+        case 2: return fill_launch_info<Cfg1x128>(M, N, dev, grid_ctas, cluster_size, tiles);
+        case 3: return fill_launch_info<Cfg2x256>(M, N, dev, grid_ctas, cluster_size, tiles);
+        case 4: return fill_launch_info<Cfg2x256d>(M, N, dev, grid_ctas, cluster_size, tiles);
+        case 5: return fill_launch_info<Cfg2x512>(M, N, dev, grid_ctas, cluster_size, tiles);
+        case 6: return fill_launch_info<Cfg4x256mc>(M, N, dev, grid_ctas, cluster_size, tiles);
         default: return GEMM_ERR_INVALID_ARG;
     }
 }
@@ -448,9 +482,9 @@ extern "C" int gemm_f16_from_host(const void *A_host, const void *B_host, void *
         DeviceInfo dev;
         if ((st = current_device_info(&dev)) != GEMM_OK) return st;
         if ((N % 8) != 0 || (K % 8) != 0) return GEMM_ERR_ALIGNMENT;
-        if ((st = check_device_buffer(A_dev, a_bytes)) != GEMM_OK) return st;
-        if ((st = check_device_buffer(B_dev, b_bytes)) != GEMM_OK) return st;
-        if ((st = check_device_buffer(C_dev, c_bytes)) != GEMM_OK) return st;
+        if ((st = check_device_buffer(A_dev, a_bytes, dev.device)) != GEMM_OK) return st;
+        if ((st = check_device_buffer(B_dev, b_bytes, dev.device)) != GEMM_OK) return st;
+        if ((st = check_device_buffer(C_dev, c_bytes, dev.device)) != GEMM_OK) return st;
         if (cudaMemcpyAsync(A_dev, A_host, a_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
             cudaMemcpyAsync(B_dev, B_host, b_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) {
             cudaGetLastError();

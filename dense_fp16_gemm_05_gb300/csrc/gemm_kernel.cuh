@@ -87,12 +87,18 @@ constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
 //   kStages    depth of the shared-memory K ring
 //   kEpiSmem   true: stage C tiles in shared memory and store them with TMA;
 //              false: store C from registers (frees shared memory for a deeper ring)
-template <int kCtaGroup, int kBN, int kStages, bool kEpiSmem = true>
+//   kPairs     CTA pairs per cluster (pair mode only).  The pairs of a cluster
+//              compute vertically adjacent tiles, so they need the same B
+//              columns: each B box is loaded once and multicast to all pairs.
+template <int kCtaGroup, int kBN, int kStages, bool kEpiSmem = true, int kPairs = 1>
 struct GemmCfg {
     static constexpr int CTA_GROUP = kCtaGroup;
+    static constexpr int PAIRS = kPairs;
+    static constexpr int CLUSTER = CTA_GROUP * PAIRS;   // CTAs per cluster
     static constexpr bool EPI_SMEM = kEpiSmem;
     static constexpr int BM = 128;                    // rows of C per CTA = TMEM lanes
-    static constexpr int TILE_M = BM * CTA_GROUP;     // rows of C per tile (the MMA's M)
+    static constexpr int TILE_M = BM * CTA_GROUP;     // rows of C per MMA tile (the MMA's M)
+    static constexpr int SUPER_M = TILE_M * PAIRS;    // rows of C per work unit (one per cluster)
     static constexpr int BN = kBN;
     static constexpr int UMMA_N = BN < 256 ? BN : 256;   // N of one MMA instruction
     static constexpr int N_MMAS = BN / UMMA_N;        // MMAs per K step
@@ -123,6 +129,7 @@ struct GemmCfg {
     static constexpr uint32_t IDESC = idesc_f16_f32(TILE_M, UMMA_N, /*A MN-major*/ false, /*B MN-major*/ true);
 
     static_assert(CTA_GROUP == 1 || CTA_GROUP == 2, "one CTA or a CTA pair");
+    static_assert(PAIRS == 1 || (PAIRS == 2 && CTA_GROUP == 2), "multicast clusters are made of CTA pairs");
     static_assert(BN % (B_BOX_N * CTA_GROUP) == 0 && BN <= 512, "whole B boxes per CTA; at most 512 TMEM columns");
     static_assert(UMMA_N % 16 == 0 && UMMA_N <= 256, "UMMA N: multiple of 16 up to 256");
     static_assert(TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation is a power of 2");
@@ -133,18 +140,20 @@ struct GemmCfg {
 // Device status word: 0 = fine; otherwise the first timeout record.
 __device__ unsigned long long g_gemm_f16_status;
 
-// Abort flag of this CTA, and (pair mode) the shared::cluster address of the
-// peer CTA's flag.
+// Abort flag of this CTA.  In a cluster, raising it also raises the flag (at
+// the same shared-memory offset) of every other CTA of the cluster.
 struct AbortFlag {
     volatile int *local;
-    uint32_t peer_addr;
-    bool pair;
+    uint32_t addr;          // shared::cta address of the flag
+    uint32_t cluster;       // CTAs in the cluster
+    uint32_t rank;          // this CTA's rank in the cluster
 
     __device__ __forceinline__ bool raised() const { return *local != 0; }
     __device__ __forceinline__ void raise(uint32_t site) const
     {
         *local = 1;
-        if (pair) st_shared_cluster_u32(peer_addr, 1u);
+        for (uint32_t i = 0; i < cluster; ++i)
+            if (i != rank) st_shared_cluster_u32(mapa_shared(addr, i), 1u);
         atomicCAS(&g_gemm_f16_status, 0ull,
                   static_cast<unsigned long long>(site) | (static_cast<unsigned long long>(blockIdx.x) << 8));
     }
@@ -277,20 +286,29 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t rank = kPair ? cluster_ctarank() : 0u;   // 0 = leader
+    const uint32_t crank = Cfg::CLUSTER > 1 ? cluster_ctarank() : 0u;   // rank in the cluster
+    const uint32_t rank = kPair ? (crank & 1u) : 0u;                    // rank in the pair; 0 = leader
+    const uint32_t pair = kPair ? (crank >> 1) : 0u;                     // pair within the cluster
+    const uint32_t leader_rank = crank & ~1u;                             // cluster rank of the pair's leader
     const bool leader = rank == 0;
-    const int cluster_id = static_cast<int>(blockIdx.x) / Cfg::CTA_GROUP;
-    const int num_clusters = static_cast<int>(gridDim.x) / Cfg::CTA_GROUP;
+    const int cluster_id = static_cast<int>(blockIdx.x) / Cfg::CLUSTER;
+    const int num_clusters = static_cast<int>(gridDim.x) / Cfg::CLUSTER;
+    // Cluster ranks with the same half (rank) in every pair: the B multicast set.
+    uint16_t same_half_mask = 0;
+    for (int i = 0; i < Cfg::PAIRS; ++i) same_half_mask |= static_cast<uint16_t>(1u << (2 * i + rank));
+    const uint16_t pair_mask = static_cast<uint16_t>(0x3u << (2 * pair));
+    const uint16_t all_mask = static_cast<uint16_t>((1u << Cfg::CLUSTER) - 1u);
 
     AbortFlag abort;
     abort.local = reinterpret_cast<volatile int *>(tmem_slot_ptr + 1);
-    abort.pair = kPair;
-    abort.peer_addr = kPair ? mapa_shared(abort_addr, rank ^ 1u) : 0u;
+    abort.addr = abort_addr;
+    abort.cluster = Cfg::CLUSTER;
+    abort.rank = crank;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < Cfg::STAGES; ++s) {
-            mbar_init(full_bar(s), Cfg::CTA_GROUP);   // each CTA's producer: arrive.expect_tx
-            mbar_init(empty_bar(s), 1);               // the leader's MMA commit
+            mbar_init(full_bar(s), Cfg::CTA_GROUP);   // each CTA of the pair: arrive.expect_tx
+            mbar_init(empty_bar(s), Cfg::PAIRS);      // one MMA commit per pair of the cluster
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull_bar(b), 1);                       // commit after a tile's last MMA
@@ -311,9 +329,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     }
     tc_fence_before_sync();
     __syncthreads();
-    if constexpr (kPair) {
-        // Both CTAs' barriers are initialised and both TMEMs allocated before
-        // either CTA signals the other.
+    if constexpr (Cfg::CLUSTER > 1) {
+        // Every CTA's barriers are initialised and its TMEM allocated before
+        // any CTA of the cluster signals another.
         cluster_arrive();
         cluster_wait();
     }
@@ -332,7 +350,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             for (int u = cluster_id; ok && u < p.num_units; u += num_clusters) {
                 int mb, col0, shift;
                 unit_coords<Cfg::BN>(u, p, mb, col0, shift);
-                const int m0 = mb * Cfg::TILE_M + static_cast<int>(rank) * Cfg::BM;
+                const int m0 = mb * Cfg::SUPER_M + static_cast<int>(pair) * Cfg::TILE_M +
+                               static_cast<int>(rank) * Cfg::BM;
                 // Unit width W = BN >> shift, issued as W / umma_n MMAs of N = umma_n.
                 // For MMA h, this CTA supplies umma_n / CTA_GROUP columns (bpm boxes),
                 // starting at tile column h * umma_n + rank * umma_n / CTA_GROUP.
@@ -357,14 +376,24 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                             tma_load_2d(b_dst + j * Cfg::B_BOX_BYTES, &tmap_b, full_bar(s),
                                         n_cta + (j / bpm) * umma_n + (j % bpm) * Cfg::B_BOX_N, k0);
                     } else {
-                        // Both CTAs' bytes land on the leader's barrier.
-                        const uint32_t fb = leader ? full_bar(s) : mapa_shared(full_bar(s), 0);
+                        // The bytes landing in both CTAs of a pair are counted on the
+                        // pair leader's barrier; each CTA announces its own bytes.
+                        const uint32_t fb = leader ? full_bar(s) : mapa_shared(full_bar(s), leader_rank);
                         if (leader) mbar_arrive_expect_tx(fb, tx);
                         else mbar_arrive_expect_tx_cluster(fb, tx);
                         tma_load_2d_pair(a_dst, &tmap_a, fb, k0, m0);
-                        for (int j = 0; j < boxes; ++j)
-                            tma_load_2d_pair(b_dst + j * Cfg::B_BOX_BYTES, &tmap_b, fb,
-                                             n_cta + (j / bpm) * umma_n + (j % bpm) * Cfg::B_BOX_N, k0);
+                        for (int j = 0; j < boxes; ++j) {
+                            const int x = n_cta + (j / bpm) * umma_n + (j % bpm) * Cfg::B_BOX_N;
+                            if constexpr (Cfg::PAIRS == 1) {
+                                tma_load_2d_pair(b_dst + j * Cfg::B_BOX_BYTES, &tmap_b, fb, x, k0);
+                            } else {
+                                // Box j is loaded by pair j % PAIRS and multicast to the
+                                // same-half CTA of every pair.
+                                if (j % Cfg::PAIRS == static_cast<int>(pair))
+                                    tma_load_2d_pair_mc(b_dst + j * Cfg::B_BOX_BYTES, &tmap_b, fb, x, k0,
+                                                        same_half_mask);
+                            }
+                        }
                     }
                     issued_mask |= 1u << s;
                     issued_parity = (issued_parity & ~(1u << s)) | (ph << s);
@@ -398,6 +427,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             uint32_t ph = 0;
             int it = 0;
             bool ok = true, issued_any = false;
+            // Stage-0 descriptors; every other operand address is a constant offset.
+            const uint64_t a_desc0 = smem_desc_sw128(sA, 16, 1024);
+            const uint64_t b_desc0 = smem_desc_sw128(sB, Cfg::B_BOX_BYTES, 1024);
             for (int u = cluster_id; ok && u < p.num_units; u += num_clusters, ++it) {
                 const int b = it % Cfg::ACC_STAGES;
                 const uint32_t acc_ph = (it / Cfg::ACC_STAGES) & 1;
@@ -422,27 +454,33 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint32_t a0 = sA + s * Cfg::A_STAGE_BYTES;
-                    const uint32_t b0 = sB + s * Cfg::B_STAGE_BYTES;
+                    // Descriptors of this stage: the start-address field (bits 0-13)
+                    // holds address >> 4, so advancing an operand by n bytes adds
+                    // n >> 4 (no carry out of the field: shared addresses < 2^18).
+                    const uint64_t a_st = a_desc0 + static_cast<uint64_t>((s * Cfg::A_STAGE_BYTES) >> 4);
+                    const uint64_t b_st = b_desc0 + static_cast<uint64_t>((s * Cfg::B_STAGE_BYTES) >> 4);
+                    const uint32_t acc0 = kb != 0 ? 1u : 0u;
 #pragma unroll
                     for (int ks = 0; ks < Cfg::BK / Cfg::UMMA_K; ++ks) {
                         // A: K-major, 8-row groups 1024 B apart; a K step of 16
                         // elements is 32 B inside the 128-byte swizzle row.
-                        const uint64_t a_desc = smem_desc_sw128(a0 + ks * (Cfg::UMMA_K * 2), 16, 1024);
+                        const uint64_t a_desc = a_st + static_cast<uint64_t>((ks * Cfg::UMMA_K * 2) >> 4);
 #pragma unroll
                         for (int h = 0; h < Cfg::N_MMAS; ++h) {
                             if (h >= n_mmas) break;
                             // B: N-major; 64-column boxes B_BOX_BYTES apart (LBO),
                             // 8-row K groups 1024 B apart (SBO); a K step of 16 rows
                             // is 16 * 128 B; MMA h starts at its own boxes.
-                            const uint64_t b_desc = smem_desc_sw128(
-                                b0 + h * bpm_bytes + ks * (Cfg::UMMA_K * 128), Cfg::B_BOX_BYTES, 1024);
+                            const uint64_t b_desc =
+                                b_st + static_cast<uint64_t>((h * bpm_bytes + ks * Cfg::UMMA_K * 128) >> 4);
                             mma_f16_ss<Cfg::CTA_GROUP>(d_tmem + h * umma_n, a_desc, b_desc, idesc,
-                                                       (kb | ks) != 0 ? 1u : 0u);
+                                                       ks != 0 ? 1u : acc0);
                         }
                     }
-                    // Frees the slot (in both CTAs) once these MMAs have read it.
-                    if constexpr (kPair) mma_commit_pair_mc(empty_bar(s), 0x3);
+                    // Frees the slot once these MMAs have read it: in both CTAs of the
+                    // pair, and in every CTA of the cluster when B boxes are shared
+                    // (another pair's multicast writes this pair's slots too).
+                    if constexpr (kPair) mma_commit_pair_mc(empty_bar(s), Cfg::PAIRS > 1 ? all_mask : pair_mask);
                     else mma_commit(empty_bar(s));
                     issued_any = true;
                     if (++s == Cfg::STAGES) {
@@ -452,14 +490,14 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 }
                 if (!ok) break;
                 // Accumulator b complete (in both CTAs' TMEM).
-                if constexpr (kPair) mma_commit_pair_mc(tfull_bar(b), 0x3);
+                if constexpr (kPair) mma_commit_pair_mc(tfull_bar(b), pair_mask);
                 else mma_commit(tfull_bar(b));
             }
             if (!ok) {
                 aborted = true;
                 if (issued_any) {
                     // Wait for this thread's MMAs before the TMEM is freed.
-                    if constexpr (kPair) mma_commit_pair_mc(drain_bar, 0x1);
+                    if constexpr (kPair) mma_commit_pair_mc(drain_bar, static_cast<uint16_t>(1u << crank));
                     else mma_commit(drain_bar);
                     wait_phase_drain(drain_bar, 0, limit, kSiteDrainMma);
                 }
@@ -472,7 +510,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         const int q = warp & 3;         // TMEM lane quarter this warp may access
         const uint32_t row_off = static_cast<uint32_t>(lane) * 128u;
         const uint32_t sw = static_cast<uint32_t>(lane & 7);
-        const uint32_t tempty_leader0 = kPair && !leader ? mapa_shared(tempty_bar(0), 0) : tempty_bar(0);
+        const uint32_t tempty_leader0 = kPair && !leader ? mapa_shared(tempty_bar(0), leader_rank) : tempty_bar(0);
         int it = 0;
         uint32_t chunk = 0;
         for (int u = cluster_id; u < p.num_units; u += num_clusters, ++it) {
@@ -490,7 +528,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 break;
             }
             tc_fence_after_sync();
-            const int row0 = mb * Cfg::TILE_M + static_cast<int>(rank) * Cfg::BM + q * 32;
+            const int row0 = mb * Cfg::SUPER_M + static_cast<int>(pair) * Cfg::TILE_M +
+                             static_cast<int>(rank) * Cfg::BM + q * 32;
 #pragma unroll 1
             for (int c = 0; c < chunks; ++c) {
                 uint32_t r[64];
@@ -558,9 +597,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 
     tc_fence_before_sync();
     __syncthreads();
-    if constexpr (kPair) {
-        // No CTA of the pair exits while the other may still signal its
-        // barriers or read its shared memory.
+    if constexpr (Cfg::CLUSTER > 1) {
+        // No CTA of the cluster exits while another may still signal its
+        // barriers or read or write its shared memory.
         cluster_arrive();
         cluster_wait();
     }
