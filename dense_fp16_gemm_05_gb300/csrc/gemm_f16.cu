@@ -310,9 +310,15 @@ int fill_launch_info(int64_t M, int64_t N, const DeviceInfo &dev, int *grid_ctas
     return GEMM_OK;
 }
 
+// Test-hook settings for a launch (all zero for normal calls).
+struct LaunchHook {
+    int producer_off = 0;          // producer issues nothing
+    uint64_t timeout_cycles = 0;   // 0: the normal budget
+};
+
 template <class Cfg, bool kRelu>
 int launch(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K, const DeviceInfo &dev,
-           cudaStream_t stream)
+           cudaStream_t stream, const LaunchHook &hook = LaunchHook())
 {
     CUtensorMap ta, tb, tc;
     int st;
@@ -337,8 +343,9 @@ int launch(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t 
     p.split_log2 = sc.shift;
     // Rasterisation panels 2048 rows high whatever the tile height.
     p.group_m = group_m_override() ? group_m_override() : (Cfg::SUPER_M >= 2048 ? 1 : 2048 / Cfg::SUPER_M);
-    p.timeout_cycles = timeout_cycles_for(K);
+    p.timeout_cycles = hook.timeout_cycles ? hook.timeout_cycles : timeout_cycles_for(K);
     p.C = static_cast<__half *>(C);
+    p.producer_off = hook.producer_off;
 
     auto kern = gemm_f16_relu_sm103a<Cfg, kRelu>;
     cudaLaunchConfig_t lc{};
@@ -369,10 +376,10 @@ int launch(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t 
 
 template <class Cfg>
 int launch_cfg(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K, int relu,
-               const DeviceInfo &dev, cudaStream_t stream)
+               const DeviceInfo &dev, cudaStream_t stream, const LaunchHook &hook = LaunchHook())
 {
-    return relu ? launch<Cfg, true>(A, B, C, M, N, K, dev, stream)
-                : launch<Cfg, false>(A, B, C, M, N, K, dev, stream);
+    return relu ? launch<Cfg, true>(A, B, C, M, N, K, dev, stream, hook)
+                : launch<Cfg, false>(A, B, C, M, N, K, dev, stream, hook);
 }
 
 thread_local uint64_t t_last_timeout_record = 0;
@@ -381,8 +388,10 @@ thread_local uint64_t t_last_timeout_record = 0;
 
 // ==================================================================== C ABI
 
-extern "C" int gemm_f16_ex(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K, int relu,
-                           int config, void *stream)
+namespace {
+
+int run_gemm(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K, int relu, int config,
+             void *stream, const LaunchHook &hook)
 {
     int st = check_sizes(M, N, K, relu);
     if (st != GEMM_OK) return st;
@@ -413,14 +422,33 @@ extern "C" int gemm_f16_ex(const void *A, const void *B, void *C, int64_t M, int
 
     const int cfg = config == 0 ? pick_config(M, N, K, dev.sm_count) : config;
     switch (cfg) {
-        case 1: return launch_cfg<Cfg1x256>(A, B, C, M, N, K, relu, dev, s);
-        case 2: return launch_cfg<Cfg1x128>(A, B, C, M, N, K, relu, dev, s);
-        case 3: return launch_cfg<Cfg2x256>(A, B, C, M, N, K, relu, dev, s);
-        case 4: return launch_cfg<Cfg2x256d>(A, B, C, M, N, K, relu, dev, s);
-        case 5: return launch_cfg<Cfg2x512>(A, B, C, M, N, K, relu, dev, s);
-        case 6: return launch_cfg<Cfg4x256mc>(A, B, C, M, N, K, relu, dev, s);
+        case 1: return launch_cfg<Cfg1x256>(A, B, C, M, N, K, relu, dev, s, hook);
+        case 2: return launch_cfg<Cfg1x128>(A, B, C, M, N, K, relu, dev, s, hook);
+        case 3: return launch_cfg<Cfg2x256>(A, B, C, M, N, K, relu, dev, s, hook);
+        case 4: return launch_cfg<Cfg2x256d>(A, B, C, M, N, K, relu, dev, s, hook);
+        case 5: return launch_cfg<Cfg2x512>(A, B, C, M, N, K, relu, dev, s, hook);
+        case 6: return launch_cfg<Cfg4x256mc>(A, B, C, M, N, K, relu, dev, s, hook);
         default: return GEMM_ERR_INVALID_ARG;
     }
+}
+
+}  // namespace
+
+extern "C" int gemm_f16_ex(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K, int relu,
+                           int config, void *stream)
+{
+    return run_gemm(A, B, C, M, N, K, relu, config, stream, LaunchHook());
+}
+
+extern "C" int gemm_f16_selftest_timeout(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
+                                         int config, uint64_t timeout_cycles, void *stream)
+{
+    if (K == 0 || M == 0 || N == 0) return GEMM_ERR_INVALID_ARG;   // nothing would be launched
+    if (timeout_cycles < (1ull << 16) || timeout_cycles > (1ull << 32)) return GEMM_ERR_INVALID_ARG;
+    LaunchHook hook;
+    hook.producer_off = 1;
+    hook.timeout_cycles = timeout_cycles;
+    return run_gemm(A, B, C, M, N, K, 1, config, stream, hook);
 }
 
 extern "C" int gemm_f16(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K, int relu,

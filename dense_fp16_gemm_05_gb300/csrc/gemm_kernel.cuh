@@ -66,6 +66,8 @@ struct GemmParams {
     int32_t split_log2;     // each tile from split_start on is 2^split_log2 units
     uint64_t timeout_cycles;
     __half *C;              // output base (used by the direct-store epilogue)
+    int32_t producer_off;   // test hook: 1 = the producer issues nothing, so the
+                            // MMA thread's first wait runs out (see gemm_f16_selftest_timeout)
 };
 
 // Where a bounded wait expired (bits 0-7 of the status word).
@@ -347,7 +349,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             uint32_t ph = 0;
             uint32_t issued_mask = 0, issued_parity = 0;
             bool ok = true;
-            for (int u = cluster_id; ok && u < p.num_units; u += num_clusters) {
+            for (int u = cluster_id; ok && p.producer_off == 0 && u < p.num_units; u += num_clusters) {
                 int mb, col0, shift;
                 unit_coords<Cfg::BN>(u, p, mb, col0, shift);
                 const int m0 = mb * Cfg::SUPER_M + static_cast<int>(pair) * Cfg::TILE_M +

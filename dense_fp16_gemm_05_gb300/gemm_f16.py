@@ -70,6 +70,8 @@ def lib() -> ctypes.CDLL:
     L.gemm_f16_config_name.restype = ctypes.c_char_p
     L.gemm_f16_auto_config.argtypes = [i64, i64, i64]
     L.gemm_f16_auto_config.restype = ci
+    L.gemm_f16_selftest_timeout.argtypes = [vp, vp, vp, i64, i64, i64, ci, ctypes.c_uint64, vp]
+    L.gemm_f16_selftest_timeout.restype = ci
     pi = ctypes.POINTER(ctypes.c_int)
     L.gemm_f16_launch_info.argtypes = [i64, i64, i64, ci, pi, pi, pi]
     L.gemm_f16_launch_info.restype = ci
@@ -196,3 +198,18 @@ def launch_info(M: int, N: int, K: int, config: int = 0) -> dict:
     if st != GEMM_OK:
         raise GemmError(st, "gemm_f16_launch_info")
     return {"grid_ctas": g.value, "cluster_size": c.value, "tiles": t.value}
+
+
+def selftest_timeout(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, config: int = 0,
+                     timeout_cycles: int = 1 << 24, stream=None) -> int:
+    """Launches the kernel with its producer switched off so that a bounded wait
+    runs out (test hook); returns the launch status.  Read the outcome with check()."""
+    M, K = A.shape
+    N = B.shape[1]
+    with torch.cuda.device(A.device):
+        return int(lib().gemm_f16_selftest_timeout(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, int(config),
+                                                   int(timeout_cycles), _stream_handle(stream, A.device)))
+
+
+def last_timeout_record() -> int:
+    return int(lib().gemm_f16_last_timeout_record())

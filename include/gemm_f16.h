@@ -136,6 +136,23 @@ int gemm_f16_from_host(const void *A_host, const void *B_host, void *C_host,
  */
 int gemm_f16_check(void *stream);
 
+/*
+ * gemm_f16_selftest_timeout -- exercises the kernels' bounded waits (a test
+ * hook; it computes nothing).  Launches the kernel of `config` (0 = automatic)
+ * for the given problem with its TMA producer switched off and a wait budget
+ * of `timeout_cycles` SM clocks (2^16 .. 2^32), so that the MMA thread's first
+ * wait for operand data runs out: the kernel records the wait site, every role
+ * leaves its loop, the tensor memory is freed and the kernel exits without
+ * writing C.  The next gemm_f16_check on `stream` returns GEMM_ERR_TIMEOUT and
+ * gemm_f16_last_timeout_record() holds the site (3: MMA waiting for operand
+ * data; 4: epilogue waiting for an accumulator, in a CTA whose MMA thread
+ * aborted first).  Buffers and sizes are validated as for gemm_f16; no copy,
+ * MMA or store is in flight when the waits give up.  Nothing in the product
+ * path calls this.
+ */
+int gemm_f16_selftest_timeout(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
+                              int config, uint64_t timeout_cycles, void *stream);
+
 /* Raw value of the last timeout record read by gemm_f16_check on this thread
  * (0 if none): bits 0-7 the wait site, bits 8-31 the block index. */
 uint64_t gemm_f16_last_timeout_record(void);

@@ -92,3 +92,11 @@ def test_binding_fails_loudly_without_library(monkeypatch):
     monkeypatch.setattr(mod._build, "LIB", "/nonexistent/libgemm_f16.so")
     with pytest.raises(mod.LibraryNotBuilt):
         mod.lib()
+
+
+def test_selftest_timeout_rejects_bad_budgets_before_any_cuda_call(g):
+    L = g.lib()
+    # K == 0 or out-of-range budgets are refused without touching the GPU
+    assert L.gemm_f16_selftest_timeout(None, None, None, 64, 64, 0, 0, 1 << 20, None) == g.GEMM_ERR_INVALID_ARG
+    assert L.gemm_f16_selftest_timeout(None, None, None, 64, 64, 64, 0, 100, None) == g.GEMM_ERR_INVALID_ARG
+    assert L.gemm_f16_selftest_timeout(None, None, None, 64, 64, 64, 0, 1 << 40, None) == g.GEMM_ERR_INVALID_ARG
