@@ -1,9 +1,11 @@
 """Builds the CUDA library ``libgemm_f16.so`` in-tree with nvcc for sm_103a.
 
-One translation unit (``csrc/gemm_f16.cu``), one ``-gencode``
-(``arch=compute_103a,code=sm_103a``), the CUDA runtime linked statically so the
-library loads on machines without a GPU driver (the symbol-export test runs
-there).  The build is skipped when the library is newer than every source.
+Translation units: ``csrc/gemm_f16.cu`` (the C ABI) and ``csrc/gemm_cfg_<id>.cu``
+(the kernel instances of each configuration), compiled in parallel with one
+``-gencode`` (``arch=compute_103a,code=sm_103a``) and linked with the CUDA
+runtime linked statically, so the library loads on machines without a GPU
+driver (the symbol-export test runs there).  The build is skipped when the
+library is newer than every source.
 """
 from __future__ import annotations
 
@@ -17,7 +19,6 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libgemm_f16.so")
-MAIN_SRC = os.path.join(CSRC, "gemm_f16.cu")
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
@@ -39,18 +40,46 @@ def nvcc() -> str:
     return "nvcc"
 
 
+def _translation_units() -> list[str]:
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+
+
 def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None) -> str:
-    """Compiles the library if it is missing or stale; returns its path."""
+    """Compiles the library if it is missing or stale; returns its path.
+
+    Each translation unit (the C ABI and one per kernel configuration) is
+    compiled to an object in parallel, then the objects are linked into one
+    shared library.
+    """
     if not force and os.path.exists(LIB):
         lib_t = os.path.getmtime(LIB)
         if all(os.path.getmtime(s) <= lib_t for s in _sources()):
             return LIB
+    import concurrent.futures
+    import tempfile
+    tmpdir = tempfile.mkdtemp(prefix="gemm_f16_build")
+    compile_flags = [f for f in NVCC_FLAGS if f not in ("-shared", "-cudart", "static")]
+    units = _translation_units()
+
+    def compile_one(src):
+        obj = os.path.join(tmpdir, os.path.basename(src) + ".o")
+        cmd = [nvcc(), *compile_flags, *(extra_flags or []), "-I", INCLUDE, "-c", "-o", obj, src]
+        if verbose:
+            print(" ".join(cmd), file=sys.stderr)
+        subprocess.run(cmd, check=True)
+        return obj
+
+    with concurrent.futures.ThreadPoolExecutor(max_workers=min(len(units), os.cpu_count() or 4)) as ex:
+        objs = list(ex.map(compile_one, units))
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc(), *NVCC_FLAGS, *(extra_flags or []), "-I", INCLUDE, "-o", tmp, MAIN_SRC]
+    link = [nvcc(), "-gencode", "arch=compute_103a,code=sm_103a", "-shared", "-cudart", "static", "-o", tmp, *objs]
     if verbose:
-        print(" ".join(cmd), file=sys.stderr)
-    subprocess.run(cmd, check=True)
+        print(" ".join(link), file=sys.stderr)
+    subprocess.run(link, check=True)
     os.replace(tmp, LIB)
+    for o in objs:
+        os.unlink(o)
+    os.rmdir(tmpdir)
     return LIB
 
 

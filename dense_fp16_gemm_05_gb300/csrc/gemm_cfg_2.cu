@@ -1,0 +1,15 @@
+// gemm_cfg_2.cu -- kernel instances of configuration 2 (1sm_128x128_s6): ReLU on and
+// off, all four operand layouts (NN, NT, TN, TT).  One translation unit per configuration so that
+// the instances compile in parallel.
+#include "gemm_launch.cuh"
+
+namespace gemm_sm103 {
+
+int launch_config_2(const LaunchArgs &a) { return launch_config<Cfg1x128, true>(a); }
+
+int launch_info_config_2(int64_t M, int64_t N, const DeviceInfo &dev, int *grid_ctas, int *cluster_size, int *tiles)
+{
+    return config_launch_info<Cfg1x128>(M, N, dev, grid_ctas, cluster_size, tiles);
+}
+
+}  // namespace gemm_sm103

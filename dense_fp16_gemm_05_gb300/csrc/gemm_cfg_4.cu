@@ -1,0 +1,15 @@
+// gemm_cfg_4.cu -- kernel instances of configuration 4 (2sm_256x256_s7_direct): ReLU on and
+// off, the NN layout only.  One translation unit per configuration so that
+// the instances compile in parallel.
+#include "gemm_launch.cuh"
+
+namespace gemm_sm103 {
+
+int launch_config_4(const LaunchArgs &a) { return launch_config<Cfg2x256d, false>(a); }
+
+int launch_info_config_4(int64_t M, int64_t N, const DeviceInfo &dev, int *grid_ctas, int *cluster_size, int *tiles)
+{
+    return config_launch_info<Cfg2x256d>(M, N, dev, grid_ctas, cluster_size, tiles);
+}
+
+}  // namespace gemm_sm103

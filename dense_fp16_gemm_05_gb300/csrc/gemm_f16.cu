@@ -1,6 +1,7 @@
 // gemm_f16.cu -- host side of the GB300 fp16 GEMM + ReLU library: argument
-// checks, TMA tensor-map encoding, configuration choice, launch, and the
-// extern "C" entry points declared in include/gemm_f16.h.
+// checks, TMA tensor-map encoding, configuration choice, the device status
+// word, and the extern "C" entry points declared in include/gemm_f16.h.  The
+// kernel instances themselves are launched from gemm_cfg_<id>.cu.
 //
 // Nothing here computes the product on the host; every element of C is
 // written by the sm_103a kernel in gemm_kernel.cuh (or, for K == 0, by one
@@ -9,43 +10,50 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
-#include <atomic>
 #include <mutex>
 
 #include "gemm_f16.h"
-#include "gemm_kernel.cuh"
+#include "gemm_launch.cuh"
 
 using namespace gemm_sm103;
 
+// Device status word of each GPU: 0 = fine; otherwise the first timeout record
+// written by a kernel (wait site | block << 8).  Kernels get its address.
+__device__ unsigned long long g_gemm_f16_status;
+
 namespace {
+
+// Reason for the last rejected call on this thread (static strings only).
+thread_local const char *t_last_detail = "";
+
+int reject(int status, const char *why)
+{
+    t_last_detail = why;
+    return status;
+}
 
 // ---------------------------------------------------------------- configurations
 
 struct ConfigInfo {
     const char *name;
-    int tile_m;       // rows of C per tile (all CTAs of the tile together)
-    int tile_n;       // columns of C per tile
+    int tile_m;       // rows of C per work unit (all CTAs of the unit together)
+    int tile_n;       // columns of C per work unit
+    int all_layouts;  // 1: NN, NT, TN and TT operand layouts; 0: NN only
 };
 
 // id 1..kNumConfigs; index 0 is "auto".
-using Cfg1x256 = GemmCfg<1, 256, 4>;
-using Cfg1x128 = GemmCfg<1, 128, 6>;
-using Cfg2x256 = GemmCfg<2, 256, 6>;
-using Cfg2x256d = GemmCfg<2, 256, 7, /*stage C in smem*/ false>;
-using Cfg2x512 = GemmCfg<2, 512, 4>;
-using Cfg4x256mc = GemmCfg<2, 256, 6, /*stage C in smem*/ true, /*pairs sharing B*/ 2>;
-
 constexpr ConfigInfo kConfigs[] = {
-    {"auto", 0, 0},
-    {"1sm_128x256_s4", Cfg1x256::SUPER_M, Cfg1x256::BN},
-    {"1sm_128x128_s6", Cfg1x128::SUPER_M, Cfg1x128::BN},
-    {"2sm_256x256_s6", Cfg2x256::SUPER_M, Cfg2x256::BN},
-    {"2sm_256x256_s7_direct", Cfg2x256d::SUPER_M, Cfg2x256d::BN},
-    {"2sm_256x512_s4", Cfg2x512::SUPER_M, Cfg2x512::BN},
-    {"4sm_512x256_mc_s6", Cfg4x256mc::SUPER_M, Cfg4x256mc::BN},
+    {"auto", 0, 0, 1},
+    {"1sm_128x256_s4", Cfg1x256::SUPER_M, Cfg1x256::BN, 1},
+    {"1sm_128x128_s6", Cfg1x128::SUPER_M, Cfg1x128::BN, 1},
+    {"2sm_256x256_s6", Cfg2x256::SUPER_M, Cfg2x256::BN, 1},
+    {"2sm_256x256_s7_direct", Cfg2x256d::SUPER_M, Cfg2x256d::BN, 0},
+    {"2sm_256x512_s4", Cfg2x512::SUPER_M, Cfg2x512::BN, 1},
+    {"4sm_512x256_mc_s6", Cfg4x256mc::SUPER_M, Cfg4x256mc::BN, 0},
 };
 constexpr int kNumConfigs = static_cast<int>(sizeof(kConfigs) / sizeof(kConfigs[0])) - 1;
 
@@ -79,17 +87,10 @@ const DriverFns &driver()
 
 // ---------------------------------------------------------------- per-device facts
 
-constexpr int kMaxDevices = 64;
-
-struct DeviceInfo {
-    int device = 0;
-    int supported = 0;      // compute capability 10.3
-    int sm_count = 0;
-};
-
 // Filled once per device; read without locking afterwards.
 std::atomic<int> g_device_state[kMaxDevices];   // 0 unknown, 1 supported, 2 unsupported
 int g_device_sms[kMaxDevices];
+std::atomic<unsigned long long *> g_status_addr[kMaxDevices];
 
 int current_device_info(DeviceInfo *out)
 {
@@ -99,6 +100,18 @@ int current_device_info(DeviceInfo *out)
         return GEMM_ERR_CUDA;
     }
     if (dev < 0 || dev >= kMaxDevices) return GEMM_ERR_UNSUPPORTED_DEVICE;
+    // Driver-level calls (cuMemGetAddressRange) need the device's primary
+    // context current on this thread; a thread whose first CUDA work is this
+    // call (e.g. the autograd engine's backward thread) has none yet.
+    // cudaSetDevice initialises the primary context and makes it current.
+    thread_local int t_bound_device = -1;
+    if (t_bound_device != dev) {
+        if (cudaSetDevice(dev) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_CUDA;
+        }
+        t_bound_device = dev;
+    }
     int state = g_device_state[dev].load(std::memory_order_acquire);
     if (state == 0) {
         int major = 0, minor = 0, sms = 0;
@@ -118,28 +131,48 @@ int current_device_info(DeviceInfo *out)
     return state == 1 ? GEMM_OK : GEMM_ERR_UNSUPPORTED_DEVICE;
 }
 
+// Device address of this GPU's status word (cached per device).
+unsigned long long *status_word(int dev)
+{
+    unsigned long long *p = g_status_addr[dev].load(std::memory_order_acquire);
+    if (p) return p;
+    void *q = nullptr;
+    if (cudaGetSymbolAddress(&q, g_gemm_f16_status) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    p = static_cast<unsigned long long *>(q);
+    g_status_addr[dev].store(p, std::memory_order_release);
+    return p;
+}
+
 // ---------------------------------------------------------------- argument checks
 
 // A device buffer of `bytes` bytes starting at p: device (or managed) memory of
-// the current device, entirely inside one allocation.
-int check_device_buffer(const void *p, uint64_t bytes, int dev)
+// device `dev`, entirely inside one allocation.
+int check_device_buffer(const void *p, uint64_t bytes, int dev, uintptr_t align = 16)
 {
-    if (p == nullptr) return GEMM_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(p) & 15u) != 0) return GEMM_ERR_ALIGNMENT;
+    if (p == nullptr) return reject(GEMM_ERR_INVALID_ARG, "a buffer pointer is NULL");
+    if ((reinterpret_cast<uintptr_t>(p) & (align - 1)) != 0)
+        return reject(GEMM_ERR_ALIGNMENT, "a buffer pointer is not aligned (16 bytes for GEMM operands)");
     cudaPointerAttributes attr{};
     if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
         cudaGetLastError();
-        return GEMM_ERR_INVALID_ARG;
+        return reject(GEMM_ERR_INVALID_ARG, "cudaPointerGetAttributes failed on a buffer pointer");
     }
-    if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged) return GEMM_ERR_INVALID_ARG;
-    if (attr.type == cudaMemoryTypeDevice && attr.device != dev) return GEMM_ERR_INVALID_ARG;
+    if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+        return reject(GEMM_ERR_INVALID_ARG, "a buffer is not device or managed memory");
+    if (attr.type == cudaMemoryTypeDevice && attr.device != dev)
+        return reject(GEMM_ERR_INVALID_ARG, "a buffer lives on another device than the current one");
     const DriverFns &fns = driver();
-    if (!fns.ok) return GEMM_ERR_CUDA;
+    if (!fns.ok) return reject(GEMM_ERR_CUDA, "driver entry points unavailable");
     CUdeviceptr base = 0;
     size_t size = 0;
-    if (fns.range(&base, &size, reinterpret_cast<CUdeviceptr>(p)) != CUDA_SUCCESS) return GEMM_ERR_INVALID_ARG;
+    if (fns.range(&base, &size, reinterpret_cast<CUdeviceptr>(p)) != CUDA_SUCCESS)
+        return reject(GEMM_ERR_INVALID_ARG, "cuMemGetAddressRange does not know a buffer pointer");
     const uint64_t off = static_cast<uint64_t>(reinterpret_cast<CUdeviceptr>(p) - base);
-    if (off > size || bytes > size - off) return GEMM_ERR_INVALID_ARG;
+    if (off > size || bytes > size - off)
+        return reject(GEMM_ERR_INVALID_ARG, "a buffer is smaller than its matrix (runs past its allocation)");
     return GEMM_OK;
 }
 
@@ -151,13 +184,15 @@ bool ranges_overlap(const void *a, uint64_t abytes, const void *b, uint64_t bbyt
 
 int check_sizes(int64_t M, int64_t N, int64_t K, int relu)
 {
-    if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
-    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return GEMM_ERR_INVALID_ARG;
-    if (relu != 0 && relu != 1) return GEMM_ERR_INVALID_ARG;
+    if (M < 0 || N < 0 || K < 0) return reject(GEMM_ERR_INVALID_ARG, "a size is negative");
+    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return reject(GEMM_ERR_INVALID_ARG, "a size exceeds INT32_MAX");
+    if (relu != 0 && relu != 1) return reject(GEMM_ERR_INVALID_ARG, "relu is not 0 or 1");
     return GEMM_OK;
 }
 
-// ---------------------------------------------------------------- tensor maps
+}  // namespace
+
+namespace gemm_sm103 {
 
 // Row-major fp16 matrix rows x cols (leading dimension cols), boxes of
 // box_cols x box_rows with 128-byte swizzle; out-of-range loads read zero.
@@ -176,14 +211,22 @@ int encode_matrix(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t col
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
-// ---------------------------------------------------------------- launch
-
-uint64_t timeout_cycles_for(int64_t K)
+// Optional rasterisation panel height (in work units) for tuning sweeps.
+int group_m_override()
 {
-    // About a second of SM clocks plus a margin that grows with the K loop of
-    // one tile; a legitimate wait is at most one tile's mainloop.
-    return (1ull << 31) + 64ull * static_cast<uint64_t>(K);
+    static int v = [] {
+        const char *e = std::getenv("GEMM_F16_GROUP_M");
+        const int x = e ? std::atoi(e) : 0;
+        return x > 0 && x <= 4096 ? x : 0;
+    }();
+    return v;
 }
+
+}  // namespace gemm_sm103
+
+namespace {
+
+// ---------------------------------------------------------------- configuration choice
 
 int pick_config(int64_t M, int64_t N, int64_t K, int sm_count)
 {
@@ -203,199 +246,18 @@ int pick_config(int64_t M, int64_t N, int64_t K, int sm_count)
     return 2;
 }
 
-int group_m_override()
-{
-    static int v = [] {
-        const char *e = std::getenv("GEMM_F16_GROUP_M");
-        const int x = e ? std::atoi(e) : 0;
-        return x > 0 && x <= 4096 ? x : 0;
-    }();
-    return v;
-}
+// ---------------------------------------------------------------- launch path
 
-// Per device and kernel instance, prepared once: the dynamic shared-memory
-// attribute is set, and the number of CTAs (or CTA clusters) of this
-// configuration that can be resident at once -- one per SM, or per group of
-// SMs as the occupancy API reports for clusters -- is cached.  forget()
-// drops the entry (after a failed launch, e.g. once the context was reset).
-template <class Cfg, bool kRelu>
-struct Prepared {
-    static std::atomic<int> slots[kMaxDevices];   // 0: not prepared
-
-    static int64_t get(int dev, int sm_count)
-    {
-        int v = slots[dev].load(std::memory_order_acquire);
-        if (v > 0) return v;
-        auto kern = gemm_f16_relu_sm103a<Cfg, kRelu>;
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) !=
-            cudaSuccess) {
-            cudaGetLastError();
-            return 0;
-        }
-        v = sm_count / Cfg::CLUSTER;
-        if (Cfg::CLUSTER > 1) {
-            cudaLaunchConfig_t lc{};
-            lc.blockDim = dim3(Cfg::THREADS, 1, 1);
-            lc.dynamicSmemBytes = Cfg::SMEM_BYTES;
-            lc.gridDim = dim3(Cfg::CLUSTER * v, 1, 1);
-            cudaLaunchAttribute attrs[1];
-            attrs[0].id = cudaLaunchAttributeClusterDimension;
-            attrs[0].val.clusterDim.x = Cfg::CLUSTER;
-            attrs[0].val.clusterDim.y = 1;
-            attrs[0].val.clusterDim.z = 1;
-            lc.attrs = attrs;
-            lc.numAttrs = 1;
-            int clusters = 0;
-            if (cudaOccupancyMaxActiveClusters(&clusters, kern, &lc) == cudaSuccess && clusters > 0)
-                v = clusters < v ? clusters : v;
-            else
-                cudaGetLastError();
-        }
-        if (v > 0) slots[dev].store(v, std::memory_order_release);
-        return v;
-    }
-
-    static void forget(int dev) { slots[dev].store(0, std::memory_order_release); }
-};
-
-template <class Cfg, bool kRelu>
-std::atomic<int> Prepared<Cfg, kRelu>::slots[kMaxDevices];
-
-// Persistent schedule: full waves of tiles, then the tiles of a partly filled
-// last wave split along N into 2^shift units while the split units still fit
-// in one wave (the tail then costs 1/2^shift of a tile time).
-struct Schedule {
-    int64_t tiles = 0, units = 0, split_start = 0, grid_units = 0;
-    int shift = 0;
-};
-
-template <class Cfg>
-Schedule make_schedule(int64_t M, int64_t N, int64_t slots)
-{
-    Schedule sc;
-    sc.tiles = ((M + Cfg::SUPER_M - 1) / Cfg::SUPER_M) * ((N + Cfg::BN - 1) / Cfg::BN);
-    sc.units = sc.tiles;
-    sc.split_start = sc.tiles;
-    if (slots <= 0) return sc;
-    const int64_t full = (sc.tiles / slots) * slots;
-    const int64_t rest = sc.tiles - full;
-    // Split shift with the shortest tail: ceil(rest * 2^s / slots) / 2^s tile
-    // times (ties go to the coarser split).
-    int shift = 0;
-    double best = 1e30;
-    for (int s = 0; rest > 0 && s <= Cfg::MAX_SPLIT_LOG2; ++s) {
-        const int64_t waves = ((rest << s) + slots - 1) / slots;
-        const double t = static_cast<double>(waves) / static_cast<double>(1 << s);
-        if (t < best - 1e-9) {
-            best = t;
-            shift = s;
-        }
-    }
-    if (shift > 0) {
-        sc.shift = shift;
-        sc.split_start = full;
-        sc.units = full + (rest << shift);
-    }
-    sc.grid_units = sc.units < slots ? sc.units : slots;
-    return sc;
-}
-
-template <class Cfg>
-int fill_launch_info(int64_t M, int64_t N, const DeviceInfo &dev, int *grid_ctas, int *cluster_size, int *tiles)
-{
-    const Schedule sc = make_schedule<Cfg>(M, N, Prepared<Cfg, true>::get(dev.device, dev.sm_count));
-    if (tiles) *tiles = static_cast<int>(sc.tiles < INT32_MAX ? sc.tiles : INT32_MAX);
-    if (cluster_size) *cluster_size = Cfg::CLUSTER;
-    if (grid_ctas) *grid_ctas = static_cast<int>(sc.grid_units * Cfg::CLUSTER);
-    return GEMM_OK;
-}
-
-// Test-hook settings for a launch (all zero for normal calls).
-struct LaunchHook {
-    int producer_off = 0;          // producer issues nothing
-    uint64_t timeout_cycles = 0;   // 0: the normal budget
-};
-
-template <class Cfg, bool kRelu>
-int launch(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K, const DeviceInfo &dev,
-           cudaStream_t stream, const LaunchHook &hook = LaunchHook())
-{
-    CUtensorMap ta, tb, tc;
-    int st;
-    if ((st = encode_matrix(&ta, A, M, K, Cfg::BK, Cfg::BM)) != GEMM_OK) return st;
-    if ((st = encode_matrix(&tb, B, K, N, Cfg::B_BOX_N, Cfg::BK)) != GEMM_OK) return st;
-    if ((st = encode_matrix(&tc, C, M, N, Cfg::EPI_COLS, 32)) != GEMM_OK) return st;
-
-    GemmParams p{};
-    p.M = static_cast<int32_t>(M);
-    p.N = static_cast<int32_t>(N);
-    p.K = static_cast<int32_t>(K);
-    p.num_m_blocks = static_cast<int32_t>((M + Cfg::SUPER_M - 1) / Cfg::SUPER_M);
-    p.num_n_blocks = static_cast<int32_t>((N + Cfg::BN - 1) / Cfg::BN);
-    p.num_k_blocks = static_cast<int32_t>((K + Cfg::BK - 1) / Cfg::BK);
-    const int64_t slots = Prepared<Cfg, kRelu>::get(dev.device, dev.sm_count);
-    if (slots <= 0) return GEMM_ERR_LAUNCH;
-    const Schedule sc = make_schedule<Cfg>(M, N, slots);
-    if (sc.units > INT32_MAX / 2) return GEMM_ERR_INVALID_ARG;
-    p.num_tiles = static_cast<int32_t>(sc.tiles);
-    p.num_units = static_cast<int32_t>(sc.units);
-    p.split_start = static_cast<int32_t>(sc.split_start);
-    p.split_log2 = sc.shift;
-    // Rasterisation panels 2048 rows high whatever the tile height.
-    p.group_m = group_m_override() ? group_m_override() : (Cfg::SUPER_M >= 2048 ? 1 : 2048 / Cfg::SUPER_M);
-    p.timeout_cycles = hook.timeout_cycles ? hook.timeout_cycles : timeout_cycles_for(K);
-    p.C = static_cast<__half *>(C);
-    p.producer_off = hook.producer_off;
-
-    auto kern = gemm_f16_relu_sm103a<Cfg, kRelu>;
-    cudaLaunchConfig_t lc{};
-    lc.blockDim = dim3(Cfg::THREADS, 1, 1);
-    lc.dynamicSmemBytes = Cfg::SMEM_BYTES;
-    lc.stream = stream;
-    cudaLaunchAttribute attrs[1];
-    attrs[0].id = cudaLaunchAttributeClusterDimension;
-    attrs[0].val.clusterDim.x = Cfg::CLUSTER;
-    attrs[0].val.clusterDim.y = 1;
-    attrs[0].val.clusterDim.z = 1;
-    lc.attrs = attrs;
-    lc.numAttrs = 1;
-
-    lc.gridDim = dim3(static_cast<unsigned>(sc.grid_units * Cfg::CLUSTER), 1, 1);
-    if (cudaLaunchKernelEx(&lc, kern, ta, tb, tc, p) != cudaSuccess) {
-        cudaGetLastError();
-        // Prepare again (the attribute may have been lost) and retry once.
-        Prepared<Cfg, kRelu>::forget(dev.device);
-        if (Prepared<Cfg, kRelu>::get(dev.device, dev.sm_count) <= 0 ||
-            cudaLaunchKernelEx(&lc, kern, ta, tb, tc, p) != cudaSuccess) {
-            cudaGetLastError();
-            return GEMM_ERR_LAUNCH;
-        }
-    }
-    return GEMM_OK;
-}
-
-template <class Cfg>
-int launch_cfg(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K, int relu,
-               const DeviceInfo &dev, cudaStream_t stream, const LaunchHook &hook = LaunchHook())
-{
-    return relu ? launch<Cfg, true>(A, B, C, M, N, K, dev, stream, hook)
-                : launch<Cfg, false>(A, B, C, M, N, K, dev, stream, hook);
-}
-
-thread_local uint64_t t_last_timeout_record = 0;
-
-}  // namespace
-
-// ==================================================================== C ABI
-
-namespace {
-
-int run_gemm(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K, int relu, int config,
-             void *stream, const LaunchHook &hook)
+int run_gemm(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K, int transa, int transb,
+             int relu, int config, void *stream, const LaunchHook &hook)
 {
     int st = check_sizes(M, N, K, relu);
     if (st != GEMM_OK) return st;
-    if (config < 0 || config > kNumConfigs) return GEMM_ERR_INVALID_ARG;
+    if ((transa != 0 && transa != 1) || (transb != 0 && transb != 1))
+        return reject(GEMM_ERR_INVALID_ARG, "transa / transb is not 0 or 1");
+    if (config < 0 || config > kNumConfigs) return reject(GEMM_ERR_INVALID_ARG, "unknown configuration id");
+    if ((transa || transb) && !kConfigs[config].all_layouts)
+        return reject(GEMM_ERR_INVALID_ARG, "this configuration has no transposed-layout kernels");
     if (M == 0 || N == 0) return GEMM_OK;
 
     DeviceInfo dev;
@@ -412,49 +274,100 @@ int run_gemm(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_
         }
         return GEMM_OK;
     }
-    if ((N % 8) != 0 || (K % 8) != 0) return GEMM_ERR_ALIGNMENT;
+    // Row pitches of the stored matrices must be multiples of 16 bytes.
+    const int64_t lda = transa ? M : K, ldb = transb ? K : N;
+    if ((lda % 8) != 0 || (ldb % 8) != 0 || (N % 8) != 0)
+        return reject(GEMM_ERR_ALIGNMENT, "a row pitch (leading dimension) is not a multiple of 8 elements");
     const uint64_t a_bytes = static_cast<uint64_t>(M) * static_cast<uint64_t>(K) * 2u;
     const uint64_t b_bytes = static_cast<uint64_t>(K) * static_cast<uint64_t>(N) * 2u;
     if ((st = check_device_buffer(A, a_bytes, dev.device)) != GEMM_OK) return st;
     if ((st = check_device_buffer(B, b_bytes, dev.device)) != GEMM_OK) return st;
     if (ranges_overlap(C, c_bytes, A, a_bytes) || ranges_overlap(C, c_bytes, B, b_bytes))
-        return GEMM_ERR_INVALID_ARG;
+        return reject(GEMM_ERR_INVALID_ARG, "C overlaps A or B");
+
+    LaunchArgs a;
+    a.A = A;
+    a.B = B;
+    a.C = C;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.relu = relu;
+    a.transa = transa;
+    a.transb = transb;
+    a.dev = dev;
+    a.stream = s;
+    a.hook = hook;
+    a.status = status_word(dev.device);
+    if (a.status == nullptr) return GEMM_ERR_CUDA;
 
     const int cfg = config == 0 ? pick_config(M, N, K, dev.sm_count) : config;
     switch (cfg) {
-        case 1: return launch_cfg<Cfg1x256>(A, B, C, M, N, K, relu, dev, s, hook);
-        case 2: return launch_cfg<Cfg1x128>(A, B, C, M, N, K, relu, dev, s, hook);
-        case 3: return launch_cfg<Cfg2x256>(A, B, C, M, N, K, relu, dev, s, hook);
-        case 4: return launch_cfg<Cfg2x256d>(A, B, C, M, N, K, relu, dev, s, hook);
-        case 5: return launch_cfg<Cfg2x512>(A, B, C, M, N, K, relu, dev, s, hook);
-        case 6: return launch_cfg<Cfg4x256mc>(A, B, C, M, N, K, relu, dev, s, hook);
+        case 1: return launch_config_1(a);
+        case 2: return launch_config_2(a);
+        case 3: return launch_config_3(a);
+        case 4: return launch_config_4(a);
+        case 5: return launch_config_5(a);
+        case 6: return launch_config_6(a);
         default: return GEMM_ERR_INVALID_ARG;
     }
 }
 
+thread_local uint64_t t_last_timeout_record = 0;
+
 }  // namespace
+
+// ==================================================================== C ABI
+
+extern "C" int gemm_f16_tx(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K, int transa,
+                           int transb, int relu, int config, void *stream)
+{
+    return run_gemm(A, B, C, M, N, K, transa, transb, relu, config, stream, LaunchHook());
+}
 
 extern "C" int gemm_f16_ex(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K, int relu,
                            int config, void *stream)
 {
-    return run_gemm(A, B, C, M, N, K, relu, config, stream, LaunchHook());
-}
-
-extern "C" int gemm_f16_selftest_timeout(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
-                                         int config, uint64_t timeout_cycles, void *stream)
-{
-    if (K == 0 || M == 0 || N == 0) return GEMM_ERR_INVALID_ARG;   // nothing would be launched
-    if (timeout_cycles < (1ull << 16) || timeout_cycles > (1ull << 32)) return GEMM_ERR_INVALID_ARG;
-    LaunchHook hook;
-    hook.producer_off = 1;
-    hook.timeout_cycles = timeout_cycles;
-    return run_gemm(A, B, C, M, N, K, 1, config, stream, hook);
+    return run_gemm(A, B, C, M, N, K, 0, 0, relu, config, stream, LaunchHook());
 }
 
 extern "C" int gemm_f16(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K, int relu,
                         void *stream)
 {
-    return gemm_f16_ex(A, B, C, M, N, K, relu, 0, stream);
+    return run_gemm(A, B, C, M, N, K, 0, 0, relu, 0, stream, LaunchHook());
+}
+
+extern "C" int gemm_f16_selftest_timeout(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
+                                         int config, uint64_t timeout_cycles, void *stream)
+{
+    if (K == 0 || M == 0 || N == 0) return reject(GEMM_ERR_INVALID_ARG, "an empty problem launches no kernel");
+    if (timeout_cycles < (1ull << 16) || timeout_cycles > (1ull << 32))
+        return reject(GEMM_ERR_INVALID_ARG, "timeout_cycles outside 2^16 .. 2^32");
+    LaunchHook hook;
+    hook.producer_off = 1;
+    hook.timeout_cycles = timeout_cycles;
+    return run_gemm(A, B, C, M, N, K, 0, 0, 1, config, stream, hook);
+}
+
+namespace gemm_sm103 {
+int relu_backward_launch(const void *dC, const void *C, void *dZ, int64_t n, int sm_count, cudaStream_t stream);
+}
+
+extern "C" int gemm_f16_relu_backward(const void *dC, const void *C, void *dZ, int64_t n, void *stream)
+{
+    if (n < 0) return reject(GEMM_ERR_INVALID_ARG, "n is negative");
+    if (n == 0) return GEMM_OK;
+    DeviceInfo dev;
+    int st = current_device_info(&dev);
+    if (st != GEMM_OK) return st;
+    const uint64_t bytes = static_cast<uint64_t>(n) * 2u;
+    if ((st = check_device_buffer(dC, bytes, dev.device, 2)) != GEMM_OK) return st;
+    if ((st = check_device_buffer(C, bytes, dev.device, 2)) != GEMM_OK) return st;
+    if ((st = check_device_buffer(dZ, bytes, dev.device, 2)) != GEMM_OK) return st;
+    // In place over dC (or C) is fine element by element; a partial overlap is not.
+    if ((dZ != dC && ranges_overlap(dZ, bytes, dC, bytes)) || (dZ != C && ranges_overlap(dZ, bytes, C, bytes)))
+        return reject(GEMM_ERR_INVALID_ARG, "dZ partly overlaps dC or C");
+    return relu_backward_launch(dC, C, dZ, n, dev.sm_count, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int gemm_f16_num_configs(void) { return kNumConfigs; }
@@ -463,6 +376,12 @@ extern "C" const char *gemm_f16_config_name(int config)
 {
     if (config < 0 || config > kNumConfigs) return nullptr;
     return kConfigs[config].name;
+}
+
+extern "C" int gemm_f16_config_layouts(int config)
+{
+    if (config < 0 || config > kNumConfigs) return reject(GEMM_ERR_INVALID_ARG, "unknown configuration id");
+    return kConfigs[config].all_layouts ? 0xF : 0x1;
 }
 
 extern "C" int gemm_f16_auto_config(int64_t M, int64_t N, int64_t K)
@@ -479,17 +398,17 @@ extern "C" int gemm_f16_launch_info(int64_t M, int64_t N, int64_t K, int config,
 {
     int st = check_sizes(M, N, K, 0);
     if (st != GEMM_OK) return st;
-    if (config < 0 || config > kNumConfigs) return GEMM_ERR_INVALID_ARG;
+    if (config < 0 || config > kNumConfigs) return reject(GEMM_ERR_INVALID_ARG, "unknown configuration id");
     DeviceInfo dev;
     if ((st = current_device_info(&dev)) != GEMM_OK) return st;
     const int cfg = config == 0 ? pick_config(M, N, K, dev.sm_count) : config;
     switch (cfg) {
-        case 1: return fill_launch_info<Cfg1x256>(M, N, dev, grid_ctas, cluster_size, tiles);
-        case 2: return fill_launch_info<Cfg1x128>(M, N, dev, grid_ctas, cluster_size, tiles);
-        case 3: return fill_launch_info<Cfg2x256>(M, N, dev, grid_ctas, cluster_size, tiles);
-        case 4: return fill_launch_info<Cfg2x256d>(M, N, dev, grid_ctas, cluster_size, tiles);
-        case 5: return fill_launch_info<Cfg2x512>(M, N, dev, grid_ctas, cluster_size, tiles);
-        case 6: return fill_launch_info<Cfg4x256mc>(M, N, dev, grid_ctas, cluster_size, tiles);
+        case 1: return launch_info_config_1(M, N, dev, grid_ctas, cluster_size, tiles);
+        case 2: return launch_info_config_2(M, N, dev, grid_ctas, cluster_size, tiles);
+        case 3: return launch_info_config_3(M, N, dev, grid_ctas, cluster_size, tiles);
+        case 4: return launch_info_config_4(M, N, dev, grid_ctas, cluster_size, tiles);
+        case 5: return launch_info_config_5(M, N, dev, grid_ctas, cluster_size, tiles);
+        case 6: return launch_info_config_6(M, N, dev, grid_ctas, cluster_size, tiles);
         default: return GEMM_ERR_INVALID_ARG;
     }
 }
@@ -500,7 +419,8 @@ extern "C" int gemm_f16_from_host(const void *A_host, const void *B_host, void *
     int st = check_sizes(M, N, K, relu);
     if (st != GEMM_OK) return st;
     if (M == 0 || N == 0) return GEMM_OK;
-    if (C_host == nullptr || (K > 0 && (A_host == nullptr || B_host == nullptr))) return GEMM_ERR_INVALID_ARG;
+    if (C_host == nullptr || (K > 0 && (A_host == nullptr || B_host == nullptr)))
+        return reject(GEMM_ERR_INVALID_ARG, "a host buffer pointer is NULL");
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     const size_t a_bytes = static_cast<size_t>(M) * static_cast<size_t>(K) * 2u;
     const size_t b_bytes = static_cast<size_t>(K) * static_cast<size_t>(N) * 2u;
@@ -509,7 +429,8 @@ extern "C" int gemm_f16_from_host(const void *A_host, const void *B_host, void *
         // Validate the device side before any copy is enqueued.
         DeviceInfo dev;
         if ((st = current_device_info(&dev)) != GEMM_OK) return st;
-        if ((N % 8) != 0 || (K % 8) != 0) return GEMM_ERR_ALIGNMENT;
+        if ((N % 8) != 0 || (K % 8) != 0)
+            return reject(GEMM_ERR_ALIGNMENT, "a row pitch (leading dimension) is not a multiple of 8 elements");
         if ((st = check_device_buffer(A_dev, a_bytes, dev.device)) != GEMM_OK) return st;
         if ((st = check_device_buffer(B_dev, b_bytes, dev.device)) != GEMM_OK) return st;
         if ((st = check_device_buffer(C_dev, c_bytes, dev.device)) != GEMM_OK) return st;
@@ -552,12 +473,14 @@ extern "C" int gemm_f16_check(void *stream)
 
 extern "C" uint64_t gemm_f16_last_timeout_record(void) { return t_last_timeout_record; }
 
+extern "C" const char *gemm_f16_last_error_detail(void) { return t_last_detail; }
+
 extern "C" const char *gemm_f16_strerror(int status)
 {
     switch (status) {
         case GEMM_OK: return "success";
         case GEMM_ERR_INVALID_ARG: return "invalid argument";
-        case GEMM_ERR_ALIGNMENT: return "misaligned pointer, or N or K not a multiple of 8";
+        case GEMM_ERR_ALIGNMENT: return "misaligned pointer, or a row pitch not a multiple of 8 elements";
         case GEMM_ERR_UNSUPPORTED_DEVICE: return "current device is not compute capability 10.3 (GB300)";
         case GEMM_ERR_LAUNCH: return "kernel launch failed";
         case GEMM_ERR_TIMEOUT: return "a kernel wait exceeded its limit; the output is incomplete";

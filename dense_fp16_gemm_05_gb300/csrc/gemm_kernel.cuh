@@ -68,6 +68,7 @@ struct GemmParams {
     __half *C;              // output base (used by the direct-store epilogue)
     int32_t producer_off;   // test hook: 1 = the producer issues nothing, so the
                             // MMA thread's first wait runs out (see gemm_f16_selftest_timeout)
+    unsigned long long *status;   // device status word of this GPU (first timeout record)
 };
 
 // Where a bounded wait expired (bits 0-7 of the status word).
@@ -139,13 +140,11 @@ struct GemmCfg {
     static_assert(SMEM_BYTES <= 232448, "shared memory per block on sm_103");
 };
 
-// Device status word: 0 = fine; otherwise the first timeout record.
-__device__ unsigned long long g_gemm_f16_status;
-
 // Abort flag of this CTA.  In a cluster, raising it also raises the flag (at
 // the same shared-memory offset) of every other CTA of the cluster.
 struct AbortFlag {
     volatile int *local;
+    unsigned long long *status;   // device status word
     uint32_t addr;          // shared::cta address of the flag
     uint32_t cluster;       // CTAs in the cluster
     uint32_t rank;          // this CTA's rank in the cluster
@@ -156,7 +155,7 @@ struct AbortFlag {
         *local = 1;
         for (uint32_t i = 0; i < cluster; ++i)
             if (i != rank) st_shared_cluster_u32(mapa_shared(addr, i), 1u);
-        atomicCAS(&g_gemm_f16_status, 0ull,
+        atomicCAS(status, 0ull,
                   static_cast<unsigned long long>(site) | (static_cast<unsigned long long>(blockIdx.x) << 8));
     }
 };
@@ -188,12 +187,13 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const 
 }
 
 // Bounded wait used while tearing down after an abort: ignores the abort flag.
-__device__ __forceinline__ bool wait_phase_drain(uint32_t bar, uint32_t parity, uint64_t limit, uint32_t site)
+__device__ __forceinline__ bool wait_phase_drain(uint32_t bar, uint32_t parity, uint64_t limit, uint32_t site,
+                                                 unsigned long long *status)
 {
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity)) {
         if (static_cast<uint64_t>(clock64() - t0) > limit) {
-            atomicCAS(&g_gemm_f16_status, 0ull,
+            atomicCAS(status, 0ull,
                       static_cast<unsigned long long>(site) | (static_cast<unsigned long long>(blockIdx.x) << 8));
             return false;
         }
@@ -260,12 +260,23 @@ __device__ __forceinline__ uint32_t pack_f16x2(uint32_t lo_bits, uint32_t hi_bit
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-template <class Cfg, bool kRelu>
+// Operand layouts (the transpose_A / transpose_B of the pages' tile GEMM):
+//   kTA = false: A stored (M,K) row-major (K-major);  true: stored (K,M) row-major,
+//                op(A) = stored^T (M-major; TMA boxes 64(M) x 64(K), two per stage).
+//   kTB = false: B stored (K,N) row-major (N-major);  true: stored (N,K) row-major,
+//                op(B) = stored^T (K-major; TMA boxes 64(K) x 64(N rows)).
+// Shared-memory offsets of every box are the same in all four layouts; only the
+// tensor-map orientation, the box coordinates and the descriptor type change.
+template <class Cfg, bool kRelu, bool kTA = false, bool kTB = false>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
     gemm_f16_relu_sm103a(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                          const __grid_constant__ CUtensorMap tmap_c, const GemmParams p)
 {
     constexpr bool kPair = Cfg::CTA_GROUP == 2;
+    // Instruction descriptor with this kernel's operand majors (bit 15: A MN-major,
+    // bit 16: B MN-major).
+    constexpr uint32_t kIdesc = (Cfg::IDESC & ~((1u << 15) | (1u << 16))) | (kTA ? (1u << 15) : 0u) |
+                                (kTB ? 0u : (1u << 16));
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
@@ -303,6 +314,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 
     AbortFlag abort;
     abort.local = reinterpret_cast<volatile int *>(tmem_slot_ptr + 1);
+    abort.status = p.status;
     abort.addr = abort_addr;
     abort.cluster = Cfg::CLUSTER;
     abort.rank = crank;
@@ -373,26 +385,39 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     const uint32_t b_dst = sB + s * Cfg::B_STAGE_BYTES;
                     if constexpr (!kPair) {
                         mbar_arrive_expect_tx(full_bar(s), tx);
-                        tma_load_2d(a_dst, &tmap_a, full_bar(s), k0, m0);
-                        for (int j = 0; j < boxes; ++j)
-                            tma_load_2d(b_dst + j * Cfg::B_BOX_BYTES, &tmap_b, full_bar(s),
-                                        n_cta + (j / bpm) * umma_n + (j % bpm) * Cfg::B_BOX_N, k0);
+                        if constexpr (!kTA) {
+                            tma_load_2d(a_dst, &tmap_a, full_bar(s), k0, m0);
+                        } else {
+                            tma_load_2d(a_dst, &tmap_a, full_bar(s), m0, k0);
+                            tma_load_2d(a_dst + Cfg::A_STAGE_BYTES / 2, &tmap_a, full_bar(s), m0 + 64, k0);
+                        }
+                        for (int j = 0; j < boxes; ++j) {
+                            const int x = n_cta + (j / bpm) * umma_n + (j % bpm) * Cfg::B_BOX_N;
+                            if constexpr (!kTB) tma_load_2d(b_dst + j * Cfg::B_BOX_BYTES, &tmap_b, full_bar(s), x, k0);
+                            else tma_load_2d(b_dst + j * Cfg::B_BOX_BYTES, &tmap_b, full_bar(s), k0, x);
+                        }
                     } else {
                         // The bytes landing in both CTAs of a pair are counted on the
                         // pair leader's barrier; each CTA announces its own bytes.
                         const uint32_t fb = leader ? full_bar(s) : mapa_shared(full_bar(s), leader_rank);
                         if (leader) mbar_arrive_expect_tx(fb, tx);
                         else mbar_arrive_expect_tx_cluster(fb, tx);
-                        tma_load_2d_pair(a_dst, &tmap_a, fb, k0, m0);
+                        if constexpr (!kTA) {
+                            tma_load_2d_pair(a_dst, &tmap_a, fb, k0, m0);
+                        } else {
+                            tma_load_2d_pair(a_dst, &tmap_a, fb, m0, k0);
+                            tma_load_2d_pair(a_dst + Cfg::A_STAGE_BYTES / 2, &tmap_a, fb, m0 + 64, k0);
+                        }
                         for (int j = 0; j < boxes; ++j) {
                             const int x = n_cta + (j / bpm) * umma_n + (j % bpm) * Cfg::B_BOX_N;
+                            const int bx = kTB ? k0 : x, by = kTB ? x : k0;
                             if constexpr (Cfg::PAIRS == 1) {
-                                tma_load_2d_pair(b_dst + j * Cfg::B_BOX_BYTES, &tmap_b, fb, x, k0);
+                                tma_load_2d_pair(b_dst + j * Cfg::B_BOX_BYTES, &tmap_b, fb, bx, by);
                             } else {
                                 // Box j is loaded by pair j % PAIRS and multicast to the
                                 // same-half CTA of every pair.
                                 if (j % Cfg::PAIRS == static_cast<int>(pair))
-                                    tma_load_2d_pair_mc(b_dst + j * Cfg::B_BOX_BYTES, &tmap_b, fb, x, k0,
+                                    tma_load_2d_pair_mc(b_dst + j * Cfg::B_BOX_BYTES, &tmap_b, fb, bx, by,
                                                         same_half_mask);
                             }
                         }
@@ -411,7 +436,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     // Let the loads in flight land before the CTA exits.
                     for (int i = 0; i < Cfg::STAGES; ++i)
                         if (issued_mask & (1u << i))
-                            wait_phase_drain(full_bar(i), (issued_parity >> i) & 1u, limit, kSiteDrainLoads);
+                            wait_phase_drain(full_bar(i), (issued_parity >> i) & 1u, limit, kSiteDrainLoads, p.status);
                 } else {
                     // This CTA's loads complete on the leader's barrier, which it
                     // cannot probe: give them a bounded time (~1e6 cycles) to land.
@@ -430,8 +455,14 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             int it = 0;
             bool ok = true, issued_any = false;
             // Stage-0 descriptors; every other operand address is a constant offset.
-            const uint64_t a_desc0 = smem_desc_sw128(sA, 16, 1024);
-            const uint64_t b_desc0 = smem_desc_sw128(sB, Cfg::B_BOX_BYTES, 1024);
+            // K-major operand: 8-row groups 1024 B apart (SBO); a K step of 16
+            // elements is 32 B inside the 128-byte swizzle row.  MN-major operand:
+            // 64-element boxes B_BOX_BYTES apart (LBO), 8-row K groups 1024 B
+            // apart (SBO); a K step of 16 rows is 16 * 128 B.
+            const uint64_t a_desc0 = kTA ? smem_desc_sw128(sA, Cfg::B_BOX_BYTES, 1024) : smem_desc_sw128(sA, 16, 1024);
+            const uint64_t b_desc0 = kTB ? smem_desc_sw128(sB, 16, 1024) : smem_desc_sw128(sB, Cfg::B_BOX_BYTES, 1024);
+            constexpr uint32_t kAStep = kTA ? Cfg::UMMA_K * 128 : Cfg::UMMA_K * 2;   // bytes per K step
+            constexpr uint32_t kBStep = kTB ? Cfg::UMMA_K * 2 : Cfg::UMMA_K * 128;
             for (int u = cluster_id; ok && u < p.num_units; u += num_clusters, ++it) {
                 const int b = it % Cfg::ACC_STAGES;
                 const uint32_t acc_ph = (it / Cfg::ACC_STAGES) & 1;
@@ -443,7 +474,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                                            Cfg::B_BOX_BYTES;
                 // The MMA's N field (bits 17-22, N >> 3) for this unit's width.
                 const uint32_t idesc =
-                    (Cfg::IDESC & ~(0x3Fu << 17)) | (static_cast<uint32_t>(umma_n >> 3) << 17);
+                    (kIdesc & ~(0x3Fu << 17)) | (static_cast<uint32_t>(umma_n >> 3) << 17);
                 if (!wait_phase(tempty_bar(b), acc_ph ^ 1u, abort, limit, kSiteMmaTmemEmpty)) {
                     ok = false;
                     break;
@@ -464,17 +495,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     const uint32_t acc0 = kb != 0 ? 1u : 0u;
 #pragma unroll
                     for (int ks = 0; ks < Cfg::BK / Cfg::UMMA_K; ++ks) {
-                        // A: K-major, 8-row groups 1024 B apart; a K step of 16
-                        // elements is 32 B inside the 128-byte swizzle row.
-                        const uint64_t a_desc = a_st + static_cast<uint64_t>((ks * Cfg::UMMA_K * 2) >> 4);
+                        const uint64_t a_desc = a_st + static_cast<uint64_t>((ks * kAStep) >> 4);
 #pragma unroll
                         for (int h = 0; h < Cfg::N_MMAS; ++h) {
                             if (h >= n_mmas) break;
-                            // B: N-major; 64-column boxes B_BOX_BYTES apart (LBO),
-                            // 8-row K groups 1024 B apart (SBO); a K step of 16 rows
-                            // is 16 * 128 B; MMA h starts at its own boxes.
-                            const uint64_t b_desc =
-                                b_st + static_cast<uint64_t>((h * bpm_bytes + ks * Cfg::UMMA_K * 128) >> 4);
+                            // MMA h starts at its own B boxes.
+                            const uint64_t b_desc = b_st + static_cast<uint64_t>((h * bpm_bytes + ks * kBStep) >> 4);
                             mma_f16_ss<Cfg::CTA_GROUP>(d_tmem + h * umma_n, a_desc, b_desc, idesc,
                                                        ks != 0 ? 1u : acc0);
                         }
@@ -501,7 +527,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     // Wait for this thread's MMAs before the TMEM is freed.
                     if constexpr (kPair) mma_commit_pair_mc(drain_bar, static_cast<uint16_t>(1u << crank));
                     else mma_commit(drain_bar);
-                    wait_phase_drain(drain_bar, 0, limit, kSiteDrainMma);
+                    wait_phase_drain(drain_bar, 0, limit, kSiteDrainMma, p.status);
                 }
             }
         }

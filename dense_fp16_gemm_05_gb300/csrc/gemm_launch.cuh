@@ -1,0 +1,263 @@
+// gemm_launch.cuh -- host-side launch machinery shared by the per-configuration
+// translation units (gemm_cfg_*.cu) and the C ABI (gemm_f16.cu): the persistent
+// schedule, the per-device preparation cache, tensor-map encoding and the
+// templated launch of gemm_f16_relu_sm103a.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+
+#include "gemm_f16.h"
+#include "gemm_kernel.cuh"
+
+namespace gemm_sm103 {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    int device = 0;
+    int supported = 0;      // compute capability 10.3
+    int sm_count = 0;
+};
+
+// Test-hook settings for a launch (all zero for normal calls).
+struct LaunchHook {
+    int producer_off = 0;          // producer issues nothing
+    uint64_t timeout_cycles = 0;   // 0: the normal budget
+};
+
+// Everything one launch needs, already validated by the C ABI.
+struct LaunchArgs {
+    const void *A = nullptr;
+    const void *B = nullptr;
+    void *C = nullptr;
+    int64_t M = 0, N = 0, K = 0;
+    int relu = 1;
+    int transa = 0;        // 1: A stored (K,M) row-major, op(A) = stored^T
+    int transb = 0;        // 1: B stored (N,K) row-major, op(B) = stored^T
+    DeviceInfo dev;
+    cudaStream_t stream = nullptr;
+    LaunchHook hook;
+    unsigned long long *status = nullptr;   // device status word of this GPU
+};
+
+// Defined in gemm_f16.cu.
+int encode_matrix(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t cols, uint32_t box_cols,
+                  uint32_t box_rows);
+int group_m_override();
+
+inline uint64_t timeout_cycles_for(int64_t K)
+{
+    // About a second of SM clocks plus a margin that grows with the K loop of
+    // one tile; a legitimate wait is at most one tile's mainloop.
+    return (1ull << 31) + 64ull * static_cast<uint64_t>(K);
+}
+
+// Per device and kernel instance, prepared once: the dynamic shared-memory
+// attribute is set, and the number of CTAs (or CTA clusters) of this
+// configuration that can be resident at once -- one per SM, or per group of
+// SMs as the occupancy API reports for clusters -- is cached.  forget()
+// drops the entry (after a failed launch, e.g. once the context was reset).
+template <class Cfg, bool kRelu, bool kTA, bool kTB>
+struct Prepared {
+    static std::atomic<int> slots[kMaxDevices];   // 0: not prepared
+
+    static int64_t get(int dev, int sm_count)
+    {
+        int v = slots[dev].load(std::memory_order_acquire);
+        if (v > 0) return v;
+        auto kern = gemm_f16_relu_sm103a<Cfg, kRelu, kTA, kTB>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        v = sm_count / Cfg::CLUSTER;
+        if (Cfg::CLUSTER > 1) {
+            cudaLaunchConfig_t lc{};
+            lc.blockDim = dim3(Cfg::THREADS, 1, 1);
+            lc.dynamicSmemBytes = Cfg::SMEM_BYTES;
+            lc.gridDim = dim3(Cfg::CLUSTER * v, 1, 1);
+            cudaLaunchAttribute attrs[1];
+            attrs[0].id = cudaLaunchAttributeClusterDimension;
+            attrs[0].val.clusterDim.x = Cfg::CLUSTER;
+            attrs[0].val.clusterDim.y = 1;
+            attrs[0].val.clusterDim.z = 1;
+            lc.attrs = attrs;
+            lc.numAttrs = 1;
+            int clusters = 0;
+            if (cudaOccupancyMaxActiveClusters(&clusters, kern, &lc) == cudaSuccess && clusters > 0)
+                v = clusters < v ? clusters : v;
+            else
+                cudaGetLastError();
+        }
+        if (v > 0) slots[dev].store(v, std::memory_order_release);
+        return v;
+    }
+
+    static void forget(int dev) { slots[dev].store(0, std::memory_order_release); }
+};
+
+template <class Cfg, bool kRelu, bool kTA, bool kTB>
+std::atomic<int> Prepared<Cfg, kRelu, kTA, kTB>::slots[kMaxDevices];
+
+// Persistent schedule: full waves of work units, then the tiles of a partly
+// filled last wave split along N into 2^shift units, with the shift that gives
+// the shortest tail.
+struct Schedule {
+    int64_t tiles = 0, units = 0, split_start = 0, grid_units = 0;
+    int shift = 0;
+};
+
+template <class Cfg>
+Schedule make_schedule(int64_t M, int64_t N, int64_t slots)
+{
+    Schedule sc;
+    sc.tiles = ((M + Cfg::SUPER_M - 1) / Cfg::SUPER_M) * ((N + Cfg::BN - 1) / Cfg::BN);
+    sc.units = sc.tiles;
+    sc.split_start = sc.tiles;
+    if (slots <= 0) return sc;
+    const int64_t full = (sc.tiles / slots) * slots;
+    const int64_t rest = sc.tiles - full;
+    // Tail time of split shift s: ceil(rest * 2^s / slots) / 2^s tile times
+    // (ties go to the coarser split).
+    int shift = 0;
+    double best = 1e30;
+    for (int s = 0; rest > 0 && s <= Cfg::MAX_SPLIT_LOG2; ++s) {
+        const int64_t waves = ((rest << s) + slots - 1) / slots;
+        const double t = static_cast<double>(waves) / static_cast<double>(1 << s);
+        if (t < best - 1e-9) {
+            best = t;
+            shift = s;
+        }
+    }
+    if (shift > 0) {
+        sc.shift = shift;
+        sc.split_start = full;
+        sc.units = full + (rest << shift);
+    }
+    sc.grid_units = sc.units < slots ? sc.units : slots;
+    return sc;
+}
+
+template <class Cfg, bool kRelu, bool kTA, bool kTB>
+int launch_one(const LaunchArgs &a)
+{
+    CUtensorMap ta, tb, tc;
+    int st;
+    // A: (M,K) with boxes 64(K) x 128(M), or stored (K,M) with boxes 64(M) x 64(K).
+    st = kTA ? encode_matrix(&ta, a.A, a.K, a.M, 64, 64) : encode_matrix(&ta, a.A, a.M, a.K, Cfg::BK, Cfg::BM);
+    if (st != GEMM_OK) return st;
+    // B: (K,N) with boxes 64(N) x 64(K), or stored (N,K) with boxes 64(K) x 64(N).
+    st = kTB ? encode_matrix(&tb, a.B, a.N, a.K, Cfg::BK, Cfg::B_BOX_N)
+             : encode_matrix(&tb, a.B, a.K, a.N, Cfg::B_BOX_N, Cfg::BK);
+    if (st != GEMM_OK) return st;
+    if ((st = encode_matrix(&tc, a.C, a.M, a.N, Cfg::EPI_COLS, 32)) != GEMM_OK) return st;
+
+    GemmParams p{};
+    p.M = static_cast<int32_t>(a.M);
+    p.N = static_cast<int32_t>(a.N);
+    p.K = static_cast<int32_t>(a.K);
+    p.num_m_blocks = static_cast<int32_t>((a.M + Cfg::SUPER_M - 1) / Cfg::SUPER_M);
+    p.num_n_blocks = static_cast<int32_t>((a.N + Cfg::BN - 1) / Cfg::BN);
+    p.num_k_blocks = static_cast<int32_t>((a.K + Cfg::BK - 1) / Cfg::BK);
+    using Prep = Prepared<Cfg, kRelu, kTA, kTB>;
+    const int64_t slots = Prep::get(a.dev.device, a.dev.sm_count);
+    if (slots <= 0) return GEMM_ERR_LAUNCH;
+    const Schedule sc = make_schedule<Cfg>(a.M, a.N, slots);
+    if (sc.units > INT32_MAX / 2) return GEMM_ERR_INVALID_ARG;
+    p.num_tiles = static_cast<int32_t>(sc.tiles);
+    p.num_units = static_cast<int32_t>(sc.units);
+    p.split_start = static_cast<int32_t>(sc.split_start);
+    p.split_log2 = sc.shift;
+    // Rasterisation panels 2048 rows high whatever the tile height.
+    p.group_m = group_m_override() ? group_m_override() : (Cfg::SUPER_M >= 2048 ? 1 : 2048 / Cfg::SUPER_M);
+    p.timeout_cycles = a.hook.timeout_cycles ? a.hook.timeout_cycles : timeout_cycles_for(a.K);
+    p.C = static_cast<__half *>(a.C);
+    p.producer_off = a.hook.producer_off;
+    p.status = a.status;
+
+    auto kern = gemm_f16_relu_sm103a<Cfg, kRelu, kTA, kTB>;
+    cudaLaunchConfig_t lc{};
+    lc.blockDim = dim3(Cfg::THREADS, 1, 1);
+    lc.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    lc.stream = a.stream;
+    cudaLaunchAttribute attrs[1];
+    attrs[0].id = cudaLaunchAttributeClusterDimension;
+    attrs[0].val.clusterDim.x = Cfg::CLUSTER;
+    attrs[0].val.clusterDim.y = 1;
+    attrs[0].val.clusterDim.z = 1;
+    lc.attrs = attrs;
+    lc.numAttrs = 1;
+    lc.gridDim = dim3(static_cast<unsigned>(sc.grid_units * Cfg::CLUSTER), 1, 1);
+    if (cudaLaunchKernelEx(&lc, kern, ta, tb, tc, p) != cudaSuccess) {
+        cudaGetLastError();
+        // Prepare again (the attribute may have been lost) and retry once.
+        Prep::forget(a.dev.device);
+        if (Prep::get(a.dev.device, a.dev.sm_count) <= 0 || cudaLaunchKernelEx(&lc, kern, ta, tb, tc, p) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_LAUNCH;
+        }
+    }
+    return GEMM_OK;
+}
+
+// Dispatch over ReLU and the operand layouts this configuration supports.
+template <class Cfg, bool kAllLayouts>
+int launch_config(const LaunchArgs &a)
+{
+    const int layout = (a.transa ? 2 : 0) | (a.transb ? 1 : 0);
+    if (!kAllLayouts && layout != 0) return GEMM_ERR_INVALID_ARG;
+    if constexpr (kAllLayouts) {
+        switch (layout | (a.relu ? 4 : 0)) {
+            case 0: return launch_one<Cfg, false, false, false>(a);
+            case 1: return launch_one<Cfg, false, false, true>(a);
+            case 2: return launch_one<Cfg, false, true, false>(a);
+            case 3: return launch_one<Cfg, false, true, true>(a);
+            case 4: return launch_one<Cfg, true, false, false>(a);
+            case 5: return launch_one<Cfg, true, false, true>(a);
+            case 6: return launch_one<Cfg, true, true, false>(a);
+            default: return launch_one<Cfg, true, true, true>(a);
+        }
+    } else {
+        return a.relu ? launch_one<Cfg, true, false, false>(a) : launch_one<Cfg, false, false, false>(a);
+    }
+}
+
+// Launch geometry of a configuration (no launch).
+template <class Cfg>
+int config_launch_info(int64_t M, int64_t N, const DeviceInfo &dev, int *grid_ctas, int *cluster_size, int *tiles)
+{
+    const Schedule sc = make_schedule<Cfg>(M, N, Prepared<Cfg, true, false, false>::get(dev.device, dev.sm_count));
+    if (tiles) *tiles = static_cast<int>(sc.tiles < INT32_MAX ? sc.tiles : INT32_MAX);
+    if (cluster_size) *cluster_size = Cfg::CLUSTER;
+    if (grid_ctas) *grid_ctas = static_cast<int>(sc.grid_units * Cfg::CLUSTER);
+    return GEMM_OK;
+}
+
+// One pair of entry points per configuration, each defined in its own
+// translation unit (gemm_cfg_<id>.cu) so that they compile in parallel.
+#define GEMM_DECLARE_CONFIG(ID)                                                                              \
+    int launch_config_##ID(const LaunchArgs &a);                                                             \
+    int launch_info_config_##ID(int64_t M, int64_t N, const DeviceInfo &dev, int *grid_ctas, int *cluster_size, \
+                                int *tiles);
+GEMM_DECLARE_CONFIG(1)
+GEMM_DECLARE_CONFIG(2)
+GEMM_DECLARE_CONFIG(3)
+GEMM_DECLARE_CONFIG(4)
+GEMM_DECLARE_CONFIG(5)
+GEMM_DECLARE_CONFIG(6)
+#undef GEMM_DECLARE_CONFIG
+
+// The configurations, by id (1-based).
+using Cfg1x256 = GemmCfg<1, 256, 4>;
+using Cfg1x128 = GemmCfg<1, 128, 6>;
+using Cfg2x256 = GemmCfg<2, 256, 6>;
+using Cfg2x256d = GemmCfg<2, 256, 7, /*stage C in smem*/ false>;
+using Cfg2x512 = GemmCfg<2, 512, 4>;
+using Cfg4x256mc = GemmCfg<2, 256, 6, /*stage C in smem*/ true, /*pairs sharing B*/ 2>;
+
+}  // namespace gemm_sm103

@@ -34,7 +34,14 @@ class LibraryNotBuilt(RuntimeError):
 class GemmError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
-        super().__init__(f"{what}: status {status} ({strerror(status)})")
+        detail = ""
+        if status in (GEMM_ERR_INVALID_ARG, GEMM_ERR_ALIGNMENT):
+            try:
+                detail = lib().gemm_f16_last_error_detail().decode()
+            except LibraryNotBuilt:
+                pass
+        self.detail = detail
+        super().__init__(f"{what}: status {status} ({strerror(status)})" + (f": {detail}" if detail else ""))
 
 
 _lib = None
@@ -60,6 +67,8 @@ def lib() -> ctypes.CDLL:
     L.gemm_f16_check.restype = ci
     L.gemm_f16_last_timeout_record.argtypes = []
     L.gemm_f16_last_timeout_record.restype = ctypes.c_uint64
+    L.gemm_f16_last_error_detail.argtypes = []
+    L.gemm_f16_last_error_detail.restype = ctypes.c_char_p
     L.gemm_f16_strerror.argtypes = [ci]
     L.gemm_f16_strerror.restype = ctypes.c_char_p
     L.gemm_f16_version.argtypes = []
@@ -70,6 +79,12 @@ def lib() -> ctypes.CDLL:
     L.gemm_f16_config_name.restype = ctypes.c_char_p
     L.gemm_f16_auto_config.argtypes = [i64, i64, i64]
     L.gemm_f16_auto_config.restype = ci
+    L.gemm_f16_tx.argtypes = [vp, vp, vp, i64, i64, i64, ci, ci, ci, ci, vp]
+    L.gemm_f16_tx.restype = ci
+    L.gemm_f16_relu_backward.argtypes = [vp, vp, vp, i64, vp]
+    L.gemm_f16_relu_backward.restype = ci
+    L.gemm_f16_config_layouts.argtypes = [ci]
+    L.gemm_f16_config_layouts.restype = ci
     L.gemm_f16_selftest_timeout.argtypes = [vp, vp, vp, i64, i64, i64, ci, ctypes.c_uint64, vp]
     L.gemm_f16_selftest_timeout.restype = ci
     pi = ctypes.POINTER(ctypes.c_int)
@@ -149,6 +164,54 @@ def gemm_f16(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None, re
     if st != GEMM_OK:
         raise GemmError(st, "gemm_f16")
     return C
+
+
+def gemm_f16_t(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None, transa: bool = False,
+               transb: bool = False, relu: bool = True, stream=None, config: int = 0) -> torch.Tensor:
+    """C = ReLU(op(A) @ op(B)) (relu=True) or op(A) @ op(B), fp16, fp32 accumulation.
+
+    op(A) = A if not transa (A is (M,K)), else A.T (A stored (K,M));
+    op(B) = B if not transb (B is (K,N)), else B.T (B stored (N,K)).
+    All tensors contiguous float16 CUDA tensors; C (M,N) is allocated if not given.
+    """
+    _check_operand(A, "A")
+    _check_operand(B, "B")
+    M, K = (A.shape[1], A.shape[0]) if transa else (A.shape[0], A.shape[1])
+    K2, N = (B.shape[1], B.shape[0]) if transb else (B.shape[0], B.shape[1])
+    if K != K2:
+        raise ValueError(f"inner sizes differ: op(A) {M}x{K}, op(B) {K2}x{N}")
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.float16, device=A.device)
+    _check_operand(C, "C")
+    if tuple(C.shape) != (M, N):
+        raise ValueError(f"C must be {(M, N)}, got {tuple(C.shape)}")
+    with torch.cuda.device(A.device):
+        st = lib().gemm_f16_tx(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, int(bool(transa)),
+                               int(bool(transb)), int(bool(relu)), int(config), _stream_handle(stream, A.device))
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_f16_tx")
+    return C
+
+
+def relu_backward(dC: torch.Tensor, C: torch.Tensor, dZ: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """dZ = dC where C > 0 else +0 (gradient through the fused ReLU), on the GPU."""
+    for t, n in ((dC, "dC"), (C, "C")):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.float16 or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous float16 tensor")
+    if dC.shape != C.shape:
+        raise ValueError(f"dC {tuple(dC.shape)} and C {tuple(C.shape)} differ")
+    if dZ is None:
+        dZ = torch.empty_like(dC)
+    with torch.cuda.device(dC.device):
+        st = lib().gemm_f16_relu_backward(dC.data_ptr(), C.data_ptr(), dZ.data_ptr(), dC.numel(),
+                                          _stream_handle(stream, dC.device))
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_f16_relu_backward")
+    return dZ
+
+
+def config_layouts(config: int) -> int:
+    return int(lib().gemm_f16_config_layouts(int(config)))
 
 
 def gemm_f16_raw(A_ptr: int, B_ptr: int, C_ptr: int, M: int, N: int, K: int, relu: int, stream: int = 0,

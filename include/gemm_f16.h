@@ -42,7 +42,7 @@
 extern "C" {
 #endif
 
-#define GEMM_F16_VERSION 1
+#define GEMM_F16_VERSION 2
 
 /* Return codes.  0 is success; every error is negative. */
 enum gemm_f16_status {
@@ -50,9 +50,10 @@ enum gemm_f16_status {
     GEMM_ERR_INVALID_ARG = -1,        /* negative size, size > INT32_MAX, relu not 0/1,
                                          NULL or non-device pointer, buffer smaller than
                                          its matrix, C overlapping A or B, bad config id */
-    GEMM_ERR_ALIGNMENT = -2,          /* a pointer not 16-byte aligned, or N or K not a
-                                         multiple of 8 (the 16-byte row-pitch rule of the
-                                         tensor-memory-access unit) */
+    GEMM_ERR_ALIGNMENT = -2,          /* a pointer not 16-byte aligned, or a row pitch
+                                         (N or K for gemm_f16) not a multiple of 8 (the
+                                         16-byte row-pitch rule of the tensor-memory-access
+                                         unit) */
     GEMM_ERR_UNSUPPORTED_DEVICE = -3, /* current device is not compute capability 10.3 */
     GEMM_ERR_LAUNCH = -4,             /* the CUDA launch itself failed */
     GEMM_ERR_TIMEOUT = -5,            /* a kernel's bounded wait expired (gemm_f16_check) */
@@ -90,6 +91,52 @@ int gemm_f16(const void *A, const void *B, void *C,
  */
 int gemm_f16_ex(const void *A, const void *B, void *C,
                 int64_t M, int64_t N, int64_t K, int relu, int config, void *stream);
+
+/*
+ * gemm_f16_tx -- C = R(op(A) @ op(B)) with transposed operand layouts (the
+ * transpose_A / transpose_B options of the tile GEMM in "Writing
+ * High-Performance Kernels in TileLang, from GEMM to MLA", section "Let's
+ * write a GEMM"; the backward pair of the autograd wrapper in the TileLang-MUSA
+ * lesson, section 6, needs op(B) = B^T for dA = dC @ B^T and op(A) = A^T for
+ * dB = A^T @ dC).  op(A) is M x K and op(B) is K x N:
+ *
+ *   transa  0: A stored (M,K) row-major (leading dim K); 1: A stored (K,M)
+ *           row-major (leading dim M) and op(A) = A^T
+ *   transb  0: B stored (K,N) row-major (leading dim N); 1: B stored (N,K)
+ *           row-major (leading dim K) and op(B) = B^T
+ *
+ * C is always (M,N) row-major.  Every stored row pitch (leading dimension)
+ * must be a multiple of 8 elements, else GEMM_ERR_ALIGNMENT.  config as for
+ * gemm_f16_ex; a configuration without transposed-layout kernels
+ * (gemm_f16_config_layouts) returns GEMM_ERR_INVALID_ARG for transa or transb.
+ * Everything else as gemm_f16.
+ */
+int gemm_f16_tx(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
+                int transa, int transb, int relu, int config, void *stream);
+
+/*
+ * gemm_f16_relu_backward -- gradient through the fused ReLU epilogue:
+ * dZ[i] = dC[i] if C[i] > 0 else +0, for i < n, where C is the stored output
+ * of gemm_f16(..., relu = 1) and dC the gradient arriving at it.  "C[i] > 0"
+ * means a positive, nonzero, non-NaN binary16 value (+inf included); the
+ * pre-activation A @ B is not kept, so its sign is read from C (a product that
+ * rounds to +0 in binary16 gets gradient 0).  The autograd wrapper of the
+ * TileLang-MUSA lesson (7yue.com, section 6) then applies dA = dZ @ B^T and
+ * dB = A^T @ dZ (gemm_f16_tx with transb = 1 and transa = 1).
+ *
+ *   dC, C, dZ  device pointers to n binary16 values, 2-byte aligned (16-byte
+ *              alignment of all three selects the vectorised path)
+ *   n          number of elements, >= 0 (0: no-op)
+ *
+ * dZ may be the same buffer as dC or C (in place); any other overlap is
+ * GEMM_ERR_INVALID_ARG.  Asynchronous on `stream`, like gemm_f16.
+ */
+int gemm_f16_relu_backward(const void *dC, const void *C, void *dZ, int64_t n, void *stream);
+
+/* Operand layouts a configuration supports: bit (transa * 2 + transb) is set
+ * for each supported (transa, transb); 0xF = all four, 0x1 = only (0,0).
+ * GEMM_ERR_INVALID_ARG for an unknown id.  config 0 (automatic) supports all. */
+int gemm_f16_config_layouts(int config);
 
 /* Number of fixed configurations accepted by gemm_f16_ex (ids 1..n). */
 int gemm_f16_num_configs(void);
@@ -156,6 +203,10 @@ int gemm_f16_selftest_timeout(const void *A, const void *B, void *C, int64_t M, 
 /* Raw value of the last timeout record read by gemm_f16_check on this thread
  * (0 if none): bits 0-7 the wait site, bits 8-31 the block index. */
 uint64_t gemm_f16_last_timeout_record(void);
+
+/* Why the last call on this thread that returned GEMM_ERR_INVALID_ARG or
+ * GEMM_ERR_ALIGNMENT was rejected (static storage; "" if none yet). */
+const char *gemm_f16_last_error_detail(void);
 
 /* Human-readable text for a status code (static storage). */
 const char *gemm_f16_strerror(int status);

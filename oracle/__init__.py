@@ -44,6 +44,8 @@ def _load():
         i64 = ctypes.c_int64
         lib.oracle_gemm_f16_rows.argtypes = [p, p, p, i64, i64, i64, ctypes.c_int, p, i64]
         lib.oracle_gemm_f16_rows.restype = ctypes.c_int
+        lib.oracle_relu_backward.argtypes = [p, p, p, i64]
+        lib.oracle_relu_backward.restype = None
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = ctypes.c_int
         _lib = lib
@@ -122,3 +124,27 @@ def time_rows(A, B, relu: bool, rows) -> tuple[np.ndarray, float]:
     t0 = time.perf_counter()
     c = gemm_f16(A, B, relu, rows=rows)
     return c, time.perf_counter() - t0
+
+
+def relu_backward(dC, C) -> np.ndarray:
+    """dZ = dC where C > 0 else +0 (the ReLU gradient), float16, by the C oracle."""
+    g = _as_f16_bits(dC)
+    c = _as_f16_bits(C)
+    if g.shape != c.shape:
+        raise ValueError(f"shape mismatch: dC {g.shape}, C {c.shape}")
+    out = np.empty(g.shape, dtype=np.uint16)
+    if g.size:
+        _load().oracle_relu_backward(g.ctypes.data, c.ctypes.data, out.ctypes.data, g.size)
+    return out.view(np.float16)
+
+
+def gemm_f16_t(A, B, relu: bool, transa: bool = False, transb: bool = False, rows=None) -> np.ndarray:
+    """C = R(op(A) @ op(B)): op(X) is X or its transpose (numpy transposes the
+    stored matrix; the product itself is the oracle's gemm_f16)."""
+    a = _as_f16_bits(A)
+    b = _as_f16_bits(B)
+    if transa:
+        a = np.ascontiguousarray(a.T)
+    if transb:
+        b = np.ascontiguousarray(b.T)
+    return gemm_f16(a, b, relu, rows=rows)

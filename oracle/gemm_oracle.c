@@ -164,3 +164,18 @@ int oracle_num_threads(void)
     }
     return n;
 }
+
+/*
+ * Gradient through the ReLU epilogue, for the backward pass of C = ReLU(A @ B):
+ * dZ[i] = dC[i] where C[i] > 0, else +0.  C is the stored forward output (its
+ * value decides the sign of the pre-activation, which is not kept); +inf > 0,
+ * NaN is not > 0.  The autograd wrapper of the TileLang-MUSA lesson (7yue.com,
+ * section 6) then forms dA = dZ @ B^T and dB = A^T @ dZ.
+ */
+void oracle_relu_backward(const uint16_t *dC, const uint16_t *C, uint16_t *dZ, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        const double c = oracle_f16_to_f64(C[i]);
+        dZ[i] = (c > 0.0) ? dC[i] : (uint16_t)0x0000u;
+    }
+}

@@ -343,3 +343,42 @@ def test_pins_catch_planted_mistakes(oracle_mod):
     assert pins_pass(correct)
     for m in (dropped_last_term, transposed_b, transposed_a, wrong_sign, relu_after_cast_keeps_minus_zero, truncating_cast):
         assert not pins_pass(m), m.__name__
+
+
+# --------------------------------------------------------------------------
+# ReLU gradient and transposed operands
+# --------------------------------------------------------------------------
+
+def test_relu_backward_hand_cases(oracle_mod):
+    with open(os.path.join(HERE, "golden", "relu_backward_cases.json")) as f:
+        case = json.load(f)
+    C = np.array([int(v, 16) for v in case["C"]], dtype=np.uint16)
+    dC = np.array([int(v, 16) for v in case["dC"]], dtype=np.uint16)
+    want = np.array([int(v, 16) for v in case["dZ"]], dtype=np.uint16)
+    got = bits(oracle_mod.relu_backward(dC, C))
+    assert np.array_equal(got, want), [hex(v) for v in got]
+
+
+def test_relu_backward_mask_matches_forward_sign(oracle_mod):
+    # where the forward output is positive the gradient passes, elsewhere +0
+    rng = np.random.default_rng(10)
+    a = rng.integers(-4, 5, (12, 20))
+    b = rng.integers(-4, 5, (20, 9))
+    C = oracle_mod.gemm_f16(a.astype(np.float16), b.astype(np.float16), relu=True)
+    dC = rng.integers(-8, 9, C.shape).astype(np.float16)
+    dZ = oracle_mod.relu_backward(dC, C)
+    z = a @ b   # exact int64 pre-activation
+    assert np.array_equal(bits(dZ), bits(np.where(z > 0, dC, np.float16(0)).astype(np.float16)))
+
+
+@pytest.mark.parametrize("transa,transb", [(False, True), (True, False), (True, True)])
+def test_transposed_layouts_vs_int64(oracle_mod, transa, transb):
+    rng = np.random.default_rng(11 + 2 * transa + transb)
+    M, N, K = 13, 17, 29
+    a = rng.integers(-4, 5, (M, K))
+    b = rng.integers(-4, 5, (K, N))
+    A_st = a.T.copy() if transa else a
+    B_st = b.T.copy() if transb else b
+    got = oracle_mod.gemm_f16_t(A_st.astype(np.float16), B_st.astype(np.float16), relu=False,
+                                transa=transa, transb=transb)
+    assert np.array_equal(bits(got), bits(int_matmul_f16(a, b, relu=False)))
