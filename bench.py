@@ -49,6 +49,22 @@ TENSOR_FLOP_PER_CLK_PER_SM = 8192   # dense fp16/bf16 tcgen05 rate per SM per cl
 
 # ---------------------------------------------------------------- helpers
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Largest value of x over all ranks (x itself when running alone)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(flops_per_step: float, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job TFLOP/s: every rank does the same steps (replicas), timed by the slowest rank."""
+    return world * flops_per_step * steps / (max_ms * 1e-3) / 1e12
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -261,12 +277,6 @@ def run_ours(args):
             dist.barrier()
         torch.cuda.synchronize()
 
-    def max_over_ranks(x: float) -> float:
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
 
     # ---- device-resident timing
     sampler = ClockSampler(local)
@@ -278,9 +288,9 @@ def run_ours(args):
     st = g.check(stream)
     if st != g.GEMM_OK:
         raise RuntimeError(f"device status {st}: {g.strerror(st)}")
-    total_ms = max_over_ranks(total_ms)
+    total_ms = max_over_ranks(total_ms, world, dev)
     ms_per_step = total_ms / args.steps
-    value = world * w.flops * args.steps / (total_ms * 1e-3) / 1e12
+    value = whole_job_rate(w.flops, args.steps, world, total_ms)
 
     avg_launch_ms = statistics.mean(per_launch)
     achieved = w.flops / (avg_launch_ms * 1e-3) / 1e12
@@ -320,6 +330,45 @@ def run_ours(args):
                      "l2": "256 MiB buffer written between launches (L2 flush); median of launches"}
         del A2, B2, C2, flush
 
+    # ---- backward pair of the same workload (training use): the ReLU gradient
+    # mask, dA = dZ @ B^T (NT layout) and dB = A^T @ dZ (TN layout)
+    backward = None
+    if not args.no_secondary:
+        dC = torch.empty_like(C).normal_()
+        dZ = torch.empty_like(C)
+        dA = torch.empty_like(A)
+        dB = torch.empty_like(B)
+        hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+
+        def timed(fn, reps):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s_ev.record(stream)
+            for _ in range(reps):
+                fn()
+            e_ev.record(stream)
+            e_ev.synchronize()
+            return s_ev.elapsed_time(e_ev) / reps
+
+        reps_b = args.steps   # as many launches as the forward loop (same power-capped regime)
+        ms_mask = timed(lambda: g.relu_backward(dC, C, dZ, stream=stream), reps_b)
+        ms_da = timed(lambda: g.gemm_f16_t(dZ, B, dA, transb=True, relu=False, stream=stream), reps_b)
+        ms_db = timed(lambda: g.gemm_f16_t(A, dZ, dB, transa=True, relu=False, stream=stream), reps_b)
+        mask_bytes = 3 * C.numel() * 2
+        backward = {
+            "relu_backward": {"ms": ms_mask, "GB_s": mask_bytes / (ms_mask * 1e-3) / 1e9,
+                              "frac_of_measured_hbm": mask_bytes / (ms_mask * 1e-3) / 1e9 / hbm,
+                              "bytes": mask_bytes, "bound": "hbm"},
+            "dA_NT": {"ms": ms_da, "TFLOP_s": w.flops / (ms_da * 1e-3) / 1e12,
+                      "kernel_config": g.config_name(g.auto_config(w.M, w.K, w.N))},
+            "dB_TN": {"ms": ms_db, "TFLOP_s": w.flops / (ms_db * 1e-3) / 1e12,
+                      "kernel_config": g.config_name(g.auto_config(w.K, w.N, w.M))},
+            "note": "back-to-back launches on resident 8192^3 operands (larger than L2), as many as the timed forward steps",
+        }
+        del dC, dZ, dA, dB
+
     # ---- end to end through the host-buffer C call
     A_h = A_cpu.pin_memory()
     B_h = B_cpu.pin_memory()
@@ -335,8 +384,8 @@ def run_ours(args):
         g.gemm_f16_from_host(A_h, B_h, C_h, A, B, C, relu=w.relu, stream=stream)
     e1.record(stream)
     barrier()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1))
-    e2e_value = world * w.flops * e2e_steps / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    e2e_value = whole_job_rate(w.flops, e2e_steps, world, e2e_ms)
 
     cpu_baseline = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -368,6 +417,8 @@ def run_ours(args):
         }
         if secondary is not None:
             line["secondary"] = secondary
+        if backward is not None:
+            line["backward"] = backward
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()

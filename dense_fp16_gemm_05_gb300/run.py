@@ -1,6 +1,11 @@
 """Runs one named workload through the C ABI a few times and prints the timings.
 
     python -m dense_fp16_gemm_05_gb300.run --workload relu_8192 --reps 4 [--config ID]
+        [--op gemm|dA_nt|dB_tn|relu_backward]
+
+--op picks the kernel: the forward GEMM (default), the two backward GEMMs of
+the workload (dA = dZ @ B^T in the NT layout, dB = A^T @ dZ in the TN layout)
+or the ReLU-gradient mask over an (M,N) gradient.
 
 A minimal program around the library (no oracle, no other kernels besides the
 input upload), suited as the target of a profiler capture: every GPU kernel it
@@ -23,6 +28,7 @@ def main(argv=None):
     p.add_argument("--reps", type=int, default=4)
     p.add_argument("--config", type=int, default=0)
     p.add_argument("--relu", type=int, default=None, help="override the workload's ReLU flag")
+    p.add_argument("--op", default="gemm", choices=["gemm", "dA_nt", "dB_tn", "relu_backward"])
     args = p.parse_args(argv)
     if args.workload in WORKLOADS:
         w = WORKLOADS[args.workload]
@@ -35,11 +41,28 @@ def main(argv=None):
     A, B = A_cpu.to(dev), B_cpu.to(dev)
     C = torch.empty((w.M, w.N), dtype=torch.float16, device=dev)
     cfg = args.config or g.auto_config(w.M, w.N, w.K)
+    dZ = dA = dB = None
+    if args.op != "gemm":
+        dZ = torch.empty((w.M, w.N), dtype=torch.float16, device=dev).normal_()
+        g.gemm_f16(A, B, C, relu=True, config=cfg)
+        dA = torch.empty_like(A) if args.op == "dA_nt" else None
+        dB = torch.empty_like(B) if args.op == "dB_tn" else None
+
+    def step():
+        if args.op == "gemm":
+            g.gemm_f16(A, B, C, relu=relu, config=cfg)
+        elif args.op == "dA_nt":
+            g.gemm_f16_t(dZ, B, dA, transb=True, relu=False, config=args.config)
+        elif args.op == "dB_tn":
+            g.gemm_f16_t(A, dZ, dB, transa=True, relu=False, config=args.config)
+        else:
+            g.relu_backward(dZ, C, dZ)
+
     times = []
     for _ in range(args.reps):
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s.record()
-        g.gemm_f16(A, B, C, relu=relu, config=cfg)
+        step()
         e.record()
         e.synchronize()
         times.append(s.elapsed_time(e))
@@ -47,9 +70,13 @@ def main(argv=None):
     if st != g.GEMM_OK:
         raise SystemExit(f"device status {st}: {g.strerror(st)}")
     best = min(times)
-    print(json.dumps({"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "relu": relu,
-                      "config": g.config_name(cfg), "ms": times,
-                      "best_tflops": w.flops / (best * 1e-3) / 1e12}))
+    out = {"workload": w.name, "op": args.op, "M": w.M, "N": w.N, "K": w.K, "relu": relu,
+           "config": g.config_name(cfg) if args.op == "gemm" else args.config, "ms": times}
+    if args.op == "relu_backward":
+        out["best_GBps"] = 3 * w.M * w.N * 2 / (best * 1e-3) / 1e9
+    else:
+        out["best_tflops"] = w.flops / (best * 1e-3) / 1e12
+    print(json.dumps(out))
 
 
 if __name__ == "__main__":
