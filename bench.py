@@ -326,7 +326,7 @@ def run_ours(args):
         tf2 = w2.flops / (ms2 * 1e-3) / 1e12
         secondary = {"workload": w2.name, "M": w2.M, "N": w2.N, "K": w2.K, "relu": False,
                      "TFLOP_s": tf2, "ms": ms2, "frac_of_measured_peak": tf2 / peak,
-                     "frac_of_theoretical_peak": tf2 / theoretical, "kernel_config": g.config_name(cfg2),
+                     "frac_of_theoretical_peak": tf2 / theoretical, "kernel_config": g.config_label(cfg2),
                      "l2": "256 MiB buffer written between launches (L2 flush); median of launches"}
         del A2, B2, C2, flush
 
@@ -362,9 +362,9 @@ def run_ours(args):
                               "frac_of_measured_hbm": mask_bytes / (ms_mask * 1e-3) / 1e9 / hbm,
                               "bytes": mask_bytes, "bound": "hbm"},
             "dA_NT": {"ms": ms_da, "TFLOP_s": w.flops / (ms_da * 1e-3) / 1e12,
-                      "kernel_config": g.config_name(g.auto_config(w.M, w.K, w.N))},
+                      "kernel_config": g.config_label(g.auto_config(w.M, w.K, w.N))},
             "dB_TN": {"ms": ms_db, "TFLOP_s": w.flops / (ms_db * 1e-3) / 1e12,
-                      "kernel_config": g.config_name(g.auto_config(w.K, w.N, w.M))},
+                      "kernel_config": g.config_label(g.auto_config(w.K, w.N, w.M))},
             "note": "back-to-back launches on resident 8192^3 operands (larger than L2), as many as the timed forward steps",
         }
         del dC, dZ, dA, dB
@@ -398,7 +398,7 @@ def run_ours(args):
             "vs_baseline": None, "dtype": "f16", "data": "synthetic",
             "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "relu": w.relu,
                        "values": "N(0,1)/sqrt(K) fp16" if w.values == "normal_scaled" else w.values,
-                       "seed": w.seed, "kernel_config": g.config_name(config), "accumulate": "f32",
+                       "seed": w.seed, "kernel_config": g.config_label(config), "accumulate": "f32",
                        "l2": "inputs 384 MiB > 126 MB L2, no flush",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "frac_of_theoretical_peak": value / world / theoretical,

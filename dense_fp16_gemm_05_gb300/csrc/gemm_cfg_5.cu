@@ -7,9 +7,10 @@ namespace gemm_sm103 {
 
 int launch_config_5(const LaunchArgs &a) { return launch_config<Cfg2x512, true>(a); }
 
-int launch_info_config_5(int64_t M, int64_t N, const DeviceInfo &dev, int *grid_ctas, int *cluster_size, int *tiles)
+int launch_info_config_5(int64_t M, int64_t N, bool allow_split, const DeviceInfo &dev, int *grid_ctas,
+                         int *cluster_size, int *tiles)
 {
-    return config_launch_info<Cfg2x512>(M, N, dev, grid_ctas, cluster_size, tiles);
+    return config_launch_info<Cfg2x512>(M, N, allow_split, dev, grid_ctas, cluster_size, tiles);
 }
 
 }  // namespace gemm_sm103

@@ -230,13 +230,12 @@ namespace {
 
 int pick_config(int64_t M, int64_t N, int64_t K, int sm_count)
 {
-    (void)K;
     const int64_t pairs = sm_count / 2;
     const int64_t tiles_256x512 = ((M + 255) / 256) * ((N + 511) / 512);
-    // Many 256x512 tiles (about 13 or more waves): the wide pair tile needs the
-    // fewest operand bytes per flop; its single accumulator costs little
-    // when tiles are long and the tail is a small share.
-    if (tiles_256x512 >= 13 * pairs) return 5;
+    // At least one full wave of 256x512 pair tiles and a long K loop: the wide
+    // tile needs the fewest operand bytes per flop.  Its tail is left whole:
+    // a split tail runs 256-column MMAs on half the operand reuse.
+    if (tiles_256x512 >= pairs && K >= 2048) return 5 | GEMM_F16_NO_SPLIT;
     const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
     // Enough 256x256 tiles to keep every SM pair busy: the CTA-pair kernel.
     if (pair_tiles >= pairs) return 3;
@@ -244,6 +243,16 @@ int pick_config(int64_t M, int64_t N, int64_t K, int sm_count)
     if (tiles256 >= sm_count / 2) return 1;
     // Few tiles: narrower tiles put more SMs to work.
     return 2;
+}
+
+// Splits a config argument into the configuration id and its flag bits;
+// false for an unknown id or flag.
+bool parse_config(int config, int *id, bool *allow_split)
+{
+    if (config < 0 || (config & ~(GEMM_F16_CONFIG_ID_MASK | GEMM_F16_NO_SPLIT)) != 0) return false;
+    *id = config & GEMM_F16_CONFIG_ID_MASK;
+    *allow_split = (config & GEMM_F16_NO_SPLIT) == 0;
+    return *id <= kNumConfigs;
 }
 
 // ---------------------------------------------------------------- launch path
@@ -255,8 +264,11 @@ int run_gemm(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_
     if (st != GEMM_OK) return st;
     if ((transa != 0 && transa != 1) || (transb != 0 && transb != 1))
         return reject(GEMM_ERR_INVALID_ARG, "transa / transb is not 0 or 1");
-    if (config < 0 || config > kNumConfigs) return reject(GEMM_ERR_INVALID_ARG, "unknown configuration id");
-    if ((transa || transb) && !kConfigs[config].all_layouts)
+    int id = 0;
+    bool allow_split = true;
+    if (!parse_config(config, &id, &allow_split))
+        return reject(GEMM_ERR_INVALID_ARG, "unknown configuration id or flag");
+    if ((transa || transb) && !kConfigs[id].all_layouts)
         return reject(GEMM_ERR_INVALID_ARG, "this configuration has no transposed-layout kernels");
     if (M == 0 || N == 0) return GEMM_OK;
 
@@ -301,7 +313,14 @@ int run_gemm(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_
     a.status = status_word(dev.device);
     if (a.status == nullptr) return GEMM_ERR_CUDA;
 
-    const int cfg = config == 0 ? pick_config(M, N, K, dev.sm_count) : config;
+    int cfg = id;
+    if (id == 0) {
+        const int picked = pick_config(M, N, K, dev.sm_count);
+        cfg = picked & GEMM_F16_CONFIG_ID_MASK;
+        a.allow_split = allow_split && (picked & GEMM_F16_NO_SPLIT) == 0;
+    } else {
+        a.allow_split = allow_split;
+    }
     switch (cfg) {
         case 1: return launch_config_1(a);
         case 2: return launch_config_2(a);
@@ -374,14 +393,19 @@ extern "C" int gemm_f16_num_configs(void) { return kNumConfigs; }
 
 extern "C" const char *gemm_f16_config_name(int config)
 {
-    if (config < 0 || config > kNumConfigs) return nullptr;
-    return kConfigs[config].name;
+    int id = 0;
+    bool allow_split = true;
+    if (!parse_config(config, &id, &allow_split)) return nullptr;
+    return kConfigs[id].name;
 }
 
 extern "C" int gemm_f16_config_layouts(int config)
 {
-    if (config < 0 || config > kNumConfigs) return reject(GEMM_ERR_INVALID_ARG, "unknown configuration id");
-    return kConfigs[config].all_layouts ? 0xF : 0x1;
+    int id = 0;
+    bool allow_split = true;
+    if (!parse_config(config, &id, &allow_split))
+        return reject(GEMM_ERR_INVALID_ARG, "unknown configuration id or flag");
+    return kConfigs[id].all_layouts ? 0xF : 0x1;
 }
 
 extern "C" int gemm_f16_auto_config(int64_t M, int64_t N, int64_t K)
@@ -398,17 +422,24 @@ extern "C" int gemm_f16_launch_info(int64_t M, int64_t N, int64_t K, int config,
 {
     int st = check_sizes(M, N, K, 0);
     if (st != GEMM_OK) return st;
-    if (config < 0 || config > kNumConfigs) return reject(GEMM_ERR_INVALID_ARG, "unknown configuration id");
+    int id = 0;
+    bool split = true;
+    if (!parse_config(config, &id, &split)) return reject(GEMM_ERR_INVALID_ARG, "unknown configuration id or flag");
     DeviceInfo dev;
     if ((st = current_device_info(&dev)) != GEMM_OK) return st;
-    const int cfg = config == 0 ? pick_config(M, N, K, dev.sm_count) : config;
+    int cfg = id;
+    if (id == 0) {
+        const int picked = pick_config(M, N, K, dev.sm_count);
+        cfg = picked & GEMM_F16_CONFIG_ID_MASK;
+        split = split && (picked & GEMM_F16_NO_SPLIT) == 0;
+    }
     switch (cfg) {
-        case 1: return launch_info_config_1(M, N, dev, grid_ctas, cluster_size, tiles);
-        case 2: return launch_info_config_2(M, N, dev, grid_ctas, cluster_size, tiles);
-        case 3: return launch_info_config_3(M, N, dev, grid_ctas, cluster_size, tiles);
-        case 4: return launch_info_config_4(M, N, dev, grid_ctas, cluster_size, tiles);
-        case 5: return launch_info_config_5(M, N, dev, grid_ctas, cluster_size, tiles);
-        case 6: return launch_info_config_6(M, N, dev, grid_ctas, cluster_size, tiles);
+        case 1: return launch_info_config_1(M, N, split, dev, grid_ctas, cluster_size, tiles);
+        case 2: return launch_info_config_2(M, N, split, dev, grid_ctas, cluster_size, tiles);
+        case 3: return launch_info_config_3(M, N, split, dev, grid_ctas, cluster_size, tiles);
+        case 4: return launch_info_config_4(M, N, split, dev, grid_ctas, cluster_size, tiles);
+        case 5: return launch_info_config_5(M, N, split, dev, grid_ctas, cluster_size, tiles);
+        case 6: return launch_info_config_6(M, N, split, dev, grid_ctas, cluster_size, tiles);
         default: return GEMM_ERR_INVALID_ARG;
     }
 }

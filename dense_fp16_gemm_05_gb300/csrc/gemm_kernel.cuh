@@ -361,6 +361,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             uint32_t ph = 0;
             uint32_t issued_mask = 0, issued_parity = 0;
             bool ok = true;
+            // The pair leader's full barrier 0 (its full[s] is 8 * s bytes further).
+            const uint32_t full_base = (kPair && !leader) ? mapa_shared(full_bar(0), leader_rank) : full_bar(0);
+            (void)full_base;
             for (int u = cluster_id; ok && p.producer_off == 0 && u < p.num_units; u += num_clusters) {
                 int mb, col0, shift;
                 unit_coords<Cfg::BN>(u, p, mb, col0, shift);
@@ -371,10 +374,18 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 // starting at tile column h * umma_n + rank * umma_n / CTA_GROUP.
                 const int width = Cfg::BN >> shift;
                 const int umma_n = width < Cfg::UMMA_N ? width : Cfg::UMMA_N;
-                const int bpm = umma_n / (Cfg::CTA_GROUP * Cfg::B_BOX_N);
+                const int bpm = umma_n / (Cfg::CTA_GROUP * Cfg::B_BOX_N);   // 1, 2 or 4
+                const int bpm_log2 = __ffs(bpm) - 1;
                 const int boxes = Cfg::B_BOXES >> shift;
                 const int n_cta = col0 + static_cast<int>(rank) * (umma_n / Cfg::CTA_GROUP);
                 const uint32_t tx = Cfg::A_STAGE_BYTES + boxes * Cfg::B_BOX_BYTES;
+                // Everything that is fixed for the unit is computed here, once: the
+                // per-stage path below is only the arrive and the TMA issues (a
+                // slot's refill waits behind it).
+                int bxs[Cfg::B_BOXES];
+#pragma unroll
+                for (int j = 0; j < Cfg::B_BOXES; ++j)
+                    bxs[j] = n_cta + (j >> bpm_log2) * umma_n + (j & (bpm - 1)) * Cfg::B_BOX_N;
                 for (int kb = 0; kb < p.num_k_blocks; ++kb) {
                     if (!wait_phase(empty_bar(s), ph ^ 1u, abort, limit, kSiteProducerEmpty)) {
                         ok = false;
@@ -384,22 +395,25 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     const uint32_t a_dst = sA + s * Cfg::A_STAGE_BYTES;
                     const uint32_t b_dst = sB + s * Cfg::B_STAGE_BYTES;
                     if constexpr (!kPair) {
-                        mbar_arrive_expect_tx(full_bar(s), tx);
+                        const uint32_t fb = full_bar(s);
+                        mbar_arrive_expect_tx(fb, tx);
                         if constexpr (!kTA) {
-                            tma_load_2d(a_dst, &tmap_a, full_bar(s), k0, m0);
+                            tma_load_2d(a_dst, &tmap_a, fb, k0, m0);
                         } else {
-                            tma_load_2d(a_dst, &tmap_a, full_bar(s), m0, k0);
-                            tma_load_2d(a_dst + Cfg::A_STAGE_BYTES / 2, &tmap_a, full_bar(s), m0 + 64, k0);
+                            tma_load_2d(a_dst, &tmap_a, fb, m0, k0);
+                            tma_load_2d(a_dst + Cfg::A_STAGE_BYTES / 2, &tmap_a, fb, m0 + 64, k0);
                         }
-                        for (int j = 0; j < boxes; ++j) {
-                            const int x = n_cta + (j / bpm) * umma_n + (j % bpm) * Cfg::B_BOX_N;
-                            if constexpr (!kTB) tma_load_2d(b_dst + j * Cfg::B_BOX_BYTES, &tmap_b, full_bar(s), x, k0);
-                            else tma_load_2d(b_dst + j * Cfg::B_BOX_BYTES, &tmap_b, full_bar(s), k0, x);
+#pragma unroll
+                        for (int j = 0; j < Cfg::B_BOXES; ++j) {
+                            if (j < boxes) {
+                                if constexpr (!kTB) tma_load_2d(b_dst + j * Cfg::B_BOX_BYTES, &tmap_b, fb, bxs[j], k0);
+                                else tma_load_2d(b_dst + j * Cfg::B_BOX_BYTES, &tmap_b, fb, k0, bxs[j]);
+                            }
                         }
                     } else {
                         // The bytes landing in both CTAs of a pair are counted on the
                         // pair leader's barrier; each CTA announces its own bytes.
-                        const uint32_t fb = leader ? full_bar(s) : mapa_shared(full_bar(s), leader_rank);
+                        const uint32_t fb = full_base + 8u * s;
                         if (leader) mbar_arrive_expect_tx(fb, tx);
                         else mbar_arrive_expect_tx_cluster(fb, tx);
                         if constexpr (!kTA) {
@@ -408,17 +422,19 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                             tma_load_2d_pair(a_dst, &tmap_a, fb, m0, k0);
                             tma_load_2d_pair(a_dst + Cfg::A_STAGE_BYTES / 2, &tmap_a, fb, m0 + 64, k0);
                         }
-                        for (int j = 0; j < boxes; ++j) {
-                            const int x = n_cta + (j / bpm) * umma_n + (j % bpm) * Cfg::B_BOX_N;
-                            const int bx = kTB ? k0 : x, by = kTB ? x : k0;
-                            if constexpr (Cfg::PAIRS == 1) {
-                                tma_load_2d_pair(b_dst + j * Cfg::B_BOX_BYTES, &tmap_b, fb, bx, by);
-                            } else {
-                                // Box j is loaded by pair j % PAIRS and multicast to the
-                                // same-half CTA of every pair.
-                                if (j % Cfg::PAIRS == static_cast<int>(pair))
-                                    tma_load_2d_pair_mc(b_dst + j * Cfg::B_BOX_BYTES, &tmap_b, fb, bx, by,
-                                                        same_half_mask);
+#pragma unroll
+                        for (int j = 0; j < Cfg::B_BOXES; ++j) {
+                            if (j < boxes) {
+                                const int bx = kTB ? k0 : bxs[j], by = kTB ? bxs[j] : k0;
+                                if constexpr (Cfg::PAIRS == 1) {
+                                    tma_load_2d_pair(b_dst + j * Cfg::B_BOX_BYTES, &tmap_b, fb, bx, by);
+                                } else {
+                                    // Box j is loaded by pair j % PAIRS and multicast to the
+                                    // same-half CTA of every pair.
+                                    if (j % Cfg::PAIRS == static_cast<int>(pair))
+                                        tma_load_2d_pair_mc(b_dst + j * Cfg::B_BOX_BYTES, &tmap_b, fb, bx, by,
+                                                            same_half_mask);
+                                }
                             }
                         }
                     }

@@ -42,6 +42,7 @@ struct LaunchArgs {
     cudaStream_t stream = nullptr;
     LaunchHook hook;
     unsigned long long *status = nullptr;   // device status word of this GPU
+    bool allow_split = true;   // false: every work unit is a whole tile (no tail split)
 };
 
 // Defined in gemm_f16.cu.
@@ -113,7 +114,7 @@ struct Schedule {
 };
 
 template <class Cfg>
-Schedule make_schedule(int64_t M, int64_t N, int64_t slots)
+Schedule make_schedule(int64_t M, int64_t N, int64_t slots, bool allow_split)
 {
     Schedule sc;
     sc.tiles = ((M + Cfg::SUPER_M - 1) / Cfg::SUPER_M) * ((N + Cfg::BN - 1) / Cfg::BN);
@@ -126,7 +127,7 @@ Schedule make_schedule(int64_t M, int64_t N, int64_t slots)
     // (ties go to the coarser split).
     int shift = 0;
     double best = 1e30;
-    for (int s = 0; rest > 0 && s <= Cfg::MAX_SPLIT_LOG2; ++s) {
+    for (int s = 0; allow_split && rest > 0 && s <= Cfg::MAX_SPLIT_LOG2; ++s) {
         const int64_t waves = ((rest << s) + slots - 1) / slots;
         const double t = static_cast<double>(waves) / static_cast<double>(1 << s);
         if (t < best - 1e-9) {
@@ -167,7 +168,7 @@ int launch_one(const LaunchArgs &a)
     using Prep = Prepared<Cfg, kRelu, kTA, kTB>;
     const int64_t slots = Prep::get(a.dev.device, a.dev.sm_count);
     if (slots <= 0) return GEMM_ERR_LAUNCH;
-    const Schedule sc = make_schedule<Cfg>(a.M, a.N, slots);
+    const Schedule sc = make_schedule<Cfg>(a.M, a.N, slots, a.allow_split);
     if (sc.units > INT32_MAX / 2) return GEMM_ERR_INVALID_ARG;
     p.num_tiles = static_cast<int32_t>(sc.tiles);
     p.num_units = static_cast<int32_t>(sc.units);
@@ -229,9 +230,11 @@ int launch_config(const LaunchArgs &a)
 
 // Launch geometry of a configuration (no launch).
 template <class Cfg>
-int config_launch_info(int64_t M, int64_t N, const DeviceInfo &dev, int *grid_ctas, int *cluster_size, int *tiles)
+int config_launch_info(int64_t M, int64_t N, bool allow_split, const DeviceInfo &dev, int *grid_ctas,
+                       int *cluster_size, int *tiles)
 {
-    const Schedule sc = make_schedule<Cfg>(M, N, Prepared<Cfg, true, false, false>::get(dev.device, dev.sm_count));
+    const Schedule sc =
+        make_schedule<Cfg>(M, N, Prepared<Cfg, true, false, false>::get(dev.device, dev.sm_count), allow_split);
     if (tiles) *tiles = static_cast<int>(sc.tiles < INT32_MAX ? sc.tiles : INT32_MAX);
     if (cluster_size) *cluster_size = Cfg::CLUSTER;
     if (grid_ctas) *grid_ctas = static_cast<int>(sc.grid_units * Cfg::CLUSTER);
@@ -242,8 +245,8 @@ int config_launch_info(int64_t M, int64_t N, const DeviceInfo &dev, int *grid_ct
 // translation unit (gemm_cfg_<id>.cu) so that they compile in parallel.
 #define GEMM_DECLARE_CONFIG(ID)                                                                              \
     int launch_config_##ID(const LaunchArgs &a);                                                             \
-    int launch_info_config_##ID(int64_t M, int64_t N, const DeviceInfo &dev, int *grid_ctas, int *cluster_size, \
-                                int *tiles);
+    int launch_info_config_##ID(int64_t M, int64_t N, bool allow_split, const DeviceInfo &dev, int *grid_ctas, \
+                                int *cluster_size, int *tiles);
 GEMM_DECLARE_CONFIG(1)
 GEMM_DECLARE_CONFIG(2)
 GEMM_DECLARE_CONFIG(3)

@@ -24,6 +24,10 @@ GEMM_ERR_LAUNCH = -4
 GEMM_ERR_TIMEOUT = -5
 GEMM_ERR_CUDA = -6
 
+# Config argument: id in the low byte, flag bits above (include/gemm_f16.h).
+GEMM_F16_CONFIG_ID_MASK = 0xFF
+GEMM_F16_NO_SPLIT = 0x100
+
 HEADER = os.path.join(_build.INCLUDE, "gemm_f16.h")
 
 
@@ -120,6 +124,14 @@ def num_configs() -> int:
 def config_name(config: int) -> str | None:
     r = lib().gemm_f16_config_name(int(config))
     return None if r is None else r.decode()
+
+
+def config_label(config: int) -> str | None:
+    """config_name plus "+nosplit" when the GEMM_F16_NO_SPLIT flag is set."""
+    name = config_name(config)
+    if name is None:
+        return None
+    return name + ("+nosplit" if int(config) & GEMM_F16_NO_SPLIT else "")
 
 
 def _stream_handle(stream, device) -> int:

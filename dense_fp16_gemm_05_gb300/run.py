@@ -71,7 +71,7 @@ def main(argv=None):
         raise SystemExit(f"device status {st}: {g.strerror(st)}")
     best = min(times)
     out = {"workload": w.name, "op": args.op, "M": w.M, "N": w.N, "K": w.K, "relu": relu,
-           "config": g.config_name(cfg) if args.op == "gemm" else args.config, "ms": times}
+           "config": g.config_label(cfg) if args.op == "gemm" else args.config, "ms": times}
     if args.op == "relu_backward":
         out["best_GBps"] = 3 * w.M * w.N * 2 / (best * 1e-3) / 1e9
     else:

@@ -42,7 +42,7 @@
 extern "C" {
 #endif
 
-#define GEMM_F16_VERSION 2
+#define GEMM_F16_VERSION 3
 
 /* Return codes.  0 is success; every error is negative. */
 enum gemm_f16_status {
@@ -81,13 +81,32 @@ int gemm_f16(const void *A, const void *B, void *C,
              int64_t M, int64_t N, int64_t K, int relu, void *stream);
 
 /*
+ * Configuration arguments.  The low byte is a configuration id: 0 for the
+ * automatic choice, 1..gemm_f16_num_configs() for a fixed tiling.  Flag bits
+ * above it change how the persistent schedule treats the last, partly filled
+ * wave of tiles:
+ *
+ *   GEMM_F16_NO_SPLIT  keep every work unit a whole tile.  Without it, the
+ *                      tiles of a partly filled last wave may be split along
+ *                      N into 2, 4 ... narrower units so that more SMs share
+ *                      the tail.  Either way every output element is the same
+ *                      K-ordered fp32 sum, so the results do not change.
+ *
+ * No other bit may be set (GEMM_ERR_INVALID_ARG).  This tail policy is an
+ * implementation choice of this library; the tile GEMM of the pages has no
+ * persistent schedule and no tail split.
+ */
+#define GEMM_F16_CONFIG_ID_MASK 0xFF
+#define GEMM_F16_NO_SPLIT 0x100
+
+/*
  * gemm_f16_ex -- gemm_f16 with an explicit kernel configuration.
  *
  *   config  0: automatic choice (what gemm_f16 uses); 1..gemm_f16_num_configs():
- *           a fixed tiling, see gemm_f16_config_name().  Every configuration
- *           computes the same function; they differ in tile shape and in the
- *           number of SMs that cooperate on one tile.  Unknown id:
- *           GEMM_ERR_INVALID_ARG.
+ *           a fixed tiling, see gemm_f16_config_name(); either may carry the
+ *           flag bits above.  Every configuration computes the same function;
+ *           they differ in tile shape and in the number of SMs that cooperate
+ *           on one tile.  Unknown id or flag: GEMM_ERR_INVALID_ARG.
  */
 int gemm_f16_ex(const void *A, const void *B, void *C,
                 int64_t M, int64_t N, int64_t K, int relu, int config, void *stream);
@@ -141,12 +160,14 @@ int gemm_f16_config_layouts(int config);
 /* Number of fixed configurations accepted by gemm_f16_ex (ids 1..n). */
 int gemm_f16_num_configs(void);
 
-/* Short name of a configuration id ("auto" for 0), or NULL for an unknown id.
- * The string is static; the caller must not free it. */
+/* Short name of a configuration id ("auto" for 0; flag bits are ignored), or
+ * NULL for an unknown id or flag.  The string is static; the caller must not
+ * free it. */
 const char *gemm_f16_config_name(int config);
 
-/* Configuration id that gemm_f16 picks for this problem size on the current
- * device (never 0), or a negative status for invalid sizes. */
+/* Configuration that gemm_f16 picks for this problem size on the current
+ * device: a nonzero id, possibly with flag bits (GEMM_F16_NO_SPLIT), which
+ * gemm_f16_ex accepts as it is; or a negative status for invalid sizes. */
 int gemm_f16_auto_config(int64_t M, int64_t N, int64_t K);
 
 /*

@@ -100,3 +100,24 @@ def test_selftest_timeout_rejects_bad_budgets_before_any_cuda_call(g):
     assert L.gemm_f16_selftest_timeout(None, None, None, 64, 64, 0, 0, 1 << 20, None) == g.GEMM_ERR_INVALID_ARG
     assert L.gemm_f16_selftest_timeout(None, None, None, 64, 64, 64, 0, 100, None) == g.GEMM_ERR_INVALID_ARG
     assert L.gemm_f16_selftest_timeout(None, None, None, 64, 64, 64, 0, 1 << 40, None) == g.GEMM_ERR_INVALID_ARG
+
+
+def test_config_flag_constants_match_header(g):
+    with open(g.HEADER) as f:
+        text = f.read()
+    assert int(re.search(r"#define GEMM_F16_CONFIG_ID_MASK (0x[0-9A-Fa-f]+)", text).group(1), 16) == \
+        g.GEMM_F16_CONFIG_ID_MASK
+    assert int(re.search(r"#define GEMM_F16_NO_SPLIT (0x[0-9A-Fa-f]+)", text).group(1), 16) == g.GEMM_F16_NO_SPLIT
+
+
+def test_config_flags_parsed_before_cuda(g):
+    # a known id with the no-split flag names the same configuration; an unknown
+    # flag bit or id is rejected without touching the GPU
+    for cfg in range(0, g.num_configs() + 1):
+        assert g.config_name(cfg | g.GEMM_F16_NO_SPLIT) == g.config_name(cfg)
+        assert g.config_layouts(cfg | g.GEMM_F16_NO_SPLIT) == g.config_layouts(cfg)
+    assert g.config_name(1 | 0x200) is None
+    assert g.config_name(g.num_configs() + 1) is None
+    assert g.config_layouts(1 | 0x400) == g.GEMM_ERR_INVALID_ARG
+    st = g.lib().gemm_f16_ex(0, 0, 0, 64, 64, 64, 1, 1 | 0x800, None)
+    assert st == g.GEMM_ERR_INVALID_ARG

@@ -235,3 +235,24 @@ def test_rejects_bad_buffers(g):
     assert raw(A.data_ptr(), B.data_ptr(), C.data_ptr(), 1 << 20, N, K, 1) in (g.GEMM_ERR_INVALID_ARG,)
     torch.cuda.synchronize()
     assert g.check() == g.GEMM_OK
+
+
+def test_no_split_flag_keeps_results_identical(g):
+    # 1000^3 leaves a partly filled last wave in every configuration, so the
+    # default schedule splits it along N; the flag keeps whole tiles.  Each
+    # output is the same K-ordered fp32 sum either way.
+    w = WORKLOADS["relu_ragged_1000"]
+    A, B = draw_workload(w)
+    ref = oracle.gemm_f16(A, B, relu=True)
+    for cfg in configs(g):
+        split = run(g, A, B, True, cfg)
+        whole = run(g, A, B, True, cfg | g.GEMM_F16_NO_SPLIT)
+        assert np.array_equal(split.view(np.uint16), whole.view(np.uint16)), cfg
+        assert_close(whole, ref, f"{w.name} cfg {cfg} no-split")
+
+
+def test_auto_choice_is_a_valid_config(g):
+    for (M, N, K) in [(8192, 8192, 8192), (4096, 4096, 4096), (1024, 1024, 1024), (64, 64, 64), (16384, 512, 64)]:
+        c = g.auto_config(M, N, K)
+        assert c > 0 and g.config_name(c) is not None
+        assert (c & ~(g.GEMM_F16_CONFIG_ID_MASK | g.GEMM_F16_NO_SPLIT)) == 0
