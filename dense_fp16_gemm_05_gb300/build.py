@@ -30,7 +30,7 @@ NVCC_FLAGS = [
 
 def _sources() -> list[str]:
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cuh"))
-                  + glob.glob(os.path.join(INCLUDE, "*.h")))
+                  + glob.glob(os.path.join(CSRC, "*.inc")) + glob.glob(os.path.join(INCLUDE, "*.h")))
 
 
 def nvcc() -> str:

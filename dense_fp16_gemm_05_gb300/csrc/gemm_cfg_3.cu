@@ -13,4 +13,9 @@ int launch_info_config_3(int64_t M, int64_t N, bool allow_split, const DeviceInf
     return config_launch_info<Cfg2x256>(M, N, allow_split, dev, grid_ctas, cluster_size, tiles);
 }
 
+double wave_eff_config_3(int64_t M, int64_t N, bool allow_split, const DeviceInfo &dev)
+{
+    return config_wave_efficiency<Cfg2x256>(M, N, allow_split, dev);
+}
+
 }  // namespace gemm_sm103

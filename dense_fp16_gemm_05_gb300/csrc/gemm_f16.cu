@@ -11,6 +11,7 @@
 #include <cudaTypedefs.h>
 
 #include <atomic>
+#include <cmath>
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
@@ -245,6 +246,86 @@ int pick_config(int64_t M, int64_t N, int64_t K, int sm_count)
     return 2;
 }
 
+// ---------------------------------------------------------------- tuned selection
+
+#if __has_include("gemm_f16_tuned.inc")
+#include "gemm_f16_tuned.inc"
+#define GEMM_F16_HAVE_TUNED 1
+#else
+#define GEMM_F16_HAVE_TUNED 0
+#endif
+
+double wave_eff(int id, int64_t M, int64_t N, bool split, const DeviceInfo &dev)
+{
+    switch (id) {
+        case 1: return wave_eff_config_1(M, N, split, dev);
+        case 2: return wave_eff_config_2(M, N, split, dev);
+        case 3: return wave_eff_config_3(M, N, split, dev);
+        case 4: return wave_eff_config_4(M, N, split, dev);
+        case 5: return wave_eff_config_5(M, N, split, dev);
+        case 6: return wave_eff_config_6(M, N, split, dev);
+        default: return 0.0;
+    }
+}
+
+// The automatic choice.  The offline sweep (tune.py) measured every candidate
+// (configuration x tail policy) on a grid of shapes.  For a problem, take the
+// nearest measured shape in log2 space (K weighted by half: it changes the
+// per-tile work but not the wave count), scale each candidate's measured
+// throughput by its wave efficiency here over its wave efficiency there, and
+// take the best.  `any_layout`: only configurations with transposed-layout
+// kernels qualify.  Without a table, the size rule above.
+int select_config(int64_t M, int64_t N, int64_t K, bool any_layout, const DeviceInfo &dev)
+{
+#if GEMM_F16_HAVE_TUNED
+    struct Last {
+        int64_t M = -1, N = -1, K = -1;
+        int device = -1, any_layout = -1, choice = 0;
+    };
+    thread_local Last last;
+    if (last.M == M && last.N == N && last.K == K && last.device == dev.device && last.any_layout == any_layout)
+        return last.choice;
+    const double lm = std::log2(static_cast<double>(M > 0 ? M : 1));
+    const double ln = std::log2(static_cast<double>(N > 0 ? N : 1));
+    const double lk = std::log2(static_cast<double>(K > 0 ? K : 1));
+    int row = 0;
+    double best_d = 1e300;
+    for (int r = 0; r < GEMM_F16_TUNED_ROWS; ++r) {
+        const TunedRow &t = kTunedRows[r];
+        const double d = std::fabs(lm - std::log2(static_cast<double>(t.M))) +
+                         std::fabs(ln - std::log2(static_cast<double>(t.N))) +
+                         0.5 * std::fabs(lk - std::log2(static_cast<double>(t.K)));
+        if (d < best_d) {
+            best_d = d;
+            row = r;
+        }
+    }
+    const TunedRow &t = kTunedRows[row];
+    int choice = 0;
+    double best = 0.0;
+    for (int i = 0; i < GEMM_F16_TUNED_CANDIDATES; ++i) {
+        const int c = kTunedCandidates[i];
+        const int id = c & GEMM_F16_CONFIG_ID_MASK;
+        if (id < 1 || id > kNumConfigs || (any_layout && !kConfigs[id].all_layouts)) continue;
+        const bool split = (c & GEMM_F16_NO_SPLIT) == 0;
+        const double here = wave_eff(id, M, N, split, dev);
+        const double there = wave_eff(id, t.M, t.N, split, dev);
+        if (here <= 0.0 || there <= 0.0) continue;
+        const double predicted = static_cast<double>(t.tflops[i]) * here / there;
+        if (predicted > best) {
+            best = predicted;
+            choice = c;
+        }
+    }
+    if (choice != 0) {
+        last = Last{M, N, K, dev.device, any_layout ? 1 : 0, choice};
+        return choice;
+    }
+#endif
+    (void)any_layout;
+    return pick_config(M, N, K, dev.sm_count);
+}
+
 // Splits a config argument into the configuration id and its flag bits;
 // false for an unknown id or flag.
 bool parse_config(int config, int *id, bool *allow_split)
@@ -315,7 +396,7 @@ int run_gemm(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_
 
     int cfg = id;
     if (id == 0) {
-        const int picked = pick_config(M, N, K, dev.sm_count);
+        const int picked = select_config(M, N, K, transa || transb, dev);
         cfg = picked & GEMM_F16_CONFIG_ID_MASK;
         a.allow_split = allow_split && (picked & GEMM_F16_NO_SPLIT) == 0;
     } else {
@@ -414,7 +495,7 @@ extern "C" int gemm_f16_auto_config(int64_t M, int64_t N, int64_t K)
     if (st != GEMM_OK) return st;
     DeviceInfo dev;
     if ((st = current_device_info(&dev)) != GEMM_OK) return st;
-    return pick_config(M, N, K, dev.sm_count);
+    return select_config(M, N, K, false, dev);
 }
 
 extern "C" int gemm_f16_launch_info(int64_t M, int64_t N, int64_t K, int config, int *grid_ctas,
@@ -429,7 +510,7 @@ extern "C" int gemm_f16_launch_info(int64_t M, int64_t N, int64_t K, int config,
     if ((st = current_device_info(&dev)) != GEMM_OK) return st;
     int cfg = id;
     if (id == 0) {
-        const int picked = pick_config(M, N, K, dev.sm_count);
+        const int picked = select_config(M, N, K, false, dev);
         cfg = picked & GEMM_F16_CONFIG_ID_MASK;
         split = split && (picked & GEMM_F16_NO_SPLIT) == 0;
     }

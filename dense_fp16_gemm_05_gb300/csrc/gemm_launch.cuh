@@ -241,12 +241,36 @@ int config_launch_info(int64_t M, int64_t N, bool allow_split, const DeviceInfo 
     return GEMM_OK;
 }
 
+// Share of the persistent grid's slot time that computes in-range outputs:
+// M*N over (slots x the busiest slot's time x tile area), where the time is
+// counted in whole-tile units (a unit split 2^s ways takes 2^-s of a tile).
+// Scales a throughput measured at one shape to another shape for the same
+// configuration; 0 when the configuration cannot be launched.
+template <class Cfg>
+double config_wave_efficiency(int64_t M, int64_t N, bool allow_split, const DeviceInfo &dev)
+{
+    const int64_t slots = Prepared<Cfg, true, false, false>::get(dev.device, dev.sm_count);
+    if (slots <= 0 || M <= 0 || N <= 0) return 0.0;
+    const Schedule sc = make_schedule<Cfg>(M, N, slots, allow_split);
+    double t;
+    if (sc.shift == 0) {
+        t = static_cast<double>((sc.tiles + slots - 1) / slots);
+    } else {
+        const int64_t tail_units = sc.units - sc.split_start;
+        t = static_cast<double>(sc.split_start / slots) +
+            static_cast<double>((tail_units + slots - 1) / slots) / static_cast<double>(1 << sc.shift);
+    }
+    const double area = static_cast<double>(Cfg::SUPER_M) * static_cast<double>(Cfg::BN);
+    return static_cast<double>(M) * static_cast<double>(N) / (static_cast<double>(slots) * t * area);
+}
+
 // One pair of entry points per configuration, each defined in its own
 // translation unit (gemm_cfg_<id>.cu) so that they compile in parallel.
 #define GEMM_DECLARE_CONFIG(ID)                                                                              \
     int launch_config_##ID(const LaunchArgs &a);                                                             \
     int launch_info_config_##ID(int64_t M, int64_t N, bool allow_split, const DeviceInfo &dev, int *grid_ctas, \
-                                int *cluster_size, int *tiles);
+                                int *cluster_size, int *tiles);                                               \
+    double wave_eff_config_##ID(int64_t M, int64_t N, bool allow_split, const DeviceInfo &dev);
 GEMM_DECLARE_CONFIG(1)
 GEMM_DECLARE_CONFIG(2)
 GEMM_DECLARE_CONFIG(3)

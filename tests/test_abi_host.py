@@ -121,3 +121,32 @@ def test_config_flags_parsed_before_cuda(g):
     assert g.config_layouts(1 | 0x400) == g.GEMM_ERR_INVALID_ARG
     st = g.lib().gemm_f16_ex(0, 0, 0, 64, 64, 64, 1, 1 | 0x800, None)
     assert st == g.GEMM_ERR_INVALID_ARG
+
+
+def _tuned_table():
+    import os
+    from dense_fp16_gemm_05_gb300 import build as gbuild
+    path = os.path.join(gbuild.CSRC, "gemm_f16_tuned.inc")
+    with open(path) as f:
+        text = f.read()
+    cands = [int(x, 16) for x in re.search(r"kTunedCandidates\[[^\]]*\] = \{([^}]*)\}", text).group(1).split(",")]
+    rows = []
+    for m in re.finditer(r"\{(\d+), (\d+), (\d+), \{([^}]*)\}\}", text):
+        vals = [float(x.strip().rstrip("f")) for x in m.group(4).split(",")]
+        rows.append((int(m.group(1)), int(m.group(2)), int(m.group(3)), vals))
+    n_rows = int(re.search(r"#define GEMM_F16_TUNED_ROWS (\d+)", text).group(1))
+    n_cands = int(re.search(r"#define GEMM_F16_TUNED_CANDIDATES (\d+)", text).group(1))
+    return cands, rows, n_rows, n_cands
+
+
+def test_tuned_table_is_well_formed(g):
+    cands, rows, n_rows, n_cands = _tuned_table()
+    assert len(cands) == n_cands and len(rows) == n_rows > 0
+    for c in cands:
+        assert 1 <= (c & g.GEMM_F16_CONFIG_ID_MASK) <= g.num_configs()
+        assert (c & ~(g.GEMM_F16_CONFIG_ID_MASK | g.GEMM_F16_NO_SPLIT)) == 0
+    shapes = [r[:3] for r in rows]
+    assert len(set(shapes)) == len(shapes)
+    for M, N, K, vals in rows:
+        assert M > 0 and N > 0 and K > 0 and len(vals) == n_cands
+        assert all(v > 0 for v in vals)

@@ -256,3 +256,18 @@ def test_auto_choice_is_a_valid_config(g):
         c = g.auto_config(M, N, K)
         assert c > 0 and g.config_name(c) is not None
         assert (c & ~(g.GEMM_F16_CONFIG_ID_MASK | g.GEMM_F16_NO_SPLIT)) == 0
+
+
+def test_auto_config_follows_the_tuned_table(g):
+    # on a measured shape the wave-efficiency rescaling is 1, so the automatic
+    # choice is the candidate with the highest measured throughput
+    import re
+    from dense_fp16_gemm_05_gb300 import build as gbuild
+    with open(f"{gbuild.CSRC}/gemm_f16_tuned.inc") as f:
+        text = f.read()
+    cands = [int(x, 16) for x in re.search(r"kTunedCandidates\[[^\]]*\] = \{([^}]*)\}", text).group(1).split(",")]
+    for m in re.finditer(r"\{(\d+), (\d+), (\d+), \{([^}]*)\}\}", text):
+        M, N, K = (int(m.group(i)) for i in (1, 2, 3))
+        vals = [float(x.strip().rstrip("f")) for x in m.group(4).split(",")]
+        best = cands[vals.index(max(vals))]
+        assert g.auto_config(M, N, K) == best, (M, N, K)
