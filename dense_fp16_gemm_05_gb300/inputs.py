@@ -72,3 +72,78 @@ WORKLOADS: dict[str, Workload] = {
 for _n in (512, 1024, 2048, 4096, 8192, 16384):
     WORKLOADS[f"sweep_{_n}"] = Workload(f"sweep_{_n}", _n, _n, _n, True, "normal_scaled",
                                         100 + int(math.log2(_n)))
+
+
+# ---------------------------------------------------------------------------
+# FP8 block-scaled operands.  The TileLang-MUSA lesson (section 8.2) feeds
+# fp8_block_scaled_linear an FP8 weight with per-128-block scales; nothing on
+# the pages says how the operands were quantized, so the inputs are made the
+# usual way (this is input synthesis, not the GEMM): each block's scale is its
+# largest magnitude over 448 (the largest finite E4M3 value), and the block is
+# divided by its scale and rounded to E4M3 by torch's float8_e4m3fn
+# conversion.  A gets one scale per row per 128 K elements, W (N,K) one per
+# 128 x 128 block.  Scales are float32.
+
+FP8_BLOCK = 128
+
+
+@dataclass(frozen=True)
+class Fp8Workload:
+    """C = R(sum_b SA[:,b] SW[n/128,b] A_b W_b^T): A (M,K), W (N,K) E4M3."""
+    name: str
+    M: int
+    N: int
+    K: int
+    relu: bool
+    values: str          # "normal" (N(0,1) quantized per block) or "integer" (exact, power-of-two scales)
+    seed: int
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.M * self.N * self.K
+
+
+def _quantize_blocks(x: torch.Tensor, rows_per_block: int, block: int) -> tuple[torch.Tensor, torch.Tensor]:
+    """x (R, K) float32 -> (E4M3 codes as uint8 (R, K), float32 scales
+    (ceil(R/rows_per_block), ceil(K/block)))."""
+    R, K = x.shape
+    RB, KB = -(-R // rows_per_block), -(-K // block)
+    pad = torch.zeros(RB * rows_per_block, KB * block, dtype=torch.float32)
+    pad[:R, :K] = x
+    blocks = pad.view(RB, rows_per_block, KB, block)
+    amax = blocks.abs().amax(dim=(1, 3))
+    scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax)).to(torch.float32)
+    q = (blocks / scale[:, None, :, None]).clamp(-448.0, 448.0)
+    codes = q.reshape(RB * rows_per_block, KB * block)[:R, :K].contiguous().to(torch.float8_e4m3fn)
+    return codes.view(torch.uint8), scale
+
+
+def draw_fp8_block_scaled(M: int, N: int, K: int, values: str, seed: int, block: int = FP8_BLOCK):
+    """CPU tensors (A codes (M,K) uint8, SA (M,KB) f32, W codes (N,K) uint8,
+    SW (NB,KB) f32) drawn from ``seed``."""
+    g = torch.Generator().manual_seed(int(seed))
+    KB, NB = -(-K // block), -(-N // block)
+    if values == "normal":
+        a = torch.randn(M, K, generator=g, dtype=torch.float32)
+        w = torch.randn(N, K, generator=g, dtype=torch.float32) * (1.0 / math.sqrt(max(K, 1)))
+        A, SA = _quantize_blocks(a, 1, block)
+        W, SW = _quantize_blocks(w, block, block)
+        return A, SA, W, SW
+    if values == "integer":
+        a = torch.randint(-4, 5, (M, K), generator=g, dtype=torch.int32).to(torch.float32)
+        w = torch.randint(-4, 5, (N, K), generator=g, dtype=torch.int32).to(torch.float32)
+        ea = torch.randint(-3, 4, (M, KB), generator=g, dtype=torch.int32)
+        ew = torch.randint(-3, 4, (NB, KB), generator=g, dtype=torch.int32)
+        SA = torch.ldexp(torch.ones(M, KB), ea.to(torch.float32)).to(torch.float32)
+        SW = torch.ldexp(torch.ones(NB, KB), ew.to(torch.float32)).to(torch.float32)
+        A = a.to(torch.float8_e4m3fn).view(torch.uint8)
+        W = w.to(torch.float8_e4m3fn).view(torch.uint8)
+        return A, SA, W, SW
+    raise ValueError(f"unknown value recipe {values!r}")
+
+
+FP8_WORKLOADS: dict[str, Fp8Workload] = {
+    "fp8_int_256": Fp8Workload("fp8_int_256", 256, 256, 384, True, "integer", 21),
+    "fp8_ragged_1000": Fp8Workload("fp8_ragged_1000", 1000, 1000, 1000, True, "normal", 22),
+    "fp8_8192": Fp8Workload("fp8_8192", 8192, 8192, 8192, False, "normal", 23),
+}

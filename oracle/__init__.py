@@ -48,6 +48,10 @@ def _load():
         lib.oracle_relu_backward.restype = None
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = ctypes.c_int
+        lib.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_to_f64.restype = ctypes.c_double
+        lib.oracle_gemm_fp8_block_scaled_rows.argtypes = [p, p, p, p, p, i64, i64, i64, i64, ctypes.c_int, p, i64]
+        lib.oracle_gemm_fp8_block_scaled_rows.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -148,3 +152,74 @@ def gemm_f16_t(A, B, relu: bool, transa: bool = False, transb: bool = False, row
     if transb:
         b = np.ascontiguousarray(b.T)
     return gemm_f16(a, b, relu, rows=rows)
+
+
+# ---------------------------------------------------------------------------
+# FP8 block-scaled GEMM (the TileLang-MUSA lesson, section 8.2,
+# fp8_block_scaled_linear with block=128; the arithmetic is written out in
+# gemm_oracle.c above oracle_gemm_fp8_block_scaled_rows).
+
+def _as_u8(x) -> np.ndarray:
+    if hasattr(x, "detach"):
+        x = x.detach()
+        if x.device.type != "cpu":
+            raise ValueError("oracle inputs must be CPU tensors")
+        if str(x.dtype).startswith("torch.float8"):
+            import torch
+            x = x.view(torch.uint8)
+        x = x.contiguous().numpy()
+    x = np.ascontiguousarray(x)
+    if x.dtype != np.uint8:
+        raise TypeError(f"expected FP8 bytes (uint8), got {x.dtype}")
+    return x
+
+
+def _as_f32(x) -> np.ndarray:
+    if hasattr(x, "detach"):
+        x = x.detach()
+        if x.device.type != "cpu":
+            raise ValueError("oracle inputs must be CPU tensors")
+        x = x.contiguous().numpy()
+    x = np.ascontiguousarray(x)
+    if x.dtype != np.float32:
+        raise TypeError(f"expected float32 scales, got {x.dtype}")
+    return x
+
+
+def e4m3_to_f64(codes) -> np.ndarray:
+    """Decodes OCP FP8 E4M3 byte codes to float64, element by element, in C."""
+    lib = _load()
+    c = np.asarray(codes, dtype=np.uint8).ravel()
+    out = np.fromiter((lib.oracle_e4m3_to_f64(int(v)) for v in c), dtype=np.float64, count=c.size)
+    return out.reshape(np.shape(codes))
+
+
+def gemm_fp8_block_scaled(A, SA, W, SW, relu: bool, block: int = 128, rows=None) -> np.ndarray:
+    """C = R(sum_b SA[:,b] SW[n/block,b] (A_b @ W_b^T)) as float16, by the C oracle.
+
+    A (M,K) and W (N,K): E4M3 codes (uint8 numpy or CPU torch uint8 /
+    float8_e4m3fn); SA (M, ceil(K/block)) and SW (ceil(N/block),
+    ceil(K/block)): float32.  ``rows`` selects output rows as in gemm_f16.
+    """
+    a, w = _as_u8(A), _as_u8(W)
+    sa, sw = _as_f32(SA), _as_f32(SW)
+    if a.ndim != 2 or w.ndim != 2 or a.shape[1] != w.shape[1]:
+        raise ValueError(f"shape mismatch: A {a.shape}, W {w.shape}")
+    M, K = a.shape
+    N = w.shape[0]
+    KB, NB = -(-K // block), -(-N // block)
+    if sa.shape != (M, KB) or sw.shape != (NB, KB):
+        raise ValueError(f"scale shapes: SA {sa.shape} (want {(M, KB)}), SW {sw.shape} (want {(NB, KB)})")
+    lib = _load()
+    if rows is None:
+        n_rows, rows_ptr = M, None
+    else:
+        rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        n_rows, rows_ptr = rows_arr.size, rows_arr.ctypes.data
+    c = np.empty((n_rows, N), dtype=np.uint16)
+    ptr = lambda x: x.ctypes.data if x.size else None
+    rc = lib.oracle_gemm_fp8_block_scaled_rows(ptr(a), ptr(sa), ptr(w), ptr(sw), ptr(c), M, N, K, block,
+                                               int(bool(relu)), rows_ptr, n_rows)
+    if rc != 0:
+        raise ValueError("oracle_gemm_fp8_block_scaled_rows rejected its arguments")
+    return c.view(np.float16)

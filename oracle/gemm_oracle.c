@@ -179,3 +179,83 @@ void oracle_relu_backward(const uint16_t *dC, const uint16_t *C, uint16_t *dZ, i
         dZ[i] = (c > 0.0) ? dC[i] : (uint16_t)0x0000u;
     }
 }
+
+/* ======================================================================
+ * FP8 block-scaled GEMM (TEST INFRASTRUCTURE ONLY, like everything above).
+ *
+ * The TileLang-MUSA lesson (7yue.com, section 8.2, "reusing TileKernels")
+ * calls a linear layer on an FP8 weight with per-block scales,
+ * fp8_block_scaled_linear(x, w_fp8, scale_w, block=128), and the nxmr.cn
+ * TileLang article (section 7) names CUTLASS-style per-block scaling as the
+ * way FP8 GEMMs are scaled.  Neither page writes out the arithmetic; the
+ * plainest reading, which this function follows, is:
+ *
+ *   C[i,j] = f16_rne( R( sum_b  SA[i,b] * SW[j/block, b] * P_b[i,j] ) ),
+ *   P_b[i,j] = sum_{k in block b, k < K} A[i,k] * W[j,k]
+ *
+ *   A (M,K) and W (N,K): row-major OCP FP8 E4M3 (the weight is stored
+ *   out-features x in-features, as a linear layer keeps it, so C = A @ W^T);
+ *   SA (M, KB): one fp32 scale per row of A per block of `block` K elements;
+ *   SW (NB, KB): one fp32 scale per `block` x `block` block of W;
+ *   KB = ceil(K/block), NB = ceil(N/block); a partial last block keeps its
+ *   own scale.  Everything is formed in fp64 (FP8 and fp32 values are exact
+ *   there); each block's P_b is summed in ascending k, multiplied by the
+ *   product of its two scales, and the blocks are added in ascending b.
+ *   R and the final binary16 rounding are those of oracle_gemm_f16_rows.
+ * ====================================================================== */
+
+/* OCP FP8 E4M3 (the "fn" variant: finite, no infinities) -> binary64,
+ * exact.  1 sign bit, 4 exponent bits (bias 7), 3 fraction bits; exponent
+ * field 0 holds zero and the subnormals m * 2^-9; exponent field 15 with
+ * fraction 7 (0x7F, 0xFF) is NaN; the largest finite magnitude is 448. */
+double oracle_e4m3_to_f64(uint8_t x)
+{
+    const int sign = (x >> 7) & 1;
+    const int e = (x >> 3) & 0xf;
+    const int m = x & 0x7;
+    double v;
+    if (e == 15 && m == 7) {
+        v = NAN;
+    } else if (e == 0) {
+        v = ldexp((double)m, -9);               /* m/8 * 2^(1-7) */
+    } else {
+        v = ldexp((double)(m + 8), e - 10);     /* (1 + m/8) * 2^(e-7) */
+    }
+    return sign ? -v : v;
+}
+
+int oracle_gemm_fp8_block_scaled_rows(const uint8_t *A, const float *SA, const uint8_t *W, const float *SW,
+                                      uint16_t *C_out, int64_t M, int64_t N, int64_t K, int64_t block, int relu,
+                                      const int64_t *rows, int64_t n_rows)
+{
+    if (M < 0 || N < 0 || K < 0 || n_rows < 0 || block <= 0) return -1;
+    if (rows == NULL && n_rows != M) return -1;
+    for (int64_t r = 0; rows != NULL && r < n_rows; ++r)
+        if (rows[r] < 0 || rows[r] >= M) return -1;
+    if (n_rows == 0 || N == 0) return 0;
+    const int64_t KB = (K + block - 1) / block;
+
+    double e4m3[256];
+    for (int v = 0; v < 256; ++v) e4m3[v] = oracle_e4m3_to_f64((uint8_t)v);
+
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < n_rows; ++r) {
+        const int64_t i = rows ? rows[r] : r;
+        const uint8_t *a_row = A + i * K;
+        uint16_t *c_row = C_out + r * N;
+        for (int64_t j = 0; j < N; ++j) {
+            const uint8_t *w_row = W + j * K;
+            double acc = 0.0;
+            for (int64_t b = 0; b < KB; ++b) {
+                const int64_t k_end = (b + 1) * block < K ? (b + 1) * block : K;
+                double p = 0.0;
+                for (int64_t k = b * block; k < k_end; ++k) p += e4m3[a_row[k]] * e4m3[w_row[k]];
+                const double s = (double)SA[i * KB + b] * (double)SW[(j / block) * KB + b];
+                acc += s * p;
+            }
+            if (relu) acc = (acc > 0.0) ? acc : 0.0;
+            c_row[j] = oracle_f64_to_f16(acc);
+        }
+    }
+    return 0;
+}
