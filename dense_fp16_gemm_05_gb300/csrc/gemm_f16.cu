@@ -18,6 +18,7 @@
 #include <mutex>
 
 #include "gemm_f16.h"
+#include "gemm_fp8_launch.cuh"
 #include "gemm_launch.cuh"
 
 using namespace gemm_sm103;
@@ -208,6 +209,23 @@ int encode_matrix(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t col
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fns.encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
                             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+// Row-major one-byte-element matrix (E4M3 codes) rows x cols, leading
+// dimension cols bytes, boxes of box_cols x box_rows with 128-byte swizzle.
+int encode_matrix_u8(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t cols, uint32_t box_cols,
+                     uint32_t box_rows)
+{
+    const DriverFns &fns = driver();
+    if (!fns.ok) return GEMM_ERR_CUDA;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fns.encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
 }
@@ -468,6 +486,65 @@ extern "C" int gemm_f16_relu_backward(const void *dC, const void *C, void *dZ, i
     if ((dZ != dC && ranges_overlap(dZ, bytes, dC, bytes)) || (dZ != C && ranges_overlap(dZ, bytes, C, bytes)))
         return reject(GEMM_ERR_INVALID_ARG, "dZ partly overlaps dC or C");
     return relu_backward_launch(dC, C, dZ, n, dev.sm_count, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int gemm_fp8_block_scaled(const void *A, const float *SA, const void *W, const float *SW, void *C,
+                                     int64_t M, int64_t N, int64_t K, int relu, void *stream)
+{
+    int st = check_sizes(M, N, K, relu);
+    if (st != GEMM_OK) return st;
+    if (M == 0 || N == 0) return GEMM_OK;
+    DeviceInfo dev;
+    if ((st = current_device_info(&dev)) != GEMM_OK) return st;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const uint64_t c_bytes = static_cast<uint64_t>(M) * static_cast<uint64_t>(N) * 2u;
+    if ((st = check_device_buffer(C, c_bytes, dev.device)) != GEMM_OK) return st;
+    if (K == 0) {
+        // Empty sum in every block: every output is R(+0) = +0.
+        if (cudaMemsetAsync(C, 0, c_bytes, s) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_CUDA;
+        }
+        return GEMM_OK;
+    }
+    if ((K % 16) != 0)
+        return reject(GEMM_ERR_ALIGNMENT, "K is not a multiple of 16 (the E4M3 row pitch of A and W is K bytes)");
+    if ((N % 8) != 0) return reject(GEMM_ERR_ALIGNMENT, "N is not a multiple of 8 (the fp16 row pitch of C)");
+    const uint64_t KB = static_cast<uint64_t>((K + 127) / 128), NB = static_cast<uint64_t>((N + 127) / 128);
+    const uint64_t a_bytes = static_cast<uint64_t>(M) * static_cast<uint64_t>(K);
+    const uint64_t w_bytes = static_cast<uint64_t>(N) * static_cast<uint64_t>(K);
+    const uint64_t sa_bytes = static_cast<uint64_t>(M) * KB * 4u, sw_bytes = NB * KB * 4u;
+    if ((st = check_device_buffer(A, a_bytes, dev.device)) != GEMM_OK) return st;
+    if ((st = check_device_buffer(W, w_bytes, dev.device)) != GEMM_OK) return st;
+    if ((st = check_device_buffer(SA, sa_bytes, dev.device, 4)) != GEMM_OK) return st;
+    if ((st = check_device_buffer(SW, sw_bytes, dev.device, 4)) != GEMM_OK) return st;
+    if (ranges_overlap(C, c_bytes, A, a_bytes) || ranges_overlap(C, c_bytes, W, w_bytes) ||
+        ranges_overlap(C, c_bytes, SA, sa_bytes) || ranges_overlap(C, c_bytes, SW, sw_bytes))
+        return reject(GEMM_ERR_INVALID_ARG, "C overlaps an input");
+    Fp8LaunchArgs a;
+    a.A = A;
+    a.SA = SA;
+    a.W = W;
+    a.SW = SW;
+    a.C = C;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.relu = relu;
+    a.dev = dev;
+    a.stream = s;
+    a.status = status_word(dev.device);
+    if (a.status == nullptr) return GEMM_ERR_CUDA;
+    return launch_fp8(a);
+}
+
+extern "C" int gemm_fp8_launch_info(int64_t M, int64_t N, int64_t K, int *grid_ctas, int *tiles)
+{
+    int st = check_sizes(M, N, K, 0);
+    if (st != GEMM_OK) return st;
+    DeviceInfo dev;
+    if ((st = current_device_info(&dev)) != GEMM_OK) return st;
+    return fp8_launch_info(M, N, dev, grid_ctas, tiles);
 }
 
 extern "C" int gemm_f16_num_configs(void) { return kNumConfigs; }

@@ -1,0 +1,127 @@
+// gemm_fp8.cu -- host-side launch of the FP8 block-scaled GEMM kernel
+// (gemm_fp8_kernel.cuh).  The C ABI entry, gemm_fp8_block_scaled in
+// gemm_f16.cu, validates every argument and calls launch_fp8.
+#include "gemm_fp8_launch.cuh"
+
+#include "gemm_fp8_kernel.cuh"
+
+namespace gemm_sm103 {
+
+namespace {
+
+// Per device and ReLU variant: the shared-memory attribute is set once and
+// the number of co-resident CTA pairs cached (as for the fp16 kernels).
+template <bool kRelu>
+struct Fp8Prepared {
+    static std::atomic<int> slots[kMaxDevices];
+
+    static int get(int dev, int sm_count)
+    {
+        int v = slots[dev].load(std::memory_order_acquire);
+        if (v > 0) return v;
+        auto kern = gemm_fp8_block_scaled_sm103a<kRelu>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Fp8Cfg::SMEM_BYTES) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        v = sm_count / 2;
+        cudaLaunchConfig_t lc{};
+        lc.blockDim = dim3(Fp8Cfg::THREADS, 1, 1);
+        lc.dynamicSmemBytes = Fp8Cfg::SMEM_BYTES;
+        lc.gridDim = dim3(2 * v, 1, 1);
+        cudaLaunchAttribute attrs[1];
+        attrs[0].id = cudaLaunchAttributeClusterDimension;
+        attrs[0].val.clusterDim.x = 2;
+        attrs[0].val.clusterDim.y = 1;
+        attrs[0].val.clusterDim.z = 1;
+        lc.attrs = attrs;
+        lc.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, kern, &lc) == cudaSuccess && clusters > 0)
+            v = clusters < v ? clusters : v;
+        else
+            cudaGetLastError();
+        if (v > 0) slots[dev].store(v, std::memory_order_release);
+        return v;
+    }
+
+    static void forget(int dev) { slots[dev].store(0, std::memory_order_release); }
+};
+
+template <bool kRelu>
+std::atomic<int> Fp8Prepared<kRelu>::slots[kMaxDevices];
+
+template <bool kRelu>
+int launch_fp8_variant(const Fp8LaunchArgs &a)
+{
+    CUtensorMap ta, tw;
+    int st;
+    // A (M,K) and W (N,K): one-byte elements, boxes of 128 (K) x 128 rows.
+    if ((st = encode_matrix_u8(&ta, a.A, a.M, a.K, Fp8Cfg::BK, Fp8Cfg::BM)) != GEMM_OK) return st;
+    if ((st = encode_matrix_u8(&tw, a.W, a.N, a.K, Fp8Cfg::BK, Fp8Cfg::BN_CTA)) != GEMM_OK) return st;
+
+    Fp8Params p{};
+    p.M = static_cast<int32_t>(a.M);
+    p.N = static_cast<int32_t>(a.N);
+    p.K = static_cast<int32_t>(a.K);
+    p.num_m_blocks = static_cast<int32_t>((a.M + Fp8Cfg::TILE_M - 1) / Fp8Cfg::TILE_M);
+    p.num_n_blocks = static_cast<int32_t>((a.N + Fp8Cfg::BN - 1) / Fp8Cfg::BN);
+    p.num_k_blocks = static_cast<int32_t>((a.K + Fp8Cfg::BK - 1) / Fp8Cfg::BK);
+    const int64_t tiles = static_cast<int64_t>(p.num_m_blocks) * p.num_n_blocks;
+    if (tiles > INT32_MAX) return GEMM_ERR_INVALID_ARG;
+    p.num_tiles = static_cast<int32_t>(tiles);
+    p.group_m = 8;   // 2048-row panels, as the fp16 kernels
+    p.timeout_cycles = a.timeout_cycles ? a.timeout_cycles : timeout_cycles_for(a.K);
+    p.C = static_cast<__half *>(a.C);
+    p.SA = a.SA;
+    p.SW = a.SW;
+    p.status = a.status;
+
+    using Prep = Fp8Prepared<kRelu>;
+    const int64_t slots = Prep::get(a.dev.device, a.dev.sm_count);
+    if (slots <= 0) return GEMM_ERR_LAUNCH;
+    const int64_t clusters = tiles < slots ? tiles : slots;
+
+    auto kern = gemm_fp8_block_scaled_sm103a<kRelu>;
+    cudaLaunchConfig_t lc{};
+    lc.blockDim = dim3(Fp8Cfg::THREADS, 1, 1);
+    lc.dynamicSmemBytes = Fp8Cfg::SMEM_BYTES;
+    lc.stream = a.stream;
+    cudaLaunchAttribute attrs[1];
+    attrs[0].id = cudaLaunchAttributeClusterDimension;
+    attrs[0].val.clusterDim.x = 2;
+    attrs[0].val.clusterDim.y = 1;
+    attrs[0].val.clusterDim.z = 1;
+    lc.attrs = attrs;
+    lc.numAttrs = 1;
+    lc.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
+    if (cudaLaunchKernelEx(&lc, kern, ta, tw, p) != cudaSuccess) {
+        cudaGetLastError();
+        Prep::forget(a.dev.device);
+        if (Prep::get(a.dev.device, a.dev.sm_count) <= 0 || cudaLaunchKernelEx(&lc, kern, ta, tw, p) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_LAUNCH;
+        }
+    }
+    return GEMM_OK;
+}
+
+}  // namespace
+
+int launch_fp8(const Fp8LaunchArgs &a)
+{
+    return a.relu ? launch_fp8_variant<true>(a) : launch_fp8_variant<false>(a);
+}
+
+int fp8_launch_info(int64_t M, int64_t N, const DeviceInfo &dev, int *grid_ctas, int *tiles)
+{
+    const int64_t t = ((M + Fp8Cfg::TILE_M - 1) / Fp8Cfg::TILE_M) * ((N + Fp8Cfg::BN - 1) / Fp8Cfg::BN);
+    const int64_t slots = Fp8Prepared<true>::get(dev.device, dev.sm_count);
+    if (slots <= 0) return GEMM_ERR_LAUNCH;
+    if (grid_ctas) *grid_ctas = static_cast<int>(2 * (t < slots ? t : slots));
+    if (tiles) *tiles = static_cast<int>(t < INT32_MAX ? t : INT32_MAX);
+    return GEMM_OK;
+}
+
+}  // namespace gemm_sm103

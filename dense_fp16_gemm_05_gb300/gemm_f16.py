@@ -91,7 +91,11 @@ def lib() -> ctypes.CDLL:
     L.gemm_f16_config_layouts.restype = ci
     L.gemm_f16_selftest_timeout.argtypes = [vp, vp, vp, i64, i64, i64, ci, ctypes.c_uint64, vp]
     L.gemm_f16_selftest_timeout.restype = ci
+    L.gemm_fp8_block_scaled.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ci, vp]
+    L.gemm_fp8_block_scaled.restype = ci
     pi = ctypes.POINTER(ctypes.c_int)
+    L.gemm_fp8_launch_info.argtypes = [i64, i64, i64, pi, pi]
+    L.gemm_fp8_launch_info.restype = ci
     L.gemm_f16_launch_info.argtypes = [i64, i64, i64, ci, pi, pi, pi]
     L.gemm_f16_launch_info.restype = ci
     _lib = L
@@ -288,3 +292,60 @@ def selftest_timeout(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, config: 
 
 def last_timeout_record() -> int:
     return int(lib().gemm_f16_last_timeout_record())
+
+
+FP8_BLOCK = 128
+
+
+def _check_fp8(t: torch.Tensor, name: str):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype not in (torch.uint8, torch.float8_e4m3fn) or t.dim() != 2 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous 2-D uint8 / float8_e4m3fn tensor, got {t.dtype} {tuple(t.shape)}")
+
+
+def _check_scales(t: torch.Tensor, name: str, shape):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != torch.float32 or not t.is_contiguous() or tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must be a contiguous float32 tensor of shape {tuple(shape)}, "
+                         f"got {t.dtype} {tuple(t.shape)}")
+
+
+def gemm_fp8_block_scaled(A: torch.Tensor, SA: torch.Tensor, W: torch.Tensor, SW: torch.Tensor,
+                          C: torch.Tensor | None = None, relu: bool = False, stream=None) -> torch.Tensor:
+    """C = R(sum_b SA[:,b] SW[n/128,b] (A_b @ W_b^T)): the FP8 block-scaled linear layer.
+
+    A (M,K) and W (N,K): E4M3 codes (uint8 or float8_e4m3fn) on one CUDA
+    device; SA (M, ceil(K/128)) and SW (ceil(N/128), ceil(K/128)) float32;
+    C (M,N) float16, allocated when not given.  Asynchronous on ``stream``.
+    """
+    _check_fp8(A, "A")
+    _check_fp8(W, "W")
+    M, K = A.shape
+    N, K2 = W.shape
+    if K != K2:
+        raise ValueError(f"inner sizes differ: A {tuple(A.shape)}, W {tuple(W.shape)}")
+    KB, NB = -(-K // FP8_BLOCK), -(-N // FP8_BLOCK)
+    _check_scales(SA, "SA", (M, KB))
+    _check_scales(SW, "SW", (NB, KB))
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.float16, device=A.device)
+    _check_operand(C, "C")
+    if tuple(C.shape) != (M, N):
+        raise ValueError(f"C must be {(M, N)}, got {tuple(C.shape)}")
+    L = lib()
+    with torch.cuda.device(A.device):
+        st = L.gemm_fp8_block_scaled(A.data_ptr(), SA.data_ptr(), W.data_ptr(), SW.data_ptr(), C.data_ptr(),
+                                     M, N, K, int(bool(relu)), _stream_handle(stream, A.device))
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_fp8_block_scaled")
+    return C
+
+
+def fp8_launch_info(M: int, N: int, K: int) -> dict:
+    g, t = ctypes.c_int(0), ctypes.c_int(0)
+    st = lib().gemm_fp8_launch_info(M, N, K, ctypes.byref(g), ctypes.byref(t))
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_fp8_launch_info")
+    return {"grid_ctas": g.value, "tiles": t.value}

@@ -144,6 +144,6 @@ def draw_fp8_block_scaled(M: int, N: int, K: int, values: str, seed: int, block:
 
 FP8_WORKLOADS: dict[str, Fp8Workload] = {
     "fp8_int_256": Fp8Workload("fp8_int_256", 256, 256, 384, True, "integer", 21),
-    "fp8_ragged_1000": Fp8Workload("fp8_ragged_1000", 1000, 1000, 1000, True, "normal", 22),
+    "fp8_ragged_1000": Fp8Workload("fp8_ragged_1000", 1000, 1000, 1040, True, "normal", 22),
     "fp8_8192": Fp8Workload("fp8_8192", 8192, 8192, 8192, False, "normal", 23),
 }

@@ -42,7 +42,7 @@
 extern "C" {
 #endif
 
-#define GEMM_F16_VERSION 3
+#define GEMM_F16_VERSION 4
 
 /* Return codes.  0 is success; every error is negative. */
 enum gemm_f16_status {
@@ -151,6 +151,42 @@ int gemm_f16_tx(const void *A, const void *B, void *C, int64_t M, int64_t N, int
  * GEMM_ERR_INVALID_ARG.  Asynchronous on `stream`, like gemm_f16.
  */
 int gemm_f16_relu_backward(const void *dC, const void *C, void *dZ, int64_t n, void *stream);
+
+/*
+ * gemm_fp8_block_scaled -- FP8 block-scaled GEMM (a linear layer on an FP8
+ * weight with per-block scales: fp8_block_scaled_linear(x, w_fp8, scale_w,
+ * block=128) in the TileLang-MUSA lesson, 7yue.com, section 8.2; the
+ * per-block scaling strategy named in the nxmr.cn TileLang article, section 7):
+ *
+ *   C[i,j] = R( sum_b SA[i,b] * SW[j/128, b] * sum_{k in block b, k < K} A[i,k] * W[j,k] )
+ *
+ * with blocks of 128 along K, accumulated in fp32 and rounded once to fp16
+ * (R as for gemm_f16).  All pointers are device pointers on the current
+ * device, owned by the caller:
+ *
+ *   A   (M,K) OCP FP8 E4M3 codes, row-major (leading dimension K bytes)
+ *   SA  (M, ceil(K/128)) float32, row-major: one scale per row of A per K block
+ *   W   (N,K) E4M3 codes, row-major: the weight as a linear layer stores it
+ *       (out-features x in-features), so C = A @ W^T
+ *   SW  (ceil(N/128), ceil(K/128)) float32, row-major: one scale per 128 x 128
+ *       block of W
+ *   C   (M,N) IEEE binary16, row-major, written in place
+ *
+ * A partial last block (K or N not a multiple of 128) keeps its own scale.
+ * Checks before any launch, as for gemm_f16: sizes and relu
+ * (GEMM_ERR_INVALID_ARG), K % 16 == 0 and N % 8 == 0 and 16-byte aligned A, W,
+ * C, 4-byte aligned SA, SW (GEMM_ERR_ALIGNMENT), every buffer inside one
+ * allocation of the current device, C overlapping no input
+ * (GEMM_ERR_INVALID_ARG).  M == 0 or N == 0: no-op; K == 0: C = +0.  Only
+ * enqueues on `stream`; device timeouts are reported by gemm_f16_check.
+ */
+int gemm_fp8_block_scaled(const void *A, const float *SA, const void *W, const float *SW, void *C,
+                          int64_t M, int64_t N, int64_t K, int relu, void *stream);
+
+/* Launch geometry of gemm_fp8_block_scaled for this problem on the current
+ * device: persistent grid in CTAs (CTA pairs over 256 x 256 output tiles) and
+ * the number of tiles.  Either pointer may be NULL.  Launches nothing. */
+int gemm_fp8_launch_info(int64_t M, int64_t N, int64_t K, int *grid_ctas, int *tiles);
 
 /* Operand layouts a configuration supports: bit (transa * 2 + transb) is set
  * for each supported (transa, transb); 0xF = all four, 0x1 = only (0,0).

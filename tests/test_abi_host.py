@@ -150,3 +150,10 @@ def test_tuned_table_is_well_formed(g):
     for M, N, K, vals in rows:
         assert M > 0 and N > 0 and K > 0 and len(vals) == n_cands
         assert all(v > 0 for v in vals)
+
+
+def test_fp8_arguments_rejected_before_cuda(g):
+    L = g.lib()
+    assert L.gemm_fp8_block_scaled(None, None, None, None, None, -1, 64, 64, 1, None) == g.GEMM_ERR_INVALID_ARG
+    assert L.gemm_fp8_block_scaled(None, None, None, None, None, 64, 64, 64, 2, None) == g.GEMM_ERR_INVALID_ARG
+    assert L.gemm_fp8_block_scaled(None, None, None, None, None, 0, 64, 64, 1, None) == g.GEMM_OK   # empty: no-op
