@@ -44,6 +44,7 @@ if ROOT not in sys.path:
 METRIC = "GEMM+ReLU TFLOP/s at 4096^3/8192^3 fp16 and % of GB300 dense FP16 peak"
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
+FP8_PER_BF16 = 2.0            # nominal dense fp8 / bf16 tensor rate (4.5 / 2.25 PFLOP/s)
 TENSOR_FLOP_PER_CLK_PER_SM = 8192   # dense fp16/bf16 tcgen05 rate per SM per clock
 
 
@@ -375,6 +376,37 @@ def run_ours(args):
         }
         del dC, dZ, dA, dB
 
+    # ---- FP8 block-scaled GEMM (the next-row extension) at the same size:
+    # E4M3 operands quantized per 128-blocks, fp32 scales, fp16 output
+    fp8 = None
+    if not args.no_secondary:
+        from dense_fp16_gemm_05_gb300.inputs import FP8_WORKLOADS, draw_fp8_block_scaled
+        w8 = FP8_WORKLOADS["fp8_8192"]
+        A8c, SA8c, W8c, SW8c = draw_fp8_block_scaled(w8.M, w8.N, w8.K, w8.values, w8.seed)
+        A8, SA8, W8, SW8 = A8c.to(dev), SA8c.to(dev), W8c.to(dev), SW8c.to(dev)
+        C8 = torch.empty((w8.M, w8.N), dtype=torch.float16, device=dev)
+        reps8 = args.steps
+        for _ in range(3):
+            g.gemm_fp8_block_scaled(A8, SA8, W8, SW8, C=C8, relu=w8.relu, stream=stream)
+        torch.cuda.synchronize()
+        s8, e8 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s8.record(stream)
+        for _ in range(reps8):
+            g.gemm_fp8_block_scaled(A8, SA8, W8, SW8, C=C8, relu=w8.relu, stream=stream)
+        e8.record(stream)
+        e8.synchronize()
+        ms8 = s8.elapsed_time(e8) / reps8
+        if g.check(stream) != g.GEMM_OK:
+            raise SystemExit("FP8 kernel reported a device error")
+        tf8 = w8.flops / (ms8 * 1e-3) / 1e12
+        peak8 = peak * FP8_PER_BF16
+        fp8 = {"workload": w8.name, "M": w8.M, "N": w8.N, "K": w8.K, "relu": w8.relu, "ms": ms8, "TFLOP_s": tf8,
+               "roofline": {"bound": "tensor", "achieved": tf8, "peak": peak8, "unit": "TFLOP/s", "frac": tf8 / peak8,
+                            "peak_source": f"{peak_src} bf16 matmul burst x {FP8_PER_BF16} (nominal fp8 / bf16 dense ratio)"},
+               "values": "N(0,1) quantized per 128-block to E4M3, fp32 scales", "launches": reps8,
+               "note": "back-to-back launches on resident operands"}
+        del A8, SA8, W8, SW8, C8
+
     # ---- end to end through the host-buffer C call
     A_h = A_cpu.pin_memory()
     B_h = B_cpu.pin_memory()
@@ -425,6 +457,8 @@ def run_ours(args):
             line["secondary"] = secondary
         if backward is not None:
             line["backward"] = backward
+        if fp8 is not None:
+            line["fp8_block_scaled"] = fp8
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()

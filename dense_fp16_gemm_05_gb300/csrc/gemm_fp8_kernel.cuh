@@ -347,8 +347,12 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
             float acc[Cfg::SCALE_BLOCK];
 #pragma unroll
             for (int c = 0; c < Cfg::SCALE_BLOCK; ++c) acc[c] = 0.0f;
+            // Scales of blocks kb and kb + 1 in registers; block kb + 2's are
+            // fetched while block kb is promoted (two blocks of latency cover).
             float s_a = row_ok ? __ldg(sa) : 0.0f;
             float s_w = cols_ok ? __ldg(sw) : 0.0f;
+            float s_a1 = (row_ok && KB > 1) ? __ldg(sa + 1) : 0.0f;
+            float s_w1 = (cols_ok && KB > 1) ? __ldg(sw + 1) : 0.0f;
             for (int kb = 0; kb < KB; ++kb) {
                 const uint32_t pb = pidx & 1u;
                 const uint32_t pph = (pidx >> 1) & 1u;
@@ -362,10 +366,11 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
                 }
                 tc_fence_after_sync();
                 const float scale = s_a * s_w;
-                // Next block's scales, fetched while this block is promoted.
-                if (kb + 1 < KB) {
-                    s_a = row_ok ? __ldg(sa + kb + 1) : 0.0f;
-                    s_w = cols_ok ? __ldg(sw + kb + 1) : 0.0f;
+                s_a = s_a1;
+                s_w = s_w1;
+                if (kb + 2 < KB) {
+                    s_a1 = row_ok ? __ldg(sa + kb + 2) : 0.0f;
+                    s_w1 = cols_ok ? __ldg(sw + kb + 2) : 0.0f;
                 }
                 const uint32_t taddr =
                     tmem_base + (static_cast<uint32_t>(q * 32) << 16) + pb * Cfg::P_COLS + half * Cfg::SCALE_BLOCK;

@@ -1,11 +1,13 @@
 """Runs one named workload through the C ABI a few times and prints the timings.
 
     python -m dense_fp16_gemm_05_gb300.run --workload relu_8192 --reps 4 [--config ID]
-        [--op gemm|dA_nt|dB_tn|relu_backward]
+        [--op gemm|dA_nt|dB_tn|relu_backward|fp8]
 
 --op picks the kernel: the forward GEMM (default), the two backward GEMMs of
 the workload (dA = dZ @ B^T in the NT layout, dB = A^T @ dZ in the TN layout)
-or the ReLU-gradient mask over an (M,N) gradient.
+or the ReLU-gradient mask over an (M,N) gradient; --op fp8 runs the FP8
+block-scaled GEMM on the workload's sizes (E4M3 operands quantized per
+128-block, fp32 scales).
 
 A minimal program around the library (no oracle, no other kernels besides the
 input upload), suited as the target of a profiler capture: every GPU kernel it
@@ -19,7 +21,7 @@ import json
 import torch
 
 from . import gemm_f16 as g
-from .inputs import WORKLOADS, Workload, draw_workload
+from .inputs import WORKLOADS, Workload, draw_fp8_block_scaled, draw_workload
 
 
 def main(argv=None):
@@ -28,7 +30,7 @@ def main(argv=None):
     p.add_argument("--reps", type=int, default=4)
     p.add_argument("--config", type=int, default=0)
     p.add_argument("--relu", type=int, default=None, help="override the workload's ReLU flag")
-    p.add_argument("--op", default="gemm", choices=["gemm", "dA_nt", "dB_tn", "relu_backward"])
+    p.add_argument("--op", default="gemm", choices=["gemm", "dA_nt", "dB_tn", "relu_backward", "fp8"])
     args = p.parse_args(argv)
     if args.workload in WORKLOADS:
         w = WORKLOADS[args.workload]
@@ -37,6 +39,8 @@ def main(argv=None):
         w = Workload(args.workload, M, N, K, True, "normal_scaled", 0)
     relu = w.relu if args.relu is None else bool(args.relu)
     dev = torch.device("cuda", 0)
+    if args.op == "fp8":
+        return run_fp8(w, relu, args.reps, dev)
     A_cpu, B_cpu = draw_workload(w)
     A, B = A_cpu.to(dev), B_cpu.to(dev)
     C = torch.empty((w.M, w.N), dtype=torch.float16, device=dev)
@@ -77,6 +81,24 @@ def main(argv=None):
     else:
         out["best_tflops"] = w.flops / (best * 1e-3) / 1e12
     print(json.dumps(out))
+
+
+def run_fp8(w, relu, reps, dev):
+    A8, SA, W8, SW = (t.to(dev) for t in draw_fp8_block_scaled(w.M, w.N, w.K, "normal", w.seed))
+    C = torch.empty((w.M, w.N), dtype=torch.float16, device=dev)
+    times = []
+    for _ in range(reps):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        g.gemm_fp8_block_scaled(A8, SA, W8, SW, C=C, relu=relu)
+        e.record()
+        e.synchronize()
+        times.append(s.elapsed_time(e))
+    st = g.check()
+    if st != g.GEMM_OK:
+        raise SystemExit(f"device status {st}: {g.strerror(st)}")
+    print(json.dumps({"workload": w.name, "op": "fp8", "M": w.M, "N": w.N, "K": w.K, "relu": relu, "ms": times,
+                      "best_tflops": w.flops / (min(times) * 1e-3) / 1e12}))
 
 
 if __name__ == "__main__":
