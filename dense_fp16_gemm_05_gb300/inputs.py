@@ -147,3 +147,55 @@ FP8_WORKLOADS: dict[str, Fp8Workload] = {
     "fp8_ragged_1000": Fp8Workload("fp8_ragged_1000", 1000, 1000, 1040, True, "normal", 22),
     "fp8_8192": Fp8Workload("fp8_8192", 8192, 8192, 8192, False, "normal", 23),
 }
+
+
+# ---------------------------------------------------------------------------
+# Attention forward operands.  The TileLang-MUSA lesson (section 5) declares
+# Q, K, V and O as (batch, heads, seq, dim) float16 buffers; they are drawn
+# as the pages draw GEMM operands (torch.randn in float32, rounded to
+# float16), Q first, then K, then V, from one generator.
+
+
+@dataclass(frozen=True)
+class AttnWorkload:
+    """O = softmax(sm_scale Q K^T [causal]) V per (batch, head)."""
+    name: str
+    batch: int
+    heads: int
+    seq: int
+    dim: int
+    causal: bool
+    seed: int
+
+    @property
+    def sm_scale(self) -> float:
+        return 1.0 / math.sqrt(self.dim)
+
+    @property
+    def flops(self) -> int:
+        # two matmuls of 2 * seq * seq * dim per (batch, head); causal: the
+        # half of the score matrix on and below the diagonal
+        full = 4 * self.batch * self.heads * self.seq * self.seq * self.dim
+        return full // 2 if self.causal else full
+
+
+def draw_attention(batch: int, heads: int, seq: int, dim: int, seed: int):
+    """CPU float16 tensors Q, K, V of shape (batch, heads, seq, dim)."""
+    g = torch.Generator().manual_seed(int(seed))
+    shape = (batch, heads, seq, dim)
+    q = torch.randn(shape, generator=g, dtype=torch.float32)
+    k = torch.randn(shape, generator=g, dtype=torch.float32)
+    v = torch.randn(shape, generator=g, dtype=torch.float32)
+    return q.half(), k.half(), v.half()
+
+
+def draw_attention_workload(w: AttnWorkload):
+    return draw_attention(w.batch, w.heads, w.seq, w.dim, w.seed)
+
+
+ATTN_WORKLOADS: dict[str, AttnWorkload] = {
+    "attn_small_d64": AttnWorkload("attn_small_d64", 1, 2, 200, 64, False, 41),
+    "attn_causal_ragged_d128": AttnWorkload("attn_causal_ragged_d128", 2, 3, 300, 128, True, 42),
+    "attn_4096_d128": AttnWorkload("attn_4096_d128", 4, 32, 4096, 128, False, 43),
+    "attn_4096_d128_causal": AttnWorkload("attn_4096_d128_causal", 4, 32, 4096, 128, True, 44),
+}

@@ -52,6 +52,9 @@ def _load():
         lib.oracle_e4m3_to_f64.restype = ctypes.c_double
         lib.oracle_gemm_fp8_block_scaled_rows.argtypes = [p, p, p, p, p, i64, i64, i64, i64, ctypes.c_int, p, i64]
         lib.oracle_gemm_fp8_block_scaled_rows.restype = ctypes.c_int
+        lib.oracle_attention_fwd_rows.argtypes = [p, p, p, p, i64, i64, i64, i64, ctypes.c_double, ctypes.c_int,
+                                                  p, i64]
+        lib.oracle_attention_fwd_rows.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -223,3 +226,36 @@ def gemm_fp8_block_scaled(A, SA, W, SW, relu: bool, block: int = 128, rows=None)
     if rc != 0:
         raise ValueError("oracle_gemm_fp8_block_scaled_rows rejected its arguments")
     return c.view(np.float16)
+
+
+# ---------------------------------------------------------------------------
+# Attention forward (the FlashAttention skeleton of the TileLang-MUSA lesson,
+# section 5; the plain definition is written out in gemm_oracle.c above
+# oracle_attention_fwd_rows).
+
+def attention_fwd(Q, K, V, sm_scale: float, causal: bool, rows=None) -> np.ndarray:
+    """O = softmax(sm_scale Q K^T [causal mask]) V per (batch, head), fp16 out.
+
+    Q, K, V: (batch, heads, seq, dim) float16 (numpy, uint16 bits or CPU
+    torch).  Without ``rows`` returns O (batch, heads, seq, dim); with
+    ``rows`` (flat indices (b*heads + h)*seq + i) returns those rows stacked,
+    shape (len(rows), dim).
+    """
+    q, k, v = _as_f16_bits(Q), _as_f16_bits(K), _as_f16_bits(V)
+    if q.ndim != 4 or q.shape != k.shape or q.shape != v.shape:
+        raise ValueError(f"Q, K, V must share one (batch, heads, seq, dim) shape: {q.shape} {k.shape} {v.shape}")
+    B, H, S, D = q.shape
+    lib = _load()
+    if rows is None:
+        n_rows, rows_ptr = B * H * S, None
+    else:
+        rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        n_rows, rows_ptr = rows_arr.size, rows_arr.ctypes.data
+    o = np.empty((n_rows, D), dtype=np.uint16)
+    ptr = lambda x: x.ctypes.data if x.size else None
+    rc = lib.oracle_attention_fwd_rows(ptr(q), ptr(k), ptr(v), ptr(o), B, H, S, D, float(sm_scale),
+                                       int(bool(causal)), rows_ptr, n_rows)
+    if rc != 0:
+        raise ValueError("oracle_attention_fwd_rows rejected its arguments")
+    o = o.view(np.float16)
+    return o.reshape(B, H, S, D) if rows is None else o

@@ -259,3 +259,78 @@ int oracle_gemm_fp8_block_scaled_rows(const uint8_t *A, const float *SA, const u
     }
     return 0;
 }
+
+/* ======================================================================
+ * Attention forward (TEST INFRASTRUCTURE ONLY, like everything above).
+ *
+ * The TileLang-MUSA lesson (7yue.com, section 5, "FlashAttention skeleton")
+ * and "Writing High-Performance Kernels in TileLang, from GEMM to MLA"
+ * (section "A real one: MLA decode", the FlashAttention loop) describe the
+ * FlashAttention forward: Q, K, V, O of shape (batch, heads, seq, dim) in
+ * float16; per query row the scores against every key, a softmax over them
+ * (computed blockwise with a running max and sum), and the probability-
+ * weighted sum of the value rows.  The blockwise online form is an
+ * implementation of the plain definition, which this function writes out:
+ *
+ *   s_j   = sm_scale * sum_d Q[b,h,i,d] * K[b,h,j,d]     for keys j allowed
+ *   O[b,h,i,d] = f16_rne( sum_j exp(s_j - max_j s_j) * V[b,h,j,d]
+ *                          / sum_j exp(s_j - max_j s_j) )
+ *
+ * Keys allowed: all j < seq; with `causal`, only j <= i.  The skeletons do
+ * not show the softmax temperature; sm_scale is a parameter (callers pass
+ * 1/sqrt(dim), the usual choice).  Everything is fp64 (fp16 inputs are exact
+ * there, exp from libm); the only rounding that matters is the final cast.
+ * ====================================================================== */
+
+int oracle_attention_fwd_rows(const uint16_t *Q, const uint16_t *K, const uint16_t *V, uint16_t *O_out,
+                              int64_t batch, int64_t heads, int64_t seq, int64_t dim, double sm_scale, int causal,
+                              const int64_t *rows, int64_t n_rows)
+{
+    if (batch < 0 || heads < 0 || seq < 0 || dim < 0 || n_rows < 0) return -1;
+    const int64_t total = batch * heads * seq;
+    if (rows == NULL && n_rows != total) return -1;
+    for (int64_t r = 0; rows != NULL && r < n_rows; ++r)
+        if (rows[r] < 0 || rows[r] >= total) return -1;
+    if (n_rows == 0 || dim == 0) return 0;
+    fill_f16_values();
+
+    int failed = 0;
+#pragma omp parallel
+    {
+        double *s = (double *)malloc((size_t)(seq > 0 ? seq : 1) * sizeof(double));
+        double *o = (double *)malloc((size_t)dim * sizeof(double));
+        if (s == NULL || o == NULL) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t r = 0; r < n_rows; ++r) {
+            if (s == NULL || o == NULL) continue;
+            const int64_t flat = rows ? rows[r] : r;     /* (b*heads + h)*seq + i */
+            const int64_t bh = flat / seq, i = flat % seq;
+            const uint16_t *q = Q + flat * dim;
+            const uint16_t *kbase = K + bh * seq * dim;
+            const uint16_t *vbase = V + bh * seq * dim;
+            const int64_t n_keys = causal ? i + 1 : seq;
+            double m = -INFINITY;
+            for (int64_t j = 0; j < n_keys; ++j) {
+                double dot = 0.0;
+                for (int64_t d = 0; d < dim; ++d) dot += g_f16_value[q[d]] * g_f16_value[kbase[j * dim + d]];
+                s[j] = sm_scale * dot;
+                if (s[j] > m) m = s[j];
+            }
+            double l = 0.0;
+            for (int64_t d = 0; d < dim; ++d) o[d] = 0.0;
+            for (int64_t j = 0; j < n_keys; ++j) {
+                const double p = exp(s[j] - m);
+                l += p;
+                for (int64_t d = 0; d < dim; ++d) o[d] += p * g_f16_value[vbase[j * dim + d]];
+            }
+            uint16_t *out = O_out + r * dim;
+            for (int64_t d = 0; d < dim; ++d) out[d] = oracle_f64_to_f16(o[d] / l);
+        }
+        free(s);
+        free(o);
+    }
+    return failed ? -1 : 0;
+}
