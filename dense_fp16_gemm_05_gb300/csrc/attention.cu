@@ -1,0 +1,74 @@
+// attention.cu -- host-side launch of the attention-forward kernel
+// (attention_kernel.cuh).  The C ABI entry, attention_fwd_f16 in gemm_f16.cu,
+// validates every argument and calls launch_attention.
+#include "attention_launch.cuh"
+
+#include <cmath>
+
+#include "attention_kernel.cuh"
+
+namespace gemm_sm103 {
+
+namespace {
+
+template <int kDim>
+struct AttnPrepared {
+    static std::atomic<int> ready[kMaxDevices];
+
+    static bool get(int dev)
+    {
+        if (ready[dev].load(std::memory_order_acquire)) return true;
+        if (cudaFuncSetAttribute(attention_fwd_sm103a<kDim>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 AttnCfg<kDim>::SMEM_BYTES) != cudaSuccess) {
+            cudaGetLastError();
+            return false;
+        }
+        ready[dev].store(1, std::memory_order_release);
+        return true;
+    }
+
+    static void forget(int dev) { ready[dev].store(0, std::memory_order_release); }
+};
+
+template <int kDim>
+std::atomic<int> AttnPrepared<kDim>::ready[kMaxDevices];
+
+template <int kDim>
+int launch_dim(const AttnLaunchArgs &a)
+{
+    using Cfg = AttnCfg<kDim>;
+    const uint64_t bh = static_cast<uint64_t>(a.batch) * static_cast<uint64_t>(a.heads);
+    CUtensorMap tq, tk, tv;
+    int st;
+    if ((st = encode_bhsd(&tq, a.Q, bh, a.seq, kDim)) != GEMM_OK) return st;
+    if ((st = encode_bhsd(&tk, a.K, bh, a.seq, kDim)) != GEMM_OK) return st;
+    if ((st = encode_bhsd(&tv, a.V, bh, a.seq, kDim)) != GEMM_OK) return st;
+    AttnParams p{};
+    p.batch = static_cast<int32_t>(a.batch);
+    p.heads = static_cast<int32_t>(a.heads);
+    p.seq = static_cast<int32_t>(a.seq);
+    p.num_q_blocks = static_cast<int32_t>((a.seq + Cfg::BQ - 1) / Cfg::BQ);
+    p.causal = a.causal;
+    p.scale_log2 = static_cast<float>(static_cast<double>(a.sm_scale) * 1.4426950408889634);   // log2(e)
+    p.timeout_cycles = timeout_cycles_for(a.seq * kDim);
+    p.O = static_cast<__half *>(a.O);
+    p.status = a.status;
+    if (!AttnPrepared<kDim>::get(a.dev.device)) return GEMM_ERR_LAUNCH;
+    const dim3 grid(static_cast<unsigned>(p.num_q_blocks), static_cast<unsigned>(a.heads),
+                    static_cast<unsigned>(a.batch));
+    attention_fwd_sm103a<kDim><<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, a.stream>>>(tq, tk, tv, p);
+    if (cudaGetLastError() != cudaSuccess) {
+        AttnPrepared<kDim>::forget(a.dev.device);
+        return GEMM_ERR_LAUNCH;
+    }
+    return GEMM_OK;
+}
+
+}  // namespace
+
+int launch_attention(const AttnLaunchArgs &a)
+{
+    return a.dim == 64 ? launch_dim<64>(a) : launch_dim<128>(a);
+}
+
+}  // namespace gemm_sm103

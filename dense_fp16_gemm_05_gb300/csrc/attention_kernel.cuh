@@ -1,0 +1,467 @@
+// attention_kernel.cuh -- attention forward for sm_103a (the FlashAttention
+// loop of the TileLang-MUSA lesson, 7yue.com, section 5, and of "Writing
+// High-Performance Kernels in TileLang, from GEMM to MLA", MLA section):
+//
+//   O[b,h,i,:] = sum_j softmax_j(sm_scale * Q[b,h,i,:] . K[b,h,j,:]) V[b,h,j,:]
+//
+// over keys j < seq (j <= i when causal); Q, K, V, O (batch, heads, seq, dim)
+// row-major fp16, dim 64 or 128.  Per query block of 128 rows the keys are
+// streamed in blocks of 128 with a running row maximum and row sum, so the
+// score matrix is never stored.
+//
+// One CTA per (query block, head, batch); 192 threads:
+//   warp 0, one lane   TMA: Q once (3-D tensor maps: rows of another head are
+//                      never read, rows past seq read as zero), then K and V
+//                      blocks through two-slot rings
+//   warp 1, one lane   MMA issuer (and TMEM owner): S_j = Q K_j^T into one of
+//                      two 128-column TMEM score buffers, O += P_j V_j into a
+//                      dim-column TMEM output accumulator; S_{j+1} is issued
+//                      before O += P_j V_j so the tensor core works on the next
+//                      scores while the softmax of this block runs
+//   warps 2..5         softmax: one query row per thread (TMEM lane); read the
+//                      row's 128 scores, mask, row max, p = 2^(s*c - m) with
+//                      c = sm_scale * log2(e), row sum, P in fp16 into shared
+//                      memory (the 128-byte-swizzled K-major layout the MMA
+//                      reads as its A operand); at the end O / l to global
+// The reference maximum m only moves when a block's maximum exceeds it by more
+// than 8 (in log2 units); then O (in TMEM) and l are multiplied by 2^(m_old -
+// m_new).  Otherwise p <= 2^8 is used as is: every weight is relative to the
+// same m, so the normalised result is the same, and fp16 holds p exactly as
+// well (relative precision does not depend on magnitude).
+// Every wait is bounded; on expiry the site is recorded in the device status
+// word and all roles leave.
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include <cstdint>
+
+#include "gemm_kernel.cuh"
+
+namespace gemm_sm103 {
+
+// ---------------------------------------------------------------- PTX
+
+// 3-D tiled load of one box into this CTA's shared memory.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int32_t x, int32_t y,
+                                            int32_t z)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::
+            "r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
+// 32 consecutive fp32 TMEM columns of the warp's 32 lanes: load (and wait),
+// and store (and wait).
+__device__ __forceinline__ void attn_tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
+          "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+          "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ void attn_tmem_st32(uint32_t taddr, const uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n\t"
+        "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+// 2^x on the special-function unit (approximate, about 2 ulp of fp32;
+// 2^-inf = +0).
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// ---------------------------------------------------------------- configuration
+
+template <int kDim>
+struct AttnCfg {
+    static constexpr int DIM = kDim;
+    static constexpr int BQ = 128;                // query rows per CTA (TMEM lanes)
+    static constexpr int BKV = 128;               // keys per block
+    static constexpr int THREADS = 192;
+    static constexpr int ATOMS = kDim / 64;       // 128-byte swizzle atoms along dim
+    static constexpr int TILE_BYTES = 128 * kDim * 2;   // Q, K or V tile of 128 rows
+    static constexpr int ATOM_BYTES = 128 * 128;        // 128 rows x 128 bytes
+    static constexpr int P_BYTES = BQ * BKV * 2;         // P tile, fp16
+    static constexpr int SMEM_Q_OFF = 0;
+    static constexpr int SMEM_K_OFF = SMEM_Q_OFF + TILE_BYTES;
+    static constexpr int SMEM_V_OFF = SMEM_K_OFF + 2 * TILE_BYTES;
+    static constexpr int SMEM_P_OFF = SMEM_V_OFF + 2 * TILE_BYTES;
+    static constexpr int SMEM_CTL_OFF = SMEM_P_OFF + 2 * P_BYTES;
+    static constexpr int SMEM_CTL_BYTES = 256;
+    static constexpr int SMEM_BYTES = 1024 + SMEM_CTL_OFF + SMEM_CTL_BYTES;
+    static constexpr int TMEM_S_COL = 0;          // two score buffers of 128 columns
+    static constexpr int TMEM_O_COL = 2 * BKV;    // output accumulator, kDim columns
+    static constexpr int TMEM_COLS = 512;
+    static constexpr uint32_t IDESC_S = idesc_f16_f32(BQ, BKV, false, false);   // Q K-major, K K-major
+    static constexpr uint32_t IDESC_O = idesc_f16_f32(BQ, kDim, false, true);   // P K-major, V MN-major
+
+    static_assert(kDim == 64 || kDim == 128, "head dimension 64 or 128");
+    static_assert(TMEM_O_COL + kDim <= TMEM_COLS, "TMEM columns");
+    static_assert(SMEM_BYTES <= 232448, "shared memory per block on sm_103");
+};
+
+struct AttnParams {
+    int32_t batch, heads, seq;
+    int32_t num_q_blocks;    // ceil(seq / 128)
+    int32_t causal;
+    float scale_log2;        // sm_scale * log2(e)
+    uint64_t timeout_cycles;
+    __half *O;
+    unsigned long long *status;
+};
+
+template <int kDim>
+__global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
+    attention_fwd_sm103a(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                         const __grid_constant__ CUtensorMap tmap_v, const AttnParams p)
+{
+    using Cfg = AttnCfg<kDim>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *base_ptr = smem_raw + (base - raw);
+    const uint32_t sQ = base + Cfg::SMEM_Q_OFF;
+    const uint32_t sK = base + Cfg::SMEM_K_OFF;
+    const uint32_t sV = base + Cfg::SMEM_V_OFF;
+    const uint32_t sP = base + Cfg::SMEM_P_OFF;
+    const uint32_t ctl = base + Cfg::SMEM_CTL_OFF;
+    // Barriers: q_full; k_full[2], k_empty[2]; v_full[2], v_empty[2];
+    // s_full[2], s_empty[2]; p_full[2], p_empty[2]; o_ready.
+    const uint32_t q_full = ctl;
+    auto k_full = [&](int i) { return ctl + 8u * (1 + i); };
+    auto k_empty = [&](int i) { return ctl + 8u * (3 + i); };
+    auto v_full = [&](int i) { return ctl + 8u * (5 + i); };
+    auto v_empty = [&](int i) { return ctl + 8u * (7 + i); };
+    auto s_full = [&](int i) { return ctl + 8u * (9 + i); };
+    auto s_empty = [&](int i) { return ctl + 8u * (11 + i); };
+    auto p_full = [&](int i) { return ctl + 8u * (13 + i); };
+    auto p_empty = [&](int i) { return ctl + 8u * (15 + i); };
+    const uint32_t o_ready = ctl + 8u * 17;
+    const uint32_t tmem_slot = ctl + 8u * 18;
+    const uint32_t abort_addr = tmem_slot + 4;
+    volatile uint32_t *tmem_slot_ptr = reinterpret_cast<volatile uint32_t *>(base_ptr + Cfg::SMEM_CTL_OFF + 8 * 18);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    // Heavier (causal) query blocks first: block index reversed.
+    const int qb = p.num_q_blocks - 1 - static_cast<int>(blockIdx.x);
+    const int head = static_cast<int>(blockIdx.y);
+    const int bh = static_cast<int>(blockIdx.z) * p.heads + head;
+    const int kv_blocks_all = (p.seq + Cfg::BKV - 1) / Cfg::BKV;
+    const int nblk = p.causal ? min(qb + 1, kv_blocks_all) : kv_blocks_all;
+
+    AbortFlag abort;
+    abort.local = reinterpret_cast<volatile int *>(tmem_slot_ptr + 1);
+    abort.status = p.status;
+    abort.addr = abort_addr;
+    abort.cluster = 1;
+    abort.rank = 0;
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(k_full(i), 1);
+            mbar_init(k_empty(i), 1);
+            mbar_init(v_full(i), 1);
+            mbar_init(v_empty(i), 1);
+            mbar_init(s_full(i), 1);
+            mbar_init(s_empty(i), 4);   // the four softmax warps
+            mbar_init(p_full(i), 4);
+            mbar_init(p_empty(i), 1);
+        }
+        mbar_init(o_ready, 1);
+        *abort.local = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&tmap_q);
+        prefetch_tensormap(&tmap_k);
+        prefetch_tensormap(&tmap_v);
+    }
+    if (warp == 1) {
+        tmem_alloc<1>(tmem_slot, Cfg::TMEM_COLS);
+        tmem_relinquish<1>();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot_ptr;
+    const uint64_t limit = p.timeout_cycles;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            bool ok = true;
+            mbar_arrive_expect_tx(q_full, Cfg::TILE_BYTES);
+#pragma unroll
+            for (int a = 0; a < Cfg::ATOMS; ++a)
+                tma_load_3d(sQ + a * Cfg::ATOM_BYTES, &tmap_q, q_full, a * 64, qb * Cfg::BQ, bh);
+            for (int j = 0; ok && j < nblk; ++j) {
+                const int slot = j & 1;
+                const uint32_t ph = (j >> 1) & 1u;
+                if (!wait_phase(k_empty(slot), ph ^ 1u, abort, limit, kSiteProducerEmpty)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(k_full(slot), Cfg::TILE_BYTES);
+#pragma unroll
+                for (int a = 0; a < Cfg::ATOMS; ++a)
+                    tma_load_3d(sK + slot * Cfg::TILE_BYTES + a * Cfg::ATOM_BYTES, &tmap_k, k_full(slot), a * 64,
+                                j * Cfg::BKV, bh);
+                if (!wait_phase(v_empty(slot), ph ^ 1u, abort, limit, kSiteProducerEmpty)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(v_full(slot), Cfg::TILE_BYTES);
+#pragma unroll
+                for (int a = 0; a < Cfg::ATOMS; ++a)
+                    tma_load_3d(sV + slot * Cfg::TILE_BYTES + a * Cfg::ATOM_BYTES, &tmap_v, v_full(slot), a * 64,
+                                j * Cfg::BKV, bh);
+            }
+            if (!ok) {
+                // Let every load this thread issued land before the CTA exits
+                // (each ring slot holds at most one load in flight).
+                const long long t0 = clock64();
+                while (clock64() - t0 < 1000000) {
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            bool ok = wait_phase(q_full, 0, abort, limit, kSiteMmaFull);
+            bool issued_any = false;
+            const uint64_t q_desc = smem_desc_sw128(sQ, 16, 1024);
+            const uint64_t k_desc0 = smem_desc_sw128(sK, 16, 1024);
+            const uint64_t v_desc0 = smem_desc_sw128(sV, Cfg::ATOM_BYTES, 1024);
+            const uint64_t p_desc0 = smem_desc_sw128(sP, 16, 1024);
+            const uint32_t o_tmem = tmem_base + Cfg::TMEM_O_COL;
+            // K step t of 16 elements along dim (K-major tiles): atom t/4, +32 B per step inside it.
+            auto dim_step = [](int t) -> uint64_t {
+                return static_cast<uint64_t>(((t >> 2) * Cfg::ATOM_BYTES + (t & 3) * 32) >> 4);
+            };
+            // O += P_j V_j for block jj (issued one block behind the scores).
+            auto issue_pv = [&](int jj) -> bool {
+                const int slot = jj & 1;
+                const uint32_t ph = (jj >> 1) & 1u;
+                if (!wait_phase(v_full(slot), ph, abort, limit, kSiteMmaFull) ||
+                    !wait_phase(p_full(slot), ph, abort, limit, kSiteMmaTmemEmpty))
+                    return false;
+                tc_fence_after_sync();
+                const uint64_t p_desc = p_desc0 + static_cast<uint64_t>((slot * Cfg::P_BYTES) >> 4);
+                const uint64_t v_desc = v_desc0 + static_cast<uint64_t>((slot * Cfg::TILE_BYTES) >> 4);
+#pragma unroll
+                for (int t = 0; t < Cfg::BKV / 16; ++t) {
+                    // P (A, K-major along keys): atom t/4, +32 B per step; V (B,
+                    // MN-major along dim): 16 key rows = +2 KB per step.
+                    const uint64_t pa = p_desc + static_cast<uint64_t>(((t >> 2) * Cfg::ATOM_BYTES + (t & 3) * 32) >> 4);
+                    const uint64_t vb = v_desc + static_cast<uint64_t>((t * 16 * 128) >> 4);
+                    mma_f16_ss<1>(o_tmem, pa, vb, Cfg::IDESC_O, (jj > 0 || t > 0) ? 1u : 0u);
+                }
+                mma_commit(v_empty(slot));
+                mma_commit(p_empty(slot));
+                mma_commit(o_ready);
+                return true;
+            };
+            for (int j = 0; ok && j < nblk; ++j) {
+                const int slot = j & 1;
+                const uint32_t ph = (j >> 1) & 1u;
+                if (!wait_phase(k_full(slot), ph, abort, limit, kSiteMmaFull) ||
+                    !wait_phase(s_empty(slot), ph ^ 1u, abort, limit, kSiteMmaTmemEmpty)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t s_tmem = tmem_base + Cfg::TMEM_S_COL + slot * Cfg::BKV;
+                const uint64_t k_desc = k_desc0 + static_cast<uint64_t>((slot * Cfg::TILE_BYTES) >> 4);
+#pragma unroll
+                for (int t = 0; t < kDim / 16; ++t)
+                    mma_f16_ss<1>(s_tmem, q_desc + dim_step(t), k_desc + dim_step(t), Cfg::IDESC_S, t > 0 ? 1u : 0u);
+                mma_commit(k_empty(slot));
+                mma_commit(s_full(slot));
+                issued_any = true;
+                if (j >= 1 && !issue_pv(j - 1)) {
+                    ok = false;
+                    break;
+                }
+            }
+            if (ok && nblk > 0) ok = issue_pv(nblk - 1);
+            if (!ok) {
+                if (issued_any) {
+                    // Wait for this thread's MMAs before the TMEM is freed.
+                    const uint32_t drain = ctl + 8u * 19;
+                    mbar_init(drain, 1);
+                    fence_mbar_init();
+                    mma_commit(drain);
+                    wait_phase_drain(drain, 0, limit, kSiteDrainMma, p.status);
+                }
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax (warps 2..5)
+        const int q = warp & 3;
+        const int row = qb * Cfg::BQ + q * 32 + lane;
+        const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
+        const uint32_t sw = static_cast<uint32_t>(lane & 7);
+        float m_ref = -INFINITY;   // reference maximum (log2 units, scaled scores)
+        float l = 0.0f;            // sum of weights relative to m_ref
+        bool ok = true;
+        for (int j = 0; j < nblk; ++j) {
+            const int slot = j & 1;
+            const uint32_t ph = (j >> 1) & 1u;
+            const bool got = wait_phase(s_full(slot), ph, abort, limit, kSiteEpilogueTmemFull);
+            if (!__all_sync(0xffffffffu, got)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+            // This row's 128 scores of block j, scaled into log2 units, masked.
+            float x[Cfg::BKV];
+            const uint32_t s_addr = tmem_base + lane_addr + Cfg::TMEM_S_COL + slot * Cfg::BKV;
+#pragma unroll
+            for (int c = 0; c < Cfg::BKV / 32; ++c) {
+                uint32_t r[32];
+                attn_tmem_ld32(s_addr + c * 32, r);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(r[i]) * p.scale_log2;
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s_empty(slot));   // the score buffer may be overwritten
+            const int key0 = j * Cfg::BKV;
+            const int last_key = p.causal ? min(row, p.seq - 1) : p.seq - 1;
+            if (key0 + Cfg::BKV - 1 > last_key) {
+#pragma unroll
+                for (int i = 0; i < Cfg::BKV; ++i)
+                    if (key0 + i > last_key) x[i] = -INFINITY;
+            }
+            float mx = x[0];
+#pragma unroll
+            for (int i = 1; i < Cfg::BKV; ++i) mx = fmaxf(mx, x[i]);
+            // Move the reference only when this block's maximum exceeds it by
+            // more than 8 (weights then stay <= 2^8).
+            float alpha = 1.0f;
+            if (mx > m_ref + 8.0f) {
+                alpha = ex2_approx(m_ref - mx);   // 0 on the first block (m_ref = -inf)
+                l *= alpha;
+                m_ref = mx;
+            }
+            const bool rescale = j > 0 && __any_sync(0xffffffffu, alpha != 1.0f);
+            // P row (fp16) into shared buffer `slot` once the MMAs of block
+            // j - 2 have read it.
+            const bool got_p = wait_phase(p_empty(slot), ph ^ 1u, abort, limit, kSiteProducerEmpty);
+            if (!__all_sync(0xffffffffu, got_p)) {
+                ok = false;
+                break;
+            }
+            const uint32_t p_row = sP + slot * Cfg::P_BYTES + static_cast<uint32_t>(q * 32 + lane) * 128u;
+            float lsum = 0.0f;
+#pragma unroll
+            for (int a = 0; a < Cfg::BKV / 64; ++a) {
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        const float p0 = ex2_approx(x[a * 64 + c * 8 + 2 * h] - m_ref);
+                        const float p1 = ex2_approx(x[a * 64 + c * 8 + 2 * h + 1] - m_ref);
+                        lsum += p0 + p1;
+                        const __half2 v = __floats2half2_rn(p0, p1);
+                        w[h] = *reinterpret_cast<const uint32_t *>(&v);
+                    }
+                    // 16-byte chunk c of this row's atom a goes to chunk c ^ (row % 8).
+                    st_shared_v4(p_row + a * Cfg::ATOM_BYTES + ((static_cast<uint32_t>(c) ^ sw) << 4), w[0], w[1],
+                                 w[2], w[3]);
+                }
+            }
+            l += lsum;
+            fence_proxy_async_smem();   // the MMA reads P through the async proxy
+            if (j > 0) {
+                // O holds blocks 0 .. j-1 once their last MMAs completed.
+                const bool got_o = wait_phase(o_ready, (j - 1) & 1u, abort, limit, kSiteEpilogueTmemFull);
+                if (!__all_sync(0xffffffffu, got_o)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                if (rescale) {
+                    const uint32_t o_addr = tmem_base + lane_addr + Cfg::TMEM_O_COL;
+#pragma unroll
+                    for (int c = 0; c < kDim / 32; ++c) {
+                        uint32_t r[32];
+                        attn_tmem_ld32(o_addr + c * 32, r);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                        attn_tmem_st32(o_addr + c * 32, r);
+                    }
+                }
+                tc_fence_before_sync();
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full(slot));
+        }
+        if (ok && nblk > 0) {
+            const bool got_o = wait_phase(o_ready, (nblk - 1) & 1u, abort, limit, kSiteEpilogueTmemFull);
+            if (__all_sync(0xffffffffu, got_o)) {
+                tc_fence_after_sync();
+                const float inv_l = 1.0f / l;
+                const uint32_t o_addr = tmem_base + lane_addr + Cfg::TMEM_O_COL;
+                __half *orow = p.O + (static_cast<int64_t>(bh) * p.seq + row) * kDim;
+#pragma unroll
+                for (int c = 0; c < kDim / 32; ++c) {
+                    uint32_t r[32];
+                    attn_tmem_ld32(o_addr + c * 32, r);
+                    if (row < p.seq) {
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int h = 0; h < 4; ++h) {
+                                const __half2 hv = __floats2half2_rn(__uint_as_float(r[8 * v + 2 * h]) * inv_l,
+                                                                     __uint_as_float(r[8 * v + 2 * h + 1]) * inv_l);
+                                w[h] = *reinterpret_cast<const uint32_t *>(&hv);
+                            }
+                            st_global_v4(orow + c * 32 + v * 8, w[0], w[1], w[2], w[3]);
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after_sync();
+        tmem_dealloc<1>(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
+}  // namespace gemm_sm103

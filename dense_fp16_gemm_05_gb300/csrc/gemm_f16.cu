@@ -18,6 +18,7 @@
 #include <mutex>
 
 #include "gemm_f16.h"
+#include "attention_launch.cuh"
 #include "gemm_fp8_launch.cuh"
 #include "gemm_launch.cuh"
 
@@ -226,6 +227,23 @@ int encode_matrix_u8(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t 
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fns.encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides, box, estr,
                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+// (batch * heads, seq, dim) fp16 tensor, dims innermost first: dim, seq,
+// batch * heads; boxes of 64 x 128 x 1 with 128-byte swizzle.  A box never
+// crosses into another head's rows: rows past seq read as zero.
+int encode_bhsd(CUtensorMap *map, const void *ptr, uint64_t bh, uint64_t seq, uint64_t dim)
+{
+    const DriverFns &fns = driver();
+    if (!fns.ok) return GEMM_ERR_CUDA;
+    cuuint64_t dims[3] = {dim, seq, bh};
+    cuuint64_t strides[2] = {dim * 2, seq * dim * 2};
+    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fns.encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
+                            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
 }
@@ -545,6 +563,45 @@ extern "C" int gemm_fp8_launch_info(int64_t M, int64_t N, int64_t K, int *grid_c
     DeviceInfo dev;
     if ((st = current_device_info(&dev)) != GEMM_OK) return st;
     return fp8_launch_info(M, N, dev, grid_ctas, tiles);
+}
+
+extern "C" int attention_fwd_f16(const void *Q, const void *K, const void *V, void *O, int64_t batch,
+                                 int64_t heads, int64_t seq, int64_t dim, float sm_scale, int causal, void *stream)
+{
+    if (batch < 0 || heads < 0 || seq < 0) return reject(GEMM_ERR_INVALID_ARG, "a size is negative");
+    if (dim != 64 && dim != 128) return reject(GEMM_ERR_INVALID_ARG, "dim is not 64 or 128");
+    if (causal != 0 && causal != 1) return reject(GEMM_ERR_INVALID_ARG, "causal is not 0 or 1");
+    if (!std::isfinite(sm_scale)) return reject(GEMM_ERR_INVALID_ARG, "sm_scale is not finite");
+    if (batch > 65535 || heads > 65535 || seq > INT32_MAX)
+        return reject(GEMM_ERR_INVALID_ARG, "batch or heads above 65535, or seq above INT32_MAX");
+    if (batch == 0 || heads == 0 || seq == 0) return GEMM_OK;
+    DeviceInfo dev;
+    int st = current_device_info(&dev);
+    if (st != GEMM_OK) return st;
+    const uint64_t bytes = static_cast<uint64_t>(batch) * static_cast<uint64_t>(heads) * static_cast<uint64_t>(seq) *
+                           static_cast<uint64_t>(dim) * 2u;
+    if ((st = check_device_buffer(Q, bytes, dev.device)) != GEMM_OK) return st;
+    if ((st = check_device_buffer(K, bytes, dev.device)) != GEMM_OK) return st;
+    if ((st = check_device_buffer(V, bytes, dev.device)) != GEMM_OK) return st;
+    if ((st = check_device_buffer(O, bytes, dev.device)) != GEMM_OK) return st;
+    if (ranges_overlap(O, bytes, Q, bytes) || ranges_overlap(O, bytes, K, bytes) || ranges_overlap(O, bytes, V, bytes))
+        return reject(GEMM_ERR_INVALID_ARG, "O overlaps Q, K or V");
+    AttnLaunchArgs a;
+    a.Q = Q;
+    a.K = K;
+    a.V = V;
+    a.O = O;
+    a.batch = batch;
+    a.heads = heads;
+    a.seq = seq;
+    a.dim = dim;
+    a.sm_scale = sm_scale;
+    a.causal = causal;
+    a.dev = dev;
+    a.stream = static_cast<cudaStream_t>(stream);
+    a.status = status_word(dev.device);
+    if (a.status == nullptr) return GEMM_ERR_CUDA;
+    return launch_attention(a);
 }
 
 extern "C" int gemm_f16_num_configs(void) { return kNumConfigs; }

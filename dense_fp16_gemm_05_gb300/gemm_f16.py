@@ -9,6 +9,7 @@ call raises :class:`LibraryNotBuilt`.
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 import re
 
@@ -91,6 +92,8 @@ def lib() -> ctypes.CDLL:
     L.gemm_f16_config_layouts.restype = ci
     L.gemm_f16_selftest_timeout.argtypes = [vp, vp, vp, i64, i64, i64, ci, ctypes.c_uint64, vp]
     L.gemm_f16_selftest_timeout.restype = ci
+    L.attention_fwd_f16.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_float, ci, vp]
+    L.attention_fwd_f16.restype = ci
     L.gemm_fp8_block_scaled.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ci, vp]
     L.gemm_fp8_block_scaled.restype = ci
     pi = ctypes.POINTER(ctypes.c_int)
@@ -349,3 +352,32 @@ def fp8_launch_info(M: int, N: int, K: int) -> dict:
     if st != GEMM_OK:
         raise GemmError(st, "gemm_fp8_launch_info")
     return {"grid_ctas": g.value, "tiles": t.value}
+
+
+def attention_fwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, O: torch.Tensor | None = None,
+                  sm_scale: float | None = None, causal: bool = False, stream=None) -> torch.Tensor:
+    """O = softmax(sm_scale Q K^T [causal]) V per (batch, head).
+
+    Q, K, V (and O): contiguous float16 CUDA tensors of one shape
+    (batch, heads, seq, dim), dim 64 or 128; sm_scale defaults to
+    1/sqrt(dim).  O is allocated when not given.  Asynchronous on ``stream``.
+    """
+    for t, n in ((Q, "Q"), (K, "K"), (V, "V")):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.float16 or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous 4-D float16 tensor")
+    if Q.shape != K.shape or Q.shape != V.shape:
+        raise ValueError(f"Q, K, V shapes differ: {tuple(Q.shape)} {tuple(K.shape)} {tuple(V.shape)}")
+    B, H, S, D = Q.shape
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    if O is None:
+        O = torch.empty_like(Q)
+    if O.dtype != torch.float16 or O.shape != Q.shape or not O.is_contiguous():
+        raise ValueError("O must be a contiguous float16 tensor shaped like Q")
+    L = lib()
+    with torch.cuda.device(Q.device):
+        st = L.attention_fwd_f16(Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), B, H, S, D,
+                                 float(sm_scale), int(bool(causal)), _stream_handle(stream, Q.device))
+    if st != GEMM_OK:
+        raise GemmError(st, "attention_fwd_f16")
+    return O

@@ -42,7 +42,7 @@
 extern "C" {
 #endif
 
-#define GEMM_F16_VERSION 4
+#define GEMM_F16_VERSION 5
 
 /* Return codes.  0 is success; every error is negative. */
 enum gemm_f16_status {
@@ -187,6 +187,29 @@ int gemm_fp8_block_scaled(const void *A, const float *SA, const void *W, const f
  * device: persistent grid in CTAs (CTA pairs over 256 x 256 output tiles) and
  * the number of tiles.  Either pointer may be NULL.  Launches nothing. */
 int gemm_fp8_launch_info(int64_t M, int64_t N, int64_t K, int *grid_ctas, int *tiles);
+
+/*
+ * attention_fwd_f16 -- attention forward (the FlashAttention loop of the
+ * TileLang-MUSA lesson, 7yue.com, section 5, "FlashAttention skeleton"; the
+ * same loop in "Writing High-Performance Kernels in TileLang, from GEMM to
+ * MLA", MLA section):
+ *
+ *   O[b,h,i,:] = sum_j softmax_j(sm_scale * Q[b,h,i,:] . K[b,h,j,:]) V[b,h,j,:]
+ *
+ * over keys j < seq, or j <= i when causal = 1.  Q, K, V, O: device pointers
+ * to (batch, heads, seq, dim) row-major IEEE binary16 tensors on the current
+ * device, owned by the caller; O is written in place and must not overlap Q,
+ * K or V.  dim is 64 or 128.  sm_scale: the softmax temperature (the pages'
+ * skeletons do not show one; 1/sqrt(dim) is the usual value).  Scores and
+ * the running row sums are fp32, the probabilities are rounded to fp16 for
+ * the second product, the output is rounded once to fp16.  Checks before any
+ * launch: sizes >= 0, batch and heads <= 65535, dim, causal and a finite
+ * sm_scale (GEMM_ERR_INVALID_ARG); 16-byte aligned buffers inside one
+ * allocation of the current device.  Any size 0: no-op.  Only enqueues on
+ * `stream`; device timeouts are reported by gemm_f16_check.
+ */
+int attention_fwd_f16(const void *Q, const void *K, const void *V, void *O, int64_t batch, int64_t heads,
+                      int64_t seq, int64_t dim, float sm_scale, int causal, void *stream);
 
 /* Operand layouts a configuration supports: bit (transa * 2 + transb) is set
  * for each supported (transa, transb); 0xF = all four, 0x1 = only (0,0).

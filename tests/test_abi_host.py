@@ -157,3 +157,12 @@ def test_fp8_arguments_rejected_before_cuda(g):
     assert L.gemm_fp8_block_scaled(None, None, None, None, None, -1, 64, 64, 1, None) == g.GEMM_ERR_INVALID_ARG
     assert L.gemm_fp8_block_scaled(None, None, None, None, None, 64, 64, 64, 2, None) == g.GEMM_ERR_INVALID_ARG
     assert L.gemm_fp8_block_scaled(None, None, None, None, None, 0, 64, 64, 1, None) == g.GEMM_OK   # empty: no-op
+
+
+def test_attention_arguments_rejected_before_cuda(g):
+    L = g.lib()
+    assert L.attention_fwd_f16(None, None, None, None, 1, 1, 64, 96, 0.1, 0, None) == g.GEMM_ERR_INVALID_ARG
+    assert L.attention_fwd_f16(None, None, None, None, -1, 1, 64, 64, 0.1, 0, None) == g.GEMM_ERR_INVALID_ARG
+    assert L.attention_fwd_f16(None, None, None, None, 1, 1, 64, 64, 0.1, 2, None) == g.GEMM_ERR_INVALID_ARG
+    assert L.attention_fwd_f16(None, None, None, None, 1, 1, 64, 64, float("inf"), 0, None) == g.GEMM_ERR_INVALID_ARG
+    assert L.attention_fwd_f16(None, None, None, None, 0, 1, 64, 64, 0.1, 0, None) == g.GEMM_OK

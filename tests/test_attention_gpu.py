@@ -1,0 +1,111 @@
+"""GPU parity of the attention forward against the CPU oracle.
+
+Definition: the FlashAttention loop of the TileLang-MUSA lesson (7yue.com,
+section 5): O = softmax(sm_scale Q K^T) V per (batch, head), keys j <= i when
+causal.  Tolerance |gpu - ref| <= 6e-3 + 2e-3 |ref|, from the arithmetic: the
+probabilities are rounded to fp16 for the P V product (relative error
+<= 2^-11 per weight, so at most 2^-11 max|V| in the normalised sum, about
+2.8e-3 for |V| <= 5.8, the largest N(0,1) draw in these tensors), the output
+rounds once to fp16 (<= 2^-11 |O|), the 2^x unit and fp32 sums add far less;
+the bound is doubled for margin.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dense_fp16_gemm_05_gb300.inputs import ATTN_WORKLOADS, draw_attention, draw_attention_workload
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+ATOL, RTOL = 6e-3, 2e-3
+
+
+@pytest.fixture(scope="module")
+def g():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from dense_fp16_gemm_05_gb300 import build as gbuild
+    gbuild.build()
+    from dense_fp16_gemm_05_gb300 import gemm_f16
+    gemm_f16.lib()
+    return gemm_f16
+
+
+def run(g, Q, K, V, causal, sm_scale=None):
+    O = g.attention_fwd(Q.to(DEV), K.to(DEV), V.to(DEV), sm_scale=sm_scale, causal=causal)
+    assert g.check() == g.GEMM_OK
+    return O.cpu().numpy()
+
+
+def assert_close(got, ref, what):
+    got64, ref64 = got.astype(np.float64), ref.astype(np.float64)
+    assert got.shape == ref.shape, what
+    assert np.isfinite(got64).all(), f"{what}: non-finite output"
+    err = np.abs(got64 - ref64)
+    bad = err > ATOL + RTOL * np.abs(ref64)
+    assert not bad.any(), f"{what}: {int(bad.sum())} of {bad.size} outside tolerance, max err {err.max():.4g}"
+
+
+@pytest.mark.parametrize("name,causal", [("attn_small_d64", False), ("attn_small_d64", True),
+                                         ("attn_causal_ragged_d128", True), ("attn_causal_ragged_d128", False)])
+def test_workloads_full(g, name, causal):
+    w = ATTN_WORKLOADS[name]
+    Q, K, V = draw_attention_workload(w)
+    ref = oracle.attention_fwd(Q, K, V, sm_scale=w.sm_scale, causal=causal)
+    assert_close(run(g, Q, K, V, causal, w.sm_scale), ref, f"{name} causal={causal}")
+
+
+@pytest.mark.parametrize("name", ["attn_4096_d128", "attn_4096_d128_causal"])
+def test_4096_sampled_rows(g, name):
+    w = ATTN_WORKLOADS[name]
+    Q, K, V = draw_attention_workload(w)
+    got = run(g, Q, K, V, w.causal, w.sm_scale).reshape(-1, w.dim)
+    rng = np.random.default_rng(1)
+    S = w.seq
+    fixed = [0, 1, 127, 128, 2047, S - 1, S * w.heads * w.batch - 1, S * 5 + 3000]
+    rows = sorted(set(fixed) | set(int(r) for r in rng.integers(0, got.shape[0], 16)))
+    ref = oracle.attention_fwd(Q, K, V, sm_scale=w.sm_scale, causal=w.causal, rows=rows)
+    assert_close(got[rows], ref, name)
+
+
+@pytest.mark.parametrize("seq", [1, 2, 127, 128, 129, 255, 384])
+@pytest.mark.parametrize("dim", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_edge_lengths(g, seq, dim, causal):
+    Q, K, V = draw_attention(2, 2, seq, dim, seed=seq * 10 + dim + int(causal))
+    sm = 1.0 / np.sqrt(dim)
+    ref = oracle.attention_fwd(Q, K, V, sm_scale=sm, causal=causal)
+    assert_close(run(g, Q, K, V, causal, sm), ref, f"seq {seq} dim {dim} causal {causal}")
+
+
+def test_zero_queries_average_the_values(g):
+    Q = torch.zeros((1, 4, 300, 128), dtype=torch.float16)
+    _, K, V = draw_attention(1, 4, 300, 128, seed=77)
+    got = run(g, Q, K, V, False).astype(np.float64)
+    mean = V.double().mean(dim=2, keepdim=True).expand_as(V).numpy()
+    assert np.abs(got - mean).max() <= ATOL
+
+
+def test_large_scores_do_not_overflow(g):
+    # scores up to ~ 3e4: the running maximum keeps every exponent <= 8
+    Q, K, V = draw_attention(1, 2, 256, 64, seed=78)
+    Q = Q * 60.0
+    ref = oracle.attention_fwd(Q.half(), K, V, sm_scale=0.125, causal=False)
+    assert_close(run(g, Q.half(), K, V, False, 0.125), ref, "large scores")
+
+
+def test_rejected_arguments(g):
+    Q = torch.zeros((1, 1, 64, 96), dtype=torch.float16, device=DEV)
+    with pytest.raises(g.GemmError) as e:
+        g.attention_fwd(Q, Q.clone(), Q.clone())
+    assert e.value.status == g.GEMM_ERR_INVALID_ARG
+    Q = torch.zeros((1, 1, 64, 64), dtype=torch.float16, device=DEV)
+    with pytest.raises(g.GemmError):
+        g.attention_fwd(Q, Q.clone(), Q.clone(), O=Q)          # O overlaps Q
+    E = torch.zeros((1, 1, 0, 64), dtype=torch.float16, device=DEV)
+    g.attention_fwd(E, E, E)                                   # empty: no-op
+    assert g.check() == g.GEMM_OK
