@@ -407,6 +407,38 @@ def run_ours(args):
                "note": "back-to-back launches on resident operands"}
         del A8, SA8, W8, SW8, C8
 
+    # ---- attention forward (the next-row extension): 4096 tokens, 32 heads,
+    # batch 4, dim 128, fp16, non-causal and causal
+    attention = None
+    if not args.no_secondary:
+        from dense_fp16_gemm_05_gb300.inputs import ATTN_WORKLOADS, draw_attention_workload
+        attention = {}
+        for name in ("attn_4096_d128", "attn_4096_d128_causal"):
+            wa = ATTN_WORKLOADS[name]
+            Qa, Ka, Va = (t.to(dev) for t in draw_attention_workload(wa))
+            Oa = torch.empty_like(Qa)
+            for _ in range(3):
+                g.attention_fwd(Qa, Ka, Va, O=Oa, causal=wa.causal, stream=stream)
+            torch.cuda.synchronize()
+            sa, ea = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            reps_a = max(10, args.steps // 2)
+            sa.record(stream)
+            for _ in range(reps_a):
+                g.attention_fwd(Qa, Ka, Va, O=Oa, causal=wa.causal, stream=stream)
+            ea.record(stream)
+            ea.synchronize()
+            msa = sa.elapsed_time(ea) / reps_a
+            if g.check(stream) != g.GEMM_OK:
+                raise SystemExit("attention kernel reported a device error")
+            tfa = wa.flops / (msa * 1e-3) / 1e12
+            attention[name] = {"batch": wa.batch, "heads": wa.heads, "seq": wa.seq, "dim": wa.dim,
+                               "causal": wa.causal, "ms": msa, "TFLOP_s": tfa,
+                               "roofline": {"bound": "tensor", "achieved": tfa, "peak": peak, "unit": "TFLOP/s",
+                                            "frac": tfa / peak,
+                                            "peak_source": f"{peak_src} bf16 matmul burst (fp16 rate)"},
+                               "flops_counted": "4 batch heads seq^2 dim (halved when causal)", "launches": reps_a}
+            del Qa, Ka, Va, Oa
+
     # ---- end to end through the host-buffer C call
     A_h = A_cpu.pin_memory()
     B_h = B_cpu.pin_memory()
@@ -459,6 +491,8 @@ def run_ours(args):
             line["backward"] = backward
         if fp8 is not None:
             line["fp8_block_scaled"] = fp8
+        if attention is not None:
+            line["attention_fwd"] = attention
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()

@@ -18,11 +18,15 @@
 //                      dim-column TMEM output accumulator; S_{j+1} is issued
 //                      before O += P_j V_j so the tensor core works on the next
 //                      scores while the softmax of this block runs
-//   warps 2..5         softmax: one query row per thread (TMEM lane); read the
-//                      row's 128 scores, mask, row max, p = 2^(s*c - m) with
-//                      c = sm_scale * log2(e), row sum, P in fp16 into shared
-//                      memory (the 128-byte-swizzled K-major layout the MMA
-//                      reads as its A operand); at the end O / l to global
+//   warps 2..9         softmax: two threads per query row (TMEM lane), one per
+//                      half of each 128-key block: read 64 scores, mask,
+//                      partial row max (exchanged through shared memory),
+//                      p = 2^(s*c - m) with c = sm_scale * log2(e), partial
+//                      row sum, P in fp16 into shared memory (the 128-byte-
+//                      swizzled K-major layout the MMA reads as its A
+//                      operand: one swizzle atom per key half); at the end
+//                      the two partial sums are added and each thread writes
+//                      O / l for half of the row's dim columns
 // The reference maximum m only moves when a block's maximum exceeds it by more
 // than 8 (in log2 units); then O (in TMEM) and l are multiplied by 2^(m_old -
 // m_new).  Otherwise p <= 2^8 is used as is: every weight is relative to the
@@ -85,6 +89,24 @@ __device__ __forceinline__ void attn_tmem_st32(uint32_t taddr, const uint32_t (&
         : "memory");
 }
 
+// One fp32 TMEM column of the warp's 32 lanes: store (and wait), load (and wait).
+__device__ __forceinline__ void attn_tmem_st1(uint32_t taddr, float v)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};\n\ttcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+                 "r"(__float_as_uint(v))
+                 : "memory");
+}
+
+__device__ __forceinline__ float attn_tmem_ld1(uint32_t taddr)
+{
+    uint32_t r;
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];\n\ttcgen05.wait::ld.sync.aligned;"
+                 : "=r"(r)
+                 : "r"(taddr)
+                 : "memory");
+    return __uint_as_float(r);
+}
+
 // 2^x on the special-function unit (approximate, about 2 ulp of fp32;
 // 2^-inf = +0).
 __device__ __forceinline__ float ex2_approx(float x)
@@ -94,6 +116,40 @@ __device__ __forceinline__ float ex2_approx(float x)
     return y;
 }
 
+// Packed fp32 pairs (two lanes of arithmetic per instruction, each rounded
+// to nearest as the scalar form): (d0, d1) = (a0, a1) * b + c, and
+// (d0, d1) += (a0, a1).
+__device__ __forceinline__ void fma2_bcast(float &d0, float &d1, float a0, float a1, float b, float c)
+{
+    asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %4};\n\t"
+        "mov.b64 rc, {%5, %5};\n\t"
+        "fma.rn.f32x2 ra, ra, rb, rc;\n\t"
+        "mov.b64 {%0, %1}, ra;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+
+__device__ __forceinline__ void add2(float &d0, float &d1, float a0, float a1)
+{
+    asm("{\n\t.reg .b64 ra, rc;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rc, {%0, %1};\n\t"
+        "add.rn.f32x2 rc, rc, ra;\n\t"
+        "mov.b64 {%0, %1}, rc;\n\t}"
+        : "+f"(d0), "+f"(d1)
+        : "f"(a0), "f"(a1));
+}
+
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float max3(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // ---------------------------------------------------------------- configuration
 
 template <int kDim>
@@ -101,7 +157,8 @@ struct AttnCfg {
     static constexpr int DIM = kDim;
     static constexpr int BQ = 128;                // query rows per CTA (TMEM lanes)
     static constexpr int BKV = 128;               // keys per block
-    static constexpr int THREADS = 192;
+    static constexpr int SOFTMAX_WARPS = 8;        // two per TMEM lane quarter
+    static constexpr int THREADS = 64 + 32 * SOFTMAX_WARPS;
     static constexpr int ATOMS = kDim / 64;       // 128-byte swizzle atoms along dim
     static constexpr int TILE_BYTES = 128 * kDim * 2;   // Q, K or V tile of 128 rows
     static constexpr int ATOM_BYTES = 128 * 128;        // 128 rows x 128 bytes
@@ -115,12 +172,14 @@ struct AttnCfg {
     static constexpr int SMEM_BYTES = 1024 + SMEM_CTL_OFF + SMEM_CTL_BYTES;
     static constexpr int TMEM_S_COL = 0;          // two score buffers of 128 columns
     static constexpr int TMEM_O_COL = 2 * BKV;    // output accumulator, kDim columns
+    static constexpr int TMEM_X_COL = 384;        // exchange between a row's two threads:
+                                                  // [block parity][key half] maxima, then [half] sums
     static constexpr int TMEM_COLS = 512;
     static constexpr uint32_t IDESC_S = idesc_f16_f32(BQ, BKV, false, false);   // Q K-major, K K-major
     static constexpr uint32_t IDESC_O = idesc_f16_f32(BQ, kDim, false, true);   // P K-major, V MN-major
 
     static_assert(kDim == 64 || kDim == 128, "head dimension 64 or 128");
-    static_assert(TMEM_O_COL + kDim <= TMEM_COLS, "TMEM columns");
+    static_assert(TMEM_O_COL + kDim <= TMEM_X_COL && TMEM_X_COL + 6 <= TMEM_COLS, "TMEM columns");
     static_assert(SMEM_BYTES <= 232448, "shared memory per block on sm_103");
 };
 
@@ -160,7 +219,13 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
     auto s_empty = [&](int i) { return ctl + 8u * (11 + i); };
     auto p_full = [&](int i) { return ctl + 8u * (13 + i); };
     auto p_empty = [&](int i) { return ctl + 8u * (15 + i); };
-    const uint32_t o_ready = ctl + 8u * 17;
+    // o_ready(b): the MMAs of O += P_j V_j for blocks j with j % 2 == b have
+    // completed (one phase per such block).
+    auto o_ready = [&](int b) { return b == 0 ? ctl + 8u * 17 : ctl + 8u * 23; };
+    // Exchange between a row's two softmax threads: every softmax warp arrives
+    // once it has stored its value (per block parity, and once at the end).
+    auto xchg = [&](int i) { return ctl + 8u * (20 + i); };
+    const uint32_t xfin = ctl + 8u * 22;
     const uint32_t tmem_slot = ctl + 8u * 18;
     const uint32_t abort_addr = tmem_slot + 4;
     volatile uint32_t *tmem_slot_ptr = reinterpret_cast<volatile uint32_t *>(base_ptr + Cfg::SMEM_CTL_OFF + 8 * 18);
@@ -189,11 +254,15 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
             mbar_init(v_full(i), 1);
             mbar_init(v_empty(i), 1);
             mbar_init(s_full(i), 1);
-            mbar_init(s_empty(i), 4);   // the four softmax warps
-            mbar_init(p_full(i), 4);
+            mbar_init(s_empty(i), Cfg::SOFTMAX_WARPS);
+            mbar_init(p_full(i), Cfg::SOFTMAX_WARPS);
             mbar_init(p_empty(i), 1);
         }
-        mbar_init(o_ready, 1);
+        mbar_init(o_ready(0), 1);
+        mbar_init(o_ready(1), 1);
+        mbar_init(xchg(0), Cfg::SOFTMAX_WARPS);
+        mbar_init(xchg(1), Cfg::SOFTMAX_WARPS);
+        mbar_init(xfin, Cfg::SOFTMAX_WARPS);
         *abort.local = 0;
         fence_mbar_init();
     }
@@ -285,7 +354,7 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
                 }
                 mma_commit(v_empty(slot));
                 mma_commit(p_empty(slot));
-                mma_commit(o_ready);
+                mma_commit(o_ready(slot));
                 return true;
             };
             for (int j = 0; ok && j < nblk; ++j) {
@@ -324,13 +393,18 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------------------ softmax (warps 2..5)
-        const int q = warp & 3;
-        const int row = qb * Cfg::BQ + q * 32 + lane;
+        // ------------------------------------------------------------ softmax (warps 2..9)
+        const int q = warp & 3;                 // TMEM lane quarter
+        const int half = (warp - 2) >> 2;       // key half of each block; dim half of the output
+        const int row_local = q * 32 + lane;
+        const int row = qb * Cfg::BQ + row_local;
         const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
         const uint32_t sw = static_cast<uint32_t>(lane & 7);
-        float m_ref = -INFINITY;   // reference maximum (log2 units, scaled scores)
-        float l = 0.0f;            // sum of weights relative to m_ref
+        // Exchange columns (TMEM, this row's lane): maxima [parity][half], sums [half].
+        const uint32_t x_addr = tmem_base + lane_addr + Cfg::TMEM_X_COL;
+        constexpr int HK = Cfg::BKV / 2;        // keys per thread per block
+        float m_ref = -INFINITY;   // reference maximum (log2 units, scaled scores), shared by the row's two threads
+        float l = 0.0f;            // this thread's partial sum of weights relative to m_ref
         bool ok = true;
         for (int j = 0; j < nblk; ++j) {
             const int slot = j & 1;
@@ -341,31 +415,55 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
                 break;
             }
             tc_fence_after_sync();
-            // This row's 128 scores of block j, scaled into log2 units, masked.
-            float x[Cfg::BKV];
-            const uint32_t s_addr = tmem_base + lane_addr + Cfg::TMEM_S_COL + slot * Cfg::BKV;
+            // This thread's 64 raw scores of block j (keys half*64 ..); the
+            // scale (positive) is applied inside the exponent's argument.
+            float x[HK];
+            const uint32_t s_addr = tmem_base + lane_addr + Cfg::TMEM_S_COL + slot * Cfg::BKV + half * HK;
 #pragma unroll
-            for (int c = 0; c < Cfg::BKV / 32; ++c) {
+            for (int c = 0; c < HK / 32; ++c) {
                 uint32_t r[32];
                 attn_tmem_ld32(s_addr + c * 32, r);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(r[i]) * p.scale_log2;
+                for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(r[i]);
             }
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(s_empty(slot));   // the score buffer may be overwritten
-            const int key0 = j * Cfg::BKV;
+            const int key0 = j * Cfg::BKV + half * HK;
             const int last_key = p.causal ? min(row, p.seq - 1) : p.seq - 1;
-            if (key0 + Cfg::BKV - 1 > last_key) {
+            if (key0 + HK - 1 > last_key) {
 #pragma unroll
-                for (int i = 0; i < Cfg::BKV; ++i)
+                for (int i = 0; i < HK; ++i)
                     if (key0 + i > last_key) x[i] = -INFINITY;
             }
-            float mx = x[0];
+            // Maximum as four independent chains of three-input maxima.
+            float m4[4];
 #pragma unroll
-            for (int i = 1; i < Cfg::BKV; ++i) mx = fmaxf(mx, x[i]);
-            // Move the reference only when this block's maximum exceeds it by
-            // more than 8 (weights then stay <= 2^8).
+            for (int k = 0; k < 4; ++k) {
+                m4[k] = max3(x[16 * k], x[16 * k + 1], x[16 * k + 2]);
+#pragma unroll
+                for (int i = 3; i < 15; i += 2) m4[k] = max3(m4[k], x[16 * k + i], x[16 * k + i + 1]);
+                m4[k] = fmaxf(m4[k], x[16 * k + 15]);
+            }
+            float mx = max3(m4[0], m4[1], fmaxf(m4[2], m4[3])) * p.scale_log2;
+            // Row maximum of the block: exchange the two halves' maxima
+            // through TMEM (parity-buffered: a thread writes parity p again
+            // only after the next barrier, which its partner reaches only
+            // after reading).
+            attn_tmem_st1(x_addr + (j & 1) * 2 + half, mx);
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(xchg(j & 1));
+            const bool got_x = wait_phase(xchg(j & 1), ph, abort, limit, kSiteEpilogueTmemFull);
+            if (!__all_sync(0xffffffffu, got_x)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+            mx = fmaxf(mx, attn_tmem_ld1(x_addr + (j & 1) * 2 + (half ^ 1)));
+            // Move the reference only when the block's maximum exceeds it by
+            // more than 8 (weights then stay <= 2^8).  Both threads of a row
+            // see the same maxima, so they decide alike.
             float alpha = 1.0f;
             if (mx > m_ref + 8.0f) {
                 alpha = ex2_approx(m_ref - mx);   // 0 on the first block (m_ref = -inf)
@@ -373,68 +471,86 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
                 m_ref = mx;
             }
             const bool rescale = j > 0 && __any_sync(0xffffffffu, alpha != 1.0f);
-            // P row (fp16) into shared buffer `slot` once the MMAs of block
-            // j - 2 have read it.
+            // P half-row (fp16) into shared buffer `slot` once the MMAs of
+            // block j - 2 have read it.
             const bool got_p = wait_phase(p_empty(slot), ph ^ 1u, abort, limit, kSiteProducerEmpty);
             if (!__all_sync(0xffffffffu, got_p)) {
                 ok = false;
                 break;
             }
-            const uint32_t p_row = sP + slot * Cfg::P_BYTES + static_cast<uint32_t>(q * 32 + lane) * 128u;
-            float lsum = 0.0f;
+            // Key half h is swizzle atom h of the P tile.
+            const uint32_t p_row = sP + slot * Cfg::P_BYTES + half * Cfg::ATOM_BYTES + static_cast<uint32_t>(row_local) * 128u;
+            float lsum0 = 0.0f, lsum1 = 0.0f;
+            const float neg_m = -m_ref;
 #pragma unroll
-            for (int a = 0; a < Cfg::BKV / 64; ++a) {
+            for (int c = 0; c < 8; ++c) {
+                uint32_t w[4];
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        const float p0 = ex2_approx(x[a * 64 + c * 8 + 2 * h] - m_ref);
-                        const float p1 = ex2_approx(x[a * 64 + c * 8 + 2 * h + 1] - m_ref);
-                        lsum += p0 + p1;
-                        const __half2 v = __floats2half2_rn(p0, p1);
-                        w[h] = *reinterpret_cast<const uint32_t *>(&v);
-                    }
-                    // 16-byte chunk c of this row's atom a goes to chunk c ^ (row % 8).
-                    st_shared_v4(p_row + a * Cfg::ATOM_BYTES + ((static_cast<uint32_t>(c) ^ sw) << 4), w[0], w[1],
-                                 w[2], w[3]);
+                for (int h = 0; h < 4; ++h) {
+                    float a0, a1;   // s * c - m for the pair, one packed instruction
+                    fma2_bcast(a0, a1, x[c * 8 + 2 * h], x[c * 8 + 2 * h + 1], p.scale_log2, neg_m);
+                    const float p0 = ex2_approx(a0);
+                    const float p1 = ex2_approx(a1);
+                    add2(lsum0, lsum1, p0, p1);
+                    const __half2 v = __floats2half2_rn(p0, p1);
+                    w[h] = *reinterpret_cast<const uint32_t *>(&v);
                 }
+                // 16-byte chunk c of this row goes to chunk c ^ (row % 8).
+                st_shared_v4(p_row + ((static_cast<uint32_t>(c) ^ sw) << 4), w[0], w[1], w[2], w[3]);
             }
-            l += lsum;
+            l += lsum0 + lsum1;
             fence_proxy_async_smem();   // the MMA reads P through the async proxy
-            if (j > 0) {
-                // O holds blocks 0 .. j-1 once their last MMAs completed.
-                const bool got_o = wait_phase(o_ready, (j - 1) & 1u, abort, limit, kSiteEpilogueTmemFull);
+            if (rescale) {
+                // O must hold exactly blocks 0 .. j-1: wait for the MMAs of
+                // block j-1 (those of j-2 completed before buffer `slot` was
+                // free, so this barrier is at most one phase behind), then
+                // rescale this thread's half of the row's dim columns.
+                const int jp = j - 1;
+                const bool got_o = wait_phase(o_ready(jp & 1), (jp >> 1) & 1u, abort, limit, kSiteEpilogueTmemFull);
                 if (!__all_sync(0xffffffffu, got_o)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
-                if (rescale) {
-                    const uint32_t o_addr = tmem_base + lane_addr + Cfg::TMEM_O_COL;
+                const uint32_t o_addr = tmem_base + lane_addr + Cfg::TMEM_O_COL + half * (kDim / 2);
 #pragma unroll
-                    for (int c = 0; c < kDim / 32; ++c) {
-                        uint32_t r[32];
-                        attn_tmem_ld32(o_addr + c * 32, r);
+                for (int c = 0; c < kDim / 64; ++c) {
+                    uint32_t r[32];
+                    attn_tmem_ld32(o_addr + c * 32, r);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                        attn_tmem_st32(o_addr + c * 32, r);
-                    }
+                    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                    attn_tmem_st32(o_addr + c * 32, r);
                 }
                 tc_fence_before_sync();
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full(slot));
         }
+        // Row sum = the two halves' partial sums (exchanged once, at the end,
+        // in columns of their own; a bounded wait, like every other).
+        if (ok) {
+            attn_tmem_st1(x_addr + 4 + half, l);
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(xfin);
+            const bool got_f = wait_phase(xfin, 0, abort, limit, kSiteEpilogueTmemFull);
+            ok = __all_sync(0xffffffffu, got_f);
+            if (ok) {
+                tc_fence_after_sync();
+                l += attn_tmem_ld1(x_addr + 4 + (half ^ 1));
+            }
+        }
         if (ok && nblk > 0) {
-            const bool got_o = wait_phase(o_ready, (nblk - 1) & 1u, abort, limit, kSiteEpilogueTmemFull);
+            // The MMAs of the last block (and, in order, of every block before it).
+            const int jl = nblk - 1;
+            const bool got_o = wait_phase(o_ready(jl & 1), (jl >> 1) & 1u, abort, limit, kSiteEpilogueTmemFull);
             if (__all_sync(0xffffffffu, got_o)) {
                 tc_fence_after_sync();
                 const float inv_l = 1.0f / l;
-                const uint32_t o_addr = tmem_base + lane_addr + Cfg::TMEM_O_COL;
-                __half *orow = p.O + (static_cast<int64_t>(bh) * p.seq + row) * kDim;
+                const uint32_t o_addr = tmem_base + lane_addr + Cfg::TMEM_O_COL + half * (kDim / 2);
+                __half *orow = p.O + (static_cast<int64_t>(bh) * p.seq + row) * kDim + half * (kDim / 2);
 #pragma unroll
-                for (int c = 0; c < kDim / 32; ++c) {
+                for (int c = 0; c < kDim / 64; ++c) {
                     uint32_t r[32];
                     attn_tmem_ld32(o_addr + c * 32, r);
                     if (row < p.seq) {

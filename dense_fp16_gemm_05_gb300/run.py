@@ -1,13 +1,14 @@
 """Runs one named workload through the C ABI a few times and prints the timings.
 
     python -m dense_fp16_gemm_05_gb300.run --workload relu_8192 --reps 4 [--config ID]
-        [--op gemm|dA_nt|dB_tn|relu_backward|fp8]
+        [--op gemm|dA_nt|dB_tn|relu_backward|fp8|attn]
 
 --op picks the kernel: the forward GEMM (default), the two backward GEMMs of
 the workload (dA = dZ @ B^T in the NT layout, dB = A^T @ dZ in the TN layout)
 or the ReLU-gradient mask over an (M,N) gradient; --op fp8 runs the FP8
 block-scaled GEMM on the workload's sizes (E4M3 operands quantized per
-128-block, fp32 scales).
+128-block, fp32 scales); --op attn runs the attention forward on an attention
+workload (--workload attn_4096_d128, ...).
 
 A minimal program around the library (no oracle, no other kernels besides the
 input upload), suited as the target of a profiler capture: every GPU kernel it
@@ -21,7 +22,8 @@ import json
 import torch
 
 from . import gemm_f16 as g
-from .inputs import WORKLOADS, Workload, draw_fp8_block_scaled, draw_workload
+from .inputs import (ATTN_WORKLOADS, WORKLOADS, Workload, draw_attention_workload, draw_fp8_block_scaled,
+                     draw_workload)
 
 
 def main(argv=None):
@@ -30,8 +32,10 @@ def main(argv=None):
     p.add_argument("--reps", type=int, default=4)
     p.add_argument("--config", type=int, default=0)
     p.add_argument("--relu", type=int, default=None, help="override the workload's ReLU flag")
-    p.add_argument("--op", default="gemm", choices=["gemm", "dA_nt", "dB_tn", "relu_backward", "fp8"])
+    p.add_argument("--op", default="gemm", choices=["gemm", "dA_nt", "dB_tn", "relu_backward", "fp8", "attn"])
     args = p.parse_args(argv)
+    if args.op == "attn":
+        return run_attention(ATTN_WORKLOADS[args.workload], args.reps, torch.device("cuda", 0))
     if args.workload in WORKLOADS:
         w = WORKLOADS[args.workload]
     else:
@@ -98,6 +102,24 @@ def run_fp8(w, relu, reps, dev):
     if st != g.GEMM_OK:
         raise SystemExit(f"device status {st}: {g.strerror(st)}")
     print(json.dumps({"workload": w.name, "op": "fp8", "M": w.M, "N": w.N, "K": w.K, "relu": relu, "ms": times,
+                      "best_tflops": w.flops / (min(times) * 1e-3) / 1e12}))
+
+
+def run_attention(w, reps, dev):
+    Q, K, V = (t.to(dev) for t in draw_attention_workload(w))
+    O = torch.empty_like(Q)
+    times = []
+    for _ in range(reps):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        g.attention_fwd(Q, K, V, O=O, sm_scale=w.sm_scale, causal=w.causal)
+        e.record()
+        e.synchronize()
+        times.append(s.elapsed_time(e))
+    st = g.check()
+    if st != g.GEMM_OK:
+        raise SystemExit(f"device status {st}: {g.strerror(st)}")
+    print(json.dumps({"workload": w.name, "op": "attn", "causal": w.causal, "ms": times,
                       "best_tflops": w.flops / (min(times) * 1e-3) / 1e12}))
 
 
