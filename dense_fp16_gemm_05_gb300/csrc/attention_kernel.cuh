@@ -12,8 +12,9 @@
 // One CTA per (query block, head, batch); 192 threads:
 //   warp 0, one lane   TMA: Q once (3-D tensor maps: rows of another head are
 //                      never read, rows past seq read as zero), then K and V
-//                      blocks through two-slot rings
-//   warp 1, one lane   MMA issuer (and TMEM owner): S_j = Q K_j^T into one of
+//                      blocks through rings of KV_STAGES slots
+//   warp 1, one lane   MMA issuer (and TMEM owner): S_j = Q K_j^T (Q read from
+//                      TMEM, where the softmax warps copied it once) into one of
 //                      two 128-column TMEM score buffers, O += P_j V_j into a
 //                      dim-column TMEM output accumulator; S_{j+1} is issued
 //                      before O += P_j V_j so the tensor core works on the next
@@ -22,11 +23,11 @@
 //                      half of each 128-key block: read 64 scores, mask,
 //                      partial row max (exchanged through shared memory),
 //                      p = 2^(s*c - m) with c = sm_scale * log2(e), partial
-//                      row sum, P in fp16 into shared memory (the 128-byte-
-//                      swizzled K-major layout the MMA reads as its A
-//                      operand: one swizzle atom per key half); at the end
-//                      the two partial sums are added and each thread writes
-//                      O / l for half of the row's dim columns
+//                      row sum, P in fp16 written back into TMEM over the
+//                      scores it came from (the MMA reads it there as its A
+//                      operand, so P costs no shared-memory traffic); at the
+//                      end the two partial sums are added and each thread
+//                      writes O / l for half of the row's dim columns
 // The reference maximum m only moves when a block's maximum exceeds it by more
 // than 8 (in log2 units); then O (in TMEM) and l are multiplied by 2^(m_old -
 // m_new).  Otherwise p <= 2^8 is used as is: every weight is relative to the
@@ -87,6 +88,23 @@ __device__ __forceinline__ void attn_tmem_st32(uint32_t taddr, const uint32_t (&
         "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
         "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
         : "memory");
+}
+
+// 16 consecutive 32-bit TMEM columns of the warp's 32 lanes: store (and wait).
+__device__ __forceinline__ void attn_tmem_st16(uint32_t taddr, const uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};\n\t"
+        "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t &a, uint32_t &b, uint32_t &c, uint32_t &d)
+{
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(a), "=r"(b), "=r"(c), "=r"(d) : "r"(addr) : "memory");
 }
 
 // One fp32 TMEM column of the warp's 32 lanes: store (and wait), load (and wait).
@@ -150,6 +168,20 @@ __device__ __forceinline__ float max3(float a, float b, float c)
     return d;
 }
 
+// D[tmem] (+)= A[tmem] * B[smem], fp16 inputs, fp32 accumulator: the A
+// operand is read from tensor memory (one row per lane, K packed two fp16 per
+// 32-bit column).
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // ---------------------------------------------------------------- configuration
 
 template <int kDim>
@@ -162,25 +194,29 @@ struct AttnCfg {
     static constexpr int ATOMS = kDim / 64;       // 128-byte swizzle atoms along dim
     static constexpr int TILE_BYTES = 128 * kDim * 2;   // Q, K or V tile of 128 rows
     static constexpr int ATOM_BYTES = 128 * 128;        // 128 rows x 128 bytes
-    static constexpr int P_BYTES = BQ * BKV * 2;         // P tile, fp16
     static constexpr int SMEM_Q_OFF = 0;
+    static constexpr int KV_STAGES = kDim == 64 ? 4 : 3;   // K and V ring depth (what shared memory holds)
     static constexpr int SMEM_K_OFF = SMEM_Q_OFF + TILE_BYTES;
-    static constexpr int SMEM_V_OFF = SMEM_K_OFF + 2 * TILE_BYTES;
-    static constexpr int SMEM_P_OFF = SMEM_V_OFF + 2 * TILE_BYTES;
-    static constexpr int SMEM_CTL_OFF = SMEM_P_OFF + 2 * P_BYTES;
+    static constexpr int SMEM_V_OFF = SMEM_K_OFF + KV_STAGES * TILE_BYTES;
+    static constexpr int SMEM_CTL_OFF = SMEM_V_OFF + KV_STAGES * TILE_BYTES;
     static constexpr int SMEM_CTL_BYTES = 256;
     static constexpr int SMEM_BYTES = 1024 + SMEM_CTL_OFF + SMEM_CTL_BYTES;
-    static constexpr int TMEM_S_COL = 0;          // two score buffers of 128 columns
+    static constexpr int TMEM_S_COL = 0;          // two score buffers of 128 columns; P (fp16 pairs)
+                                                  // overwrites the first 64 of its buffer
     static constexpr int TMEM_O_COL = 2 * BKV;    // output accumulator, kDim columns
     static constexpr int TMEM_X_COL = 384;        // exchange between a row's two threads:
                                                   // [block parity][key half] maxima, then [half] sums
+    static constexpr int TMEM_Q_COL = 448;        // Q as the A operand: kDim / 2 columns
     static constexpr int TMEM_COLS = 512;
     static constexpr uint32_t IDESC_S = idesc_f16_f32(BQ, BKV, false, false);   // Q K-major, K K-major
     static constexpr uint32_t IDESC_O = idesc_f16_f32(BQ, kDim, false, true);   // P K-major, V MN-major
 
     static_assert(kDim == 64 || kDim == 128, "head dimension 64 or 128");
-    static_assert(TMEM_O_COL + kDim <= TMEM_X_COL && TMEM_X_COL + 6 <= TMEM_COLS, "TMEM columns");
+    static_assert(TMEM_O_COL + kDim <= TMEM_X_COL && TMEM_X_COL + 6 <= TMEM_Q_COL &&
+                      TMEM_Q_COL + kDim / 2 <= TMEM_COLS,
+                  "TMEM columns");
     static_assert(SMEM_BYTES <= 232448, "shared memory per block on sm_103");
+    static_assert((13 + 4 * KV_STAGES) * 8 <= SMEM_CTL_BYTES, "control block");
 };
 
 struct AttnParams {
@@ -206,29 +242,36 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
     const uint32_t sQ = base + Cfg::SMEM_Q_OFF;
     const uint32_t sK = base + Cfg::SMEM_K_OFF;
     const uint32_t sV = base + Cfg::SMEM_V_OFF;
-    const uint32_t sP = base + Cfg::SMEM_P_OFF;
     const uint32_t ctl = base + Cfg::SMEM_CTL_OFF;
     // Barriers: q_full; k_full[2], k_empty[2]; v_full[2], v_empty[2];
-    // s_full[2], s_empty[2]; p_full[2], p_empty[2]; o_ready.
+    // Barriers (8 bytes each): q_full; k_full, k_empty, v_full, v_empty
+    // [KV_STAGES] (the K and V rings); s_full[2], p_full[2], o_ready[2] (the
+    // two TMEM score buffers); xchg[2], xfin, q_ready (softmax threads);
+    // drain; then the TMEM address slot and the abort flag.  A score buffer is
+    // reused for the scores of block j+2 only after O += P_j V_j read P_j from
+    // it, and P_j is written only after S_j completed, i.e. after the MMAs of
+    // block j-2 that read P_{j-2}: the in-order MMA stream orders both
+    // hand-offs.  o_ready(b): the MMAs of O += P_j V_j for blocks j with
+    // j % 2 == b have completed (one phase per such block).
+    constexpr int S = Cfg::KV_STAGES;
     const uint32_t q_full = ctl;
     auto k_full = [&](int i) { return ctl + 8u * (1 + i); };
-    auto k_empty = [&](int i) { return ctl + 8u * (3 + i); };
-    auto v_full = [&](int i) { return ctl + 8u * (5 + i); };
-    auto v_empty = [&](int i) { return ctl + 8u * (7 + i); };
-    auto s_full = [&](int i) { return ctl + 8u * (9 + i); };
-    auto s_empty = [&](int i) { return ctl + 8u * (11 + i); };
-    auto p_full = [&](int i) { return ctl + 8u * (13 + i); };
-    auto p_empty = [&](int i) { return ctl + 8u * (15 + i); };
-    // o_ready(b): the MMAs of O += P_j V_j for blocks j with j % 2 == b have
-    // completed (one phase per such block).
-    auto o_ready = [&](int b) { return b == 0 ? ctl + 8u * 17 : ctl + 8u * 23; };
+    auto k_empty = [&](int i) { return ctl + 8u * (1 + S + i); };
+    auto v_full = [&](int i) { return ctl + 8u * (1 + 2 * S + i); };
+    auto v_empty = [&](int i) { return ctl + 8u * (1 + 3 * S + i); };
+    auto s_full = [&](int i) { return ctl + 8u * (1 + 4 * S + i); };
+    auto p_full = [&](int i) { return ctl + 8u * (3 + 4 * S + i); };
+    auto o_ready = [&](int b) { return ctl + 8u * (5 + 4 * S + b); };
     // Exchange between a row's two softmax threads: every softmax warp arrives
     // once it has stored its value (per block parity, and once at the end).
-    auto xchg = [&](int i) { return ctl + 8u * (20 + i); };
-    const uint32_t xfin = ctl + 8u * 22;
-    const uint32_t tmem_slot = ctl + 8u * 18;
+    auto xchg = [&](int i) { return ctl + 8u * (7 + 4 * S + i); };
+    const uint32_t xfin = ctl + 8u * (9 + 4 * S);
+    const uint32_t q_ready = ctl + 8u * (10 + 4 * S);   // Q copied into TMEM by every softmax warp
+    const uint32_t drain = ctl + 8u * (11 + 4 * S);
+    const uint32_t tmem_slot = ctl + 8u * (12 + 4 * S);
     const uint32_t abort_addr = tmem_slot + 4;
-    volatile uint32_t *tmem_slot_ptr = reinterpret_cast<volatile uint32_t *>(base_ptr + Cfg::SMEM_CTL_OFF + 8 * 18);
+    volatile uint32_t *tmem_slot_ptr =
+        reinterpret_cast<volatile uint32_t *>(base_ptr + Cfg::SMEM_CTL_OFF + 8 * (12 + 4 * S));
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -248,21 +291,22 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < S; ++i) {
             mbar_init(k_full(i), 1);
             mbar_init(k_empty(i), 1);
             mbar_init(v_full(i), 1);
             mbar_init(v_empty(i), 1);
-            mbar_init(s_full(i), 1);
-            mbar_init(s_empty(i), Cfg::SOFTMAX_WARPS);
-            mbar_init(p_full(i), Cfg::SOFTMAX_WARPS);
-            mbar_init(p_empty(i), 1);
         }
-        mbar_init(o_ready(0), 1);
-        mbar_init(o_ready(1), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(s_full(i), 1);
+            mbar_init(p_full(i), Cfg::SOFTMAX_WARPS);
+            mbar_init(o_ready(i), 1);
+        }
+        mbar_init(drain, 1);
         mbar_init(xchg(0), Cfg::SOFTMAX_WARPS);
         mbar_init(xchg(1), Cfg::SOFTMAX_WARPS);
         mbar_init(xfin, Cfg::SOFTMAX_WARPS);
+        mbar_init(q_ready, Cfg::SOFTMAX_WARPS);
         *abort.local = 0;
         fence_mbar_init();
     }
@@ -290,8 +334,8 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
             for (int a = 0; a < Cfg::ATOMS; ++a)
                 tma_load_3d(sQ + a * Cfg::ATOM_BYTES, &tmap_q, q_full, a * 64, qb * Cfg::BQ, bh);
             for (int j = 0; ok && j < nblk; ++j) {
-                const int slot = j & 1;
-                const uint32_t ph = (j >> 1) & 1u;
+                const int slot = j % S;
+                const uint32_t ph = (j / S) & 1u;
                 if (!wait_phase(k_empty(slot), ph ^ 1u, abort, limit, kSiteProducerEmpty)) {
                     ok = false;
                     break;
@@ -323,12 +367,11 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            bool ok = wait_phase(q_full, 0, abort, limit, kSiteMmaFull);
+            bool ok = wait_phase(q_ready, 0, abort, limit, kSiteMmaFull);
             bool issued_any = false;
-            const uint64_t q_desc = smem_desc_sw128(sQ, 16, 1024);
+            const uint32_t q_tmem = tmem_base + Cfg::TMEM_Q_COL;
             const uint64_t k_desc0 = smem_desc_sw128(sK, 16, 1024);
             const uint64_t v_desc0 = smem_desc_sw128(sV, Cfg::ATOM_BYTES, 1024);
-            const uint64_t p_desc0 = smem_desc_sw128(sP, 16, 1024);
             const uint32_t o_tmem = tmem_base + Cfg::TMEM_O_COL;
             // K step t of 16 elements along dim (K-major tiles): atom t/4, +32 B per step inside it.
             auto dim_step = [](int t) -> uint64_t {
@@ -336,42 +379,40 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
             };
             // O += P_j V_j for block jj (issued one block behind the scores).
             auto issue_pv = [&](int jj) -> bool {
-                const int slot = jj & 1;
+                const int slot = jj & 1;              // score / P buffer
                 const uint32_t ph = (jj >> 1) & 1u;
-                if (!wait_phase(v_full(slot), ph, abort, limit, kSiteMmaFull) ||
+                const int vs = jj % S;                 // V ring slot
+                if (!wait_phase(v_full(vs), (jj / S) & 1u, abort, limit, kSiteMmaFull) ||
                     !wait_phase(p_full(slot), ph, abort, limit, kSiteMmaTmemEmpty))
                     return false;
                 tc_fence_after_sync();
-                const uint64_t p_desc = p_desc0 + static_cast<uint64_t>((slot * Cfg::P_BYTES) >> 4);
-                const uint64_t v_desc = v_desc0 + static_cast<uint64_t>((slot * Cfg::TILE_BYTES) >> 4);
+                const uint32_t p_tmem = tmem_base + Cfg::TMEM_S_COL + slot * Cfg::BKV;
+                const uint64_t v_desc = v_desc0 + static_cast<uint64_t>((vs * Cfg::TILE_BYTES) >> 4);
 #pragma unroll
                 for (int t = 0; t < Cfg::BKV / 16; ++t) {
-                    // P (A, K-major along keys): atom t/4, +32 B per step; V (B,
+                    // P (A, in TMEM): 16 keys = 8 columns per step; V (B,
                     // MN-major along dim): 16 key rows = +2 KB per step.
-                    const uint64_t pa = p_desc + static_cast<uint64_t>(((t >> 2) * Cfg::ATOM_BYTES + (t & 3) * 32) >> 4);
                     const uint64_t vb = v_desc + static_cast<uint64_t>((t * 16 * 128) >> 4);
-                    mma_f16_ss<1>(o_tmem, pa, vb, Cfg::IDESC_O, (jj > 0 || t > 0) ? 1u : 0u);
+                    mma_f16_ts(o_tmem, p_tmem + t * 8, vb, Cfg::IDESC_O, (jj > 0 || t > 0) ? 1u : 0u);
                 }
-                mma_commit(v_empty(slot));
-                mma_commit(p_empty(slot));
+                mma_commit(v_empty(vs));
                 mma_commit(o_ready(slot));
                 return true;
             };
             for (int j = 0; ok && j < nblk; ++j) {
-                const int slot = j & 1;
-                const uint32_t ph = (j >> 1) & 1u;
-                if (!wait_phase(k_full(slot), ph, abort, limit, kSiteMmaFull) ||
-                    !wait_phase(s_empty(slot), ph ^ 1u, abort, limit, kSiteMmaTmemEmpty)) {
+                const int slot = j & 1;   // score buffer
+                const int ks = j % S;     // K ring slot
+                if (!wait_phase(k_full(ks), (j / S) & 1u, abort, limit, kSiteMmaFull)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
                 const uint32_t s_tmem = tmem_base + Cfg::TMEM_S_COL + slot * Cfg::BKV;
-                const uint64_t k_desc = k_desc0 + static_cast<uint64_t>((slot * Cfg::TILE_BYTES) >> 4);
+                const uint64_t k_desc = k_desc0 + static_cast<uint64_t>((ks * Cfg::TILE_BYTES) >> 4);
 #pragma unroll
                 for (int t = 0; t < kDim / 16; ++t)
-                    mma_f16_ss<1>(s_tmem, q_desc + dim_step(t), k_desc + dim_step(t), Cfg::IDESC_S, t > 0 ? 1u : 0u);
-                mma_commit(k_empty(slot));
+                    mma_f16_ts(s_tmem, q_tmem + t * 8, k_desc + dim_step(t), Cfg::IDESC_S, t > 0 ? 1u : 0u);
+                mma_commit(k_empty(ks));
                 mma_commit(s_full(slot));
                 issued_any = true;
                 if (j >= 1 && !issue_pv(j - 1)) {
@@ -383,9 +424,6 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
             if (!ok) {
                 if (issued_any) {
                     // Wait for this thread's MMAs before the TMEM is freed.
-                    const uint32_t drain = ctl + 8u * 19;
-                    mbar_init(drain, 1);
-                    fence_mbar_init();
                     mma_commit(drain);
                     wait_phase_drain(drain, 0, limit, kSiteDrainMma, p.status);
                 }
@@ -399,10 +437,36 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
         const int row_local = q * 32 + lane;
         const int row = qb * Cfg::BQ + row_local;
         const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
-        const uint32_t sw = static_cast<uint32_t>(lane & 7);
         // Exchange columns (TMEM, this row's lane): maxima [parity][half], sums [half].
         const uint32_t x_addr = tmem_base + lane_addr + Cfg::TMEM_X_COL;
         constexpr int HK = Cfg::BKV / 2;        // keys per thread per block
+        // Copy this row's half of Q (dim columns half*kDim/2 ..) from the
+        // swizzled shared tile into TMEM, packed two fp16 per column.
+        {
+            const bool got_q = wait_phase(q_full, 0, abort, limit, kSiteEpilogueTmemFull);
+            if (__all_sync(0xffffffffu, got_q)) {
+                constexpr int kChunks = kDim / 16;     // 16-byte chunks in half a row
+                uint32_t qv[kChunks * 4];
+                const uint32_t sw = static_cast<uint32_t>(lane & 7);
+#pragma unroll
+                for (int c = 0; c < kChunks; ++c) {
+                    const int e = half * (kDim / 2) + c * 8;          // first element of the chunk
+                    const uint32_t atom = static_cast<uint32_t>(e / 64), cin = static_cast<uint32_t>((e % 64) / 8);
+                    ld_shared_v4(sQ + atom * Cfg::ATOM_BYTES + static_cast<uint32_t>(row_local) * 128u +
+                                     ((cin ^ sw) << 4),
+                                 qv[4 * c], qv[4 * c + 1], qv[4 * c + 2], qv[4 * c + 3]);
+                }
+                const uint32_t q_addr = tmem_base + lane_addr + Cfg::TMEM_Q_COL + half * (kDim / 4);
+                if constexpr (kDim == 128) {
+                    attn_tmem_st32(q_addr, qv);
+                } else {
+                    attn_tmem_st16(q_addr, qv);
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(q_ready);
+            }
+        }
         float m_ref = -INFINITY;   // reference maximum (log2 units, scaled scores), shared by the row's two threads
         float l = 0.0f;            // this thread's partial sum of weights relative to m_ref
         bool ok = true;
@@ -426,9 +490,6 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
 #pragma unroll
                 for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(r[i]);
             }
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(s_empty(slot));   // the score buffer may be overwritten
             const int key0 = j * Cfg::BKV + half * HK;
             const int last_key = p.causal ? min(row, p.seq - 1) : p.seq - 1;
             if (key0 + HK - 1 > last_key) {
@@ -471,35 +532,25 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
                 m_ref = mx;
             }
             const bool rescale = j > 0 && __any_sync(0xffffffffu, alpha != 1.0f);
-            // P half-row (fp16) into shared buffer `slot` once the MMAs of
-            // block j - 2 have read it.
-            const bool got_p = wait_phase(p_empty(slot), ph ^ 1u, abort, limit, kSiteProducerEmpty);
-            if (!__all_sync(0xffffffffu, got_p)) {
-                ok = false;
-                break;
-            }
-            // Key half h is swizzle atom h of the P tile.
-            const uint32_t p_row = sP + slot * Cfg::P_BYTES + half * Cfg::ATOM_BYTES + static_cast<uint32_t>(row_local) * 128u;
+            // P half-row (fp16 pairs) into TMEM over the scores of this block:
+            // keys half*64 .. +63 are columns half*32 .. +31 of the buffer.
+            // Every softmax thread has read its scores before the maxima
+            // exchange above, so no score is overwritten before it is read.
             float lsum0 = 0.0f, lsum1 = 0.0f;
             const float neg_m = -m_ref;
+            uint32_t w[HK / 2];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                uint32_t w[4];
-#pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    float a0, a1;   // s * c - m for the pair, one packed instruction
-                    fma2_bcast(a0, a1, x[c * 8 + 2 * h], x[c * 8 + 2 * h + 1], p.scale_log2, neg_m);
-                    const float p0 = ex2_approx(a0);
-                    const float p1 = ex2_approx(a1);
-                    add2(lsum0, lsum1, p0, p1);
-                    const __half2 v = __floats2half2_rn(p0, p1);
-                    w[h] = *reinterpret_cast<const uint32_t *>(&v);
-                }
-                // 16-byte chunk c of this row goes to chunk c ^ (row % 8).
-                st_shared_v4(p_row + ((static_cast<uint32_t>(c) ^ sw) << 4), w[0], w[1], w[2], w[3]);
+            for (int i = 0; i < HK / 2; ++i) {
+                float a0, a1;   // s * c - m for the pair, one packed instruction
+                fma2_bcast(a0, a1, x[2 * i], x[2 * i + 1], p.scale_log2, neg_m);
+                const float p0 = ex2_approx(a0);
+                const float p1 = ex2_approx(a1);
+                add2(lsum0, lsum1, p0, p1);
+                const __half2 v = __floats2half2_rn(p0, p1);
+                w[i] = *reinterpret_cast<const uint32_t *>(&v);
             }
+            attn_tmem_st32(tmem_base + lane_addr + Cfg::TMEM_S_COL + slot * Cfg::BKV + half * (HK / 2), w);
             l += lsum0 + lsum1;
-            fence_proxy_async_smem();   // the MMA reads P through the async proxy
             if (rescale) {
                 // O must hold exactly blocks 0 .. j-1: wait for the MMAs of
                 // block j-1 (those of j-2 completed before buffer `slot` was
@@ -523,6 +574,7 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
                 }
                 tc_fence_before_sync();
             }
+            tc_fence_before_sync();   // P (and a rescaled O) in TMEM before the MMA is told
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full(slot));
         }
