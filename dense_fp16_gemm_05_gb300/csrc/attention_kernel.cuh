@@ -9,7 +9,7 @@
 // streamed in blocks of 128 with a running row maximum and row sum, so the
 // score matrix is never stored.
 //
-// One CTA per (query block, head, batch); 192 threads:
+// One CTA per (query block, head, batch); 320 threads:
 //   warp 0, one lane   TMA: Q once (3-D tensor maps: rows of another head are
 //                      never read, rows past seq read as zero), then K and V
 //                      blocks through rings of KV_STAGES slots
