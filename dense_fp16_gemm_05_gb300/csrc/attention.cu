@@ -54,8 +54,9 @@ int launch_dim(const AttnLaunchArgs &a)
     p.O = static_cast<__half *>(a.O);
     p.status = a.status;
     if (!AttnPrepared<kDim>::get(a.dev.device)) return GEMM_ERR_LAUNCH;
-    const dim3 grid(static_cast<unsigned>(p.num_q_blocks), static_cast<unsigned>(a.heads),
-                    static_cast<unsigned>(a.batch));
+    // One CTA per pair of query blocks (its two tiles), per head and batch.
+    const dim3 grid(static_cast<unsigned>((p.num_q_blocks + Cfg::TILES - 1) / Cfg::TILES),
+                    static_cast<unsigned>(a.heads), static_cast<unsigned>(a.batch));
     attention_fwd_sm103a<kDim><<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, a.stream>>>(tq, tk, tv, p);
     if (cudaGetLastError() != cudaSuccess) {
         AttnPrepared<kDim>::forget(a.dev.device);

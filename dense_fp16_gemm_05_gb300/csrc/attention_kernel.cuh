@@ -186,37 +186,35 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
 
 template <int kDim>
 struct AttnCfg {
-    static constexpr int DIM = kDim;
-    static constexpr int BQ = 128;                // query rows per CTA (TMEM lanes)
+    static constexpr int TILES = 2;               // query tiles per CTA, sharing every K/V block
+    static constexpr int BQ = 128;                // query rows per tile (TMEM lanes)
     static constexpr int BKV = 128;               // keys per block
-    static constexpr int SOFTMAX_WARPS = 8;        // two per TMEM lane quarter
+    static constexpr int TILE_WARPS = 8;          // softmax warps per tile: two per TMEM lane quarter
+    static constexpr int SOFTMAX_WARPS = TILES * TILE_WARPS;
     static constexpr int THREADS = 64 + 32 * SOFTMAX_WARPS;
     static constexpr int ATOMS = kDim / 64;       // 128-byte swizzle atoms along dim
     static constexpr int TILE_BYTES = 128 * kDim * 2;   // Q, K or V tile of 128 rows
     static constexpr int ATOM_BYTES = 128 * 128;        // 128 rows x 128 bytes
-    static constexpr int SMEM_Q_OFF = 0;
-    static constexpr int KV_STAGES = kDim == 64 ? 4 : 3;   // K and V ring depth (what shared memory holds)
-    static constexpr int SMEM_K_OFF = SMEM_Q_OFF + TILE_BYTES;
+    static constexpr int KV_STAGES = kDim == 64 ? 4 : 2;   // K and V ring depth (what shared memory holds)
+    static constexpr int SMEM_Q_OFF = 0;                   // TILES query tiles
+    static constexpr int SMEM_K_OFF = SMEM_Q_OFF + TILES * TILE_BYTES;
     static constexpr int SMEM_V_OFF = SMEM_K_OFF + KV_STAGES * TILE_BYTES;
-    static constexpr int SMEM_CTL_OFF = SMEM_V_OFF + KV_STAGES * TILE_BYTES;
+    static constexpr int SMEM_X_OFF = SMEM_V_OFF + KV_STAGES * TILE_BYTES;
+    static constexpr int SMEM_X_BYTES = TILES * 2 * 2 * BQ * 4;   // fp32 [tile][block parity][key half][row]
+    static constexpr int SMEM_CTL_OFF = SMEM_X_OFF + SMEM_X_BYTES;
     static constexpr int SMEM_CTL_BYTES = 256;
     static constexpr int SMEM_BYTES = 1024 + SMEM_CTL_OFF + SMEM_CTL_BYTES;
-    static constexpr int TMEM_S_COL = 0;          // two score buffers of 128 columns; P (fp16 pairs)
-                                                  // overwrites the first 64 of its buffer
-    static constexpr int TMEM_O_COL = 2 * BKV;    // output accumulator, kDim columns
-    static constexpr int TMEM_X_COL = 384;        // exchange between a row's two threads:
-                                                  // [block parity][key half] maxima, then [half] sums
-    static constexpr int TMEM_Q_COL = 448;        // Q as the A operand: kDim / 2 columns
+    static constexpr int TMEM_S_COL = 0;          // per tile one 128-column score buffer; P (fp16
+                                                  // pairs) overwrites the first 64 of it
+    static constexpr int TMEM_O_COL = TILES * BKV;   // per tile a 128-column output accumulator
     static constexpr int TMEM_COLS = 512;
     static constexpr uint32_t IDESC_S = idesc_f16_f32(BQ, BKV, false, false);   // Q K-major, K K-major
     static constexpr uint32_t IDESC_O = idesc_f16_f32(BQ, kDim, false, true);   // P K-major, V MN-major
 
     static_assert(kDim == 64 || kDim == 128, "head dimension 64 or 128");
-    static_assert(TMEM_O_COL + kDim <= TMEM_X_COL && TMEM_X_COL + 6 <= TMEM_Q_COL &&
-                      TMEM_Q_COL + kDim / 2 <= TMEM_COLS,
-                  "TMEM columns");
+    static_assert(TMEM_O_COL + TILES * 128 <= TMEM_COLS, "TMEM columns");
     static_assert(SMEM_BYTES <= 232448, "shared memory per block on sm_103");
-    static_assert((13 + 4 * KV_STAGES) * 8 <= SMEM_CTL_BYTES, "control block");
+    static_assert((16 + 4 * KV_STAGES) * 8 <= SMEM_CTL_BYTES, "control block");
 };
 
 struct AttnParams {
@@ -242,45 +240,50 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
     const uint32_t sQ = base + Cfg::SMEM_Q_OFF;
     const uint32_t sK = base + Cfg::SMEM_K_OFF;
     const uint32_t sV = base + Cfg::SMEM_V_OFF;
+    float *xbuf = reinterpret_cast<float *>(base_ptr + Cfg::SMEM_X_OFF);
     const uint32_t ctl = base + Cfg::SMEM_CTL_OFF;
-    // Barriers: q_full; k_full[2], k_empty[2]; v_full[2], v_empty[2];
     // Barriers (8 bytes each): q_full; k_full, k_empty, v_full, v_empty
-    // [KV_STAGES] (the K and V rings); s_full[2], p_full[2], o_ready[2] (the
-    // two TMEM score buffers); xchg[2], xfin, q_ready (softmax threads);
-    // drain; then the TMEM address slot and the abort flag.  A score buffer is
-    // reused for the scores of block j+2 only after O += P_j V_j read P_j from
-    // it, and P_j is written only after S_j completed, i.e. after the MMAs of
-    // block j-2 that read P_{j-2}: the in-order MMA stream orders both
-    // hand-offs.  o_ready(b): the MMAs of O += P_j V_j for blocks j with
-    // j % 2 == b have completed (one phase per such block).
+    // [KV_STAGES] (the K and V rings); per tile s_full, p_full, o_ready; per
+    // tile and block parity xchg; per tile xfin; drain; then the TMEM address
+    // slot and the abort flag.
+    //
+    // Order of the MMA stream: S^0_0, S^1_0, then per block j and tile t:
+    // O^t += P^t_j V_j, S^t_{j+1}.  Tile t's score buffer is rewritten by
+    // S^t_{j+1} only after O^t += P^t_j V_j (issued before it) read P^t_j, and
+    // S^t_j completes after O^t += P^t_{j-1} V_{j-1}: when the softmax sees
+    // the scores of block j, tile t's output holds blocks 0 .. j-1 exactly.
     constexpr int S = Cfg::KV_STAGES;
     const uint32_t q_full = ctl;
     auto k_full = [&](int i) { return ctl + 8u * (1 + i); };
     auto k_empty = [&](int i) { return ctl + 8u * (1 + S + i); };
     auto v_full = [&](int i) { return ctl + 8u * (1 + 2 * S + i); };
     auto v_empty = [&](int i) { return ctl + 8u * (1 + 3 * S + i); };
-    auto s_full = [&](int i) { return ctl + 8u * (1 + 4 * S + i); };
-    auto p_full = [&](int i) { return ctl + 8u * (3 + 4 * S + i); };
-    auto o_ready = [&](int b) { return ctl + 8u * (5 + 4 * S + b); };
-    // Exchange between a row's two softmax threads: every softmax warp arrives
-    // once it has stored its value (per block parity, and once at the end).
-    auto xchg = [&](int i) { return ctl + 8u * (7 + 4 * S + i); };
-    const uint32_t xfin = ctl + 8u * (9 + 4 * S);
-    const uint32_t q_ready = ctl + 8u * (10 + 4 * S);   // Q copied into TMEM by every softmax warp
-    const uint32_t drain = ctl + 8u * (11 + 4 * S);
-    const uint32_t tmem_slot = ctl + 8u * (12 + 4 * S);
+    auto s_full = [&](int t) { return ctl + 8u * (1 + 4 * S + t); };
+    auto p_full = [&](int t) { return ctl + 8u * (3 + 4 * S + t); };
+    auto o_ready = [&](int t) { return ctl + 8u * (5 + 4 * S + t); };
+    // Exchange between a row's two softmax threads: the tile's eight warps
+    // arrive once they have stored their values (per block parity, and once
+    // at the end).
+    auto xchg = [&](int t, int par) { return ctl + 8u * (7 + 4 * S + 2 * t + par); };
+    auto xfin = [&](int t) { return ctl + 8u * (11 + 4 * S + t); };
+    const uint32_t drain = ctl + 8u * (13 + 4 * S);
+    const uint32_t tmem_slot = ctl + 8u * (14 + 4 * S);
     const uint32_t abort_addr = tmem_slot + 4;
     volatile uint32_t *tmem_slot_ptr =
-        reinterpret_cast<volatile uint32_t *>(base_ptr + Cfg::SMEM_CTL_OFF + 8 * (12 + 4 * S));
+        reinterpret_cast<volatile uint32_t *>(base_ptr + Cfg::SMEM_CTL_OFF + 8 * (14 + 4 * S));
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // Heavier (causal) query blocks first: block index reversed.
-    const int qb = p.num_q_blocks - 1 - static_cast<int>(blockIdx.x);
+    // Heavier (causal) query-block pairs first: index reversed.  Tile t
+    // covers query block 2 * grp + t.
+    const int grp = static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x);
     const int head = static_cast<int>(blockIdx.y);
     const int bh = static_cast<int>(blockIdx.z) * p.heads + head;
     const int kv_blocks_all = (p.seq + Cfg::BKV - 1) / Cfg::BKV;
-    const int nblk = p.causal ? min(qb + 1, kv_blocks_all) : kv_blocks_all;
+    // Key blocks of each tile (tile 1 never needs fewer than tile 0; both >= 1).
+    auto tile_blocks = [&](int t) { return p.causal ? min(2 * grp + t + 1, kv_blocks_all) : kv_blocks_all; };
+    const int nb0 = tile_blocks(0);
+    const int nb1 = tile_blocks(1);
 
     AbortFlag abort;
     abort.local = reinterpret_cast<volatile int *>(tmem_slot_ptr + 1);
@@ -297,16 +300,15 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
             mbar_init(v_full(i), 1);
             mbar_init(v_empty(i), 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(s_full(i), 1);
-            mbar_init(p_full(i), Cfg::SOFTMAX_WARPS);
-            mbar_init(o_ready(i), 1);
+        for (int t = 0; t < Cfg::TILES; ++t) {
+            mbar_init(s_full(t), 1);
+            mbar_init(p_full(t), Cfg::TILE_WARPS);
+            mbar_init(o_ready(t), 1);
+            mbar_init(xchg(t, 0), Cfg::TILE_WARPS);
+            mbar_init(xchg(t, 1), Cfg::TILE_WARPS);
+            mbar_init(xfin(t), Cfg::TILE_WARPS);
         }
         mbar_init(drain, 1);
-        mbar_init(xchg(0), Cfg::SOFTMAX_WARPS);
-        mbar_init(xchg(1), Cfg::SOFTMAX_WARPS);
-        mbar_init(xfin, Cfg::SOFTMAX_WARPS);
-        mbar_init(q_ready, Cfg::SOFTMAX_WARPS);
         *abort.local = 0;
         fence_mbar_init();
     }
@@ -329,11 +331,14 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             bool ok = true;
-            mbar_arrive_expect_tx(q_full, Cfg::TILE_BYTES);
+            mbar_arrive_expect_tx(q_full, Cfg::TILES * Cfg::TILE_BYTES);
+            for (int t = 0; t < Cfg::TILES; ++t) {
 #pragma unroll
-            for (int a = 0; a < Cfg::ATOMS; ++a)
-                tma_load_3d(sQ + a * Cfg::ATOM_BYTES, &tmap_q, q_full, a * 64, qb * Cfg::BQ, bh);
-            for (int j = 0; ok && j < nblk; ++j) {
+                for (int a = 0; a < Cfg::ATOMS; ++a)
+                    tma_load_3d(sQ + t * Cfg::TILE_BYTES + a * Cfg::ATOM_BYTES, &tmap_q, q_full, a * 64,
+                                (2 * grp + t) * Cfg::BQ, bh);
+            }
+            for (int j = 0; ok && j < nb1; ++j) {
                 const int slot = j % S;
                 const uint32_t ph = (j / S) & 1u;
                 if (!wait_phase(k_empty(slot), ph ^ 1u, abort, limit, kSiteProducerEmpty)) {
@@ -367,60 +372,68 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            bool ok = wait_phase(q_ready, 0, abort, limit, kSiteMmaFull);
+            bool ok = wait_phase(q_full, 0, abort, limit, kSiteMmaFull);
             bool issued_any = false;
-            const uint32_t q_tmem = tmem_base + Cfg::TMEM_Q_COL;
+            const uint64_t q_desc0 = smem_desc_sw128(sQ, 16, 1024);
             const uint64_t k_desc0 = smem_desc_sw128(sK, 16, 1024);
             const uint64_t v_desc0 = smem_desc_sw128(sV, Cfg::ATOM_BYTES, 1024);
-            const uint32_t o_tmem = tmem_base + Cfg::TMEM_O_COL;
-            // K step t of 16 elements along dim (K-major tiles): atom t/4, +32 B per step inside it.
+            // K step t of 16 elements along dim (K-major tiles of 128 rows):
+            // atom t/4, +32 B per step inside it.
             auto dim_step = [](int t) -> uint64_t {
                 return static_cast<uint64_t>(((t >> 2) * Cfg::ATOM_BYTES + (t & 3) * 32) >> 4);
             };
-            // O += P_j V_j for block jj (issued one block behind the scores).
-            auto issue_pv = [&](int jj) -> bool {
-                const int slot = jj & 1;              // score / P buffer
-                const uint32_t ph = (jj >> 1) & 1u;
-                const int vs = jj % S;                 // V ring slot
-                if (!wait_phase(v_full(vs), (jj / S) & 1u, abort, limit, kSiteMmaFull) ||
-                    !wait_phase(p_full(slot), ph, abort, limit, kSiteMmaTmemEmpty))
-                    return false;
-                tc_fence_after_sync();
-                const uint32_t p_tmem = tmem_base + Cfg::TMEM_S_COL + slot * Cfg::BKV;
-                const uint64_t v_desc = v_desc0 + static_cast<uint64_t>((vs * Cfg::TILE_BYTES) >> 4);
-#pragma unroll
-                for (int t = 0; t < Cfg::BKV / 16; ++t) {
-                    // P (A, in TMEM): 16 keys = 8 columns per step; V (B,
-                    // MN-major along dim): 16 key rows = +2 KB per step.
-                    const uint64_t vb = v_desc + static_cast<uint64_t>((t * 16 * 128) >> 4);
-                    mma_f16_ts(o_tmem, p_tmem + t * 8, vb, Cfg::IDESC_O, (jj > 0 || t > 0) ? 1u : 0u);
-                }
-                mma_commit(v_empty(vs));
-                mma_commit(o_ready(slot));
-                return true;
-            };
-            for (int j = 0; ok && j < nblk; ++j) {
-                const int slot = j & 1;   // score buffer
-                const int ks = j % S;     // K ring slot
-                if (!wait_phase(k_full(ks), (j / S) & 1u, abort, limit, kSiteMmaFull)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after_sync();
-                const uint32_t s_tmem = tmem_base + Cfg::TMEM_S_COL + slot * Cfg::BKV;
+            // S^t_j = Q^t K_j^T into tile t's score buffer; the second user of
+            // a K slot (tile 1) releases it.
+            auto issue_s = [&](int t, int j) -> bool {
+                const int ks = j % S;
+                if (!wait_phase(k_full(ks), (j / S) & 1u, abort, limit, kSiteMmaFull)) return false;
+                const uint32_t s_tmem = tmem_base + Cfg::TMEM_S_COL + t * Cfg::BKV;
+                const uint64_t q_desc = q_desc0 + static_cast<uint64_t>((t * Cfg::TILE_BYTES) >> 4);
                 const uint64_t k_desc = k_desc0 + static_cast<uint64_t>((ks * Cfg::TILE_BYTES) >> 4);
 #pragma unroll
-                for (int t = 0; t < kDim / 16; ++t)
-                    mma_f16_ts(s_tmem, q_tmem + t * 8, k_desc + dim_step(t), Cfg::IDESC_S, t > 0 ? 1u : 0u);
-                mma_commit(k_empty(ks));
-                mma_commit(s_full(slot));
+                for (int k = 0; k < kDim / 16; ++k)
+                    mma_f16_ss<1>(s_tmem, q_desc + dim_step(k), k_desc + dim_step(k), Cfg::IDESC_S,
+                                  k > 0 ? 1u : 0u);
+                if (t == 1) mma_commit(k_empty(ks));
+                mma_commit(s_full(t));
                 issued_any = true;
-                if (j >= 1 && !issue_pv(j - 1)) {
+                return true;
+            };
+            // O^t += P^t_j V_j (P in TMEM, over the scores it came from); the
+            // second user of a V slot (tile 1) releases it.
+            auto issue_pv = [&](int t, int j) -> bool {
+                const int vs = j % S;
+                if (!wait_phase(v_full(vs), (j / S) & 1u, abort, limit, kSiteMmaFull) ||
+                    !wait_phase(p_full(t), j & 1u, abort, limit, kSiteMmaTmemEmpty))
+                    return false;
+                tc_fence_after_sync();
+                const uint32_t p_tmem = tmem_base + Cfg::TMEM_S_COL + t * Cfg::BKV;
+                const uint32_t o_tmem = tmem_base + Cfg::TMEM_O_COL + t * 128;
+                const uint64_t v_desc = v_desc0 + static_cast<uint64_t>((vs * Cfg::TILE_BYTES) >> 4);
+#pragma unroll
+                for (int k = 0; k < Cfg::BKV / 16; ++k) {
+                    // P (A, in TMEM): 16 keys = 8 columns per step; V (B,
+                    // MN-major along dim): 16 key rows = +2 KB per step.
+                    const uint64_t vb = v_desc + static_cast<uint64_t>((k * 16 * 128) >> 4);
+                    mma_f16_ts(o_tmem, p_tmem + k * 8, vb, Cfg::IDESC_O, (j > 0 || k > 0) ? 1u : 0u);
+                }
+                if (t == 1) mma_commit(v_empty(vs));
+                mma_commit(o_ready(t));
+                return true;
+            };
+            if (ok) ok = issue_s(0, 0) && issue_s(1, 0);
+            for (int j = 0; ok && j < nb1; ++j) {
+                if (j < nb0) {
+                    if (!issue_pv(0, j) || (j + 1 < nb0 && !issue_s(0, j + 1))) {
+                        ok = false;
+                        break;
+                    }
+                }
+                if (!issue_pv(1, j) || (j + 1 < nb1 && !issue_s(1, j + 1))) {
                     ok = false;
                     break;
                 }
             }
-            if (ok && nblk > 0) ok = issue_pv(nblk - 1);
             if (!ok) {
                 if (issued_any) {
                     // Wait for this thread's MMAs before the TMEM is freed.
@@ -431,49 +444,29 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------------------ softmax (warps 2..9)
-        const int q = warp & 3;                 // TMEM lane quarter
-        const int half = (warp - 2) >> 2;       // key half of each block; dim half of the output
+        // ------------------------------------------------------------ softmax (warps 2..17)
+        const int t = (warp - 2) / Cfg::TILE_WARPS;                  // query tile
+        const int q = warp & 3;                                     // TMEM lane quarter
+        const int half = ((warp - 2) % Cfg::TILE_WARPS) >> 2;       // key half of each block; dim half of the output
         const int row_local = q * 32 + lane;
-        const int row = qb * Cfg::BQ + row_local;
+        const int row = (2 * grp + t) * Cfg::BQ + row_local;
+        const int nblk = t == 0 ? nb0 : nb1;
         const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
-        // Exchange columns (TMEM, this row's lane): maxima [parity][half], sums [half].
-        const uint32_t x_addr = tmem_base + lane_addr + Cfg::TMEM_X_COL;
+        const uint32_t s_base = tmem_base + lane_addr + Cfg::TMEM_S_COL + t * Cfg::BKV;
+        const uint32_t o_addr = tmem_base + lane_addr + Cfg::TMEM_O_COL + t * 128 + half * (kDim / 2);
+        // Exchange slots (shared memory) of this row: xs(par, h) holds the
+        // block maximum of key half h for blocks of parity par, and at the end
+        // the partial sum of half h (in the parity no block uses any more).
+        auto xs = [&](int par, int h) -> volatile float & {
+            return xbuf[((t * 2 + par) * 2 + h) * Cfg::BQ + row_local];
+        };
         constexpr int HK = Cfg::BKV / 2;        // keys per thread per block
-        // Copy this row's half of Q (dim columns half*kDim/2 ..) from the
-        // swizzled shared tile into TMEM, packed two fp16 per column.
-        {
-            const bool got_q = wait_phase(q_full, 0, abort, limit, kSiteEpilogueTmemFull);
-            if (__all_sync(0xffffffffu, got_q)) {
-                constexpr int kChunks = kDim / 16;     // 16-byte chunks in half a row
-                uint32_t qv[kChunks * 4];
-                const uint32_t sw = static_cast<uint32_t>(lane & 7);
-#pragma unroll
-                for (int c = 0; c < kChunks; ++c) {
-                    const int e = half * (kDim / 2) + c * 8;          // first element of the chunk
-                    const uint32_t atom = static_cast<uint32_t>(e / 64), cin = static_cast<uint32_t>((e % 64) / 8);
-                    ld_shared_v4(sQ + atom * Cfg::ATOM_BYTES + static_cast<uint32_t>(row_local) * 128u +
-                                     ((cin ^ sw) << 4),
-                                 qv[4 * c], qv[4 * c + 1], qv[4 * c + 2], qv[4 * c + 3]);
-                }
-                const uint32_t q_addr = tmem_base + lane_addr + Cfg::TMEM_Q_COL + half * (kDim / 4);
-                if constexpr (kDim == 128) {
-                    attn_tmem_st32(q_addr, qv);
-                } else {
-                    attn_tmem_st16(q_addr, qv);
-                }
-                tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(q_ready);
-            }
-        }
         float m_ref = -INFINITY;   // reference maximum (log2 units, scaled scores), shared by the row's two threads
         float l = 0.0f;            // this thread's partial sum of weights relative to m_ref
         bool ok = true;
         for (int j = 0; j < nblk; ++j) {
-            const int slot = j & 1;
-            const uint32_t ph = (j >> 1) & 1u;
-            const bool got = wait_phase(s_full(slot), ph, abort, limit, kSiteEpilogueTmemFull);
+            const uint32_t ph = (j >> 1) & 1u;   // phase of the parity barriers xchg(t, j & 1)
+            const bool got = wait_phase(s_full(t), j & 1u, abort, limit, kSiteEpilogueTmemFull);
             if (!__all_sync(0xffffffffu, got)) {
                 ok = false;
                 break;
@@ -482,7 +475,7 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
             // This thread's 64 raw scores of block j (keys half*64 ..); the
             // scale (positive) is applied inside the exponent's argument.
             float x[HK];
-            const uint32_t s_addr = tmem_base + lane_addr + Cfg::TMEM_S_COL + slot * Cfg::BKV + half * HK;
+            const uint32_t s_addr = s_base + half * HK;
 #pragma unroll
             for (int c = 0; c < HK / 32; ++c) {
                 uint32_t r[32];
@@ -508,20 +501,18 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
             }
             float mx = max3(m4[0], m4[1], fmaxf(m4[2], m4[3])) * p.scale_log2;
             // Row maximum of the block: exchange the two halves' maxima
-            // through TMEM (parity-buffered: a thread writes parity p again
-            // only after the next barrier, which its partner reaches only
-            // after reading).
-            attn_tmem_st1(x_addr + (j & 1) * 2 + half, mx);
-            tc_fence_before_sync();
+            // through shared memory (parity-buffered: a thread writes parity
+            // p again only after the next barrier, which its partner reaches
+            // only after reading).
+            xs(j & 1, half) = mx;
             __syncwarp();
-            if (lane == 0) mbar_arrive(xchg(j & 1));
-            const bool got_x = wait_phase(xchg(j & 1), ph, abort, limit, kSiteEpilogueTmemFull);
+            if (lane == 0) mbar_arrive(xchg(t, j & 1));
+            const bool got_x = wait_phase(xchg(t, j & 1), ph, abort, limit, kSiteEpilogueTmemFull);
             if (!__all_sync(0xffffffffu, got_x)) {
                 ok = false;
                 break;
             }
-            tc_fence_after_sync();
-            mx = fmaxf(mx, attn_tmem_ld1(x_addr + (j & 1) * 2 + (half ^ 1)));
+            mx = fmaxf(mx, xs(j & 1, half ^ 1));
             // Move the reference only when the block's maximum exceeds it by
             // more than 8 (weights then stay <= 2^8).  Both threads of a row
             // see the same maxima, so they decide alike.
@@ -534,8 +525,9 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
             const bool rescale = j > 0 && __any_sync(0xffffffffu, alpha != 1.0f);
             // P half-row (fp16 pairs) into TMEM over the scores of this block:
             // keys half*64 .. +63 are columns half*32 .. +31 of the buffer.
-            // Every softmax thread has read its scores before the maxima
-            // exchange above, so no score is overwritten before it is read.
+            // Every softmax thread of the tile has read its scores before the
+            // maxima exchange above, so no score is overwritten before it is
+            // read.
             float lsum0 = 0.0f, lsum1 = 0.0f;
             const float neg_m = -m_ref;
             uint32_t w[HK / 2];
@@ -549,21 +541,11 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
                 const __half2 v = __floats2half2_rn(p0, p1);
                 w[i] = *reinterpret_cast<const uint32_t *>(&v);
             }
-            attn_tmem_st32(tmem_base + lane_addr + Cfg::TMEM_S_COL + slot * Cfg::BKV + half * (HK / 2), w);
+            attn_tmem_st32(s_base + half * (HK / 2), w);
             l += lsum0 + lsum1;
             if (rescale) {
-                // O must hold exactly blocks 0 .. j-1: wait for the MMAs of
-                // block j-1 (those of j-2 completed before buffer `slot` was
-                // free, so this barrier is at most one phase behind), then
-                // rescale this thread's half of the row's dim columns.
-                const int jp = j - 1;
-                const bool got_o = wait_phase(o_ready(jp & 1), (jp >> 1) & 1u, abort, limit, kSiteEpilogueTmemFull);
-                if (!__all_sync(0xffffffffu, got_o)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after_sync();
-                const uint32_t o_addr = tmem_base + lane_addr + Cfg::TMEM_O_COL + half * (kDim / 2);
+                // The output holds exactly blocks 0 .. j-1 (see the MMA order
+                // above): rescale this thread's half of the row's dim columns.
 #pragma unroll
                 for (int c = 0; c < kDim / 64; ++c) {
                     uint32_t r[32];
@@ -572,34 +554,31 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
                     for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
                     attn_tmem_st32(o_addr + c * 32, r);
                 }
-                tc_fence_before_sync();
             }
             tc_fence_before_sync();   // P (and a rescaled O) in TMEM before the MMA is told
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full(slot));
+            if (lane == 0) mbar_arrive(p_full(t));
         }
-        // Row sum = the two halves' partial sums (exchanged once, at the end,
-        // in columns of their own; a bounded wait, like every other).
+        // Row sum = the two halves' partial sums, exchanged once at the end in
+        // the parity slots of block nblk (no block of that parity is left: the
+        // partner read them, for block nblk-2, before it arrived at the last
+        // maxima barrier this thread passed).
         if (ok) {
-            attn_tmem_st1(x_addr + 4 + half, l);
-            tc_fence_before_sync();
+            xs(nblk & 1, half) = l;
             __syncwarp();
-            if (lane == 0) mbar_arrive(xfin);
-            const bool got_f = wait_phase(xfin, 0, abort, limit, kSiteEpilogueTmemFull);
+            if (lane == 0) mbar_arrive(xfin(t));
+            const bool got_f = wait_phase(xfin(t), 0, abort, limit, kSiteEpilogueTmemFull);
             ok = __all_sync(0xffffffffu, got_f);
-            if (ok) {
-                tc_fence_after_sync();
-                l += attn_tmem_ld1(x_addr + 4 + (half ^ 1));
-            }
+            if (ok) l += xs(nblk & 1, half ^ 1);
         }
-        if (ok && nblk > 0) {
-            // The MMAs of the last block (and, in order, of every block before it).
+        if (ok) {
+            // The MMAs of the tile's last block (one phase per block; those of
+            // the block before completed before its scores did).
             const int jl = nblk - 1;
-            const bool got_o = wait_phase(o_ready(jl & 1), (jl >> 1) & 1u, abort, limit, kSiteEpilogueTmemFull);
+            const bool got_o = wait_phase(o_ready(t), jl & 1u, abort, limit, kSiteEpilogueTmemFull);
             if (__all_sync(0xffffffffu, got_o)) {
                 tc_fence_after_sync();
                 const float inv_l = 1.0f / l;
-                const uint32_t o_addr = tmem_base + lane_addr + Cfg::TMEM_O_COL + half * (kDim / 2);
                 __half *orow = p.O + (static_cast<int64_t>(bh) * p.seq + row) * kDim + half * (kDim / 2);
 #pragma unroll
                 for (int c = 0; c < kDim / 64; ++c) {
