@@ -9,25 +9,26 @@
 // streamed in blocks of 128 with a running row maximum and row sum, so the
 // score matrix is never stored.
 //
-// One CTA per (query block, head, batch); 320 threads:
-//   warp 0, one lane   TMA: Q once (3-D tensor maps: rows of another head are
-//                      never read, rows past seq read as zero), then K and V
-//                      blocks through rings of KV_STAGES slots
-//   warp 1, one lane   MMA issuer (and TMEM owner): S_j = Q K_j^T (Q read from
-//                      TMEM, where the softmax warps copied it once) into one of
-//                      two 128-column TMEM score buffers, O += P_j V_j into a
-//                      dim-column TMEM output accumulator; S_{j+1} is issued
-//                      before O += P_j V_j so the tensor core works on the next
-//                      scores while the softmax of this block runs
-//   warps 2..9         softmax: two threads per query row (TMEM lane), one per
-//                      half of each 128-key block: read 64 scores, mask,
-//                      partial row max (exchanged through shared memory),
-//                      p = 2^(s*c - m) with c = sm_scale * log2(e), partial
-//                      row sum, P in fp16 written back into TMEM over the
-//                      scores it came from (the MMA reads it there as its A
-//                      operand, so P costs no shared-memory traffic); at the
-//                      end the two partial sums are added and each thread
-//                      writes O / l for half of the row's dim columns
+// One CTA per (pair of query blocks, head, batch): two query tiles of 128
+// rows that share every K/V block; 320 threads:
+//   warp 0, one lane   TMA: the two Q tiles once (3-D tensor maps: rows of
+//                      another head are never read, rows past seq read as
+//                      zero), then K and V blocks through rings of KV_STAGES
+//                      slots, each loaded once for both tiles
+//   warp 1, one lane   MMA issuer (and TMEM owner): per tile t,
+//                      S^t_j = Q^t K_j^T (both from shared memory) into the
+//                      tile's 128-column TMEM score buffer and
+//                      O^t += P^t_j V_j into its TMEM output accumulator.  The
+//                      stream alternates tiles (O^0 += P^0_j V_j, S^0_{j+1},
+//                      O^1 += P^1_j V_j, S^1_{j+1}), so the tensor core works
+//                      on one tile while the other tile's softmax runs
+//   warps 2..9         softmax, four warps per tile, one thread per query row
+//                      (TMEM lane) and all 128 keys of a block: masked
+//                      scores, row maximum, p = 2^(s*c - m) with
+//                      c = sm_scale * log2(e), row sum, P in fp16 written back
+//                      into TMEM over the scores it came from (the MMA reads
+//                      it there as its A operand, so P costs no shared-memory
+//                      traffic); at the end each thread writes its row O / l
 // The reference maximum m only moves when a block's maximum exceeds it by more
 // than 8 (in log2 units); then O (in TMEM) and l are multiplied by 2^(m_old -
 // m_new).  Otherwise p <= 2^8 is used as is: every weight is relative to the
@@ -90,39 +91,43 @@ __device__ __forceinline__ void attn_tmem_st32(uint32_t taddr, const uint32_t (&
         : "memory");
 }
 
-// 16 consecutive 32-bit TMEM columns of the warp's 32 lanes: store (and wait).
-__device__ __forceinline__ void attn_tmem_st16(uint32_t taddr, const uint32_t (&r)[16])
+// 32 consecutive 32-bit TMEM columns of the warp's 32 lanes: load without
+// waiting (the registers are valid after attn_tmem_wait_ld).
+__device__ __forceinline__ void attn_tmem_ld32_nowait(uint32_t taddr, uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
+          "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+          "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ void attn_tmem_wait_ld()
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// 16 consecutive 32-bit TMEM columns of the warp's 32 lanes: store without
+// waiting (complete after attn_tmem_wait_st).
+__device__ __forceinline__ void attn_tmem_st16_nowait(uint32_t taddr, const uint32_t (&r)[16])
 {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};\n\t"
-        "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
         "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
         "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
         : "memory");
 }
 
-__device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t &a, uint32_t &b, uint32_t &c, uint32_t &d)
+__device__ __forceinline__ void attn_tmem_wait_st()
 {
-    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(a), "=r"(b), "=r"(c), "=r"(d) : "r"(addr) : "memory");
-}
-
-// One fp32 TMEM column of the warp's 32 lanes: store (and wait), load (and wait).
-__device__ __forceinline__ void attn_tmem_st1(uint32_t taddr, float v)
-{
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};\n\ttcgen05.wait::st.sync.aligned;" ::"r"(taddr),
-                 "r"(__float_as_uint(v))
-                 : "memory");
-}
-
-__device__ __forceinline__ float attn_tmem_ld1(uint32_t taddr)
-{
-    uint32_t r;
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];\n\ttcgen05.wait::ld.sync.aligned;"
-                 : "=r"(r)
-                 : "r"(taddr)
-                 : "memory");
-    return __uint_as_float(r);
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // 2^x on the special-function unit (approximate, about 2 ulp of fp32;
@@ -189,7 +194,7 @@ struct AttnCfg {
     static constexpr int TILES = 2;               // query tiles per CTA, sharing every K/V block
     static constexpr int BQ = 128;                // query rows per tile (TMEM lanes)
     static constexpr int BKV = 128;               // keys per block
-    static constexpr int TILE_WARPS = 8;          // softmax warps per tile: two per TMEM lane quarter
+    static constexpr int TILE_WARPS = 4;          // softmax warps per tile: one per TMEM lane quarter
     static constexpr int SOFTMAX_WARPS = TILES * TILE_WARPS;
     static constexpr int THREADS = 64 + 32 * SOFTMAX_WARPS;
     static constexpr int ATOMS = kDim / 64;       // 128-byte swizzle atoms along dim
@@ -199,9 +204,7 @@ struct AttnCfg {
     static constexpr int SMEM_Q_OFF = 0;                   // TILES query tiles
     static constexpr int SMEM_K_OFF = SMEM_Q_OFF + TILES * TILE_BYTES;
     static constexpr int SMEM_V_OFF = SMEM_K_OFF + KV_STAGES * TILE_BYTES;
-    static constexpr int SMEM_X_OFF = SMEM_V_OFF + KV_STAGES * TILE_BYTES;
-    static constexpr int SMEM_X_BYTES = TILES * 2 * 2 * BQ * 4;   // fp32 [tile][block parity][key half][row]
-    static constexpr int SMEM_CTL_OFF = SMEM_X_OFF + SMEM_X_BYTES;
+    static constexpr int SMEM_CTL_OFF = SMEM_V_OFF + KV_STAGES * TILE_BYTES;
     static constexpr int SMEM_CTL_BYTES = 256;
     static constexpr int SMEM_BYTES = 1024 + SMEM_CTL_OFF + SMEM_CTL_BYTES;
     static constexpr int TMEM_S_COL = 0;          // per tile one 128-column score buffer; P (fp16
@@ -214,7 +217,7 @@ struct AttnCfg {
     static_assert(kDim == 64 || kDim == 128, "head dimension 64 or 128");
     static_assert(TMEM_O_COL + TILES * 128 <= TMEM_COLS, "TMEM columns");
     static_assert(SMEM_BYTES <= 232448, "shared memory per block on sm_103");
-    static_assert((16 + 4 * KV_STAGES) * 8 <= SMEM_CTL_BYTES, "control block");
+    static_assert((10 + 4 * KV_STAGES) * 8 <= SMEM_CTL_BYTES, "control block");
 };
 
 struct AttnParams {
@@ -240,12 +243,10 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
     const uint32_t sQ = base + Cfg::SMEM_Q_OFF;
     const uint32_t sK = base + Cfg::SMEM_K_OFF;
     const uint32_t sV = base + Cfg::SMEM_V_OFF;
-    float *xbuf = reinterpret_cast<float *>(base_ptr + Cfg::SMEM_X_OFF);
     const uint32_t ctl = base + Cfg::SMEM_CTL_OFF;
     // Barriers (8 bytes each): q_full; k_full, k_empty, v_full, v_empty
-    // [KV_STAGES] (the K and V rings); per tile s_full, p_full, o_ready; per
-    // tile and block parity xchg; per tile xfin; drain; then the TMEM address
-    // slot and the abort flag.
+    // [KV_STAGES] (the K and V rings); per tile s_full, p_full, o_ready;
+    // drain; then the TMEM address slot and the abort flag.
     //
     // Order of the MMA stream: S^0_0, S^1_0, then per block j and tile t:
     // O^t += P^t_j V_j, S^t_{j+1}.  Tile t's score buffer is rewritten by
@@ -261,16 +262,11 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
     auto s_full = [&](int t) { return ctl + 8u * (1 + 4 * S + t); };
     auto p_full = [&](int t) { return ctl + 8u * (3 + 4 * S + t); };
     auto o_ready = [&](int t) { return ctl + 8u * (5 + 4 * S + t); };
-    // Exchange between a row's two softmax threads: the tile's eight warps
-    // arrive once they have stored their values (per block parity, and once
-    // at the end).
-    auto xchg = [&](int t, int par) { return ctl + 8u * (7 + 4 * S + 2 * t + par); };
-    auto xfin = [&](int t) { return ctl + 8u * (11 + 4 * S + t); };
-    const uint32_t drain = ctl + 8u * (13 + 4 * S);
-    const uint32_t tmem_slot = ctl + 8u * (14 + 4 * S);
+    const uint32_t drain = ctl + 8u * (7 + 4 * S);
+    const uint32_t tmem_slot = ctl + 8u * (8 + 4 * S);
     const uint32_t abort_addr = tmem_slot + 4;
     volatile uint32_t *tmem_slot_ptr =
-        reinterpret_cast<volatile uint32_t *>(base_ptr + Cfg::SMEM_CTL_OFF + 8 * (14 + 4 * S));
+        reinterpret_cast<volatile uint32_t *>(base_ptr + Cfg::SMEM_CTL_OFF + 8 * (8 + 4 * S));
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -304,9 +300,6 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
             mbar_init(s_full(t), 1);
             mbar_init(p_full(t), Cfg::TILE_WARPS);
             mbar_init(o_ready(t), 1);
-            mbar_init(xchg(t, 0), Cfg::TILE_WARPS);
-            mbar_init(xchg(t, 1), Cfg::TILE_WARPS);
-            mbar_init(xfin(t), Cfg::TILE_WARPS);
         }
         mbar_init(drain, 1);
         *abort.local = 0;
@@ -444,78 +437,60 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------------------ softmax (warps 2..17)
-        const int t = (warp - 2) / Cfg::TILE_WARPS;                  // query tile
-        const int q = warp & 3;                                     // TMEM lane quarter
-        const int half = ((warp - 2) % Cfg::TILE_WARPS) >> 2;       // key half of each block; dim half of the output
+        // ------------------------------------------------------------ softmax (warps 2..9)
+        // One thread per query row (TMEM lane) and all 128 keys of a block.
+        const int t = (warp - 2) / Cfg::TILE_WARPS;   // query tile
+        const int q = warp & 3;                      // TMEM lane quarter
         const int row_local = q * 32 + lane;
         const int row = (2 * grp + t) * Cfg::BQ + row_local;
         const int nblk = t == 0 ? nb0 : nb1;
         const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
         const uint32_t s_base = tmem_base + lane_addr + Cfg::TMEM_S_COL + t * Cfg::BKV;
-        const uint32_t o_addr = tmem_base + lane_addr + Cfg::TMEM_O_COL + t * 128 + half * (kDim / 2);
-        // Exchange slots (shared memory) of this row: xs(par, h) holds the
-        // block maximum of key half h for blocks of parity par, and at the end
-        // the partial sum of half h (in the parity no block uses any more).
-        auto xs = [&](int par, int h) -> volatile float & {
-            return xbuf[((t * 2 + par) * 2 + h) * Cfg::BQ + row_local];
-        };
-        constexpr int HK = Cfg::BKV / 2;        // keys per thread per block
-        float m_ref = -INFINITY;   // reference maximum (log2 units, scaled scores), shared by the row's two threads
-        float l = 0.0f;            // this thread's partial sum of weights relative to m_ref
+        const uint32_t o_addr = tmem_base + lane_addr + Cfg::TMEM_O_COL + t * 128;
+        constexpr int NK = Cfg::BKV;   // keys per block
+        float m_ref = -INFINITY;       // reference maximum (log2 units, scaled scores)
+        float l = 0.0f;                // row sum of weights relative to m_ref
         bool ok = true;
         for (int j = 0; j < nblk; ++j) {
-            const uint32_t ph = (j >> 1) & 1u;   // phase of the parity barriers xchg(t, j & 1)
             const bool got = wait_phase(s_full(t), j & 1u, abort, limit, kSiteEpilogueTmemFull);
             if (!__all_sync(0xffffffffu, got)) {
                 ok = false;
                 break;
             }
             tc_fence_after_sync();
-            // This thread's 64 raw scores of block j (keys half*64 ..); the
-            // scale (positive) is applied inside the exponent's argument.
-            float x[HK];
-            const uint32_t s_addr = s_base + half * HK;
+            // The row's 128 raw scores of block j; the scale (positive) is
+            // applied inside the exponent's argument.
+            float x[NK];
+            {
+                uint32_t r[4][32];
 #pragma unroll
-            for (int c = 0; c < HK / 32; ++c) {
-                uint32_t r[32];
-                attn_tmem_ld32(s_addr + c * 32, r);
+                for (int c = 0; c < 4; ++c) attn_tmem_ld32_nowait(s_base + c * 32, r[c]);
+                attn_tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(r[i]);
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(r[c][i]);
             }
-            const int key0 = j * Cfg::BKV + half * HK;
+            const int key0 = j * Cfg::BKV;
             const int last_key = p.causal ? min(row, p.seq - 1) : p.seq - 1;
-            if (key0 + HK - 1 > last_key) {
+            if (key0 + NK - 1 > last_key) {
 #pragma unroll
-                for (int i = 0; i < HK; ++i)
+                for (int i = 0; i < NK; ++i)
                     if (key0 + i > last_key) x[i] = -INFINITY;
             }
-            // Maximum as four independent chains of three-input maxima.
-            float m4[4];
+            // Maximum as eight independent chains of three-input maxima.
+            float m8[8];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                m4[k] = max3(x[16 * k], x[16 * k + 1], x[16 * k + 2]);
+            for (int k = 0; k < 8; ++k) {
+                m8[k] = max3(x[16 * k], x[16 * k + 1], x[16 * k + 2]);
 #pragma unroll
-                for (int i = 3; i < 15; i += 2) m4[k] = max3(m4[k], x[16 * k + i], x[16 * k + i + 1]);
-                m4[k] = fmaxf(m4[k], x[16 * k + 15]);
+                for (int i = 3; i < 15; i += 2) m8[k] = max3(m8[k], x[16 * k + i], x[16 * k + i + 1]);
+                m8[k] = fmaxf(m8[k], x[16 * k + 15]);
             }
-            float mx = max3(m4[0], m4[1], fmaxf(m4[2], m4[3])) * p.scale_log2;
-            // Row maximum of the block: exchange the two halves' maxima
-            // through shared memory (parity-buffered: a thread writes parity
-            // p again only after the next barrier, which its partner reaches
-            // only after reading).
-            xs(j & 1, half) = mx;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(xchg(t, j & 1));
-            const bool got_x = wait_phase(xchg(t, j & 1), ph, abort, limit, kSiteEpilogueTmemFull);
-            if (!__all_sync(0xffffffffu, got_x)) {
-                ok = false;
-                break;
-            }
-            mx = fmaxf(mx, xs(j & 1, half ^ 1));
+            const float mx = max3(max3(m8[0], m8[1], m8[2]), max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7])) *
+                             p.scale_log2;
             // Move the reference only when the block's maximum exceeds it by
-            // more than 8 (weights then stay <= 2^8).  Both threads of a row
-            // see the same maxima, so they decide alike.
+            // more than 8 (weights then stay <= 2^8).
             float alpha = 1.0f;
             if (mx > m_ref + 8.0f) {
                 alpha = ex2_approx(m_ref - mx);   // 0 on the first block (m_ref = -inf)
@@ -523,31 +498,32 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
                 m_ref = mx;
             }
             const bool rescale = j > 0 && __any_sync(0xffffffffu, alpha != 1.0f);
-            // P half-row (fp16 pairs) into TMEM over the scores of this block:
-            // keys half*64 .. +63 are columns half*32 .. +31 of the buffer.
-            // Every softmax thread of the tile has read its scores before the
-            // maxima exchange above, so no score is overwritten before it is
-            // read.
+            // P (fp16 pairs) into TMEM over the scores of this block: keys
+            // 32c .. 32c+31 are columns 16c .. 16c+15 of the buffer, scores
+            // this thread has already read into registers.
             float lsum0 = 0.0f, lsum1 = 0.0f;
             const float neg_m = -m_ref;
-            uint32_t w[HK / 2];
 #pragma unroll
-            for (int i = 0; i < HK / 2; ++i) {
-                float a0, a1;   // s * c - m for the pair, one packed instruction
-                fma2_bcast(a0, a1, x[2 * i], x[2 * i + 1], p.scale_log2, neg_m);
-                const float p0 = ex2_approx(a0);
-                const float p1 = ex2_approx(a1);
-                add2(lsum0, lsum1, p0, p1);
-                const __half2 v = __floats2half2_rn(p0, p1);
-                w[i] = *reinterpret_cast<const uint32_t *>(&v);
+            for (int c = 0; c < 4; ++c) {
+                uint32_t w[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float a0, a1;   // s * c - m for the pair, one packed instruction
+                    fma2_bcast(a0, a1, x[32 * c + 2 * i], x[32 * c + 2 * i + 1], p.scale_log2, neg_m);
+                    const float p0 = ex2_approx(a0);
+                    const float p1 = ex2_approx(a1);
+                    add2(lsum0, lsum1, p0, p1);
+                    const __half2 v = __floats2half2_rn(p0, p1);
+                    w[i] = *reinterpret_cast<const uint32_t *>(&v);
+                }
+                attn_tmem_st16_nowait(s_base + c * 16, w);
             }
-            attn_tmem_st32(s_base + half * (HK / 2), w);
             l += lsum0 + lsum1;
             if (rescale) {
                 // The output holds exactly blocks 0 .. j-1 (see the MMA order
-                // above): rescale this thread's half of the row's dim columns.
+                // above): rescale the row's dim columns.
 #pragma unroll
-                for (int c = 0; c < kDim / 64; ++c) {
+                for (int c = 0; c < kDim / 32; ++c) {
                     uint32_t r[32];
                     attn_tmem_ld32(o_addr + c * 32, r);
 #pragma unroll
@@ -555,21 +531,10 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
                     attn_tmem_st32(o_addr + c * 32, r);
                 }
             }
+            attn_tmem_wait_st();
             tc_fence_before_sync();   // P (and a rescaled O) in TMEM before the MMA is told
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full(t));
-        }
-        // Row sum = the two halves' partial sums, exchanged once at the end in
-        // the parity slots of block nblk (no block of that parity is left: the
-        // partner read them, for block nblk-2, before it arrived at the last
-        // maxima barrier this thread passed).
-        if (ok) {
-            xs(nblk & 1, half) = l;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(xfin(t));
-            const bool got_f = wait_phase(xfin(t), 0, abort, limit, kSiteEpilogueTmemFull);
-            ok = __all_sync(0xffffffffu, got_f);
-            if (ok) l += xs(nblk & 1, half ^ 1);
         }
         if (ok) {
             // The MMAs of the tile's last block (one phase per block; those of
@@ -579,9 +544,9 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
             if (__all_sync(0xffffffffu, got_o)) {
                 tc_fence_after_sync();
                 const float inv_l = 1.0f / l;
-                __half *orow = p.O + (static_cast<int64_t>(bh) * p.seq + row) * kDim + half * (kDim / 2);
+                __half *orow = p.O + (static_cast<int64_t>(bh) * p.seq + row) * kDim;
 #pragma unroll
-                for (int c = 0; c < kDim / 64; ++c) {
+                for (int c = 0; c < kDim / 32; ++c) {
                     uint32_t r[32];
                     attn_tmem_ld32(o_addr + c * 32, r);
                     if (row < p.seq) {
