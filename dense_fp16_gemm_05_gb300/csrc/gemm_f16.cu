@@ -291,6 +291,47 @@ int pick_config(int64_t M, int64_t N, int64_t K, int sm_count)
 #define GEMM_F16_HAVE_TUNED 0
 #endif
 
+int config_info(int cfg, int64_t M, int64_t N, bool split, const DeviceInfo &dev, int *grid_ctas, int *cluster_size,
+                int *tiles)
+{
+    switch (cfg) {
+        case 1: return launch_info_config_1(M, N, split, dev, grid_ctas, cluster_size, tiles);
+        case 2: return launch_info_config_2(M, N, split, dev, grid_ctas, cluster_size, tiles);
+        case 3: return launch_info_config_3(M, N, split, dev, grid_ctas, cluster_size, tiles);
+        case 4: return launch_info_config_4(M, N, split, dev, grid_ctas, cluster_size, tiles);
+        case 5: return launch_info_config_5(M, N, split, dev, grid_ctas, cluster_size, tiles);
+        case 6: return launch_info_config_6(M, N, split, dev, grid_ctas, cluster_size, tiles);
+        default: return GEMM_ERR_INVALID_ARG;
+    }
+}
+
+// Resident CTAs (or clusters) of configuration `cfg` on this device: the grid
+// of a problem large enough to fill every slot.
+int64_t config_slots(int cfg, const DeviceInfo &dev)
+{
+    int grid = 0, cluster = 1, tiles = 0;
+    if (config_info(cfg, int64_t{1} << 16, int64_t{1} << 16, false, dev, &grid, &cluster, &tiles) != GEMM_OK ||
+        cluster <= 0)
+        return 0;
+    return grid / cluster;
+}
+
+// The slice count of GEMM_F16_KSPLIT_AUTO for configuration `cfg` (1: none):
+// if its tiles are fewer than its CTA slots, as many slices as fill the slots
+// once, at least 16 K blocks each, at most 16.
+int rule_k_splits(int cfg, int64_t M, int64_t N, int64_t K, const DeviceInfo &dev)
+{
+    int grid = 0, cluster = 1, tiles = 0;
+    if (config_info(cfg, M, N, false, dev, &grid, &cluster, &tiles) != GEMM_OK || cluster <= 0) return 1;
+    const int64_t slots = config_slots(cfg, dev);
+    const int64_t k_blocks = (K + 63) / 64;
+    if (tiles <= 0 || tiles >= slots) return 1;
+    int64_t n = slots / tiles;
+    if (n > k_blocks / 16) n = k_blocks / 16;
+    if (n > 16) n = 16;
+    return n >= 2 ? static_cast<int>(n) : 1;
+}
+
 double wave_eff(int id, int64_t M, int64_t N, bool split, const DeviceInfo &dev)
 {
     switch (id) {
@@ -302,6 +343,22 @@ double wave_eff(int id, int64_t M, int64_t N, bool split, const DeviceInfo &dev)
         case 6: return wave_eff_config_6(M, N, split, dev);
         default: return 0.0;
     }
+}
+
+// Wave efficiency of configuration `id` with GEMM_F16_KSPLIT_AUTO: whole tiles
+// in rule_k_splits slices, or the plain schedule (tail split allowed) when the
+// rule does not split.
+double ksplit_wave_eff(int id, int64_t M, int64_t N, int64_t K, const DeviceInfo &dev)
+{
+    const KSplit kk = k_split_for((K + 63) / 64, rule_k_splits(id, M, N, K, dev));
+    if (kk.count < 2) return wave_eff(id, M, N, true, dev);
+    int grid = 0, cluster = 1, tiles = 0;
+    if (config_info(id, M, N, false, dev, &grid, &cluster, &tiles) != GEMM_OK) return 0.0;
+    const int64_t slots = config_slots(id, dev);
+    const int64_t units = static_cast<int64_t>(tiles) * kk.count;
+    if (slots <= 0 || units <= 0) return 0.0;
+    const int64_t waves = (units + slots - 1) / slots;
+    return static_cast<double>(units) / static_cast<double>(waves * slots);
 }
 
 // The automatic choice.  The offline sweep (tune.py) measured every candidate
@@ -344,10 +401,12 @@ int select_config(int64_t M, int64_t N, int64_t K, bool any_layout, const Device
         const int id = c & GEMM_F16_CONFIG_ID_MASK;
         if (id < 1 || id > kNumConfigs || (any_layout && !kConfigs[id].all_layouts)) continue;
         const bool split = (c & GEMM_F16_NO_SPLIT) == 0;
-        const double here = wave_eff(id, M, N, split, dev);
-        const double there = wave_eff(id, t.M, t.N, split, dev);
+        const bool krule = (c & GEMM_F16_KSPLIT_AUTO) != 0;
+        const double here = krule ? ksplit_wave_eff(id, M, N, K, dev) : wave_eff(id, M, N, split, dev);
+        const double there = krule ? ksplit_wave_eff(id, t.M, t.N, t.K, dev) : wave_eff(id, t.M, t.N, split, dev);
         if (here <= 0.0 || there <= 0.0) continue;
-        const double predicted = static_cast<double>(t.tflops[i]) * here / there;
+        // (ratio first: exactly 1 on a measured shape, so ties keep table order)
+        const double predicted = static_cast<double>(t.tflops[i]) * (here / there);
         if (predicted > best) {
             best = predicted;
             choice = c;
@@ -362,14 +421,39 @@ int select_config(int64_t M, int64_t N, int64_t K, bool any_layout, const Device
     return pick_config(M, N, K, dev.sm_count);
 }
 
+// K-split requests of a config word (parse_config's *k_request).
+constexpr int kKsplitNone = 0;     // no K-split bit set
+constexpr int kKsplitNever = -1;   // GEMM_F16_NO_KSPLIT
+constexpr int kKsplitRule = -2;    // GEMM_F16_KSPLIT_AUTO
+                                   // n >= 2: GEMM_F16_KSPLIT(n)
+
 // Splits a config argument into the configuration id and its flag bits;
-// false for an unknown id or flag.
-bool parse_config(int config, int *id, bool *allow_split)
+// false for an unknown id or flag or contradictory K-split bits.
+bool parse_config(int config, int *id, bool *allow_split, int *k_request = nullptr)
 {
-    if (config < 0 || (config & ~(GEMM_F16_CONFIG_ID_MASK | GEMM_F16_NO_SPLIT)) != 0) return false;
+    constexpr int kKnown = GEMM_F16_CONFIG_ID_MASK | GEMM_F16_NO_SPLIT | GEMM_F16_NO_KSPLIT | GEMM_F16_KSPLIT_AUTO |
+                           GEMM_F16_KSPLIT_MASK;
+    if (config < 0 || (config & ~kKnown) != 0) return false;
+    const int n = (config & GEMM_F16_KSPLIT_MASK) >> GEMM_F16_KSPLIT_SHIFT;
+    const bool never = (config & GEMM_F16_NO_KSPLIT) != 0;
+    const bool rule = (config & GEMM_F16_KSPLIT_AUTO) != 0;
+    if (n == 1 || n > 16 || static_cast<int>(never) + static_cast<int>(rule) + static_cast<int>(n != 0) > 1)
+        return false;
     *id = config & GEMM_F16_CONFIG_ID_MASK;
     *allow_split = (config & GEMM_F16_NO_SPLIT) == 0;
+    if (k_request) *k_request = never ? kKsplitNever : rule ? kKsplitRule : n;
     return *id <= kNumConfigs;
+}
+
+// Slice count for a parsed request on configuration `cfg` (id: the id the
+// caller gave, 0 = automatic; picked: the automatic choice's config word).
+int k_splits_for(int k_request, int id, int picked, int cfg, int64_t M, int64_t N, int64_t K,
+                 const DeviceInfo &dev)
+{
+    if (k_request >= 2) return k_request;
+    if (k_request == kKsplitRule || (k_request == kKsplitNone && id == 0 && (picked & GEMM_F16_KSPLIT_AUTO)))
+        return rule_k_splits(cfg, M, N, K, dev);
+    return 1;
 }
 
 // ---------------------------------------------------------------- launch path
@@ -381,9 +465,9 @@ int run_gemm(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_
     if (st != GEMM_OK) return st;
     if ((transa != 0 && transa != 1) || (transb != 0 && transb != 1))
         return reject(GEMM_ERR_INVALID_ARG, "transa / transb is not 0 or 1");
-    int id = 0;
+    int id = 0, k_request = 0;
     bool allow_split = true;
-    if (!parse_config(config, &id, &allow_split))
+    if (!parse_config(config, &id, &allow_split, &k_request))
         return reject(GEMM_ERR_INVALID_ARG, "unknown configuration id or flag");
     if ((transa || transb) && !kConfigs[id].all_layouts)
         return reject(GEMM_ERR_INVALID_ARG, "this configuration has no transposed-layout kernels");
@@ -430,14 +514,16 @@ int run_gemm(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_
     a.status = status_word(dev.device);
     if (a.status == nullptr) return GEMM_ERR_CUDA;
 
-    int cfg = id;
+    int cfg = id, picked = 0;
     if (id == 0) {
-        const int picked = select_config(M, N, K, transa || transb, dev);
+        picked = select_config(M, N, K, transa || transb, dev);
         cfg = picked & GEMM_F16_CONFIG_ID_MASK;
         a.allow_split = allow_split && (picked & GEMM_F16_NO_SPLIT) == 0;
     } else {
         a.allow_split = allow_split;
     }
+    a.k_splits = k_splits_for(k_request, id, picked, cfg, M, N, K, dev);
+    if (hook.producer_off) a.k_splits = 1;   // the timeout self-test never writes C
     switch (cfg) {
         case 1: return launch_config_1(a);
         case 2: return launch_config_2(a);
@@ -629,7 +715,13 @@ extern "C" int gemm_f16_auto_config(int64_t M, int64_t N, int64_t K)
     if (st != GEMM_OK) return st;
     DeviceInfo dev;
     if ((st = current_device_info(&dev)) != GEMM_OK) return st;
-    return select_config(M, N, K, false, dev);
+    const int picked = select_config(M, N, K, false, dev);
+    const int cfg = picked & GEMM_F16_CONFIG_ID_MASK;
+    const int ks = k_splits_for(kKsplitNone, 0, picked, cfg, M, N, K, dev);
+    const KSplit kk = k_split_for((K + 63) / 64, ks);
+    // The rule resolved for this problem: gemm_f16_ex computes the same with it.
+    const int base = picked & ~GEMM_F16_KSPLIT_AUTO;
+    return kk.count >= 2 ? (base | GEMM_F16_NO_SPLIT | GEMM_F16_KSPLIT(kk.count)) : base;
 }
 
 extern "C" int gemm_f16_launch_info(int64_t M, int64_t N, int64_t K, int config, int *grid_ctas,
@@ -637,26 +729,31 @@ extern "C" int gemm_f16_launch_info(int64_t M, int64_t N, int64_t K, int config,
 {
     int st = check_sizes(M, N, K, 0);
     if (st != GEMM_OK) return st;
-    int id = 0;
+    int id = 0, k_request = 0;
     bool split = true;
-    if (!parse_config(config, &id, &split)) return reject(GEMM_ERR_INVALID_ARG, "unknown configuration id or flag");
+    if (!parse_config(config, &id, &split, &k_request))
+        return reject(GEMM_ERR_INVALID_ARG, "unknown configuration id or flag");
     DeviceInfo dev;
     if ((st = current_device_info(&dev)) != GEMM_OK) return st;
-    int cfg = id;
+    int cfg = id, picked = 0;
     if (id == 0) {
-        const int picked = select_config(M, N, K, false, dev);
+        picked = select_config(M, N, K, false, dev);
         cfg = picked & GEMM_F16_CONFIG_ID_MASK;
         split = split && (picked & GEMM_F16_NO_SPLIT) == 0;
     }
-    switch (cfg) {
-        case 1: return launch_info_config_1(M, N, split, dev, grid_ctas, cluster_size, tiles);
-        case 2: return launch_info_config_2(M, N, split, dev, grid_ctas, cluster_size, tiles);
-        case 3: return launch_info_config_3(M, N, split, dev, grid_ctas, cluster_size, tiles);
-        case 4: return launch_info_config_4(M, N, split, dev, grid_ctas, cluster_size, tiles);
-        case 5: return launch_info_config_5(M, N, split, dev, grid_ctas, cluster_size, tiles);
-        case 6: return launch_info_config_6(M, N, split, dev, grid_ctas, cluster_size, tiles);
-        default: return GEMM_ERR_INVALID_ARG;
+    const KSplit kk = k_split_for((K + 63) / 64, k_splits_for(k_request, id, picked, cfg, M, N, K, dev));
+    int grid = 0, cluster = 1, n_tiles = 0;
+    if ((st = config_info(cfg, M, N, split && kk.count == 1, dev, &grid, &cluster, &n_tiles)) != GEMM_OK) return st;
+    if (kk.count > 1) {
+        // Whole tiles, each in kk.count K slices, on at most one CTA (cluster) per slot.
+        const int64_t slots = config_slots(cfg, dev);
+        const int64_t units = static_cast<int64_t>(n_tiles) * kk.count;
+        grid = static_cast<int>((units < slots ? units : slots) * cluster);
     }
+    if (grid_ctas) *grid_ctas = grid;
+    if (cluster_size) *cluster_size = cluster;
+    if (tiles) *tiles = n_tiles;
+    return GEMM_OK;
 }
 
 extern "C" int gemm_f16_from_host(const void *A_host, const void *B_host, void *C_host, void *A_dev, void *B_dev,

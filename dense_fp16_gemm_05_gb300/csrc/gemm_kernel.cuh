@@ -64,6 +64,11 @@ struct GemmParams {
     int32_t num_units;      // split_start + (num_tiles - split_start) << split_log2
     int32_t split_start;    // first split tile (== num_tiles: no split)
     int32_t split_log2;     // each tile from split_start on is 2^split_log2 units
+    int32_t k_splits;       // > 1: unit u is slice u % k_splits of tile u / k_splits (K blocks
+                            // [slice * k_per_split, +k_per_split) clipped at num_k_blocks); the
+                            // epilogue then writes the fp32 partial to ws instead of C
+    int32_t k_per_split;    // K blocks per slice
+    float *ws;              // k_splits fp32 (M,N) row-major partial matrices, slice-major
     uint64_t timeout_cycles;
     __half *C;              // output base (used by the direct-store epilogue)
     int32_t producer_off;   // test hook: 1 = the producer issues nothing, so the
@@ -215,11 +220,26 @@ __device__ __forceinline__ void tile_coords(int t, const GemmParams &p, int &mb,
     nb = r / rows;
 }
 
+// K blocks [kb0, kb1) of work unit u, and its K slice (0 without K split).
+__device__ __forceinline__ void unit_k_range(int u, const GemmParams &p, int &kb0, int &kb1, int &slice)
+{
+    slice = 0;
+    kb0 = 0;
+    kb1 = p.num_k_blocks;
+    if (p.k_splits > 1) {
+        slice = u % p.k_splits;
+        kb0 = slice * p.k_per_split;
+        kb1 = min(p.num_k_blocks, kb0 + p.k_per_split);
+    }
+}
+
 // Work unit u -> tile row block mb, first output column col0 of the unit, and
-// the split shift (the unit is BN >> shift columns wide).
+// the split shift (the unit is BN >> shift columns wide).  With a K split the
+// unit's tile is u / k_splits (no N split then: split_start = num_tiles).
 template <int kBN>
 __device__ __forceinline__ void unit_coords(int u, const GemmParams &p, int &mb, int &col0, int &shift)
 {
+    if (p.k_splits > 1) u /= p.k_splits;
     int t = u, sub = 0;
     shift = 0;
     if (u >= p.split_start) {
@@ -365,8 +385,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             const uint32_t full_base = (kPair && !leader) ? mapa_shared(full_bar(0), leader_rank) : full_bar(0);
             (void)full_base;
             for (int u = cluster_id; ok && p.producer_off == 0 && u < p.num_units; u += num_clusters) {
-                int mb, col0, shift;
+                int mb, col0, shift, kb0, kb1, slice;
                 unit_coords<Cfg::BN>(u, p, mb, col0, shift);
+                unit_k_range(u, p, kb0, kb1, slice);
                 const int m0 = mb * Cfg::SUPER_M + static_cast<int>(pair) * Cfg::TILE_M +
                                static_cast<int>(rank) * Cfg::BM;
                 // Unit width W = BN >> shift, issued as W / umma_n MMAs of N = umma_n.
@@ -386,7 +407,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 #pragma unroll
                 for (int j = 0; j < Cfg::B_BOXES; ++j)
                     bxs[j] = n_cta + (j >> bpm_log2) * umma_n + (j & (bpm - 1)) * Cfg::B_BOX_N;
-                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_phase(empty_bar(s), ph ^ 1u, abort, limit, kSiteProducerEmpty)) {
                         ok = false;
                         break;
@@ -482,7 +503,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             for (int u = cluster_id; ok && u < p.num_units; u += num_clusters, ++it) {
                 const int b = it % Cfg::ACC_STAGES;
                 const uint32_t acc_ph = (it / Cfg::ACC_STAGES) & 1;
-                const int shift = u >= p.split_start ? p.split_log2 : 0;
+                const int shift = (p.k_splits <= 1 && u >= p.split_start) ? p.split_log2 : 0;
+                int kb0, kb1, slice;
+                unit_k_range(u, p, kb0, kb1, slice);
                 const int width = Cfg::BN >> shift;
                 const int umma_n = width < Cfg::UMMA_N ? width : Cfg::UMMA_N;
                 const int n_mmas = width / umma_n;
@@ -497,7 +520,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + b * Cfg::ACC_COLS;
-                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!wait_phase(full_bar(s), ph, abort, limit, kSiteMmaFull)) {
                         ok = false;
                         break;
@@ -508,7 +531,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     // n >> 4 (no carry out of the field: shared addresses < 2^18).
                     const uint64_t a_st = a_desc0 + static_cast<uint64_t>((s * Cfg::A_STAGE_BYTES) >> 4);
                     const uint64_t b_st = b_desc0 + static_cast<uint64_t>((s * Cfg::B_STAGE_BYTES) >> 4);
-                    const uint32_t acc0 = kb != 0 ? 1u : 0u;
+                    const uint32_t acc0 = kb != kb0 ? 1u : 0u;
 #pragma unroll
                     for (int ks = 0; ks < Cfg::BK / Cfg::UMMA_K; ++ks) {
                         const uint64_t a_desc = a_st + static_cast<uint64_t>((ks * kAStep) >> 4);
@@ -558,8 +581,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         int it = 0;
         uint32_t chunk = 0;
         for (int u = cluster_id; u < p.num_units; u += num_clusters, ++it) {
-            int mb, col0_unit, shift;
+            int mb, col0_unit, shift, kb0, kb1, slice;
             unit_coords<Cfg::BN>(u, p, mb, col0_unit, shift);
+            unit_k_range(u, p, kb0, kb1, slice);
             const int chunks = (Cfg::BN >> shift) / Cfg::EPI_COLS;
             const int b = it % Cfg::ACC_STAGES;
             const uint32_t acc_ph = (it / Cfg::ACC_STAGES) & 1;
@@ -590,7 +614,20 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     }
                 }
                 const int col0 = col0_unit + c * Cfg::EPI_COLS;
-                if constexpr (Cfg::EPI_SMEM) {
+                if (p.k_splits > 1) {
+                    // K slice: this row's 64 fp32 partial sums, as they are, into the
+                    // slice's workspace matrix (16-byte pieces; N is a multiple of 8,
+                    // so every piece is wholly in or out).
+                    const int row = row0 + lane;
+                    if (row < p.M) {
+                        float *wrow = p.ws + (static_cast<int64_t>(slice) * p.M + row) * p.N + col0;
+#pragma unroll
+                        for (int j = 0; j < Cfg::EPI_COLS / 4; ++j) {
+                            if (col0 + 4 * j < p.N)
+                                st_global_v4(wrow + 4 * j, r[4 * j + 0], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+                        }
+                    }
+                } else if constexpr (Cfg::EPI_SMEM) {
                     const bool in_range = row0 < p.M && col0 < p.N;
                     const uint32_t cbuf = sC + (ew * 2 + (chunk & 1u)) * Cfg::C_BUF_BYTES;
                     ++chunk;

@@ -43,12 +43,37 @@ struct LaunchArgs {
     LaunchHook hook;
     unsigned long long *status = nullptr;   // device status word of this GPU
     bool allow_split = true;   // false: every work unit is a whole tile (no tail split)
+    int k_splits = 1;          // > 1: split every tile's K loop into (up to) this many slices,
+                               // fp32 partials in a stream-ordered workspace, then a reduction
 };
 
 // Defined in gemm_f16.cu.
 int encode_matrix(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t cols, uint32_t box_cols,
                   uint32_t box_rows);
 int group_m_override();
+
+// C = R(sum of `splits` fp32 (M,N) partial matrices at ws), fp16 (splitk_reduce.cu).
+int launch_splitk_reduce(const float *ws, void *C, int64_t M, int64_t N, int splits, int relu, int sm_count,
+                         cudaStream_t stream);
+
+// K slices for a requested split count: `per` K blocks each, `count` of them
+// (count <= requested; every slice non-empty).  count == 1: no K split.
+struct KSplit {
+    int count = 1;
+    int per = 0;
+};
+
+inline KSplit k_split_for(int64_t k_blocks, int requested)
+{
+    KSplit ks;
+    ks.per = static_cast<int>(k_blocks);
+    if (requested > 1 && k_blocks >= 2) {
+        const int64_t per = (k_blocks + requested - 1) / requested;
+        ks.per = static_cast<int>(per);
+        ks.count = static_cast<int>((k_blocks + per - 1) / per);
+    }
+    return ks;
+}
 
 inline uint64_t timeout_cycles_for(int64_t K)
 {
@@ -168,12 +193,41 @@ int launch_one(const LaunchArgs &a)
     using Prep = Prepared<Cfg, kRelu, kTA, kTB>;
     const int64_t slots = Prep::get(a.dev.device, a.dev.sm_count);
     if (slots <= 0) return GEMM_ERR_LAUNCH;
-    const Schedule sc = make_schedule<Cfg>(a.M, a.N, slots, a.allow_split);
-    if (sc.units > INT32_MAX / 2) return GEMM_ERR_INVALID_ARG;
+    KSplit ks = k_split_for(p.num_k_blocks, a.k_splits);
+    float *ws = nullptr;
+    if (ks.count > 1) {
+        // Stream-ordered workspace: ordered with this call's kernels, private
+        // to it, and legal inside a stream capture.  If it cannot be had, the
+        // call runs without a K split.
+        const size_t ws_bytes = static_cast<size_t>(ks.count) * static_cast<size_t>(a.M) *
+                                static_cast<size_t>(a.N) * sizeof(float);
+        if (cudaMallocAsync(reinterpret_cast<void **>(&ws), ws_bytes, a.stream) != cudaSuccess) {
+            cudaGetLastError();
+            ws = nullptr;
+            ks = KSplit{1, p.num_k_blocks};
+        }
+    }
+    Schedule sc = make_schedule<Cfg>(a.M, a.N, slots, a.allow_split && ks.count == 1);
+    if (ks.count > 1) {
+        sc.units = sc.tiles * ks.count;   // whole tiles, each in ks.count K slices
+        sc.split_start = sc.tiles;
+        sc.shift = 0;
+        sc.grid_units = sc.units < slots ? sc.units : slots;
+    }
+    auto release_ws = [&]() {
+        if (ws != nullptr && cudaFreeAsync(ws, a.stream) != cudaSuccess) cudaGetLastError();
+    };
+    if (sc.units > INT32_MAX / 2) {
+        release_ws();
+        return GEMM_ERR_INVALID_ARG;
+    }
     p.num_tiles = static_cast<int32_t>(sc.tiles);
     p.num_units = static_cast<int32_t>(sc.units);
     p.split_start = static_cast<int32_t>(sc.split_start);
     p.split_log2 = sc.shift;
+    p.k_splits = ks.count;
+    p.k_per_split = ks.per;
+    p.ws = ws;
     // Rasterisation panels 2048 rows high whatever the tile height.
     p.group_m = group_m_override() ? group_m_override() : (Cfg::SUPER_M >= 2048 ? 1 : 2048 / Cfg::SUPER_M);
     p.timeout_cycles = a.hook.timeout_cycles ? a.hook.timeout_cycles : timeout_cycles_for(a.K);
@@ -200,8 +254,14 @@ int launch_one(const LaunchArgs &a)
         Prep::forget(a.dev.device);
         if (Prep::get(a.dev.device, a.dev.sm_count) <= 0 || cudaLaunchKernelEx(&lc, kern, ta, tb, tc, p) != cudaSuccess) {
             cudaGetLastError();
+            release_ws();
             return GEMM_ERR_LAUNCH;
         }
+    }
+    if (ks.count > 1) {
+        const int st2 = launch_splitk_reduce(ws, a.C, a.M, a.N, ks.count, a.relu, a.dev.sm_count, a.stream);
+        release_ws();
+        if (st2 != GEMM_OK) return st2;
     }
     return GEMM_OK;
 }

@@ -28,6 +28,15 @@ GEMM_ERR_CUDA = -6
 # Config argument: id in the low byte, flag bits above (include/gemm_f16.h).
 GEMM_F16_CONFIG_ID_MASK = 0xFF
 GEMM_F16_NO_SPLIT = 0x100
+GEMM_F16_NO_KSPLIT = 0x200
+GEMM_F16_KSPLIT_AUTO = 0x400
+GEMM_F16_KSPLIT_SHIFT = 12
+GEMM_F16_KSPLIT_MASK = 0x1F000
+
+
+def ksplit(n: int) -> int:
+    """Config flag: cut K into at most n slices (2 <= n <= 16), see gemm_f16.h."""
+    return int(n) << GEMM_F16_KSPLIT_SHIFT
 
 HEADER = os.path.join(_build.INCLUDE, "gemm_f16.h")
 
@@ -134,11 +143,14 @@ def config_name(config: int) -> str | None:
 
 
 def config_label(config: int) -> str | None:
-    """config_name plus "+nosplit" when the GEMM_F16_NO_SPLIT flag is set."""
+    """config_name plus "+nosplit" / "+ksplitN" / "+ksplitauto" / "+noksplit" for the flag bits."""
     name = config_name(config)
     if name is None:
         return None
-    return name + ("+nosplit" if int(config) & GEMM_F16_NO_SPLIT else "")
+    c = int(config)
+    n = (c & GEMM_F16_KSPLIT_MASK) >> GEMM_F16_KSPLIT_SHIFT
+    return (name + ("+nosplit" if c & GEMM_F16_NO_SPLIT else "") + (f"+ksplit{n}" if n else "")
+            + ("+ksplitauto" if c & GEMM_F16_KSPLIT_AUTO else "") + ("+noksplit" if c & GEMM_F16_NO_KSPLIT else ""))
 
 
 def _stream_handle(stream, device) -> int:

@@ -42,7 +42,7 @@
 extern "C" {
 #endif
 
-#define GEMM_F16_VERSION 5
+#define GEMM_F16_VERSION 6
 
 /* Return codes.  0 is success; every error is negative. */
 enum gemm_f16_status {
@@ -92,12 +92,50 @@ int gemm_f16(const void *A, const void *B, void *C,
  *                      the tail.  Either way every output element is the same
  *                      K-ordered fp32 sum, so the results do not change.
  *
- * No other bit may be set (GEMM_ERR_INVALID_ARG).  This tail policy is an
+ * The K-split bits below may also be set; no other bit may be set
+ * (GEMM_ERR_INVALID_ARG).  This tail policy is an
  * implementation choice of this library; the tile GEMM of the pages has no
  * persistent schedule and no tail split.
  */
 #define GEMM_F16_CONFIG_ID_MASK 0xFF
 #define GEMM_F16_NO_SPLIT 0x100
+
+/*
+ * K split (bits 9, 10 and 12-16 of a config word).  When a problem has fewer
+ * output tiles than the GPU has SMs (or SM pairs) for them, the K loop of every
+ * tile can be cut into slices that run on different SMs: each slice writes its
+ * fp32 partial product to a workspace taken from the stream-ordered allocator
+ * (cudaMallocAsync / cudaFreeAsync on `stream`: private to the call, ordered
+ * with its kernels, legal inside a stream capture), and a second kernel adds
+ * the slices in ascending order, applies the ReLU and rounds once to fp16.
+ * Each output is then the fp32 sum of per-slice fp32 sums, a different order
+ * of the same terms than without a split (results may differ in the last
+ * bits; ReLU is still exactly max(plain, +0)).  The workspace holds
+ * slices x M x N floats.  With a K split every work unit is a whole tile
+ * (GEMM_F16_NO_SPLIT is implied).
+ *
+ *   GEMM_F16_KSPLIT(n)    n = 2 .. 16: cut K into at most n slices of whole
+ *                         64-element blocks (fewer if K has fewer blocks; none
+ *                         for K <= 64).
+ *   GEMM_F16_KSPLIT_AUTO  the slice count of a rule: if the configuration's
+ *                         tiles are fewer than its CTA slots (one per SM, or
+ *                         per SM pair or cluster), as many slices as fill the
+ *                         slots once, at least 16 K blocks each, at most 16;
+ *                         none if that is fewer than 2.
+ *   GEMM_F16_NO_KSPLIT    never split K.
+ *
+ * Configuration 0 takes whatever the offline-measured table chose for the
+ * nearest measured shape; its candidates include every configuration with
+ * GEMM_F16_KSPLIT_AUTO.  A fixed configuration id without these bits does not
+ * split K.  If the workspace cannot be allocated the call runs without a K
+ * split.  The pages' tile GEMM keeps each tile's K loop in one block; this is
+ * a scheduling choice of this library.
+ */
+#define GEMM_F16_NO_KSPLIT 0x200
+#define GEMM_F16_KSPLIT_AUTO 0x400
+#define GEMM_F16_KSPLIT_SHIFT 12
+#define GEMM_F16_KSPLIT_MASK 0x1F000
+#define GEMM_F16_KSPLIT(n) ((n) << GEMM_F16_KSPLIT_SHIFT)
 
 /*
  * gemm_f16_ex -- gemm_f16 with an explicit kernel configuration.
@@ -225,8 +263,9 @@ int gemm_f16_num_configs(void);
 const char *gemm_f16_config_name(int config);
 
 /* Configuration that gemm_f16 picks for this problem size on the current
- * device: a nonzero id, possibly with flag bits (GEMM_F16_NO_SPLIT), which
- * gemm_f16_ex accepts as it is; or a negative status for invalid sizes. */
+ * device: a nonzero id, possibly with flag bits (GEMM_F16_NO_SPLIT,
+ * GEMM_F16_KSPLIT(n)), which gemm_f16_ex accepts as it is; or a negative
+ * status for invalid sizes. */
 int gemm_f16_auto_config(int64_t M, int64_t N, int64_t K);
 
 /*

@@ -255,7 +255,7 @@ def test_auto_choice_is_a_valid_config(g):
     for (M, N, K) in [(8192, 8192, 8192), (4096, 4096, 4096), (1024, 1024, 1024), (64, 64, 64), (16384, 512, 64)]:
         c = g.auto_config(M, N, K)
         assert c > 0 and g.config_name(c) is not None
-        assert (c & ~(g.GEMM_F16_CONFIG_ID_MASK | g.GEMM_F16_NO_SPLIT)) == 0
+        assert (c & ~(g.GEMM_F16_CONFIG_ID_MASK | g.GEMM_F16_NO_SPLIT | g.GEMM_F16_KSPLIT_MASK)) == 0
 
 
 def test_auto_config_follows_the_tuned_table(g):
@@ -270,4 +270,11 @@ def test_auto_config_follows_the_tuned_table(g):
         M, N, K = (int(m.group(i)) for i in (1, 2, 3))
         vals = [float(x.strip().rstrip("f")) for x in m.group(4).split(",")]
         best = cands[vals.index(max(vals))]
-        assert g.auto_config(M, N, K) == best, (M, N, K)
+        got = g.auto_config(M, N, K)
+        if best & g.GEMM_F16_KSPLIT_AUTO:
+            # the rule's slice count, resolved for this shape (whole tiles then)
+            n = (got & g.GEMM_F16_KSPLIT_MASK) >> g.GEMM_F16_KSPLIT_SHIFT
+            plain = best & ~g.GEMM_F16_KSPLIT_AUTO
+            assert got == plain or (n >= 2 and got == plain | g.GEMM_F16_NO_SPLIT | g.ksplit(n)), (M, N, K, hex(got))
+        else:
+            assert got == best, (M, N, K, hex(got))
