@@ -459,7 +459,7 @@ int k_splits_for(int k_request, int id, int picked, int cfg, int64_t M, int64_t 
 // ---------------------------------------------------------------- launch path
 
 int run_gemm(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K, int transa, int transb,
-             int relu, int config, void *stream, const LaunchHook &hook)
+             int relu, int config, void *stream, const LaunchHook &hook, bool noalloc = false)
 {
     int st = check_sizes(M, N, K, relu);
     if (st != GEMM_OK) return st;
@@ -524,6 +524,23 @@ int run_gemm(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_
     }
     a.k_splits = k_splits_for(k_request, id, picked, cfg, M, N, K, dev);
     if (hook.producer_off) a.k_splits = 1;   // the timeout self-test never writes C
+    if (noalloc) {
+        // K-slice partials go to the library's fixed scratch: reject what does
+        // not fit before anything is launched.
+        const KSplit kk = k_split_for((K + 63) / 64, a.k_splits);
+        if (kk.count > 1) {
+            float *scratch = nullptr;
+            size_t scratch_bytes = 0;
+            if ((st = noalloc_scratch(dev.device, &scratch, &scratch_bytes)) != GEMM_OK) return st;
+            const uint64_t need = static_cast<uint64_t>(kk.count) * static_cast<uint64_t>(M) *
+                                  static_cast<uint64_t>(N) * sizeof(float);
+            if (need > scratch_bytes)
+                return reject(GEMM_ERR_INVALID_ARG, "the K-slice partials exceed the 16 MiB scratch of "
+                                                    "gemm_f16_ex_noalloc");
+            a.fixed_ws = scratch;
+            a.fixed_ws_bytes = scratch_bytes;
+        }
+    }
     switch (cfg) {
         case 1: return launch_config_1(a);
         case 2: return launch_config_2(a);
@@ -551,6 +568,12 @@ extern "C" int gemm_f16_ex(const void *A, const void *B, void *C, int64_t M, int
                            int config, void *stream)
 {
     return run_gemm(A, B, C, M, N, K, 0, 0, relu, config, stream, LaunchHook());
+}
+
+extern "C" int gemm_f16_ex_noalloc(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K, int relu,
+                                   int config, void *stream)
+{
+    return run_gemm(A, B, C, M, N, K, 0, 0, relu, config, stream, LaunchHook{}, true);
 }
 
 extern "C" int gemm_f16(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K, int relu,

@@ -45,6 +45,8 @@ struct LaunchArgs {
     bool allow_split = true;   // false: every work unit is a whole tile (no tail split)
     int k_splits = 1;          // > 1: split every tile's K loop into (up to) this many slices,
                                // fp32 partials in a stream-ordered workspace, then a reduction
+    float *fixed_ws = nullptr; // non-null: the K-slice workspace to use instead (the caller
+    size_t fixed_ws_bytes = 0; // checked that it is large enough)
 };
 
 // Defined in gemm_f16.cu.
@@ -55,6 +57,10 @@ int group_m_override();
 // C = R(sum of `splits` fp32 (M,N) partial matrices at ws), fp16 (splitk_reduce.cu).
 int launch_splitk_reduce(const float *ws, void *C, int64_t M, int64_t N, int splits, int relu, int sm_count,
                          cudaStream_t stream);
+
+// Device address and size of the fixed K-slice scratch of gemm_f16_ex_noalloc
+// on device `dev` (splitk_reduce.cu).
+int noalloc_scratch(int dev, float **ptr, size_t *bytes);
 
 // K slices for a requested split count: `per` K blocks each, `count` of them
 // (count <= requested; every slice non-empty).  count == 1: no K split.
@@ -195,7 +201,13 @@ int launch_one(const LaunchArgs &a)
     if (slots <= 0) return GEMM_ERR_LAUNCH;
     KSplit ks = k_split_for(p.num_k_blocks, a.k_splits);
     float *ws = nullptr;
-    if (ks.count > 1) {
+    const bool own_ws = a.fixed_ws == nullptr;
+    if (ks.count > 1 && !own_ws) {
+        const size_t need = static_cast<size_t>(ks.count) * static_cast<size_t>(a.M) *
+                            static_cast<size_t>(a.N) * sizeof(float);
+        if (need > a.fixed_ws_bytes) return GEMM_ERR_INVALID_ARG;   // checked by the caller first
+        ws = a.fixed_ws;
+    } else if (ks.count > 1) {
         // Stream-ordered workspace: ordered with this call's kernels, private
         // to it, and legal inside a stream capture.  If it cannot be had, the
         // call runs without a K split.
@@ -215,7 +227,7 @@ int launch_one(const LaunchArgs &a)
         sc.grid_units = sc.units < slots ? sc.units : slots;
     }
     auto release_ws = [&]() {
-        if (ws != nullptr && cudaFreeAsync(ws, a.stream) != cudaSuccess) cudaGetLastError();
+        if (own_ws && ws != nullptr && cudaFreeAsync(ws, a.stream) != cudaSuccess) cudaGetLastError();
     };
     if (sc.units > INT32_MAX / 2) {
         release_ws();

@@ -11,6 +11,8 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+#include <cstddef>
 #include <cstdint>
 
 #include "gemm_f16.h"
@@ -60,6 +62,39 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float4 *__rest
 }  // namespace
 
 namespace gemm_sm103 {
+
+namespace {
+
+// Scratch of gemm_f16_ex_noalloc (16 MiB per device): K-slice partials live
+// here instead of in a stream-ordered allocation.  Nothing in it needs to
+// start at zero: every element the reduction reads was written by the GEMM
+// kernel of the same call.
+constexpr size_t kNoallocScratchFloats = size_t{4} << 20;
+static __device__ __align__(256) float g_noalloc_scratch[kNoallocScratchFloats];
+
+std::atomic<float *> g_noalloc_ptr[kMaxDevices];
+
+}  // namespace
+
+int noalloc_scratch(int dev, float **ptr, size_t *bytes)
+{
+    if (dev < 0 || dev >= kMaxDevices) return GEMM_ERR_CUDA;
+    float *p = g_noalloc_ptr[dev].load(std::memory_order_acquire);
+    if (p == nullptr) {
+        // Once per device, outside any stream capture (the first call may
+        // load the module's device data).
+        void *sym = nullptr;
+        if (cudaGetSymbolAddress(&sym, g_noalloc_scratch) != cudaSuccess || sym == nullptr) {
+            cudaGetLastError();
+            return GEMM_ERR_CUDA;
+        }
+        p = static_cast<float *>(sym);
+        g_noalloc_ptr[dev].store(p, std::memory_order_release);
+    }
+    *ptr = p;
+    *bytes = kNoallocScratchFloats * sizeof(float);
+    return GEMM_OK;
+}
 
 int launch_splitk_reduce(const float *ws, void *C, int64_t M, int64_t N, int splits, int relu, int sm_count,
                          cudaStream_t stream)

@@ -75,6 +75,8 @@ def lib() -> ctypes.CDLL:
     L.gemm_f16.restype = ci
     L.gemm_f16_ex.argtypes = [vp, vp, vp, i64, i64, i64, ci, ci, vp]
     L.gemm_f16_ex.restype = ci
+    L.gemm_f16_ex_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, ci, ci, vp]
+    L.gemm_f16_ex_noalloc.restype = ci
     L.gemm_f16_from_host.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, ci, vp]
     L.gemm_f16_from_host.restype = ci
     L.gemm_f16_check.argtypes = [vp]
@@ -194,6 +196,28 @@ def gemm_f16(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None, re
                            _stream_handle(stream, A.device))
     if st != GEMM_OK:
         raise GemmError(st, "gemm_f16")
+    return C
+
+
+def gemm_f16_noalloc(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, relu: bool = True, stream=None,
+                     config: int = 0) -> torch.Tensor:
+    """gemm_f16 through gemm_f16_ex_noalloc: K-slice partials in the library's
+    fixed 16 MiB scratch instead of an allocation (see gemm_f16.h for the size
+    limit and the rule that overlapping calls on one device race).  C must be
+    given: nothing is allocated."""
+    _check_operand(A, "A")
+    _check_operand(B, "B")
+    _check_operand(C, "C")
+    M, K = A.shape
+    K2, N = B.shape
+    if K != K2 or tuple(C.shape) != (M, N):
+        raise ValueError(f"shapes A {tuple(A.shape)}, B {tuple(B.shape)}, C {tuple(C.shape)} do not match")
+    L = lib()
+    with torch.cuda.device(A.device):
+        st = L.gemm_f16_ex_noalloc(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, int(bool(relu)), int(config),
+                                   _stream_handle(stream, A.device))
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_f16_ex_noalloc")
     return C
 
 

@@ -150,6 +150,30 @@ int gemm_f16_ex(const void *A, const void *B, void *C,
                 int64_t M, int64_t N, int64_t K, int relu, int config, void *stream);
 
 /*
+ * gemm_f16_ex_noalloc -- gemm_f16_ex that allocates nothing.  When the call
+ * splits K (GEMM_F16_KSPLIT(n), GEMM_F16_KSPLIT_AUTO, or a split configuration
+ * 0 chose), the fp32 slice partials go to a fixed scratch array of this
+ * library on the current device (16 MiB, a file-scope device array) instead of
+ * a stream-ordered allocation; without a K split it is gemm_f16_ex.  The pages
+ * have no counterpart: their tile GEMM has no K split and no workspace.
+ *
+ * Arguments, layouts, ownership and checks as for gemm_f16_ex.  In addition:
+ *  - slices x M x N x 4 bytes must fit the 16 MiB (e.g. 1024 x 1024 with 4
+ *    slices); a larger split is rejected (GEMM_ERR_INVALID_ARG) before any
+ *    launch, whether requested or chosen by configuration 0
+ *    (GEMM_F16_NO_KSPLIT never uses the scratch);
+ *  - the scratch's address is looked up once per device, by the first call
+ *    that splits K: make that call outside any stream capture;
+ *  - nothing in the scratch has to start at zero: every element the reduction
+ *    reads was written by the GEMM kernel of the same call;
+ *  - calls that overlap in time on one device (other streams, other threads,
+ *    graph replays running concurrently) share the one scratch and race, with
+ *    undefined results: serialise them (one stream, or events).
+ */
+int gemm_f16_ex_noalloc(const void *A, const void *B, void *C,
+                        int64_t M, int64_t N, int64_t K, int relu, int config, void *stream);
+
+/*
  * gemm_f16_tx -- C = R(op(A) @ op(B)) with transposed operand layouts (the
  * transpose_A / transpose_B options of the tile GEMM in "Writing
  * High-Performance Kernels in TileLang, from GEMM to MLA", section "Let's
