@@ -33,6 +33,8 @@ namespace {
 // Reason for the last rejected call on this thread (static strings only).
 thread_local const char *t_last_detail = "";
 
+constexpr int kMaxFromHostPanels = 8;   // row panels of gemm_f16_from_host
+
 int reject(int status, const char *why)
 {
     t_last_detail = why;
@@ -779,6 +781,56 @@ extern "C" int gemm_f16_launch_info(int64_t M, int64_t N, int64_t K, int config,
     return GEMM_OK;
 }
 
+namespace {
+
+// Per device: the two streams the host-buffer entry point moves data on
+// (uploads, downloads), created by its first call on that device.
+struct CopyStreams {
+    cudaStream_t in = nullptr, out = nullptr;
+    int status = GEMM_ERR_CUDA;
+};
+CopyStreams g_copy_streams[kMaxDevices];
+std::once_flag g_copy_once[kMaxDevices];
+
+int copy_streams(int dev, CopyStreams **out)
+{
+    if (dev < 0 || dev >= kMaxDevices) return GEMM_ERR_CUDA;
+    std::call_once(g_copy_once[dev], [dev]() {
+        CopyStreams &c = g_copy_streams[dev];
+        if (cudaStreamCreateWithFlags(&c.in, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&c.out, cudaStreamNonBlocking) == cudaSuccess) {
+            c.status = GEMM_OK;
+        } else {
+            cudaGetLastError();
+        }
+    });
+    *out = &g_copy_streams[dev];
+    return g_copy_streams[dev].status;
+}
+
+// Events of one call, destroyed once enqueued (they are released when the
+// work they mark completes).
+struct EventSet {
+    cudaEvent_t ev[2 * kMaxFromHostPanels + 2] = {};
+    int n = 0;
+    bool make(int count)
+    {
+        for (n = 0; n < count; ++n) {
+            if (cudaEventCreateWithFlags(&ev[n], cudaEventDisableTiming) != cudaSuccess) {
+                cudaGetLastError();
+                return false;
+            }
+        }
+        return true;
+    }
+    ~EventSet()
+    {
+        for (int i = 0; i < n; ++i) cudaEventDestroy(ev[i]);
+    }
+};
+
+}  // namespace
+
 extern "C" int gemm_f16_from_host(const void *A_host, const void *B_host, void *C_host, void *A_dev, void *B_dev,
                                   void *C_dev, int64_t M, int64_t N, int64_t K, int relu, void *stream)
 {
@@ -791,26 +843,79 @@ extern "C" int gemm_f16_from_host(const void *A_host, const void *B_host, void *
     const size_t a_bytes = static_cast<size_t>(M) * static_cast<size_t>(K) * 2u;
     const size_t b_bytes = static_cast<size_t>(K) * static_cast<size_t>(N) * 2u;
     const size_t c_bytes = static_cast<size_t>(M) * static_cast<size_t>(N) * 2u;
-    if (K > 0) {
-        // Validate the device side before any copy is enqueued.
-        DeviceInfo dev;
-        if ((st = current_device_info(&dev)) != GEMM_OK) return st;
-        if ((N % 8) != 0 || (K % 8) != 0)
-            return reject(GEMM_ERR_ALIGNMENT, "a row pitch (leading dimension) is not a multiple of 8 elements");
-        if ((st = check_device_buffer(A_dev, a_bytes, dev.device)) != GEMM_OK) return st;
-        if ((st = check_device_buffer(B_dev, b_bytes, dev.device)) != GEMM_OK) return st;
-        if ((st = check_device_buffer(C_dev, c_bytes, dev.device)) != GEMM_OK) return st;
-        if (cudaMemcpyAsync(A_dev, A_host, a_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-            cudaMemcpyAsync(B_dev, B_host, b_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+    if (K == 0) {
+        if ((st = gemm_f16(A_dev, B_dev, C_dev, M, N, K, relu, stream)) != GEMM_OK) return st;
+        if (cudaMemcpyAsync(C_host, C_dev, c_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) {
             cudaGetLastError();
             return GEMM_ERR_CUDA;
         }
+        return GEMM_OK;
     }
-    if ((st = gemm_f16(A_dev, B_dev, C_dev, M, N, K, relu, stream)) != GEMM_OK) return st;
-    if (cudaMemcpyAsync(C_host, C_dev, c_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) {
+    // Validate the device side before anything is enqueued.
+    DeviceInfo dev;
+    if ((st = current_device_info(&dev)) != GEMM_OK) return st;
+    if ((N % 8) != 0 || (K % 8) != 0)
+        return reject(GEMM_ERR_ALIGNMENT, "a row pitch (leading dimension) is not a multiple of 8 elements");
+    if ((st = check_device_buffer(A_dev, a_bytes, dev.device)) != GEMM_OK) return st;
+    if ((st = check_device_buffer(B_dev, b_bytes, dev.device)) != GEMM_OK) return st;
+    if ((st = check_device_buffer(C_dev, c_bytes, dev.device)) != GEMM_OK) return st;
+    if (ranges_overlap(C_dev, c_bytes, A_dev, a_bytes) || ranges_overlap(C_dev, c_bytes, B_dev, b_bytes))
+        return reject(GEMM_ERR_INVALID_ARG, "C overlaps A or B");
+    CopyStreams *cs = nullptr;
+    if ((st = copy_streams(dev.device, &cs)) != GEMM_OK) return st;
+
+    // Row panels of A and C (multiples of 256 rows, at least 1024 each, at
+    // most kMaxFromHostPanels): B goes up first, then panel i of A; the GEMM
+    // of panel i runs on `stream` once its rows are up; panel i of C comes
+    // down while later panels are uploaded and computed.
+    int64_t panels = M / 1024;
+    if (panels < 1) panels = 1;
+    if (panels > kMaxFromHostPanels) panels = kMaxFromHostPanels;
+    const int64_t rows = ((M + panels - 1) / panels + 255) / 256 * 256;
+    panels = (M + rows - 1) / rows;
+    const int np = static_cast<int>(panels);
+    EventSet evs;
+    if (!evs.make(2 * np + 2)) return GEMM_ERR_CUDA;
+    cudaEvent_t e_start = evs.ev[0], e_done = evs.ev[1];
+    auto ea = [&](int i) { return evs.ev[2 + i]; };        // panel i of A is up
+    auto ec = [&](int i) { return evs.ev[2 + np + i]; };   // panel i of C is computed
+    auto fail = []() {
         cudaGetLastError();
         return GEMM_ERR_CUDA;
+    };
+    // The copy streams start after everything already enqueued on `stream`
+    // (which may still use A_dev, B_dev or C_dev).
+    if (cudaEventRecord(e_start, s) != cudaSuccess || cudaStreamWaitEvent(cs->in, e_start, 0) != cudaSuccess ||
+        cudaStreamWaitEvent(cs->out, e_start, 0) != cudaSuccess)
+        return fail();
+    if (cudaMemcpyAsync(B_dev, B_host, b_bytes, cudaMemcpyHostToDevice, cs->in) != cudaSuccess) return fail();
+    for (int i = 0; i < np; ++i) {
+        const int64_t r0 = i * rows, mi = (M - r0 < rows) ? M - r0 : rows;
+        const size_t off = static_cast<size_t>(r0) * static_cast<size_t>(K) * 2u;
+        if (cudaMemcpyAsync(static_cast<char *>(A_dev) + off, static_cast<const char *>(A_host) + off,
+                            static_cast<size_t>(mi) * static_cast<size_t>(K) * 2u, cudaMemcpyHostToDevice,
+                            cs->in) != cudaSuccess ||
+            cudaEventRecord(ea(i), cs->in) != cudaSuccess)
+            return fail();
     }
+    for (int i = 0; i < np; ++i) {
+        const int64_t r0 = i * rows, mi = (M - r0 < rows) ? M - r0 : rows;
+        if (cudaStreamWaitEvent(s, ea(i), 0) != cudaSuccess) return fail();
+        st = gemm_f16(static_cast<const char *>(A_dev) + static_cast<size_t>(r0) * static_cast<size_t>(K) * 2u,
+                      B_dev, static_cast<char *>(C_dev) + static_cast<size_t>(r0) * static_cast<size_t>(N) * 2u, mi,
+                      N, K, relu, stream);
+        if (st != GEMM_OK) return st;
+        if (cudaEventRecord(ec(i), s) != cudaSuccess || cudaStreamWaitEvent(cs->out, ec(i), 0) != cudaSuccess)
+            return fail();
+        const size_t off = static_cast<size_t>(r0) * static_cast<size_t>(N) * 2u;
+        if (cudaMemcpyAsync(static_cast<char *>(C_host) + off, static_cast<const char *>(C_dev) + off,
+                            static_cast<size_t>(mi) * static_cast<size_t>(N) * 2u, cudaMemcpyDeviceToHost,
+                            cs->out) != cudaSuccess)
+            return fail();
+    }
+    // `stream` covers the downloads: synchronising it is enough to read C_host.
+    if (cudaEventRecord(e_done, cs->out) != cudaSuccess || cudaStreamWaitEvent(s, e_done, 0) != cudaSuccess)
+        return fail();
     return GEMM_OK;
 }
 

@@ -278,11 +278,12 @@ def gemm_f16_raw(A_ptr: int, B_ptr: int, C_ptr: int, M: int, N: int, K: int, rel
 def gemm_f16_from_host(A_host: torch.Tensor, B_host: torch.Tensor, C_host: torch.Tensor,
                        A_dev: torch.Tensor, B_dev: torch.Tensor, C_dev: torch.Tensor,
                        relu: bool = True, stream=None) -> None:
-    """End-to-end call: host A, B -> device, GEMM, device C -> host, all on ``stream``.
+    """End-to-end call: host A, B -> device, GEMM, device C -> host, ordered on ``stream``.
 
-    The host tensors should be pinned (``pin_memory()``) for asynchronous
-    copies.  Returns after enqueueing; synchronise the stream before reading
-    C_host.
+    A and C move in row panels so that copies and GEMMs overlap (see
+    gemm_f16.h); the host tensors should be pinned (``pin_memory()``) for
+    asynchronous copies.  Returns after enqueueing; synchronising the stream
+    is enough before reading C_host.
     """
     for t, n in ((A_host, "A_host"), (B_host, "B_host"), (C_host, "C_host"),
                  (A_dev, "A_dev"), (B_dev, "B_dev"), (C_dev, "C_dev")):

@@ -305,13 +305,20 @@ int gemm_f16_launch_info(int64_t M, int64_t N, int64_t K, int config, int *grid_
 /*
  * gemm_f16_from_host -- end-to-end call on host buffers.
  *
- * Enqueues on `stream`: a copy of A_host into A_dev and of B_host into B_dev,
- * gemm_f16(A_dev, B_dev, C_dev, ...), and a copy of C_dev into C_host.  All
- * six buffers belong to the caller (host ones ideally page-locked, so that
- * the copies are asynchronous; device ones sized as for gemm_f16).  Returns
- * after enqueueing; the caller synchronises `stream` before reading C_host.
- * Errors as gemm_f16, plus GEMM_ERR_INVALID_ARG for a NULL host pointer and
- * GEMM_ERR_CUDA when a copy cannot be enqueued.
+ * Computes what gemm_f16(A_dev, B_dev, C_dev, ...) computes from A_host and
+ * B_host and leaves the result in C_host: B is copied up, then A in row
+ * panels (multiples of 256 rows, at least 1024, at most 8 panels); the GEMM of
+ * each panel runs on `stream` as soon as its rows are on the device, and the
+ * panel's rows of C are copied down while later panels are uploaded and
+ * computed.  The copies run on two streams of this library per device
+ * (created by the first call on that device; make it outside any stream
+ * capture), ordered after the work already on `stream` and joined back into
+ * it: synchronising `stream` is enough before reading C_host.  All six buffers
+ * belong to the caller (host ones page-locked for asynchronous copies; device
+ * ones sized as for gemm_f16); A_dev, B_dev and C_dev are overwritten.
+ * Returns after enqueueing.  Errors as gemm_f16, plus GEMM_ERR_INVALID_ARG for
+ * a NULL host pointer and GEMM_ERR_CUDA when a copy, event or stream cannot be
+ * created or enqueued (work enqueued before that point still runs).
  */
 int gemm_f16_from_host(const void *A_host, const void *B_host, void *C_host,
                        void *A_dev, void *B_dev, void *C_dev,

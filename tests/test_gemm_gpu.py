@@ -208,6 +208,26 @@ def test_from_host_matches_oracle(g):
     assert_close(Ch.numpy(), oracle.gemm_f16(A, B, relu=True), "from_host")
 
 
+@pytest.mark.parametrize("M", [3000, 4096, 9000])
+def test_from_host_row_panels(g, M):
+    # 2, 4 and 8 row panels (the last one ragged for 3000 and 9000); the side
+    # stream alone covers uploads, GEMMs and downloads
+    N, K = 264, 520
+    A, B = draw(M, N, K, "normal_scaled", seed=M)
+    Ah, Bh = A.pin_memory(), B.pin_memory()
+    Ch = torch.full((M, N), 9.0, dtype=torch.float16).pin_memory()
+    Ad = torch.empty_like(A, device=DEV)
+    Bd = torch.empty_like(B, device=DEV)
+    Cd = torch.empty((M, N), dtype=torch.float16, device=DEV)
+    s = torch.cuda.Stream()
+    g.gemm_f16_from_host(Ah, Bh, Ch, Ad, Bd, Cd, relu=True, stream=s)
+    s.synchronize()
+    assert g.check(stream=s) == g.GEMM_OK
+    rows = sample_rows(M, seed=M)
+    assert_close(Ch.numpy()[rows], oracle.gemm_f16(A, B, relu=True, rows=rows), f"from_host M={M}")
+    assert not np.any(Ch.numpy() == np.float16(9.0))
+
+
 # ---------------------------------------------------------------- argument errors (nothing launched)
 
 def test_rejects_bad_buffers(g):
