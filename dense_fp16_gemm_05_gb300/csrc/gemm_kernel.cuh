@@ -295,6 +295,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     constexpr bool kPair = Cfg::CTA_GROUP == 2;
     // Instruction descriptor with this kernel's operand majors (bit 15: A MN-major,
     // bit 16: B MN-major).
+    // One accumulator of two 256-column N halves (the 256 x 512 pair tile): the
+    // epilogue hands the halves back separately, so the next unit's MMAs start
+    // on half 0 while half 1 is still being read.
+    constexpr bool kHalfRelease = Cfg::ACC_STAGES == 1 && Cfg::N_MMAS == 2;
     constexpr uint32_t kIdesc = (Cfg::IDESC & ~((1u << 15) | (1u << 16))) | (kTA ? (1u << 15) : 0u) |
                                 (kTB ? 0u : (1u << 16));
 
@@ -514,41 +518,90 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 // The MMA's N field (bits 17-22, N >> 3) for this unit's width.
                 const uint32_t idesc =
                     (kIdesc & ~(0x3Fu << 17)) | (static_cast<uint32_t>(umma_n >> 3) << 17);
-                if (!wait_phase(tempty_bar(b), acc_ph ^ 1u, abort, limit, kSiteMmaTmemEmpty)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + b * Cfg::ACC_COLS;
-                for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!wait_phase(full_bar(s), ph, abort, limit, kSiteMmaFull)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after_sync();
+                // The MMAs of K block kb (ring slot st), N halves [h_lo, h_hi).
+                auto issue = [&](int kb, int st, int h_lo, int h_hi) {
                     // Descriptors of this stage: the start-address field (bits 0-13)
                     // holds address >> 4, so advancing an operand by n bytes adds
                     // n >> 4 (no carry out of the field: shared addresses < 2^18).
-                    const uint64_t a_st = a_desc0 + static_cast<uint64_t>((s * Cfg::A_STAGE_BYTES) >> 4);
-                    const uint64_t b_st = b_desc0 + static_cast<uint64_t>((s * Cfg::B_STAGE_BYTES) >> 4);
+                    const uint64_t a_st = a_desc0 + static_cast<uint64_t>((st * Cfg::A_STAGE_BYTES) >> 4);
+                    const uint64_t b_st = b_desc0 + static_cast<uint64_t>((st * Cfg::B_STAGE_BYTES) >> 4);
                     const uint32_t acc0 = kb != kb0 ? 1u : 0u;
 #pragma unroll
                     for (int ks = 0; ks < Cfg::BK / Cfg::UMMA_K; ++ks) {
                         const uint64_t a_desc = a_st + static_cast<uint64_t>((ks * kAStep) >> 4);
 #pragma unroll
                         for (int h = 0; h < Cfg::N_MMAS; ++h) {
-                            if (h >= n_mmas) break;
+                            if (h < h_lo) continue;
+                            if (h >= h_hi || h >= n_mmas) break;
                             // MMA h starts at its own B boxes.
                             const uint64_t b_desc = b_st + static_cast<uint64_t>((h * bpm_bytes + ks * kBStep) >> 4);
                             mma_f16_ss<Cfg::CTA_GROUP>(d_tmem + h * umma_n, a_desc, b_desc, idesc,
                                                        ks != 0 ? 1u : acc0);
                         }
                     }
-                    // Frees the slot once these MMAs have read it: in both CTAs of the
-                    // pair, and in every CTA of the cluster when B boxes are shared
-                    // (another pair's multicast writes this pair's slots too).
-                    if constexpr (kPair) mma_commit_pair_mc(empty_bar(s), Cfg::PAIRS > 1 ? all_mask : pair_mask);
-                    else mma_commit(empty_bar(s));
+                };
+                // Frees slot st once the MMAs issued so far have read it: in both CTAs
+                // of the pair, and in every CTA of the cluster when B boxes are shared
+                // (another pair's multicast writes this pair's slots too).
+                auto release = [&](int st) {
+                    if constexpr (kPair) mma_commit_pair_mc(empty_bar(st), Cfg::PAIRS > 1 ? all_mask : pair_mask);
+                    else mma_commit(empty_bar(st));
+                };
+                int kb = kb0;
+                if (kHalfRelease && n_mmas == 2) {
+                    // One accumulator of two N halves: the epilogue of the previous
+                    // unit hands each half back as soon as it has read it.  Start
+                    // on half 0 with the K blocks already in the ring, then run
+                    // half 1 over the same slots once it is free.
+                    if (!wait_phase(tempty_bar(0), acc_ph ^ 1u, abort, limit, kSiteMmaTmemEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const int npre = min(Cfg::STAGES, kb1 - kb0);
+                    int pre_slot[Cfg::STAGES];
+                    for (int i = 0; i < npre; ++i) {
+                        if (!wait_phase(full_bar(s), ph, abort, limit, kSiteMmaFull)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after_sync();
+                        pre_slot[i] = s;
+                        issue(kb0 + i, s, 0, 1);
+                        issued_any = true;
+                        if (++s == Cfg::STAGES) {
+                            s = 0;
+                            ph ^= 1u;
+                        }
+                    }
+                    if (!ok) break;
+                    if (!wait_phase(tempty_bar(1), acc_ph ^ 1u, abort, limit, kSiteMmaTmemEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    for (int i = 0; i < npre; ++i) {
+                        issue(kb0 + i, pre_slot[i], 1, 2);
+                        release(pre_slot[i]);
+                    }
+                    kb = kb0 + npre;
+                } else {
+                    if (!wait_phase(tempty_bar(b), acc_ph ^ 1u, abort, limit, kSiteMmaTmemEmpty) ||
+                        (kHalfRelease && !wait_phase(tempty_bar(1), acc_ph ^ 1u, abort, limit, kSiteMmaTmemEmpty))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                }
+                for (; kb < kb1; ++kb) {
+                    if (!wait_phase(full_bar(s), ph, abort, limit, kSiteMmaFull)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    issue(kb, s, 0, Cfg::N_MMAS);
+                    release(s);
                     issued_any = true;
                     if (++s == Cfg::STAGES) {
                         s = 0;
@@ -604,7 +657,22 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 tmem_load_32x32b_x64(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * Cfg::ACC_COLS +
                                          c * Cfg::EPI_COLS,
                                      r);
-                if (c == chunks - 1) {
+                if constexpr (kHalfRelease) {
+                    // One accumulator in two N halves of 256 columns (chunks 0-3
+                    // and 4-7): hand each back once this warp has read it (both at
+                    // the last chunk of a narrower unit).
+                    const int half0_last = chunks < 4 ? chunks - 1 : 3;
+                    if (c == half0_last || c == chunks - 1) {
+                        tc_fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0) {
+                            for (int h = (c == half0_last ? 0 : 1); h <= (c == chunks - 1 ? 1 : 0); ++h) {
+                                if (kPair && !leader) mbar_arrive_cluster(tempty_leader0 + 8u * h);
+                                else mbar_arrive(tempty_bar(h));
+                            }
+                        }
+                    }
+                } else if (c == chunks - 1) {
                     // All TMEM reads of accumulator b by this warp are done.
                     tc_fence_before_sync();
                     __syncwarp();
