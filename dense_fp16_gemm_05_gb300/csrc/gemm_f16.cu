@@ -363,6 +363,24 @@ double ksplit_wave_eff(int id, int64_t M, int64_t N, int64_t K, const DeviceInfo
     return static_cast<double>(units) / static_cast<double>(waves * slots);
 }
 
+// Wave efficiency of configuration `id` with GEMM_F16_KSPLIT_TAIL: full waves
+// of whole tiles, then the last wave's tiles in K slices (time in tile units:
+// full waves + ceil(slices of the tail / slots) / slices).
+double tail_wave_eff(int id, int64_t M, int64_t N, int64_t K, const DeviceInfo &dev)
+{
+    int grid = 0, cluster = 1, tiles = 0;
+    if (config_info(id, M, N, false, dev, &grid, &cluster, &tiles) != GEMM_OK) return 0.0;
+    const int64_t slots = config_slots(id, dev);
+    if (slots <= 0 || tiles <= 0) return 0.0;
+    const KPlan kp = plan_k_split(tiles, slots, (K + 63) / 64, 1, true);
+    if (kp.ks.count < 2) return wave_eff(id, M, N, false, dev);
+    const int64_t full_waves = kp.ks_start / slots;
+    const int64_t tail_units = (tiles - kp.ks_start) * kp.ks.count;
+    const double time = static_cast<double>(full_waves) +
+                        static_cast<double>((tail_units + slots - 1) / slots) / static_cast<double>(kp.ks.count);
+    return static_cast<double>(tiles) / (static_cast<double>(slots) * time);
+}
+
 // The automatic choice.  The offline sweep (tune.py) measured every candidate
 // (configuration x tail policy) on a grid of shapes.  For a problem, take the
 // nearest measured shape in log2 space (K weighted by half: it changes the
@@ -404,8 +422,13 @@ int select_config(int64_t M, int64_t N, int64_t K, bool any_layout, const Device
         if (id < 1 || id > kNumConfigs || (any_layout && !kConfigs[id].all_layouts)) continue;
         const bool split = (c & GEMM_F16_NO_SPLIT) == 0;
         const bool krule = (c & GEMM_F16_KSPLIT_AUTO) != 0;
-        const double here = krule ? ksplit_wave_eff(id, M, N, K, dev) : wave_eff(id, M, N, split, dev);
-        const double there = krule ? ksplit_wave_eff(id, t.M, t.N, t.K, dev) : wave_eff(id, t.M, t.N, split, dev);
+        const bool ktail = (c & GEMM_F16_KSPLIT_TAIL) != 0;
+        const double here = krule   ? ksplit_wave_eff(id, M, N, K, dev)
+                            : ktail ? tail_wave_eff(id, M, N, K, dev)
+                                    : wave_eff(id, M, N, split, dev);
+        const double there = krule   ? ksplit_wave_eff(id, t.M, t.N, t.K, dev)
+                             : ktail ? tail_wave_eff(id, t.M, t.N, t.K, dev)
+                                     : wave_eff(id, t.M, t.N, split, dev);
         if (here <= 0.0 || there <= 0.0) continue;
         // (ratio first: exactly 1 on a measured shape, so ties keep table order)
         const double predicted = static_cast<double>(t.tflops[i]) * (here / there);
@@ -427,6 +450,7 @@ int select_config(int64_t M, int64_t N, int64_t K, bool any_layout, const Device
 constexpr int kKsplitNone = 0;     // no K-split bit set
 constexpr int kKsplitNever = -1;   // GEMM_F16_NO_KSPLIT
 constexpr int kKsplitRule = -2;    // GEMM_F16_KSPLIT_AUTO
+constexpr int kKsplitTail = -3;    // GEMM_F16_KSPLIT_TAIL
                                    // n >= 2: GEMM_F16_KSPLIT(n)
 
 // Splits a config argument into the configuration id and its flag bits;
@@ -434,16 +458,18 @@ constexpr int kKsplitRule = -2;    // GEMM_F16_KSPLIT_AUTO
 bool parse_config(int config, int *id, bool *allow_split, int *k_request = nullptr)
 {
     constexpr int kKnown = GEMM_F16_CONFIG_ID_MASK | GEMM_F16_NO_SPLIT | GEMM_F16_NO_KSPLIT | GEMM_F16_KSPLIT_AUTO |
-                           GEMM_F16_KSPLIT_MASK;
+                           GEMM_F16_KSPLIT_TAIL | GEMM_F16_KSPLIT_MASK;
     if (config < 0 || (config & ~kKnown) != 0) return false;
     const int n = (config & GEMM_F16_KSPLIT_MASK) >> GEMM_F16_KSPLIT_SHIFT;
     const bool never = (config & GEMM_F16_NO_KSPLIT) != 0;
     const bool rule = (config & GEMM_F16_KSPLIT_AUTO) != 0;
-    if (n == 1 || n > 16 || static_cast<int>(never) + static_cast<int>(rule) + static_cast<int>(n != 0) > 1)
+    const bool tail = (config & GEMM_F16_KSPLIT_TAIL) != 0;
+    if (n == 1 || n > 16 ||
+        static_cast<int>(never) + static_cast<int>(rule) + static_cast<int>(tail) + static_cast<int>(n != 0) > 1)
         return false;
     *id = config & GEMM_F16_CONFIG_ID_MASK;
     *allow_split = (config & GEMM_F16_NO_SPLIT) == 0;
-    if (k_request) *k_request = never ? kKsplitNever : rule ? kKsplitRule : n;
+    if (k_request) *k_request = never ? kKsplitNever : rule ? kKsplitRule : tail ? kKsplitTail : n;
     return *id <= kNumConfigs;
 }
 
@@ -525,17 +551,24 @@ int run_gemm(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_
         a.allow_split = allow_split;
     }
     a.k_splits = k_splits_for(k_request, id, picked, cfg, M, N, K, dev);
-    if (hook.producer_off) a.k_splits = 1;   // the timeout self-test never writes C
+    a.k_split_tail = k_request == kKsplitTail ||
+                     (k_request == kKsplitNone && id == 0 && (picked & GEMM_F16_KSPLIT_TAIL) != 0);
+    if (hook.producer_off) {
+        // the timeout self-test never writes C
+        a.k_splits = 1;
+        a.k_split_tail = false;
+    }
     if (noalloc) {
         // K-slice partials go to the library's fixed scratch: reject what does
         // not fit before anything is launched.
-        const KSplit kk = k_split_for((K + 63) / 64, a.k_splits);
-        if (kk.count > 1) {
+        const int64_t tm = kConfigs[cfg].tile_m, tn = kConfigs[cfg].tile_n;
+        const int64_t tiles = ((M + tm - 1) / tm) * ((N + tn - 1) / tn);
+        const KPlan kp = plan_k_split(tiles, config_slots(cfg, dev), (K + 63) / 64, a.k_splits, a.k_split_tail);
+        if (kp.ks.count > 1) {
             float *scratch = nullptr;
             size_t scratch_bytes = 0;
             if ((st = noalloc_scratch(dev.device, &scratch, &scratch_bytes)) != GEMM_OK) return st;
-            const uint64_t need = static_cast<uint64_t>(kk.count) * static_cast<uint64_t>(M) *
-                                  static_cast<uint64_t>(N) * sizeof(float);
+            const uint64_t need = static_cast<uint64_t>(kp.ws_floats(tiles, tm, tn)) * sizeof(float);
             if (need > scratch_bytes)
                 return reject(GEMM_ERR_INVALID_ARG, "the K-slice partials exceed the 16 MiB scratch of "
                                                     "gemm_f16_ex_noalloc");
@@ -766,13 +799,17 @@ extern "C" int gemm_f16_launch_info(int64_t M, int64_t N, int64_t K, int config,
         cfg = picked & GEMM_F16_CONFIG_ID_MASK;
         split = split && (picked & GEMM_F16_NO_SPLIT) == 0;
     }
-    const KSplit kk = k_split_for((K + 63) / 64, k_splits_for(k_request, id, picked, cfg, M, N, K, dev));
+    const int k_req = k_splits_for(k_request, id, picked, cfg, M, N, K, dev);
+    const bool tail = k_request == kKsplitTail ||
+                      (k_request == kKsplitNone && id == 0 && (picked & GEMM_F16_KSPLIT_TAIL) != 0);
     int grid = 0, cluster = 1, n_tiles = 0;
-    if ((st = config_info(cfg, M, N, split && kk.count == 1, dev, &grid, &cluster, &n_tiles)) != GEMM_OK) return st;
-    if (kk.count > 1) {
-        // Whole tiles, each in kk.count K slices, on at most one CTA (cluster) per slot.
-        const int64_t slots = config_slots(cfg, dev);
-        const int64_t units = static_cast<int64_t>(n_tiles) * kk.count;
+    if ((st = config_info(cfg, M, N, split && k_req <= 1 && !tail, dev, &grid, &cluster, &n_tiles)) != GEMM_OK)
+        return st;
+    const int64_t slots = config_slots(cfg, dev);
+    const KPlan kp = plan_k_split(n_tiles, slots, (K + 63) / 64, k_req, tail);
+    if (kp.ks.count > 1) {
+        // Whole tiles, then K slices, on at most one CTA (cluster) per slot.
+        const int64_t units = kp.units(n_tiles);
         grid = static_cast<int>((units < slots ? units : slots) * cluster);
     }
     if (grid_ctas) *grid_ctas = grid;

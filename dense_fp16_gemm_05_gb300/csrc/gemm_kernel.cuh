@@ -64,11 +64,14 @@ struct GemmParams {
     int32_t num_units;      // split_start + (num_tiles - split_start) << split_log2
     int32_t split_start;    // first split tile (== num_tiles: no split)
     int32_t split_log2;     // each tile from split_start on is 2^split_log2 units
-    int32_t k_splits;       // > 1: unit u is slice u % k_splits of tile u / k_splits (K blocks
-                            // [slice * k_per_split, +k_per_split) clipped at num_k_blocks); the
-                            // epilogue then writes the fp32 partial to ws instead of C
+    int32_t k_splits;       // > 1: tiles from ks_start on are cut into k_splits K slices: unit
+                            // ks_start + (t - ks_start) * k_splits + s is slice s of tile t (K blocks
+                            // [s * k_per_split, +k_per_split) clipped at num_k_blocks), and its
+                            // epilogue writes the fp32 partial to ws instead of C
     int32_t k_per_split;    // K blocks per slice
-    float *ws;              // k_splits fp32 (M,N) row-major partial matrices, slice-major
+    int32_t ks_start;       // first tile cut into slices (0: every tile; num_tiles: none)
+    float *ws;              // per split tile and slice, a SUPER_M x BN fp32 row-major partial:
+                            // ws[((t - ks_start) * k_splits + s) * SUPER_M * BN + r * BN + c]
     uint64_t timeout_cycles;
     __half *C;              // output base (used by the direct-store epilogue)
     int32_t producer_off;   // test hook: 1 = the producer issues nothing, so the
@@ -220,26 +223,33 @@ __device__ __forceinline__ void tile_coords(int t, const GemmParams &p, int &mb,
     nb = r / rows;
 }
 
-// K blocks [kb0, kb1) of work unit u, and its K slice (0 without K split).
+// K blocks [kb0, kb1) of work unit u, and its K slice (-1: a whole tile, no
+// K split).
 __device__ __forceinline__ void unit_k_range(int u, const GemmParams &p, int &kb0, int &kb1, int &slice)
 {
-    slice = 0;
+    slice = -1;
     kb0 = 0;
     kb1 = p.num_k_blocks;
-    if (p.k_splits > 1) {
-        slice = u % p.k_splits;
+    if (p.k_splits > 1 && u >= p.ks_start) {
+        slice = (u - p.ks_start) % p.k_splits;
         kb0 = slice * p.k_per_split;
         kb1 = min(p.num_k_blocks, kb0 + p.k_per_split);
     }
 }
 
+// Tile of work unit u under a K split (units of one split tile are adjacent).
+__device__ __forceinline__ int unit_tile_k(int u, const GemmParams &p)
+{
+    return (p.k_splits > 1 && u >= p.ks_start) ? p.ks_start + (u - p.ks_start) / p.k_splits : u;
+}
+
 // Work unit u -> tile row block mb, first output column col0 of the unit, and
-// the split shift (the unit is BN >> shift columns wide).  With a K split the
-// unit's tile is u / k_splits (no N split then: split_start = num_tiles).
+// the split shift (the unit is BN >> shift columns wide).  With a K split
+// there is no N split (split_start = num_tiles).
 template <int kBN>
 __device__ __forceinline__ void unit_coords(int u, const GemmParams &p, int &mb, int &col0, int &shift)
 {
-    if (p.k_splits > 1) u /= p.k_splits;
+    if (p.k_splits > 1) u = unit_tile_k(u, p);
     int t = u, sub = 0;
     shift = 0;
     if (u >= p.split_start) {
@@ -682,13 +692,19 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     }
                 }
                 const int col0 = col0_unit + c * Cfg::EPI_COLS;
-                if (p.k_splits > 1) {
+                if (slice >= 0) {
                     // K slice: this row's 64 fp32 partial sums, as they are, into the
-                    // slice's workspace matrix (16-byte pieces; N is a multiple of 8,
-                    // so every piece is wholly in or out).
+                    // slice's tile in the workspace (16-byte pieces; N is a multiple
+                    // of 8, so every piece is wholly in or out; rows and columns
+                    // outside C are not written, nor read by the reduction).
                     const int row = row0 + lane;
                     if (row < p.M) {
-                        float *wrow = p.ws + (static_cast<int64_t>(slice) * p.M + row) * p.N + col0;
+                        const int t = unit_tile_k(u, p);
+                        const int64_t tile_base =
+                            (static_cast<int64_t>(t - p.ks_start) * p.k_splits + slice) *
+                            static_cast<int64_t>(Cfg::SUPER_M * Cfg::BN);
+                        float *wrow = p.ws + tile_base + static_cast<int64_t>(row - mb * Cfg::SUPER_M) * Cfg::BN +
+                                      (col0 - (col0_unit - (col0_unit % Cfg::BN)));
 #pragma unroll
                         for (int j = 0; j < Cfg::EPI_COLS / 4; ++j) {
                             if (col0 + 4 * j < p.N)

@@ -45,6 +45,7 @@ struct LaunchArgs {
     bool allow_split = true;   // false: every work unit is a whole tile (no tail split)
     int k_splits = 1;          // > 1: split every tile's K loop into (up to) this many slices,
                                // fp32 partials in a stream-ordered workspace, then a reduction
+    bool k_split_tail = false; // split only the tiles of a partly filled last wave in K
     float *fixed_ws = nullptr; // non-null: the K-slice workspace to use instead (the caller
     size_t fixed_ws_bytes = 0; // checked that it is large enough)
 };
@@ -54,9 +55,10 @@ int encode_matrix(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t col
                   uint32_t box_rows);
 int group_m_override();
 
-// C = R(sum of `splits` fp32 (M,N) partial matrices at ws), fp16 (splitk_reduce.cu).
-int launch_splitk_reduce(const float *ws, void *C, int64_t M, int64_t N, int splits, int relu, int sm_count,
-                         cudaStream_t stream);
+// For every tile from p.ks_start on: C = R(sum of its p.k_splits fp32 partial
+// tiles in ws), fp16 (splitk_reduce.cu).
+int launch_splitk_reduce(const float *ws, void *C, const GemmParams &p, int super_m, int bn, int relu,
+                         int sm_count, cudaStream_t stream);
 
 // Device address and size of the fixed K-slice scratch of gemm_f16_ex_noalloc
 // on device `dev` (splitk_reduce.cu).
@@ -68,6 +70,50 @@ struct KSplit {
     int count = 1;
     int per = 0;
 };
+
+inline KSplit k_split_for(int64_t k_blocks, int requested);
+
+// Which tiles a launch cuts into K slices, and into how many: with a requested
+// count (k_req >= 2) every tile; with `tail` only the tiles of a partly filled
+// last wave (as many slices as fill the slots once, at most 8, at least 8 K
+// blocks each); otherwise none (ks_start = tiles).
+struct KPlan {
+    KSplit ks;
+    int64_t ks_start = 0;
+    int64_t units(int64_t tiles) const { return ks_start + (tiles - ks_start) * ks.count; }
+    int64_t ws_floats(int64_t tiles, int64_t tile_m, int64_t tile_n) const
+    {
+        return ks.count > 1 ? (tiles - ks_start) * ks.count * tile_m * tile_n : 0;
+    }
+};
+
+inline KPlan plan_k_split(int64_t tiles, int64_t slots, int64_t k_blocks, int k_req, bool tail)
+{
+    KPlan kp;
+    kp.ks.count = 1;
+    kp.ks.per = static_cast<int>(k_blocks);
+    kp.ks_start = tiles;
+    if (k_req > 1) {
+        const KSplit ks = k_split_for(k_blocks, k_req);
+        if (ks.count > 1) {
+            kp.ks = ks;
+            kp.ks_start = 0;
+        }
+    } else if (tail && slots > 0) {
+        const int64_t full = (tiles / slots) * slots, rest = tiles - full;
+        int64_t n = rest > 0 ? slots / rest : 0;
+        if (n > 8) n = 8;
+        if (n > k_blocks / 8) n = k_blocks / 8;
+        if (n >= 2) {
+            const KSplit ks = k_split_for(k_blocks, static_cast<int>(n));
+            if (ks.count > 1) {
+                kp.ks = ks;
+                kp.ks_start = full;
+            }
+        }
+    }
+    return kp;
+}
 
 inline KSplit k_split_for(int64_t k_blocks, int requested)
 {
@@ -199,29 +245,28 @@ int launch_one(const LaunchArgs &a)
     using Prep = Prepared<Cfg, kRelu, kTA, kTB>;
     const int64_t slots = Prep::get(a.dev.device, a.dev.sm_count);
     if (slots <= 0) return GEMM_ERR_LAUNCH;
-    KSplit ks = k_split_for(p.num_k_blocks, a.k_splits);
+    Schedule sc = make_schedule<Cfg>(a.M, a.N, slots, a.allow_split && a.k_splits <= 1 && !a.k_split_tail);
+    KPlan kp = plan_k_split(sc.tiles, slots, p.num_k_blocks, a.k_splits, a.k_split_tail);
     float *ws = nullptr;
     const bool own_ws = a.fixed_ws == nullptr;
-    if (ks.count > 1 && !own_ws) {
-        const size_t need = static_cast<size_t>(ks.count) * static_cast<size_t>(a.M) *
-                            static_cast<size_t>(a.N) * sizeof(float);
-        if (need > a.fixed_ws_bytes) return GEMM_ERR_INVALID_ARG;   // checked by the caller first
-        ws = a.fixed_ws;
-    } else if (ks.count > 1) {
-        // Stream-ordered workspace: ordered with this call's kernels, private
-        // to it, and legal inside a stream capture.  If it cannot be had, the
-        // call runs without a K split.
-        const size_t ws_bytes = static_cast<size_t>(ks.count) * static_cast<size_t>(a.M) *
-                                static_cast<size_t>(a.N) * sizeof(float);
-        if (cudaMallocAsync(reinterpret_cast<void **>(&ws), ws_bytes, a.stream) != cudaSuccess) {
+    if (kp.ks.count > 1) {
+        const size_t need = static_cast<size_t>(kp.ws_floats(sc.tiles, Cfg::SUPER_M, Cfg::BN)) * sizeof(float);
+        if (!own_ws) {
+            if (need > a.fixed_ws_bytes) return GEMM_ERR_INVALID_ARG;   // checked by the caller first
+            ws = a.fixed_ws;
+        } else if (cudaMallocAsync(reinterpret_cast<void **>(&ws), need, a.stream) != cudaSuccess) {
+            // Stream-ordered workspace: ordered with this call's kernels, private
+            // to it, and legal inside a stream capture.  If it cannot be had, the
+            // call runs without a K split.
             cudaGetLastError();
             ws = nullptr;
-            ks = KSplit{1, p.num_k_blocks};
+            kp = plan_k_split(sc.tiles, slots, p.num_k_blocks, 1, false);
+            sc = make_schedule<Cfg>(a.M, a.N, slots, a.allow_split);
         }
     }
-    Schedule sc = make_schedule<Cfg>(a.M, a.N, slots, a.allow_split && ks.count == 1);
-    if (ks.count > 1) {
-        sc.units = sc.tiles * ks.count;   // whole tiles, each in ks.count K slices
+    if (kp.ks.count > 1) {
+        // Whole tiles before ks_start, then each later tile as ks.count K slices.
+        sc.units = kp.units(sc.tiles);
         sc.split_start = sc.tiles;
         sc.shift = 0;
         sc.grid_units = sc.units < slots ? sc.units : slots;
@@ -237,8 +282,9 @@ int launch_one(const LaunchArgs &a)
     p.num_units = static_cast<int32_t>(sc.units);
     p.split_start = static_cast<int32_t>(sc.split_start);
     p.split_log2 = sc.shift;
-    p.k_splits = ks.count;
-    p.k_per_split = ks.per;
+    p.k_splits = kp.ks.count;
+    p.k_per_split = kp.ks.per;
+    p.ks_start = static_cast<int32_t>(kp.ks_start);
     p.ws = ws;
     // Rasterisation panels 2048 rows high whatever the tile height.
     p.group_m = group_m_override() ? group_m_override() : (Cfg::SUPER_M >= 2048 ? 1 : 2048 / Cfg::SUPER_M);
@@ -270,8 +316,8 @@ int launch_one(const LaunchArgs &a)
             return GEMM_ERR_LAUNCH;
         }
     }
-    if (ks.count > 1) {
-        const int st2 = launch_splitk_reduce(ws, a.C, a.M, a.N, ks.count, a.relu, a.dev.sm_count, a.stream);
+    if (kp.ks.count > 1) {
+        const int st2 = launch_splitk_reduce(ws, a.C, p, Cfg::SUPER_M, Cfg::BN, a.relu, a.dev.sm_count, a.stream);
         release_ws();
         if (st2 != GEMM_OK) return st2;
     }

@@ -1,13 +1,16 @@
-// splitk_reduce.cu -- second step of a K-split GEMM: C = R(sum_s P_s) where P_s
-// (s = 0 .. splits-1) are the fp32 partial products of K slice s that the GEMM
-// kernel wrote to its workspace, R the optional ReLU (x > 0 ? x : +0), and the
-// result is rounded once to fp16 (round to nearest even), as the one-pass
-// epilogue does.  The slices are added in ascending order, so the result does
-// not depend on which CTA finished first.
+// splitk_reduce.cu -- second step of a K-split GEMM: for every tile the GEMM
+// kernel cut into K slices, C = R(sum_s P_s) over that tile, where P_s
+// (s = 0 .. splits-1) are the fp32 partial products the slices wrote to the
+// workspace (one SUPER_M x BN block per split tile and slice), R the optional
+// ReLU (x > 0 ? x : +0), and the result is rounded once to fp16 (round to
+// nearest even), as the one-pass epilogue does.  The slices are added in
+// ascending order, so the result does not depend on which CTA finished first.
+// Tiles are located with the GEMM's own rasterisation (tile_coords).
 //
 // HBM/L2-bound: per output element 4 bytes per slice read, 2 bytes written.
 // 16-byte accesses (8 outputs per thread and iteration: two float4 per slice,
-// one uint4 of fp16); M * N is a multiple of 8 (N is), so there is no tail.
+// one uint4 of fp16); N is a multiple of 8, so a group of 8 columns is wholly
+// inside or outside C.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -28,15 +31,29 @@ __device__ __forceinline__ float reduce_out(float x)
 }
 
 template <bool kRelu>
-__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float4 *__restrict__ ws, uint4 *__restrict__ C,
-                                                            int64_t n_vec, int64_t slice_vec4, int splits)
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float *__restrict__ ws, __half *__restrict__ C,
+                                                            const gemm_sm103::GemmParams p, int super_m, int bn,
+                                                            int64_t n_vec)
 {
+    const int64_t per_row = bn / 8;
+    const int64_t per_tile = static_cast<int64_t>(super_m) * per_row;
+    const int64_t tile_elems = static_cast<int64_t>(super_m) * bn;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n_vec; i += stride) {
-        float4 lo = ws[2 * i], hi = ws[2 * i + 1];
-        for (int s = 1; s < splits; ++s) {
-            const float4 a = ws[s * slice_vec4 + 2 * i];
-            const float4 b = ws[s * slice_vec4 + 2 * i + 1];
+        const int64_t tr = i / per_tile;             // split tile, relative to ks_start
+        const int64_t e = i - tr * per_tile;
+        const int r = static_cast<int>(e / per_row);
+        const int c = static_cast<int>(e - static_cast<int64_t>(r) * per_row) * 8;
+        int mb, nb;
+        gemm_sm103::tile_coords(p.ks_start + static_cast<int>(tr), p, mb, nb);
+        const int64_t row = static_cast<int64_t>(mb) * super_m + r;
+        const int64_t col = static_cast<int64_t>(nb) * bn + c;
+        if (row >= p.M || col >= p.N) continue;
+        const float *w = ws + tr * p.k_splits * tile_elems + static_cast<int64_t>(r) * bn + c;
+        float4 lo = *reinterpret_cast<const float4 *>(w), hi = *reinterpret_cast<const float4 *>(w + 4);
+        for (int sl = 1; sl < p.k_splits; ++sl) {
+            const float4 a = *reinterpret_cast<const float4 *>(w + sl * tile_elems);
+            const float4 b = *reinterpret_cast<const float4 *>(w + sl * tile_elems + 4);
             lo.x += a.x;
             lo.y += a.y;
             lo.z += a.z;
@@ -55,7 +72,7 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float4 *__rest
         o.y = *reinterpret_cast<const uint32_t *>(&h1);
         o.z = *reinterpret_cast<const uint32_t *>(&h2);
         o.w = *reinterpret_cast<const uint32_t *>(&h3);
-        C[i] = o;
+        *reinterpret_cast<uint4 *>(C + row * p.N + col) = o;
     }
 }
 
@@ -96,19 +113,18 @@ int noalloc_scratch(int dev, float **ptr, size_t *bytes)
     return GEMM_OK;
 }
 
-int launch_splitk_reduce(const float *ws, void *C, int64_t M, int64_t N, int splits, int relu, int sm_count,
-                         cudaStream_t stream)
+int launch_splitk_reduce(const float *ws, void *C, const GemmParams &p, int super_m, int bn, int relu,
+                         int sm_count, cudaStream_t stream)
 {
-    const int64_t elems = M * N;              // a multiple of 8
-    const int64_t n_vec = elems / 8;
-    if (n_vec == 0) return GEMM_OK;
+    const int64_t split_tiles = static_cast<int64_t>(p.num_tiles) - p.ks_start;
+    const int64_t n_vec = split_tiles * super_m * (bn / 8);
+    if (n_vec <= 0) return GEMM_OK;
     const int64_t want = (n_vec + 255) / 256;
     const int64_t cap = static_cast<int64_t>(sm_count > 0 ? sm_count : 1) * 8;
     const unsigned blocks = static_cast<unsigned>(want < cap ? want : cap);
-    const float4 *w = reinterpret_cast<const float4 *>(ws);
-    uint4 *c = static_cast<uint4 *>(C);
-    if (relu) splitk_reduce_kernel<true><<<blocks, 256, 0, stream>>>(w, c, n_vec, elems / 4, splits);
-    else splitk_reduce_kernel<false><<<blocks, 256, 0, stream>>>(w, c, n_vec, elems / 4, splits);
+    __half *c = static_cast<__half *>(C);
+    if (relu) splitk_reduce_kernel<true><<<blocks, 256, 0, stream>>>(ws, c, p, super_m, bn, n_vec);
+    else splitk_reduce_kernel<false><<<blocks, 256, 0, stream>>>(ws, c, p, super_m, bn, n_vec);
     if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_LAUNCH;
     return GEMM_OK;
 }

@@ -30,6 +30,7 @@ GEMM_F16_CONFIG_ID_MASK = 0xFF
 GEMM_F16_NO_SPLIT = 0x100
 GEMM_F16_NO_KSPLIT = 0x200
 GEMM_F16_KSPLIT_AUTO = 0x400
+GEMM_F16_KSPLIT_TAIL = 0x800
 GEMM_F16_KSPLIT_SHIFT = 12
 GEMM_F16_KSPLIT_MASK = 0x1F000
 
@@ -152,7 +153,8 @@ def config_label(config: int) -> str | None:
     c = int(config)
     n = (c & GEMM_F16_KSPLIT_MASK) >> GEMM_F16_KSPLIT_SHIFT
     return (name + ("+nosplit" if c & GEMM_F16_NO_SPLIT else "") + (f"+ksplit{n}" if n else "")
-            + ("+ksplitauto" if c & GEMM_F16_KSPLIT_AUTO else "") + ("+noksplit" if c & GEMM_F16_NO_KSPLIT else ""))
+            + ("+ksplitauto" if c & GEMM_F16_KSPLIT_AUTO else "") + ("+ksplittail" if c & GEMM_F16_KSPLIT_TAIL else "")
+            + ("+noksplit" if c & GEMM_F16_NO_KSPLIT else ""))
 
 
 def _stream_handle(stream, device) -> int:

@@ -101,18 +101,19 @@ int gemm_f16(const void *A, const void *B, void *C,
 #define GEMM_F16_NO_SPLIT 0x100
 
 /*
- * K split (bits 9, 10 and 12-16 of a config word).  When a problem has fewer
- * output tiles than the GPU has SMs (or SM pairs) for them, the K loop of every
- * tile can be cut into slices that run on different SMs: each slice writes its
- * fp32 partial product to a workspace taken from the stream-ordered allocator
- * (cudaMallocAsync / cudaFreeAsync on `stream`: private to the call, ordered
- * with its kernels, legal inside a stream capture), and a second kernel adds
- * the slices in ascending order, applies the ReLU and rounds once to fp16.
- * Each output is then the fp32 sum of per-slice fp32 sums, a different order
- * of the same terms than without a split (results may differ in the last
- * bits; ReLU is still exactly max(plain, +0)).  The workspace holds
- * slices x M x N floats.  With a K split every work unit is a whole tile
- * (GEMM_F16_NO_SPLIT is implied).
+ * K split (bits 9-11 and 12-16 of a config word).  The K loop of a tile can
+ * be cut into slices that run on different SMs: when a problem has fewer
+ * output tiles than the GPU has SMs (or SM pairs) for them, or for the tiles
+ * of a partly filled last wave.  Each slice writes its fp32 partial product to
+ * a workspace taken from the stream-ordered allocator (cudaMallocAsync /
+ * cudaFreeAsync on `stream`: private to the call, ordered with its kernels,
+ * legal inside a stream capture), and a second kernel adds the slices in
+ * ascending order, applies the ReLU and rounds once to fp16.  Each such output
+ * is then the fp32 sum of per-slice fp32 sums, a different order of the same
+ * terms than without a split (results may differ in the last bits; ReLU is
+ * still exactly max(plain, +0)).  The workspace holds slices x (split tiles)
+ * x (tile area) floats.  With a K split every work unit is a whole tile or a
+ * slice of one (GEMM_F16_NO_SPLIT is implied).
  *
  *   GEMM_F16_KSPLIT(n)    n = 2 .. 16: cut K into at most n slices of whole
  *                         64-element blocks (fewer if K has fewer blocks; none
@@ -122,17 +123,23 @@ int gemm_f16(const void *A, const void *B, void *C,
  *                         per SM pair or cluster), as many slices as fill the
  *                         slots once, at least 16 K blocks each, at most 16;
  *                         none if that is fewer than 2.
+ *   GEMM_F16_KSPLIT_TAIL  only the tiles of a partly filled last wave, into as
+ *                         many slices as fill the CTA slots once (at most 8, at
+ *                         least 8 K blocks each); whole tiles before them.
  *   GEMM_F16_NO_KSPLIT    never split K.
  *
  * Configuration 0 takes whatever the offline-measured table chose for the
  * nearest measured shape; its candidates include every configuration with
- * GEMM_F16_KSPLIT_AUTO.  A fixed configuration id without these bits does not
+ * GEMM_F16_KSPLIT_AUTO.  (GEMM_F16_KSPLIT_TAIL is not among them: under the
+ * power cap the extra workspace traffic costs more than the idle SMs of a
+ * last wave do.)  A fixed configuration id without these bits does not
  * split K.  If the workspace cannot be allocated the call runs without a K
  * split.  The pages' tile GEMM keeps each tile's K loop in one block; this is
  * a scheduling choice of this library.
  */
 #define GEMM_F16_NO_KSPLIT 0x200
 #define GEMM_F16_KSPLIT_AUTO 0x400
+#define GEMM_F16_KSPLIT_TAIL 0x800
 #define GEMM_F16_KSPLIT_SHIFT 12
 #define GEMM_F16_KSPLIT_MASK 0x1F000
 #define GEMM_F16_KSPLIT(n) ((n) << GEMM_F16_KSPLIT_SHIFT)
@@ -158,10 +165,10 @@ int gemm_f16_ex(const void *A, const void *B, void *C,
  * have no counterpart: their tile GEMM has no K split and no workspace.
  *
  * Arguments, layouts, ownership and checks as for gemm_f16_ex.  In addition:
- *  - slices x M x N x 4 bytes must fit the 16 MiB (e.g. 1024 x 1024 with 4
- *    slices); a larger split is rejected (GEMM_ERR_INVALID_ARG) before any
- *    launch, whether requested or chosen by configuration 0
- *    (GEMM_F16_NO_KSPLIT never uses the scratch);
+ *  - slices x (split tiles) x (tile area) x 4 bytes must fit the 16 MiB (e.g.
+ *    1024 x 1024 in 128 x 128 tiles with 4 slices); a larger split is rejected
+ *    (GEMM_ERR_INVALID_ARG) before any launch, whether requested or chosen by
+ *    configuration 0 (GEMM_F16_NO_KSPLIT never uses the scratch);
  *  - the scratch's address is looked up once per device, by the first call
  *    that splits K: make that call outside any stream capture;
  *  - nothing in the scratch has to start at zero: every element the reduction

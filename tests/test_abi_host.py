@@ -111,6 +111,8 @@ def test_config_flag_constants_match_header(g):
     assert int(re.search(r"#define GEMM_F16_NO_KSPLIT (0x[0-9A-Fa-f]+)", text).group(1), 16) == g.GEMM_F16_NO_KSPLIT
     assert int(re.search(r"#define GEMM_F16_KSPLIT_AUTO (0x[0-9A-Fa-f]+)", text).group(1), 16) == \
         g.GEMM_F16_KSPLIT_AUTO
+    assert int(re.search(r"#define GEMM_F16_KSPLIT_TAIL (0x[0-9A-Fa-f]+)", text).group(1), 16) == \
+        g.GEMM_F16_KSPLIT_TAIL
     assert int(re.search(r"#define GEMM_F16_KSPLIT_SHIFT (\d+)", text).group(1)) == g.GEMM_F16_KSPLIT_SHIFT
     assert int(re.search(r"#define GEMM_F16_KSPLIT_MASK (0x[0-9A-Fa-f]+)", text).group(1), 16) == \
         g.GEMM_F16_KSPLIT_MASK
@@ -124,10 +126,10 @@ def test_config_flags_parsed_before_cuda(g):
         assert g.config_name(cfg | g.GEMM_F16_NO_SPLIT) == g.config_name(cfg)
         assert g.config_layouts(cfg | g.GEMM_F16_NO_SPLIT) == g.config_layouts(cfg)
     assert g.config_name(1 | 0x20000) is None
-    assert g.config_name(1 | 0x800) is None
+    assert g.config_name(1 | 0x40000) is None
     assert g.config_name(g.num_configs() + 1) is None
-    assert g.config_layouts(1 | 0x800) == g.GEMM_ERR_INVALID_ARG
-    st = g.lib().gemm_f16_ex(0, 0, 0, 64, 64, 64, 1, 1 | 0x800, None)
+    assert g.config_layouts(1 | 0x40000) == g.GEMM_ERR_INVALID_ARG
+    st = g.lib().gemm_f16_ex(0, 0, 0, 64, 64, 64, 1, 1 | 0x40000, None)
     assert st == g.GEMM_ERR_INVALID_ARG
 
 
@@ -139,9 +141,12 @@ def test_ksplit_flags_parsed_before_cuda(g):
             assert g.config_name(cfg | g.ksplit(n)) == g.config_name(cfg)
         assert g.config_name(cfg | g.GEMM_F16_NO_KSPLIT) == g.config_name(cfg)
         assert g.config_name(cfg | g.GEMM_F16_KSPLIT_AUTO) == g.config_name(cfg)
+        assert g.config_name(cfg | g.GEMM_F16_KSPLIT_TAIL) == g.config_name(cfg)
         assert g.config_name(cfg | g.GEMM_F16_NO_SPLIT | g.ksplit(4)) == g.config_name(cfg)
     for bad in (g.ksplit(1), g.ksplit(17), g.ksplit(31), g.GEMM_F16_NO_KSPLIT | g.ksplit(2),
-                g.GEMM_F16_KSPLIT_AUTO | g.ksplit(2), g.GEMM_F16_KSPLIT_AUTO | g.GEMM_F16_NO_KSPLIT):
+                g.GEMM_F16_KSPLIT_AUTO | g.ksplit(2), g.GEMM_F16_KSPLIT_AUTO | g.GEMM_F16_NO_KSPLIT,
+                g.GEMM_F16_KSPLIT_TAIL | g.ksplit(4), g.GEMM_F16_KSPLIT_TAIL | g.GEMM_F16_KSPLIT_AUTO,
+                g.GEMM_F16_KSPLIT_TAIL | g.GEMM_F16_NO_KSPLIT):
         assert g.config_name(1 | bad) is None
         assert g.config_layouts(1 | bad) == g.GEMM_ERR_INVALID_ARG
     assert g.config_label(3 | g.ksplit(4)) == g.config_name(3) + "+ksplit4"
@@ -168,7 +173,8 @@ def test_tuned_table_is_well_formed(g):
     assert len(cands) == n_cands and len(rows) == n_rows > 0
     for c in cands:
         assert 1 <= (c & g.GEMM_F16_CONFIG_ID_MASK) <= g.num_configs()
-        assert (c & ~(g.GEMM_F16_CONFIG_ID_MASK | g.GEMM_F16_NO_SPLIT | g.GEMM_F16_KSPLIT_AUTO)) == 0
+        assert (c & ~(g.GEMM_F16_CONFIG_ID_MASK | g.GEMM_F16_NO_SPLIT | g.GEMM_F16_KSPLIT_AUTO
+                      | g.GEMM_F16_KSPLIT_TAIL)) == 0
     shapes = [r[:3] for r in rows]
     assert len(set(shapes)) == len(shapes)
     for M, N, K, vals in rows:

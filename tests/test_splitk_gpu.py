@@ -183,3 +183,31 @@ def test_launch_info_counts_slices(g):
     cut = g.launch_info(256, 256, 16384, 2 | g.ksplit(8))
     assert plain["tiles"] == cut["tiles"] == 4
     assert plain["grid_ctas"] == 4 and cut["grid_ctas"] == 32 <= sms
+
+
+def test_tail_split_integers_bit_exact(g):
+    # configuration 2 (128 x 128 tiles) at 1920 x 1920: 225 tiles, 152 slots,
+    # so the last 73 tiles run as 2 K slices each; exact integer sums give the
+    # same bits as whole tiles and as the oracle
+    A, B = draw(1920, 1920, 2048, "integer", seed=61)
+    whole = run(g, A, B, True, 2 | g.GEMM_F16_NO_SPLIT | g.GEMM_F16_NO_KSPLIT)
+    tail = run(g, A, B, True, 2 | g.GEMM_F16_KSPLIT_TAIL)
+    assert np.array_equal(whole.view(np.uint16), tail.view(np.uint16))
+    rows = [0, 640, 1279, 1280, 1700, 1919]
+    assert np.array_equal(tail[rows].view(np.uint16), oracle.gemm_f16(A, B, relu=True, rows=rows).view(np.uint16))
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 5])
+def test_tail_split_normal_values(g, cfg):
+    M, N, K = 2300, 1800, 3000
+    A, B = draw(M, N, K, "normal_scaled", seed=62 + cfg)
+    got = run(g, A, B, True, cfg | g.GEMM_F16_KSPLIT_TAIL)
+    rows = sorted(set([0, 255, 256, 1023, 1024, 2047, 2048, 2299] + list(range(2200, 2300, 7))))
+    assert_close(got[rows], oracle.gemm_f16(A, B, relu=True, rows=rows), f"tail split cfg {cfg}")
+
+
+def test_tail_split_headline_shape(g):
+    A, B = draw(8192, 8192, 8192, "normal_scaled", seed=5)
+    got = run(g, A, B, True, 5 | g.GEMM_F16_KSPLIT_TAIL)
+    rows = [0, 4095, 7680, 7935, 7936, 8191]
+    assert_close(got[rows], oracle.gemm_f16(A, B, relu=True, rows=rows), "tail split 8192^3")
