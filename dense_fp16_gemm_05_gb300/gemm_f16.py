@@ -157,8 +157,43 @@ def config_label(config: int) -> str | None:
             + ("+noksplit" if c & GEMM_F16_NO_KSPLIT else ""))
 
 
+# Raw handle of torch's current stream on a device, without building a
+# torch.cuda.Stream object (a few microseconds per call on small problems).
+_current_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+class _NoSwitch:
+    __slots__ = ()
+
+    def __enter__(self):
+        return None
+
+    def __exit__(self, *exc):
+        return False
+
+
+_NO_SWITCH = _NoSwitch()
+
+
+def _device_index(device) -> int:
+    if isinstance(device, int):
+        return device
+    idx = (device if isinstance(device, torch.device) else torch.device(device)).index
+    return idx if idx is not None else torch.cuda.current_device()
+
+
+def _device_scope(device):
+    """Makes ``device`` (a torch.device, index or name) current for the call;
+    no switch when it already is."""
+    if _device_index(device) == torch.cuda.current_device():
+        return _NO_SWITCH
+    return torch.cuda.device(device)
+
+
 def _stream_handle(stream, device) -> int:
     if stream is None:
+        if _current_raw_stream is not None:
+            return int(_current_raw_stream(_device_index(device)))
         stream = torch.cuda.current_stream(device)
     if isinstance(stream, torch.cuda.Stream):
         return int(stream.cuda_stream)
@@ -192,8 +227,8 @@ def gemm_f16(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None, re
     _check_operand(C, "C")
     if tuple(C.shape) != (M, N):
         raise ValueError(f"C must be {(M, N)}, got {tuple(C.shape)}")
-    L = lib()
-    with torch.cuda.device(A.device):
+    L = _lib if _lib is not None else lib()
+    with _device_scope(A.device):
         st = L.gemm_f16_ex(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, int(bool(relu)), int(config),
                            _stream_handle(stream, A.device))
     if st != GEMM_OK:
@@ -215,7 +250,7 @@ def gemm_f16_noalloc(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, relu: bo
     if K != K2 or tuple(C.shape) != (M, N):
         raise ValueError(f"shapes A {tuple(A.shape)}, B {tuple(B.shape)}, C {tuple(C.shape)} do not match")
     L = lib()
-    with torch.cuda.device(A.device):
+    with _device_scope(A.device):
         st = L.gemm_f16_ex_noalloc(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, int(bool(relu)), int(config),
                                    _stream_handle(stream, A.device))
     if st != GEMM_OK:
@@ -242,7 +277,7 @@ def gemm_f16_t(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None, 
     _check_operand(C, "C")
     if tuple(C.shape) != (M, N):
         raise ValueError(f"C must be {(M, N)}, got {tuple(C.shape)}")
-    with torch.cuda.device(A.device):
+    with _device_scope(A.device):
         st = lib().gemm_f16_tx(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, int(bool(transa)),
                                int(bool(transb)), int(bool(relu)), int(config), _stream_handle(stream, A.device))
     if st != GEMM_OK:
@@ -259,7 +294,7 @@ def relu_backward(dC: torch.Tensor, C: torch.Tensor, dZ: torch.Tensor | None = N
         raise ValueError(f"dC {tuple(dC.shape)} and C {tuple(C.shape)} differ")
     if dZ is None:
         dZ = torch.empty_like(dC)
-    with torch.cuda.device(dC.device):
+    with _device_scope(dC.device):
         st = lib().gemm_f16_relu_backward(dC.data_ptr(), C.data_ptr(), dZ.data_ptr(), dC.numel(),
                                           _stream_handle(stream, dC.device))
     if st != GEMM_OK:
@@ -293,7 +328,7 @@ def gemm_f16_from_host(A_host: torch.Tensor, B_host: torch.Tensor, C_host: torch
     M, K = A_host.shape
     N = B_host.shape[1]
     L = lib()
-    with torch.cuda.device(A_dev.device):
+    with _device_scope(A_dev.device):
         st = L.gemm_f16_from_host(A_host.data_ptr(), B_host.data_ptr(), C_host.data_ptr(), A_dev.data_ptr(),
                                   B_dev.data_ptr(), C_dev.data_ptr(), M, N, K, int(bool(relu)),
                                   _stream_handle(stream, A_dev.device))
@@ -304,7 +339,7 @@ def gemm_f16_from_host(A_host: torch.Tensor, B_host: torch.Tensor, C_host: torch
 def check(stream=None, device=None) -> int:
     """Synchronises the stream and returns the device status (GEMM_OK or an error code)."""
     dev = device if device is not None else torch.cuda.current_device()
-    with torch.cuda.device(dev):
+    with _device_scope(dev):
         return int(lib().gemm_f16_check(_stream_handle(stream, dev)))
 
 
@@ -327,7 +362,7 @@ def selftest_timeout(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, config: 
     runs out (test hook); returns the launch status.  Read the outcome with check()."""
     M, K = A.shape
     N = B.shape[1]
-    with torch.cuda.device(A.device):
+    with _device_scope(A.device):
         return int(lib().gemm_f16_selftest_timeout(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, int(config),
                                                    int(timeout_cycles), _stream_handle(stream, A.device)))
 
@@ -377,7 +412,7 @@ def gemm_fp8_block_scaled(A: torch.Tensor, SA: torch.Tensor, W: torch.Tensor, SW
     if tuple(C.shape) != (M, N):
         raise ValueError(f"C must be {(M, N)}, got {tuple(C.shape)}")
     L = lib()
-    with torch.cuda.device(A.device):
+    with _device_scope(A.device):
         st = L.gemm_fp8_block_scaled(A.data_ptr(), SA.data_ptr(), W.data_ptr(), SW.data_ptr(), C.data_ptr(),
                                      M, N, K, int(bool(relu)), _stream_handle(stream, A.device))
     if st != GEMM_OK:
@@ -414,7 +449,7 @@ def attention_fwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, O: torch.Te
     if O.dtype != torch.float16 or O.shape != Q.shape or not O.is_contiguous():
         raise ValueError("O must be a contiguous float16 tensor shaped like Q")
     L = lib()
-    with torch.cuda.device(Q.device):
+    with _device_scope(Q.device):
         st = L.attention_fwd_f16(Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), B, H, S, D,
                                  float(sm_scale), int(bool(causal)), _stream_handle(stream, Q.device))
     if st != GEMM_OK:
