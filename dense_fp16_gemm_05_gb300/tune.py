@@ -16,8 +16,10 @@ Method: for each shape, every candidate runs ``rounds`` times in interleaved
 order (so slow drift of the power-capped clock hits all candidates alike);
 each round times about 150 ms of back-to-back launches on resident operands
 with CUDA events (the sustained regime: short bursts run at a higher clock
-than the power cap allows for long) and keeps the mean time per launch; a
-candidate's figure is the median over rounds.  Needs one sm_103 GPU and the
+than the power cap allows for long), replayed from a CUDA graph so that the
+per-call host cost does not hide the kernels' differences on small problems,
+and keeps the mean time per launch; a candidate's figure is the median over
+rounds.  Needs one sm_103 GPU and the
 built library.
 """
 from __future__ import annotations
@@ -59,25 +61,42 @@ def candidates() -> list[int]:
 def time_candidate(A, B, C, cfg: int, min_ms: float) -> float:
     """Mean ms per launch over back-to-back launches on resident operands,
     about ``min_ms`` of them: long enough for the power-capped clock to settle
-    as it does in a sustained run."""
-    for _ in range(2):
+    as it does in a sustained run.  The launches are captured once in a CUDA
+    graph (up to 200 of them, every stream-ordered workspace allocation
+    included) and the graph is replayed, so no host work sits between two
+    launches: on small problems the per-call host cost would otherwise set
+    the pace for every candidate alike and hide the kernels' differences."""
+    def run():
         g.gemm_f16(A, B, C, relu=True, config=cfg)
+
+    for _ in range(2):
+        run()                      # the first calls also do the library's per-device set-up
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     s.record()
-    g.gemm_f16(A, B, C, relu=True, config=cfg)
+    run()
     e.record()
     e.synchronize()
     one = max(s.elapsed_time(e), 1e-3)
-    n = int(min(20000, max(3, min_ms / one)))
+    per_graph = int(min(200, max(1, 20.0 / one)))
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for _ in range(per_graph):
+            run()
+    replays = int(min(20000, max(2, min_ms / (one * per_graph))))
+    graph.replay()
+    torch.cuda.synchronize()
     s.record()
-    for _ in range(n):
-        g.gemm_f16(A, B, C, relu=True, config=cfg)
+    for _ in range(replays):
+        graph.replay()
     e.record()
     e.synchronize()
     st = g.check()
     if st != g.GEMM_OK:
         raise RuntimeError(f"config {cfg:#x}: device status {st} ({g.strerror(st)})")
-    return s.elapsed_time(e) / n
+    del graph
+    return s.elapsed_time(e) / (replays * per_graph)
 
 
 def sweep(shapes, rounds: int, min_ms: float, log=sys.stderr) -> list[dict]:
@@ -120,7 +139,7 @@ def write_include(rows, path: str, rounds: int, min_ms: float):
         "// Generated by `python -m dense_fp16_gemm_05_gb300.tune`; do not edit by hand.",
         f"// Device: {props.name}, {props.multi_processor_count} SMs; {datetime.date.today().isoformat()};",
         f"// kernel sources {kernel_hash()}; {rounds} interleaved rounds per shape, median;",
-        f"// about {min_ms:.0f} ms of back-to-back launches per candidate and round.",
+        f"// about {min_ms:.0f} ms of back-to-back launches (CUDA graph replays) per candidate and round.",
         "// Each row: M, N, K, then the measured TFLOP/s of every candidate in",
         "// kTunedCandidates order (ReLU on, N(0,1) operands, back-to-back launches).",
         f"#define GEMM_F16_TUNED_CANDIDATES {len(cands)}",
