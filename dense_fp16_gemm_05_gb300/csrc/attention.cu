@@ -57,8 +57,17 @@ int launch_dim(const AttnLaunchArgs &a)
     // One CTA per pair of query blocks (its two tiles), per head and batch.
     const dim3 grid(static_cast<unsigned>((p.num_q_blocks + Cfg::TILES - 1) / Cfg::TILES),
                     static_cast<unsigned>(a.heads), static_cast<unsigned>(a.batch));
-    attention_fwd_sm103a<kDim><<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, a.stream>>>(tq, tk, tv, p);
-    if (cudaGetLastError() != cudaSuccess) {
+    cudaLaunchConfig_t lc{};
+    lc.gridDim = grid;
+    lc.blockDim = dim3(Cfg::THREADS, 1, 1);
+    lc.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    lc.stream = a.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // programmatic dependent launch
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    if (cudaLaunchKernelEx(&lc, attention_fwd_sm103a<kDim>, tq, tk, tv, p) != cudaSuccess) {
         AttnPrepared<kDim>::forget(a.dev.device);
         return GEMM_ERR_LAUNCH;
     }

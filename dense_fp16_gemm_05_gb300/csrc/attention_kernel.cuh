@@ -317,6 +317,10 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
+    // Set-up above may overlap the previous kernel of the stream; nothing
+    // below runs before its results are visible (programmatic dependent launch).
+    griddep_wait();
+    griddep_launch_dependents();
     const uint32_t tmem_base = *tmem_slot_ptr;
     const uint64_t limit = p.timeout_cycles;
 

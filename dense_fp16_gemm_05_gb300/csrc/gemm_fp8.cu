@@ -88,13 +88,15 @@ int launch_fp8_variant(const Fp8LaunchArgs &a)
     lc.blockDim = dim3(Fp8Cfg::THREADS, 1, 1);
     lc.dynamicSmemBytes = Fp8Cfg::SMEM_BYTES;
     lc.stream = a.stream;
-    cudaLaunchAttribute attrs[1];
+    cudaLaunchAttribute attrs[2];
     attrs[0].id = cudaLaunchAttributeClusterDimension;
     attrs[0].val.clusterDim.x = 2;
     attrs[0].val.clusterDim.y = 1;
     attrs[0].val.clusterDim.z = 1;
+    attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // programmatic dependent launch
+    attrs[1].val.programmaticStreamSerializationAllowed = 1;
     lc.attrs = attrs;
-    lc.numAttrs = 1;
+    lc.numAttrs = 2;
     lc.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
     if (cudaLaunchKernelEx(&lc, kern, ta, tw, p) != cudaSuccess) {
         cudaGetLastError();

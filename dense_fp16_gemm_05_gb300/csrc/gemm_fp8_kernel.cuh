@@ -233,6 +233,10 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
     cluster_arrive();
     cluster_wait();
     tc_fence_after_sync();
+    // Set-up above may overlap the previous kernel of the stream; nothing
+    // below runs before its results are visible (programmatic dependent launch).
+    griddep_wait();
+    griddep_launch_dependents();
     const uint32_t tmem_base = *tmem_slot_ptr;
     const uint64_t limit = p.timeout_cycles;
     const int KB = p.num_k_blocks;

@@ -384,6 +384,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         cluster_wait();
     }
     tc_fence_after_sync();
+    // The set-up above touches no global memory of this call, so it may run
+    // while the previous kernel of the stream finishes; everything below
+    // waits for that kernel's results.  The next kernel may then be
+    // scheduled on SMs this grid leaves free (it waits the same way).
+    griddep_wait();
+    griddep_launch_dependents();
     const uint32_t tmem_base = *tmem_slot_ptr;
     const uint64_t limit = p.timeout_cycles;
     bool aborted = false;

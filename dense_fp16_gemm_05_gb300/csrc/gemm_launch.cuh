@@ -298,13 +298,18 @@ int launch_one(const LaunchArgs &a)
     lc.blockDim = dim3(Cfg::THREADS, 1, 1);
     lc.dynamicSmemBytes = Cfg::SMEM_BYTES;
     lc.stream = a.stream;
-    cudaLaunchAttribute attrs[1];
+    cudaLaunchAttribute attrs[2];
     attrs[0].id = cudaLaunchAttributeClusterDimension;
     attrs[0].val.clusterDim.x = Cfg::CLUSTER;
     attrs[0].val.clusterDim.y = 1;
     attrs[0].val.clusterDim.z = 1;
+    // Programmatic dependent launch: the kernel's set-up may overlap the end
+    // of the previous kernel on the stream (the kernel waits for it before
+    // touching memory).
+    attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[1].val.programmaticStreamSerializationAllowed = 1;
     lc.attrs = attrs;
-    lc.numAttrs = 1;
+    lc.numAttrs = 2;
     lc.gridDim = dim3(static_cast<unsigned>(sc.grid_units * Cfg::CLUSTER), 1, 1);
     if (cudaLaunchKernelEx(&lc, kern, ta, tb, tc, p) != cudaSuccess) {
         cudaGetLastError();

@@ -33,6 +33,8 @@ __global__ void __launch_bounds__(256) relu_backward_vec_kernel(const uint4 *__r
                                                                 const uint4 *__restrict__ C, uint4 *__restrict__ dZ,
                                                                 int64_t n_vec)
 {
+    gemm_sm103::griddep_wait();   // dC and C may come from the kernel just before
+    gemm_sm103::griddep_launch_dependents();
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n_vec; i += stride) {
         const uint4 c = C[i];
@@ -51,6 +53,8 @@ __global__ void __launch_bounds__(256) relu_backward_scalar_kernel(const uint16_
                                                                    uint16_t *__restrict__ dZ, int64_t begin,
                                                                    int64_t n)
 {
+    gemm_sm103::griddep_wait();
+    gemm_sm103::griddep_launch_dependents();
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t i = begin + static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
         const uint32_t c = C[i];
@@ -62,6 +66,31 @@ __global__ void __launch_bounds__(256) relu_backward_scalar_kernel(const uint16_
 
 namespace gemm_sm103 {
 
+namespace {
+
+// Launch as a programmatic dependent of the previous kernel on the stream
+// (the kernels wait for it before touching memory).
+template <class... Args>
+int launch_pdl(void (*kern)(Args...), int64_t blocks, cudaStream_t stream, Args... args)
+{
+    cudaLaunchConfig_t lc{};
+    lc.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+    lc.blockDim = dim3(256, 1, 1);
+    lc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    if (cudaLaunchKernelEx(&lc, kern, args...) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    return GEMM_OK;
+}
+
+}  // namespace
+
 int relu_backward_launch(const void *dC, const void *C, void *dZ, int64_t n, int sm_count, cudaStream_t stream)
 {
     const bool aligned = ((reinterpret_cast<uintptr_t>(dC) | reinterpret_cast<uintptr_t>(C) |
@@ -71,18 +100,17 @@ int relu_backward_launch(const void *dC, const void *C, void *dZ, int64_t n, int
     if (n_vec > 0) {
         int64_t blocks = (n_vec + 255) / 256;
         if (blocks > max_blocks) blocks = max_blocks;
-        relu_backward_vec_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-            static_cast<const uint4 *>(dC), static_cast<const uint4 *>(C), static_cast<uint4 *>(dZ), n_vec);
-        if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_LAUNCH;
+        const int st = launch_pdl(relu_backward_vec_kernel, blocks, stream, static_cast<const uint4 *>(dC),
+                                  static_cast<const uint4 *>(C), static_cast<uint4 *>(dZ), n_vec);
+        if (st != GEMM_OK) return st;
     }
     const int64_t done = n_vec * 8;
     if (done < n) {
         int64_t blocks = (n - done + 255) / 256;
         if (blocks > max_blocks) blocks = max_blocks;
-        relu_backward_scalar_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-            static_cast<const uint16_t *>(dC), static_cast<const uint16_t *>(C), static_cast<uint16_t *>(dZ), done,
-            n);
-        if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_LAUNCH;
+        const int st = launch_pdl(relu_backward_scalar_kernel, blocks, stream, static_cast<const uint16_t *>(dC),
+                                  static_cast<const uint16_t *>(C), static_cast<uint16_t *>(dZ), done, n);
+        if (st != GEMM_OK) return st;
     }
     return GEMM_OK;
 }

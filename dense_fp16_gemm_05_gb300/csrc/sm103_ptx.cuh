@@ -106,6 +106,25 @@ __device__ __forceinline__ void cluster_wait()
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+
+// Waits until every kernel this grid depends on (the previous kernel of the
+// stream, when this one was launched with programmatic stream serialisation)
+// has completed and its memory operations are visible.  Without such a
+// dependency it returns at once.
+__device__ __forceinline__ void griddep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Lets the next kernel of the stream (if launched with programmatic stream
+// serialisation) be scheduled once every CTA of this grid has run this or
+// exited; that kernel still waits in griddep_wait for this grid to complete.
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map)

@@ -35,6 +35,10 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float *__restr
                                                             const gemm_sm103::GemmParams p, int super_m, int bn,
                                                             int64_t n_vec)
 {
+    // The partials come from the GEMM kernel just before this one on the
+    // stream (launched as its programmatic dependent).
+    gemm_sm103::griddep_wait();
+    gemm_sm103::griddep_launch_dependents();
     const int64_t per_row = bn / 8;
     const int64_t per_tile = static_cast<int64_t>(super_m) * per_row;
     const int64_t tile_elems = static_cast<int64_t>(super_m) * bn;
@@ -123,9 +127,21 @@ int launch_splitk_reduce(const float *ws, void *C, const GemmParams &p, int supe
     const int64_t cap = static_cast<int64_t>(sm_count > 0 ? sm_count : 1) * 8;
     const unsigned blocks = static_cast<unsigned>(want < cap ? want : cap);
     __half *c = static_cast<__half *>(C);
-    if (relu) splitk_reduce_kernel<true><<<blocks, 256, 0, stream>>>(ws, c, p, super_m, bn, n_vec);
-    else splitk_reduce_kernel<false><<<blocks, 256, 0, stream>>>(ws, c, p, super_m, bn, n_vec);
-    if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_LAUNCH;
+    cudaLaunchConfig_t lc{};
+    lc.gridDim = dim3(blocks, 1, 1);
+    lc.blockDim = dim3(256, 1, 1);
+    lc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    const cudaError_t e = relu ? cudaLaunchKernelEx(&lc, splitk_reduce_kernel<true>, ws, c, p, super_m, bn, n_vec)
+                               : cudaLaunchKernelEx(&lc, splitk_reduce_kernel<false>, ws, c, p, super_m, bn, n_vec);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
     return GEMM_OK;
 }
 
