@@ -24,7 +24,12 @@
  * cudaStream_t; NULL is the legacy default stream) and return without
  * synchronising.  Argument errors are reported synchronously by the return
  * value and launch nothing.  A device-side timeout is reported later, by
- * gemm_f16_check.
+ * gemm_f16_check.  Every kernel of this library is launched as a
+ * programmatic dependent of the kernel before it on the stream: its set-up
+ * (barriers, tensor memory, descriptor prefetch) may run while that kernel
+ * finishes, but it reads and writes no global memory before that kernel has
+ * completed and its writes are visible, so the results are those of plain
+ * stream order (also inside a CUDA graph capture).
  *
  * Thread safety.  All entry points may be called from several host threads.
  * Tensor-map descriptors are built on the host per call and passed by value
