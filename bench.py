@@ -114,7 +114,8 @@ def recorded_traffic(workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clock and throttle reasons during a region."""
+    """nvidia-smi sampling of SM clock and throttle reasons during a region
+    (every interval_ms; the headline loop samples every 20 ms)."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.sw_power_cap,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -286,7 +287,7 @@ def run_ours(args):
 
 
     # ---- device-resident timing
-    sampler = ClockSampler(local)
+    sampler = ClockSampler(local, interval_ms=20)
     sampler.start()
     barrier()
     total_ms, per_launch = time_device(g, A, B, C, w.relu, config, args.steps, args.warmup, stream)
