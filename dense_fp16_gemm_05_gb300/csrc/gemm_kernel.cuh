@@ -385,10 +385,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     }
     tc_fence_after_sync();
     // The set-up above touches no global memory of this call, so it may run
-    // while the previous kernel of the stream finishes; everything below
-    // waits for that kernel's results.  The next kernel may then be
-    // scheduled on SMs this grid leaves free (it waits the same way).
-    griddep_wait();
+    // while the previous kernel of the stream finishes.  Each role waits for
+    // that kernel's results (griddep_wait) just before its own first global
+    // access: the producer before its first load, the epilogue before its
+    // first store; the MMA thread touches only shared and tensor memory.  The
+    // next kernel may be scheduled on SMs this grid leaves free (it waits the
+    // same way).
     griddep_launch_dependents();
     const uint32_t tmem_base = *tmem_slot_ptr;
     const uint64_t limit = p.timeout_cycles;
@@ -404,6 +406,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             // The pair leader's full barrier 0 (its full[s] is 8 * s bytes further).
             const uint32_t full_base = (kPair && !leader) ? mapa_shared(full_bar(0), leader_rank) : full_bar(0);
             (void)full_base;
+            bool dep_waited = false;
             for (int u = cluster_id; ok && p.producer_off == 0 && u < p.num_units; u += num_clusters) {
                 int mb, col0, shift, kb0, kb1, slice;
                 unit_coords<Cfg::BN>(u, p, mb, col0, shift);
@@ -431,6 +434,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     if (!wait_phase(empty_bar(s), ph ^ 1u, abort, limit, kSiteProducerEmpty)) {
                         ok = false;
                         break;
+                    }
+                    if (!dep_waited) {
+                        griddep_wait();   // the operands may come from the previous kernel
+                        dep_waited = true;
                     }
                     const int k0 = kb * Cfg::BK;
                     const uint32_t a_dst = sA + s * Cfg::A_STAGE_BYTES;
@@ -664,6 +671,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 aborted = true;
                 break;
             }
+            if (it == 0) griddep_wait();   // before this warp's first store of C (or of partials)
             tc_fence_after_sync();
             const int row0 = mb * Cfg::SUPER_M + static_cast<int>(pair) * Cfg::TILE_M +
                              static_cast<int>(rank) * Cfg::BM + q * 32;
