@@ -675,12 +675,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             tc_fence_after_sync();
             const int row0 = mb * Cfg::SUPER_M + static_cast<int>(pair) * Cfg::TILE_M +
                              static_cast<int>(rank) * Cfg::BM + q * 32;
-#pragma unroll 1
-            for (int c = 0; c < chunks; ++c) {
-                uint32_t r[64];
-                tmem_load_32x32b_x64(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * Cfg::ACC_COLS +
-                                         c * Cfg::EPI_COLS,
-                                     r);
+            const uint32_t acc_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * Cfg::ACC_COLS;
+            // Chunk c (64 columns) of the accumulator: hand back TMEM when this
+            // warp's reads of it are complete, then convert and store it.
+            auto chunk_out = [&](const uint32_t (&r)[64], int c) {
                 if constexpr (kHalfRelease) {
                     // One accumulator in two N halves of 256 columns (chunks 0-3
                     // and 4-7): hand each back once this warp has read it (both at
@@ -764,6 +762,21 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                                              pack_f16x2<kRelu>(r[8 * j + 6], r[8 * j + 7]));
                         }
                     }
+                }
+            };
+            // Double-buffered: the TMEM load of chunk c + 1 runs while chunk c
+            // is converted and stored.
+            uint32_t ra[64], rb[64];
+            tmem_load_32x32b_x64_async(acc_addr, ra);
+#pragma unroll 1
+            for (int c = 0; c < chunks; c += 2) {
+                tmem_wait_ld_x64(ra);
+                if (c + 1 < chunks) tmem_load_32x32b_x64_async(acc_addr + (c + 1) * Cfg::EPI_COLS, rb);
+                chunk_out(ra, c);
+                if (c + 1 < chunks) {
+                    tmem_wait_ld_x64(rb);
+                    if (c + 2 < chunks) tmem_load_32x32b_x64_async(acc_addr + (c + 2) * Cfg::EPI_COLS, ra);
+                    chunk_out(rb, c + 1);
                 }
             }
         }
