@@ -174,9 +174,11 @@ struct AbortFlag {
 // default (CTA-scope) form also for barriers another CTA arrives on: TMA bytes
 // become visible through the barrier's transaction count, and TMEM hand-offs
 // are ordered by the tcgen05 fences around the waits.
-// kSleepNs > 0 adds a short sleep to each slow-path probe: for waits off the
-// critical path (the epilogue waiting for a whole tile), it spends fewer issue
-// slots, and so less power, on polling.
+// kSleepNs > 0 adds a short sleep to each slow-path probe (fewer issue slots
+// spent on polling).  No wait uses it: a 256 ns sleep in the epilogue's wait
+// for a finished accumulator delayed the hand-back of TMEM to the next tile
+// and measured 1.6 % slower (the try_wait probe already suspends the thread
+// for a while when the phase is not complete).
 template <int kSleepNs = 0>
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const AbortFlag &abort, uint64_t limit,
                                            uint32_t site)
@@ -665,7 +667,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             const uint32_t acc_ph = (it / Cfg::ACC_STAGES) & 1;
             int ok = 1;
             if (lane == 0)
-                ok = wait_phase<256>(tfull_bar(b), acc_ph, abort, limit, kSiteEpilogueTmemFull) ? 1 : 0;
+                ok = wait_phase(tfull_bar(b), acc_ph, abort, limit, kSiteEpilogueTmemFull) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) {
                 aborted = true;
