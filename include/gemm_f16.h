@@ -16,9 +16,13 @@
  * stride arguments, as in the pages' T.Tensor((M,K)) ... declarations).
  *
  * Ownership.  The caller owns every buffer.  The library allocates nothing per
- * call; its only device state is one status word per GPU (a __device__
- * variable of the library's module) that the kernels set when a bounded wait
- * expires.  C must not overlap A or B.
+ * call except the workspace of a GEMM it cuts into K slices (taken from and
+ * returned to the stream-ordered allocator on `stream`; gemm_f16_ex_noalloc
+ * uses a fixed scratch instead).  Its device state is one status word per GPU
+ * (a __device__ variable of the library's module) that the kernels set when
+ * a bounded wait expires, the 16 MiB scratch of gemm_f16_ex_noalloc, and the
+ * two copy streams per device that the first gemm_f16_from_host call
+ * creates.  C must not overlap A or B.
  *
  * Asynchrony.  gemm_f16 and gemm_f16_ex only enqueue work on `stream` (a
  * cudaStream_t; NULL is the legacy default stream) and return without
