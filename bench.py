@@ -15,7 +15,14 @@ Prints ONE JSON line:
   roofline     tensor-core bound: achieved TFLOP/s per launch against the
                measured bf16 matmul peak of this machine (fp16 has the same rate)
   cpu_baseline the CPU oracle, as it stands, on a bounded sample of rows
-  clocks       SM clocks / throttle reasons sampled during the timed region
+  clocks       SM clock, power and throttle reasons polled through NVML
+               (read-only, ~1 ms) inside the timed region
+  sweep        every square configuration of the benchmark description
+               (64^3 integers, 1000^3, 1024^3, n^3 for n = 512 .. 16384):
+               TFLOP/s of single launches (L2 flushed where the operands fit)
+               and of back-to-back launches replayed from a CUDA graph
+  sustained    the headline workload back to back for a few seconds, with
+               the clock samples inside that loop
 
 ``--impl reference`` times the CPU oracle instead (the reference arm: a
 deliberately slow, obviously correct program on the host cores).
@@ -32,9 +39,7 @@ import json
 import math
 import os
 import statistics
-import subprocess
 import sys
-import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -114,66 +119,94 @@ def recorded_traffic(workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clock and throttle reasons during a region
-    (every interval_ms; the headline loop samples every 20 ms)."""
+    """Read-only NVML polling of the SM clock, the board power and the active
+    clock-event (throttle) reasons, in a background thread about every
+    millisecond, through the driver's own libnvidia-ml (ctypes; queries only,
+    no setting is touched).  Each sample carries its host time, so a timed
+    region -- host times taken right after the synchronisations that bracket
+    it -- selects exactly the samples that fall inside it."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.sw_power_cap,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown")
+    REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                   0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, device_index: int, interval_ms: int = 50):
+    def __init__(self, device_index: int, interval_s: float = 0.001):
         self.device_index = device_index
-        self.interval_ms = interval_ms
-        self.proc = None
-        self.path = None
+        self.interval_s = interval_s
+        self.samples = []          # (host time, SM MHz, power W, reason bits)
+        self.max_mhz = None
+        self.error = None
+        self._stop = False
+        self._thread = None
 
-    def _gpu_id(self):
-        try:
-            import torch
-            u = str(torch.cuda.get_device_properties(self.device_index).uuid)
-            return u if u.startswith("GPU-") else "GPU-" + u
-        except Exception:
-            return str(self.device_index)
+    def _open(self):
+        import ctypes
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if nv.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        handle = ctypes.c_void_p()
+        import torch
+        uuid = str(torch.cuda.get_device_properties(self.device_index).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        if nv.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(handle)) != 0:
+            if nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.device_index), ctypes.byref(handle)) != 0:
+                raise OSError("no NVML handle for the device")
+        reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        if nv.nvmlDeviceGetMaxClockInfo(handle, ctypes.c_int(1), ctypes.byref(mx)) == 0:   # NVML_CLOCK_SM
+            self.max_mhz = float(mx.value)
+        return nv, handle, reasons_fn
+
+    def _run(self, nv, handle, reasons_fn):
+        import ctypes
+        clk, mw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop:
+            t = time.perf_counter()
+            ok = nv.nvmlDeviceGetClockInfo(handle, ctypes.c_int(1), ctypes.byref(clk)) == 0
+            pw = nv.nvmlDeviceGetPowerUsage(handle, ctypes.byref(mw)) == 0
+            rr = reasons_fn(handle, ctypes.byref(rs)) == 0
+            if ok:
+                self.samples.append((t, float(clk.value), mw.value / 1000.0 if pw else float("nan"),
+                                     int(rs.value) if rr else 0))
+            time.sleep(self.interval_s)
 
     def start(self):
-        fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
-        os.close(fd)
+        import threading
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", self._gpu_id(), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", str(self.interval_ms)],
-                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
-        except OSError:
-            self.proc = None
-        time.sleep(0.3)
+            nv, handle, reasons_fn = self._open()
+        except (OSError, AttributeError) as e:
+            self.error = f"NVML unavailable: {e}"
+            return self
+        self._thread = threading.Thread(target=self._run, args=(nv, handle, reasons_fn), daemon=True)
+        self._thread.start()
+        time.sleep(0.05)
+        return self
 
     def stop(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        time.sleep(0.1)
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        rows = []
-        with open(self.path) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 7:
-                    continue
-                try:
-                    rows.append((float(parts[0]), float(parts[1]), float(parts[2]), parts[3:7]))
-                except ValueError:
-                    continue
-        os.unlink(self.path)
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        loaded = [r for r in rows if r[2] > 300.0] or rows   # samples under load (power draw)
-        names = ("sw_power_cap", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
-        reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[3]) if v.lower() == "active"})
-        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
-                "power_w_max": max(r[2] for r in rows), "samples": len(loaded), "reasons": reasons}
+        self._stop = True
+        if self._thread is not None:
+            self._thread.join(timeout=5)
+
+    def region(self, t0: float, t1: float, ms: float | None = None) -> dict:
+        """Summary of the samples taken between host times t0 and t1."""
+        if self.error:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [self.error], "samples": 0}
+        inside = [x for x in self.samples if t0 <= x[0] <= t1]
+        out = {"samples": len(inside), "sm_max_mhz": self.max_mhz, "source": "NVML, read-only, ~1 ms polling"}
+        if not inside:
+            out.update({"sm_mhz": None, "reasons": ["no sample inside the region"]})
+            return out
+        mhz = statistics.median(x[1] for x in inside)
+        bits = 0
+        for x in inside:
+            bits |= x[3]
+        powers = [x[2] for x in inside if x[2] == x[2]]
+        out.update({"sm_mhz": mhz, "sm_mhz_min": min(x[1] for x in inside),
+                    "power_w_max": max(powers) if powers else None,
+                    "reasons": sorted(name for bit, name in self.REASON_BITS.items() if bits & bit)})
+        if ms is not None:
+            out["ms_x_median_mhz"] = ms * mhz   # clock-normalised duration (kilocycles at the median clock)
+        return out
 
 
 def oracle_cpu_baseline(A, B, relu: bool, budget_s: float, workload_name: str, M: int):
@@ -193,6 +226,15 @@ def oracle_cpu_baseline(A, B, relu: bool, budget_s: float, workload_name: str, M
     return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"{len(rows)} of {M} output rows (all {N} columns, full K={K}) of {workload_name}, "
                       f"{secs:.1f} s"}, secs
+
+
+VALUES_LABEL = {"normal_scaled": "N(0,1)/sqrt(K) fp16", "normal": "N(0,1) fp16", "integer": "integers -4..4 fp16"}
+
+
+def workload_config(w) -> dict:
+    """The `config` of the JSON line: the workload only, identical in both arms."""
+    return {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "relu": w.relu,
+            "values": VALUES_LABEL.get(w.values, w.values), "seed": w.seed}
 
 
 # ---------------------------------------------------------------- reference arm
@@ -226,10 +268,10 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "gpu_launches": 0,
-        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "relu": w.relu, "values": w.values,
-                   "seed": w.seed, "sample_rows_per_step": n_rows},
+        "config": workload_config(w),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{n_rows} of {w.M} output rows per step (all {w.N} columns, full K)"},
+                         "sample": f"{n_rows} of {w.M} output rows per step (all {w.N} columns, full K)",
+                         "sample_rows_per_step": n_rows},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -238,12 +280,15 @@ def run_reference(args):
 
 # ---------------------------------------------------------------- our arm
 
-def time_device(g, A, B, C, relu, config, steps, warmup, stream):
-    """Returns (total_ms over the timed steps, list of per-launch ms)."""
+def time_device(g, A, B, C, relu, config, steps, warmup, stream, barrier=None):
+    """Returns (total_ms over the timed steps, list of per-launch ms, host
+    time right after the synchronisation before the steps, host time right
+    after the one after them)."""
     import torch
     for _ in range(warmup):
         g.gemm_f16(A, B, C, relu=relu, stream=stream, config=config)
-    torch.cuda.synchronize()
+    (barrier or torch.cuda.synchronize)()
+    h0 = time.perf_counter()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     t0 = torch.cuda.Event(enable_timing=True)
@@ -254,8 +299,137 @@ def time_device(g, A, B, C, relu, config, steps, warmup, stream):
         g.gemm_f16(A, B, C, relu=relu, stream=stream, config=config)
         ends[i].record(stream)
     t1.record(stream)
+    (barrier or torch.cuda.synchronize)()
+    h1 = time.perf_counter()
+    return t0.elapsed_time(t1), [s.elapsed_time(e) for s, e in zip(starts, ends)], h0, h1
+
+
+SWEEP_WORKLOADS = ("int_64", "relu_ragged_1000", "relu_1024", "sweep_512", "sweep_1024", "sweep_2048",
+                   "sweep_4096", "sweep_8192", "sweep_16384")
+
+
+def run_sweep(g, dev, stream, peak, theoretical, sampler):
+    """Every square configuration of the benchmark description, each in the
+    automatic kernel configuration, timed two ways: single launches with L2
+    flushed before each (where the operands fit in L2; median of the launches,
+    all enqueued back to back), and back-to-back launches replayed from a CUDA
+    graph (warm L2; the per-launch GPU time a chain of GEMMs sees)."""
+    import torch
+    from dense_fp16_gemm_05_gb300.inputs import WORKLOADS, draw_on_device, draw_workload
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 1000 * 1000))
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+    out = []
+    for name in SWEEP_WORKLOADS:
+        w = WORKLOADS[name]
+        if w.M * w.K <= 4096 * 4096:
+            A, B = (t.to(dev) for t in draw_workload(w))
+            drawn = "host generator (the parity tests' inputs)"
+        else:
+            A, B = draw_on_device(w.M, w.N, w.K, w.values, w.seed, dev)
+            drawn = "seeded device generator (same distribution)"
+        C = torch.empty((w.M, w.N), dtype=torch.float16, device=dev)
+        cfg = g.auto_config(w.M, w.N, w.K)
+        op_bytes = 2 * (w.M * w.K + w.K * w.N + w.M * w.N)
+        fits = op_bytes < l2
+
+        def call():
+            g.gemm_f16(A, B, C, relu=w.relu, stream=stream)
+
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s_ev.record(stream)
+        call()
+        e_ev.record(stream)
+        e_ev.synchronize()
+        one = max(s_ev.elapsed_time(e_ev), 1e-3)
+        reps = int(min(50, max(7, 40.0 / one)))
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        h0 = time.perf_counter()
+        for a_ev, b_ev in evs:
+            if fits:
+                flush.zero_()
+            a_ev.record(stream)
+            call()
+            b_ev.record(stream)
+        torch.cuda.synchronize()
+        h1 = time.perf_counter()
+        ms = statistics.median(a.elapsed_time(b) for a, b in evs)
+        # back to back from a CUDA graph
+        per_graph = int(min(200, max(1, 10.0 / one)))
+        cap = torch.cuda.Stream(device=dev)
+        cap.wait_stream(torch.cuda.current_stream(dev))
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap):
+            for _ in range(per_graph):
+                g.gemm_f16(A, B, C, relu=w.relu)
+        replays = int(min(500, max(3, 30.0 / (one * per_graph))))
+        graph.replay()
+        torch.cuda.synchronize()
+        s_ev.record()
+        for _ in range(replays):
+            graph.replay()
+        e_ev.record()
+        e_ev.synchronize()
+        ms_graph = s_ev.elapsed_time(e_ev) / (replays * per_graph)
+        del graph
+        st = g.check(stream)
+        if st != g.GEMM_OK:
+            raise RuntimeError(f"{name}: device status {st}: {g.strerror(st)}")
+        tf = w.flops / (ms * 1e-3) / 1e12
+        tf_graph = w.flops / (ms_graph * 1e-3) / 1e12
+        clk = sampler.region(h0, h1)
+        out.append({"workload": name, "M": w.M, "N": w.N, "K": w.K, "relu": w.relu,
+                    "values": VALUES_LABEL.get(w.values, w.values), "seed": w.seed, "inputs": drawn,
+                    "kernel_config": g.config_label(cfg), "ms": ms, "TFLOP_s": tf,
+                    "frac_of_measured_peak": tf / peak, "frac_of_theoretical_peak": tf / theoretical,
+                    "l2": ("L2 flushed (a 2x-L2 buffer written) before each launch; median of launches"
+                           if fits else "operands larger than L2, no flush; median of launches"),
+                    "launches": reps, "sm_mhz": clk.get("sm_mhz"), "clock_samples": clk.get("samples"),
+                    "graph_replay": {"us_per_launch": ms_graph * 1e3, "TFLOP_s": tf_graph,
+                                     "frac_of_measured_peak": tf_graph / peak,
+                                     "launches": replays * per_graph,
+                                     "l2": "warm: back-to-back launches replayed from a CUDA graph"}})
+        del A, B, C
+    del flush
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_sustained(g, A, B, C, w, config, stream, sampler, seconds, peaks, peak_src, theoretical):
+    """The headline workload back to back for `seconds` (the power-capped
+    regime of a long run), with the clock samples taken inside the loop."""
+    import torch
+    s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
-    return t0.elapsed_time(t1), [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    s_ev.record(stream)
+    for _ in range(5):
+        g.gemm_f16(A, B, C, relu=w.relu, stream=stream, config=config)
+    e_ev.record(stream)
+    e_ev.synchronize()
+    one = s_ev.elapsed_time(e_ev) / 5
+    n = int(max(10, seconds * 1e3 / one))
+    torch.cuda.synchronize()
+    h0 = time.perf_counter()
+    s_ev.record(stream)
+    for _ in range(n):
+        g.gemm_f16(A, B, C, relu=w.relu, stream=stream, config=config)
+    e_ev.record(stream)
+    torch.cuda.synchronize()
+    h1 = time.perf_counter()
+    ms = s_ev.elapsed_time(e_ev)
+    st = g.check(stream)
+    if st != g.GEMM_OK:
+        raise RuntimeError(f"sustained loop: device status {st}: {g.strerror(st)}")
+    tf = n * w.flops / (ms * 1e-3) / 1e12
+    sus = peaks.get("bf16_tflops_sustained")
+    return {"workload": w.name, "kernel_config": g.config_label(config), "launches": n, "seconds": ms / 1e3,
+            "TFLOP_s": tf, "frac_of_theoretical_peak": tf / theoretical,
+            "frac_of_measured_sustained_peak": tf / sus if sus else None, "peak_sustained": sus,
+            "peak_source": f"{peak_src} bf16 matmul, back to back for seconds (fp16 has the same tensor rate)",
+            "clocks": sampler.region(h0, h1, ms / n)}
 
 
 def run_ours(args):
@@ -287,12 +461,10 @@ def run_ours(args):
 
 
     # ---- device-resident timing
-    sampler = ClockSampler(local, interval_ms=20)
-    sampler.start()
-    barrier()
-    total_ms, per_launch = time_device(g, A, B, C, w.relu, config, args.steps, args.warmup, stream)
-    barrier()
-    clocks = sampler.stop()
+    sampler = ClockSampler(local).start()
+    total_ms, per_launch, h0, h1 = time_device(g, A, B, C, w.relu, config, args.steps, args.warmup, stream,
+                                               barrier)
+    clocks = sampler.region(h0, h1, total_ms / args.steps)
     st = g.check(stream)
     if st != g.GEMM_OK:
         raise RuntimeError(f"device status {st}: {g.strerror(st)}")
@@ -440,6 +612,14 @@ def run_ours(args):
                                "flops_counted": "4 batch heads seq^2 dim (halved when causal)", "launches": reps_a}
             del Qa, Ka, Va, Oa
 
+    # ---- every configuration of the benchmark description (the shape sweep
+    # and the named sizes) and a seconds-long loop of the headline workload
+    sweep = sustained = None
+    if not args.no_secondary and world == 1:
+        sweep = run_sweep(g, dev, stream, peak, theoretical, sampler)
+        sustained = run_sustained(g, A, B, C, w, config, stream, sampler, args.sustained_s, peaks, peak_src,
+                                  theoretical)
+
     # ---- end to end through the host-buffer C call
     A_h = A_cpu.pin_memory()
     B_h = B_cpu.pin_memory()
@@ -458,6 +638,7 @@ def run_ours(args):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     e2e_value = whole_job_rate(w.flops, e2e_steps, world, e2e_ms)
 
+    sampler.stop()
     cpu_baseline = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu_baseline, _ = oracle_cpu_baseline(A_cpu, B_cpu, w.relu, args.cpu_budget, w.name, w.M)
@@ -467,9 +648,8 @@ def run_ours(args):
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-            "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "relu": w.relu,
-                       "values": "N(0,1)/sqrt(K) fp16" if w.values == "normal_scaled" else w.values,
-                       "seed": w.seed, "kernel_config": g.config_label(config), "accumulate": "f32",
+            "config": workload_config(w),
+            "kernel": {"config": g.config_label(config), "accumulate": "f32",
                        "l2": "inputs 384 MiB > 126 MB L2, no flush",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "frac_of_theoretical_peak": value / world / theoretical,
@@ -478,12 +658,7 @@ def run_ours(args):
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "traffic": recorded_traffic(w.name),
                          "peak_source": f"{peak_src} bf16 matmul burst (fp16 has the same tensor rate)",
-                         "avg_launch_ms": avg_launch_ms,
-                         # context: the same loop runs under the power cap, the regime of the
-                         # driver's seconds-long (sustained) bf16 measurement
-                         "peak_sustained": peaks.get("bf16_tflops_sustained"),
-                         "frac_sustained": (achieved / peaks["bf16_tflops_sustained"]
-                                            if peaks.get("bf16_tflops_sustained") else None)},
+                         "avg_launch_ms": avg_launch_ms},
             "e2e": {"value": e2e_value, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": int(A_h.numel() * 2 + B_h.numel() * 2),
                     "d2h_bytes_per_step": int(C_h.numel() * 2), "steps": e2e_steps},
@@ -499,6 +674,10 @@ def run_ours(args):
             line["fp8_block_scaled"] = fp8
         if attention is not None:
             line["attention_fwd"] = attention
+        if sweep is not None:
+            line["sweep"] = sweep
+        if sustained is not None:
+            line["sustained"] = sustained
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()
@@ -517,6 +696,7 @@ def main(argv=None):
     p.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-secondary", action="store_true")
+    p.add_argument("--sustained-s", type=float, default=2.5, help="seconds of the sustained headline loop")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be at least 3")

@@ -58,7 +58,6 @@ constexpr ConfigInfo kConfigs[] = {
     {"2sm_256x256_s6", Cfg2x256::SUPER_M, Cfg2x256::BN, 1},
     {"2sm_256x256_s7_direct", Cfg2x256d::SUPER_M, Cfg2x256d::BN, 0},
     {"2sm_256x512_s4", Cfg2x512::SUPER_M, Cfg2x512::BN, 1},
-    {"4sm_512x256_mc_s6", Cfg4x256mc::SUPER_M, Cfg4x256mc::BN, 0},
 };
 constexpr int kNumConfigs = static_cast<int>(sizeof(kConfigs) / sizeof(kConfigs[0])) - 1;
 
@@ -302,7 +301,6 @@ int config_info(int cfg, int64_t M, int64_t N, bool split, const DeviceInfo &dev
         case 3: return launch_info_config_3(M, N, split, dev, grid_ctas, cluster_size, tiles);
         case 4: return launch_info_config_4(M, N, split, dev, grid_ctas, cluster_size, tiles);
         case 5: return launch_info_config_5(M, N, split, dev, grid_ctas, cluster_size, tiles);
-        case 6: return launch_info_config_6(M, N, split, dev, grid_ctas, cluster_size, tiles);
         default: return GEMM_ERR_INVALID_ARG;
     }
 }
@@ -342,7 +340,6 @@ double wave_eff(int id, int64_t M, int64_t N, bool split, const DeviceInfo &dev)
         case 3: return wave_eff_config_3(M, N, split, dev);
         case 4: return wave_eff_config_4(M, N, split, dev);
         case 5: return wave_eff_config_5(M, N, split, dev);
-        case 6: return wave_eff_config_6(M, N, split, dev);
         default: return 0.0;
     }
 }
@@ -558,33 +555,21 @@ int run_gemm(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_
         a.k_splits = 1;
         a.k_split_tail = false;
     }
-    if (noalloc) {
-        // K-slice partials go to the library's fixed scratch: reject what does
-        // not fit before anything is launched.
-        const int64_t tm = kConfigs[cfg].tile_m, tn = kConfigs[cfg].tile_n;
-        const int64_t tiles = ((M + tm - 1) / tm) * ((N + tn - 1) / tn);
-        const KPlan kp = plan_k_split(tiles, config_slots(cfg, dev), (K + 63) / 64, a.k_splits, a.k_split_tail);
-        if (kp.ks.count > 1) {
-            float *scratch = nullptr;
-            size_t scratch_bytes = 0;
-            if ((st = noalloc_scratch(dev.device, &scratch, &scratch_bytes)) != GEMM_OK) return st;
-            const uint64_t need = static_cast<uint64_t>(kp.ws_floats(tiles, tm, tn)) * sizeof(float);
-            if (need > scratch_bytes)
-                return reject(GEMM_ERR_INVALID_ARG, "the K-slice partials exceed the 16 MiB scratch of "
-                                                    "gemm_f16_ex_noalloc");
-            a.fixed_ws = scratch;
-            a.fixed_ws_bytes = scratch_bytes;
-        }
-    }
+    // K-slice partials of a noalloc call go to the library's fixed scratch;
+    // the launch rejects a split that does not fit before it enqueues anything.
+    a.noalloc = noalloc;
     switch (cfg) {
-        case 1: return launch_config_1(a);
-        case 2: return launch_config_2(a);
-        case 3: return launch_config_3(a);
-        case 4: return launch_config_4(a);
-        case 5: return launch_config_5(a);
-        case 6: return launch_config_6(a);
+        case 1: st = launch_config_1(a); break;
+        case 2: st = launch_config_2(a); break;
+        case 3: st = launch_config_3(a); break;
+        case 4: st = launch_config_4(a); break;
+        case 5: st = launch_config_5(a); break;
         default: return GEMM_ERR_INVALID_ARG;
     }
+    if (st == GEMM_ERR_INVALID_ARG)
+        return reject(st, noalloc ? "the K-slice partials exceed the 16 MiB scratch of gemm_f16_ex_noalloc"
+                                  : "the problem has too many work units");
+    return st;
 }
 
 thread_local uint64_t t_last_timeout_record = 0;
@@ -627,6 +612,36 @@ extern "C" int gemm_f16_selftest_timeout(const void *A, const void *B, void *C, 
     hook.producer_off = 1;
     hook.timeout_cycles = timeout_cycles;
     return run_gemm(A, B, C, M, N, K, 0, 0, 1, config, stream, hook);
+}
+
+namespace gemm_sm103 {
+int tma_box_image_launch(const void *X, int64_t rows, int64_t cols, int box_rows, int x, int y, void *out,
+                         unsigned long long *status, cudaStream_t stream);
+}
+
+extern "C" int gemm_f16_tma_box_image(const void *X, int64_t rows, int64_t cols, int64_t box_rows, int64_t x,
+                                      int64_t y, void *out, void *stream)
+{
+    if (rows < 1 || cols < 1 || rows > INT32_MAX || cols > INT32_MAX)
+        return reject(GEMM_ERR_INVALID_ARG, "rows and cols must be 1 .. INT32_MAX");
+    if (box_rows < 1 || box_rows > 256) return reject(GEMM_ERR_INVALID_ARG, "box_rows must be 1 .. 256");
+    if (x < INT32_MIN || x > INT32_MAX || y < INT32_MIN || y > INT32_MAX)
+        return reject(GEMM_ERR_INVALID_ARG, "a box coordinate is outside the 32-bit range");
+    if ((cols % 8) != 0) return reject(GEMM_ERR_ALIGNMENT, "cols (the row pitch) is not a multiple of 8 elements");
+    if ((x % 8) != 0)
+        return reject(GEMM_ERR_ALIGNMENT, "x is not a multiple of 8 elements (a box starts on a 16-byte boundary)");
+    DeviceInfo dev;
+    int st = current_device_info(&dev);
+    if (st != GEMM_OK) return st;
+    const uint64_t x_bytes = static_cast<uint64_t>(rows) * static_cast<uint64_t>(cols) * 2u;
+    const uint64_t out_bytes = static_cast<uint64_t>(box_rows) * 128u;
+    if ((st = check_device_buffer(X, x_bytes, dev.device)) != GEMM_OK) return st;
+    if ((st = check_device_buffer(out, out_bytes, dev.device)) != GEMM_OK) return st;
+    if (ranges_overlap(out, out_bytes, X, x_bytes)) return reject(GEMM_ERR_INVALID_ARG, "out overlaps X");
+    unsigned long long *status = status_word(dev.device);
+    if (status == nullptr) return GEMM_ERR_CUDA;
+    return tma_box_image_launch(X, rows, cols, static_cast<int>(box_rows), static_cast<int>(x), static_cast<int>(y),
+                                out, status, static_cast<cudaStream_t>(stream));
 }
 
 namespace gemm_sm103 {

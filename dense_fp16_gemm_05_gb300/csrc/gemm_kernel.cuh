@@ -87,6 +87,7 @@ enum WaitSite : uint32_t {
     kSiteEpilogueTmemFull = 4,
     kSiteDrainLoads = 5,
     kSiteDrainMma = 6,
+    kSiteBoxImage = 7,   // the layout diagnostic's wait for its one box (tma_box_image.cu)
 };
 
 constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
@@ -98,18 +99,16 @@ constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
 //   kStages    depth of the shared-memory K ring
 //   kEpiSmem   true: stage C tiles in shared memory and store them with TMA;
 //              false: store C from registers (frees shared memory for a deeper ring)
-//   kPairs     CTA pairs per cluster (pair mode only).  The pairs of a cluster
-//              compute vertically adjacent tiles, so they need the same B
-//              columns: each B box is loaded once and multicast to all pairs.
-template <int kCtaGroup, int kBN, int kStages, bool kEpiSmem = true, int kPairs = 1>
+// Every CTA loads its operand boxes from global memory itself (no load is
+// shared across a cluster by multicast).
+template <int kCtaGroup, int kBN, int kStages, bool kEpiSmem = true>
 struct GemmCfg {
     static constexpr int CTA_GROUP = kCtaGroup;
-    static constexpr int PAIRS = kPairs;
-    static constexpr int CLUSTER = CTA_GROUP * PAIRS;   // CTAs per cluster
+    static constexpr int CLUSTER = CTA_GROUP;         // CTAs per cluster (the pair, or one CTA)
     static constexpr bool EPI_SMEM = kEpiSmem;
     static constexpr int BM = 128;                    // rows of C per CTA = TMEM lanes
     static constexpr int TILE_M = BM * CTA_GROUP;     // rows of C per MMA tile (the MMA's M)
-    static constexpr int SUPER_M = TILE_M * PAIRS;    // rows of C per work unit (one per cluster)
+    static constexpr int SUPER_M = TILE_M;            // rows of C per work unit (one per cluster)
     static constexpr int BN = kBN;
     static constexpr int UMMA_N = BN < 256 ? BN : 256;   // N of one MMA instruction
     static constexpr int N_MMAS = BN / UMMA_N;        // MMAs per K step
@@ -140,7 +139,6 @@ struct GemmCfg {
     static constexpr uint32_t IDESC = idesc_f16_f32(TILE_M, UMMA_N, /*A MN-major*/ false, /*B MN-major*/ true);
 
     static_assert(CTA_GROUP == 1 || CTA_GROUP == 2, "one CTA or a CTA pair");
-    static_assert(PAIRS == 1 || (PAIRS == 2 && CTA_GROUP == 2), "multicast clusters are made of CTA pairs");
     static_assert(BN % (B_BOX_N * CTA_GROUP) == 0 && BN <= 512, "whole B boxes per CTA; at most 512 TMEM columns");
     static_assert(UMMA_N % 16 == 0 && UMMA_N <= 256, "UMMA N: multiple of 16 up to 256");
     static_assert(TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation is a power of 2");
@@ -277,12 +275,17 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                  : "memory");
 }
 
+// R(x) of the epilogue.  Without ReLU the value is x + (+0): the pages' tile
+// GEMM clears its accumulator to +0 before adding the products, and
+// +0 + (-0) = +0, so a sum whose terms are all -0 is +0 (the MMA's first
+// product with accumulate = 0 does not add that +0 itself).  No other value
+// changes.
 template <bool kRelu>
 __device__ __forceinline__ float epilogue_value(uint32_t bits)
 {
     const float x = __uint_as_float(bits);
     if constexpr (kRelu) return x > 0.0f ? x : 0.0f;  // -0, NaN and negatives give +0
-    else return x;
+    else return __fadd_rn(x, 0.0f);
 }
 
 template <bool kRelu>
@@ -337,16 +340,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     const int lane = threadIdx.x & 31;
     const uint32_t crank = Cfg::CLUSTER > 1 ? cluster_ctarank() : 0u;   // rank in the cluster
     const uint32_t rank = kPair ? (crank & 1u) : 0u;                    // rank in the pair; 0 = leader
-    const uint32_t pair = kPair ? (crank >> 1) : 0u;                     // pair within the cluster
-    const uint32_t leader_rank = crank & ~1u;                             // cluster rank of the pair's leader
+    const uint32_t leader_rank = 0u;                                      // cluster rank of the pair's leader
     const bool leader = rank == 0;
     const int cluster_id = static_cast<int>(blockIdx.x) / Cfg::CLUSTER;
     const int num_clusters = static_cast<int>(gridDim.x) / Cfg::CLUSTER;
-    // Cluster ranks with the same half (rank) in every pair: the B multicast set.
-    uint16_t same_half_mask = 0;
-    for (int i = 0; i < Cfg::PAIRS; ++i) same_half_mask |= static_cast<uint16_t>(1u << (2 * i + rank));
-    const uint16_t pair_mask = static_cast<uint16_t>(0x3u << (2 * pair));
-    const uint16_t all_mask = static_cast<uint16_t>((1u << Cfg::CLUSTER) - 1u);
+    const uint16_t pair_mask = 0x3u;   // both CTAs of the pair
 
     AbortFlag abort;
     abort.local = reinterpret_cast<volatile int *>(tmem_slot_ptr + 1);
@@ -358,7 +356,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < Cfg::STAGES; ++s) {
             mbar_init(full_bar(s), Cfg::CTA_GROUP);   // each CTA of the pair: arrive.expect_tx
-            mbar_init(empty_bar(s), Cfg::PAIRS);      // one MMA commit per pair of the cluster
+            mbar_init(empty_bar(s), 1);               // one MMA commit (by the pair leader)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull_bar(b), 1);                       // commit after a tile's last MMA
@@ -413,8 +411,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 int mb, col0, shift, kb0, kb1, slice;
                 unit_coords<Cfg::BN>(u, p, mb, col0, shift);
                 unit_k_range(u, p, kb0, kb1, slice);
-                const int m0 = mb * Cfg::SUPER_M + static_cast<int>(pair) * Cfg::TILE_M +
-                               static_cast<int>(rank) * Cfg::BM;
+                const int m0 = mb * Cfg::SUPER_M + static_cast<int>(rank) * Cfg::BM;
                 // Unit width W = BN >> shift, issued as W / umma_n MMAs of N = umma_n.
                 // For MMA h, this CTA supplies umma_n / CTA_GROUP columns (bpm boxes),
                 // starting at tile column h * umma_n + rank * umma_n / CTA_GROUP.
@@ -476,15 +473,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         for (int j = 0; j < Cfg::B_BOXES; ++j) {
                             if (j < boxes) {
                                 const int bx = kTB ? k0 : bxs[j], by = kTB ? bxs[j] : k0;
-                                if constexpr (Cfg::PAIRS == 1) {
-                                    tma_load_2d_pair(b_dst + j * Cfg::B_BOX_BYTES, &tmap_b, fb, bx, by);
-                                } else {
-                                    // Box j is loaded by pair j % PAIRS and multicast to the
-                                    // same-half CTA of every pair.
-                                    if (j % Cfg::PAIRS == static_cast<int>(pair))
-                                        tma_load_2d_pair_mc(b_dst + j * Cfg::B_BOX_BYTES, &tmap_b, fb, bx, by,
-                                                            same_half_mask);
-                                }
+                                tma_load_2d_pair(b_dst + j * Cfg::B_BOX_BYTES, &tmap_b, fb, bx, by);
                             }
                         }
                     }
@@ -566,11 +555,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         }
                     }
                 };
-                // Frees slot st once the MMAs issued so far have read it: in both CTAs
-                // of the pair, and in every CTA of the cluster when B boxes are shared
-                // (another pair's multicast writes this pair's slots too).
+                // Frees slot st once the MMAs issued so far have read it, in both CTAs
+                // of the pair.
                 auto release = [&](int st) {
-                    if constexpr (kPair) mma_commit_pair_mc(empty_bar(st), Cfg::PAIRS > 1 ? all_mask : pair_mask);
+                    if constexpr (kPair) mma_commit_pair_mc(empty_bar(st), pair_mask);
                     else mma_commit(empty_bar(st));
                 };
                 int kb = kb0;
@@ -675,8 +663,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             }
             if (it == 0) griddep_wait();   // before this warp's first store of C (or of partials)
             tc_fence_after_sync();
-            const int row0 = mb * Cfg::SUPER_M + static_cast<int>(pair) * Cfg::TILE_M +
-                             static_cast<int>(rank) * Cfg::BM + q * 32;
+            const int row0 = mb * Cfg::SUPER_M + static_cast<int>(rank) * Cfg::BM + q * 32;
             const uint32_t acc_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * Cfg::ACC_COLS;
             // Chunk c (64 columns) of the accumulator: hand back TMEM when this
             // warp's reads of it are complete, then convert and store it.

@@ -46,8 +46,9 @@ struct LaunchArgs {
     int k_splits = 1;          // > 1: split every tile's K loop into (up to) this many slices,
                                // fp32 partials in a stream-ordered workspace, then a reduction
     bool k_split_tail = false; // split only the tiles of a partly filled last wave in K
-    float *fixed_ws = nullptr; // non-null: the K-slice workspace to use instead (the caller
-    size_t fixed_ws_bytes = 0; // checked that it is large enough)
+    bool noalloc = false;      // never allocate: K-slice partials go to the library's fixed
+                               // scratch (noalloc_scratch); a split that does not fit it is
+                               // rejected before anything is launched
 };
 
 // Defined in gemm_f16.cu.
@@ -248,12 +249,15 @@ int launch_one(const LaunchArgs &a)
     Schedule sc = make_schedule<Cfg>(a.M, a.N, slots, a.allow_split && a.k_splits <= 1 && !a.k_split_tail);
     KPlan kp = plan_k_split(sc.tiles, slots, p.num_k_blocks, a.k_splits, a.k_split_tail);
     float *ws = nullptr;
-    const bool own_ws = a.fixed_ws == nullptr;
+    const bool own_ws = !a.noalloc;
     if (kp.ks.count > 1) {
+        // The workspace check is made on the plan this launch runs, before
+        // anything is enqueued.
         const size_t need = static_cast<size_t>(kp.ws_floats(sc.tiles, Cfg::SUPER_M, Cfg::BN)) * sizeof(float);
-        if (!own_ws) {
-            if (need > a.fixed_ws_bytes) return GEMM_ERR_INVALID_ARG;   // checked by the caller first
-            ws = a.fixed_ws;
+        if (a.noalloc) {
+            size_t have = 0;
+            if (noalloc_scratch(a.dev.device, &ws, &have) != GEMM_OK) return GEMM_ERR_CUDA;
+            if (need > have) return GEMM_ERR_INVALID_ARG;
         } else if (cudaMallocAsync(reinterpret_cast<void **>(&ws), need, a.stream) != cudaSuccess) {
             // Stream-ordered workspace: ordered with this call's kernels, private
             // to it, and legal inside a stream capture.  If it cannot be had, the
@@ -399,7 +403,6 @@ GEMM_DECLARE_CONFIG(2)
 GEMM_DECLARE_CONFIG(3)
 GEMM_DECLARE_CONFIG(4)
 GEMM_DECLARE_CONFIG(5)
-GEMM_DECLARE_CONFIG(6)
 #undef GEMM_DECLARE_CONFIG
 
 // The configurations, by id (1-based).
@@ -408,6 +411,5 @@ using Cfg1x128 = GemmCfg<1, 128, 6>;
 using Cfg2x256 = GemmCfg<2, 256, 6>;
 using Cfg2x256d = GemmCfg<2, 256, 7, /*stage C in smem*/ false>;
 using Cfg2x512 = GemmCfg<2, 512, 4>;
-using Cfg4x256mc = GemmCfg<2, 256, 6, /*stage C in smem*/ true, /*pairs sharing B*/ 2>;
 
 }  // namespace gemm_sm103

@@ -156,20 +156,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
-// Pair-mode load multicast to every CTA of the cluster named in `cta_mask`
-// (bit i = cluster rank i), at the same shared-memory offset `dst` in each.
-// Completion is counted on the barrier at the offset of `bar` in the even
-// (leader) CTA of each destination CTA's pair.
-__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const CUtensorMap *map, uint32_t bar, int32_t x,
-                                                    int32_t y, uint16_t cta_mask)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "h"(cta_mask)
-        : "memory");
-}
-
 // 2-D tiled store of one box from this CTA's shared memory; out-of-range
 // elements of the box are not written.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int32_t x, int32_t y)

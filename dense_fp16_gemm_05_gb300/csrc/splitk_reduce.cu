@@ -27,7 +27,7 @@ template <bool kRelu>
 __device__ __forceinline__ float reduce_out(float x)
 {
     if constexpr (kRelu) return x > 0.0f ? x : 0.0f;   // -0, NaN and negatives give +0
-    else return x;
+    else return __fadd_rn(x, 0.0f);                       // the cleared accumulator: -0 sums give +0
 }
 
 template <bool kRelu>

@@ -113,6 +113,8 @@ def lib() -> ctypes.CDLL:
     L.gemm_fp8_launch_info.restype = ci
     L.gemm_f16_launch_info.argtypes = [i64, i64, i64, ci, pi, pi, pi]
     L.gemm_f16_launch_info.restype = ci
+    L.gemm_f16_tma_box_image.argtypes = [vp, i64, i64, i64, i64, i64, vp, vp]
+    L.gemm_f16_tma_box_image.restype = ci
     _lib = L
     return L
 
@@ -300,6 +302,22 @@ def relu_backward(dC: torch.Tensor, C: torch.Tensor, dZ: torch.Tensor | None = N
     if st != GEMM_OK:
         raise GemmError(st, "gemm_f16_relu_backward")
     return dZ
+
+
+def tma_box_image(X: torch.Tensor, box_rows: int, x: int, y: int, stream=None) -> torch.Tensor:
+    """Raw shared-memory image (uint8, box_rows * 128 bytes) of one box of
+    box_rows x 64 elements of the 2-D fp16 tensor X at column x, row y, loaded
+    by TMA with the GEMM's operand encoding (gemm_f16_tma_box_image)."""
+    _check_operand(X, "X")
+    rows, cols = X.shape
+    out = torch.empty(int(box_rows) * 128, dtype=torch.uint8, device=X.device)
+    L = lib()
+    with _device_scope(X.device):
+        st = L.gemm_f16_tma_box_image(X.data_ptr(), rows, cols, int(box_rows), int(x), int(y), out.data_ptr(),
+                                      _stream_handle(stream, X.device))
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_f16_tma_box_image")
+    return out
 
 
 def config_layouts(config: int) -> int:

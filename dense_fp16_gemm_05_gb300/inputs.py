@@ -61,6 +61,24 @@ def draw_workload(w: Workload) -> tuple[torch.Tensor, torch.Tensor]:
     return draw(w.M, w.N, w.K, w.values, w.seed)
 
 
+def draw_on_device(M: int, N: int, K: int, values: str, seed: int,
+                   device: torch.device) -> tuple[torch.Tensor, torch.Tensor]:
+    """The ``normal`` / ``normal_scaled`` recipe drawn by a seeded generator on
+    ``device`` (same distribution as ``draw``, other bits): for timing runs
+    whose operands are too large to draw quickly on the host and that compare
+    nothing against the oracle."""
+    if values not in ("normal", "normal_scaled"):
+        raise ValueError(f"device drawing supports the normal recipes, not {values!r}")
+    g = torch.Generator(device=device).manual_seed(int(seed))
+    a = torch.randn(M, K, generator=g, dtype=torch.float32, device=device)
+    b = torch.randn(K, N, generator=g, dtype=torch.float32, device=device)
+    if values == "normal_scaled" and K > 0:
+        s = torch.tensor(1.0 / math.sqrt(K), dtype=torch.float32, device=device)
+        a = a * s
+        b = b * s
+    return a.half(), b.half()
+
+
 # The five configurations of the benchmark description, with their seeds.
 WORKLOADS: dict[str, Workload] = {
     "relu_1024": Workload("relu_1024", 1024, 1024, 1024, True, "normal", 1),

@@ -366,6 +366,37 @@ int gemm_f16_check(void *stream);
 int gemm_f16_selftest_timeout(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
                               int config, uint64_t timeout_cycles, void *stream);
 
+/*
+ * gemm_f16_tma_box_image -- layout diagnostic (nothing in the GEMM calls it).
+ * Loads one box of box_rows x 64 binary16 values (128 bytes per row) at column
+ * x, row y of the row-major matrix X (rows x cols) into shared memory exactly
+ * as the GEMM loads its operand tiles -- the same tensor-map encoding (128-byte
+ * swizzle, elements outside X read as zero) and the same TMA instruction --
+ * and copies the raw shared-memory image, box_rows * 128 bytes, to `out`.
+ * With the 128-byte swizzle, element (y + r, x + c) of X sits at byte
+ * r * 128 + ((c / 8) ^ (r % 8)) * 16 + (c % 8) * 2 of the image, the layout
+ * the GEMM's MMA descriptors read.  The pages discuss shared-memory tile
+ * layout and bank conflicts ("Writing High-Performance Kernels in TileLang,
+ * from GEMM to MLA"; the nxmr.cn A100 article, sections 3.3 and 6.2, where a
+ * layout that disagrees with the copy's swizzle misplaces data by 16 bytes);
+ * this call lets a test check that layout directly.
+ *
+ *   X         device pointer, rows * cols binary16 values, 16-byte aligned
+ *   rows,cols 1 .. INT32_MAX; cols % 8 == 0 (GEMM_ERR_ALIGNMENT)
+ *   box_rows  1 .. 256
+ *   x, y      box origin (column, row); may lie partly or wholly outside X
+ *             (negative too); x % 8 == 0 (a box starts on a 16-byte
+ *             boundary, GEMM_ERR_ALIGNMENT)
+ *   out       device pointer to box_rows * 128 bytes, 16-byte aligned, not
+ *             overlapping X; written
+ *
+ * Asynchronous on `stream`; a load that does not land within its wait bound
+ * is reported by gemm_f16_check (GEMM_ERR_TIMEOUT, site 7) and leaves `out`
+ * unwritten.
+ */
+int gemm_f16_tma_box_image(const void *X, int64_t rows, int64_t cols, int64_t box_rows, int64_t x, int64_t y,
+                           void *out, void *stream);
+
 /* Raw value of the last timeout record read by gemm_f16_check on this thread
  * (0 if none): bits 0-7 the wait site, bits 8-31 the block index. */
 uint64_t gemm_f16_last_timeout_record(void);

@@ -40,7 +40,7 @@ def g():
 
 def chain_configs(g):
     k = g.ksplit
-    return [0, 2, 3 | k(4), 5, 1 | k(3), 4, 6, 2 | k(2), 0, 5, 3, 1 | k(4)]
+    return [0, 2, 3 | k(4), 5, 1 | k(3), 4, 5 | k(2), 2 | k(2), 0, 5, 3, 1 | k(4)]
 
 
 @pytest.mark.parametrize("graph", [False, True])

@@ -78,11 +78,32 @@ def test_int64_bit_exact(g, relu):
     ref = oracle.gemm_f16(A, B, relu=relu)
     for cfg in configs(g):
         got = run(g, A, B, relu, cfg)
-        if relu:
-            assert np.array_equal(got.view(np.uint16), ref.view(np.uint16)), cfg
-        else:
-            # the sign of an exact zero sum is not fixed by the definition
-            assert np.array_equal(got.astype(np.float64), ref.astype(np.float64)), cfg
+        # bit for bit, zero signs included: every exact zero sum is +0 (the
+        # accumulator starts at +0), with or without ReLU
+        assert np.array_equal(got.view(np.uint16), ref.view(np.uint16)), cfg
+
+
+@pytest.mark.parametrize("ksplit", [0, 3])
+def test_zero_sums_are_plus_zero_without_relu(g, ksplit):
+    # Sums that are exactly zero: all terms -0 (a -0 row times a positive
+    # column), exact cancellation of +-1 terms, and zeros mixed in.  The
+    # oracle's sum starts at +0 (the cleared accumulator of the pages' tile
+    # GEMM), so each of these is +0 (0x0000); a -0 would fail the bit test.
+    M, N, K = 300, 264, 448
+    rng = np.random.default_rng(81)
+    a = rng.integers(-4, 5, (M, K)).astype(np.float16)
+    b = rng.integers(-4, 5, (K, N)).astype(np.float16)
+    a[0::3, :] = np.float16(-0.0)                          # every product -0 against b >= 0
+    b[:, 0::2] = np.abs(b[:, 0::2])
+    a[1::3, :] = np.where(np.arange(K) % 2 == 0, 1.0, -1.0).astype(np.float16)
+    b[:, 1::4] = 1.0                                       # alternating +-1 terms cancel exactly
+    A, B = torch.from_numpy(a), torch.from_numpy(b)
+    ref = oracle.gemm_f16(A, B, relu=False)
+    assert np.count_nonzero(ref.view(np.uint16) == 0) > M * N // 6
+    assert not np.any(ref.view(np.uint16) == 0x8000)
+    for cfg in configs(g):
+        got = run(g, A, B, False, cfg | (g.ksplit(ksplit) if ksplit else 0))
+        assert np.array_equal(got.view(np.uint16), ref.view(np.uint16)), (cfg, ksplit)
 
 
 def test_relu_1024_full(g):

@@ -1,11 +1,19 @@
-"""GPU test of gemm_f16_ex_noalloc, the entry point whose K-slice partials
-live in the library's fixed 16 MiB device scratch instead of an allocation.
+"""GPU test of gemm_f16_ex_noalloc, the GEMM entry point that never allocates.
+
+Some callers of a GEMM may not allocate device memory while they run: code
+that reserved its whole memory budget up front (a serving process whose pool
+already holds the GPU's memory, where a stream-ordered allocation from the
+default pool can fail), plug-ins whose host framework forbids allocation in
+their execute step, and latency-bound loops that must not go through the
+allocator at all.  For them the K-slice partials of a split GEMM live in the
+library's fixed 16 MiB device scratch instead of a per-call workspace.
 
 Collected last (file name) so that it also runs after every other GPU test in
-the same process; it passes alone as well.  Two consecutive calls on
-different problems must each give exactly the bits of gemm_f16_ex with the
-same configuration (same kernels, same slice order), so stale scratch
-contents from an earlier call can never leak into a result.
+the same process; it passes alone as well.  Every call must give exactly the
+bits of gemm_f16_ex with the same configuration (same kernels, same slice
+order), also when several calls follow each other on one stream with no
+synchronisation in between, so stale scratch contents from an earlier call
+can never leak into a result.
 """
 from __future__ import annotations
 
@@ -75,3 +83,44 @@ def test_oversize_split_is_rejected_before_launch(g):
     torch.cuda.synchronize()
     assert torch.all(C == 3.0)
     assert g.check() == g.GEMM_OK
+
+
+def test_back_to_back_calls_without_sync(g):
+    # three different split problems enqueued one after the other on one
+    # stream: each GEMM's slices overwrite the scratch the previous call's
+    # reduction read, which stream order (and the kernels' dependency waits)
+    # must keep apart
+    k = g.ksplit
+    sms = torch.cuda.get_device_properties(DEV).multi_processor_count
+    # a tail split on the 128 x 128 configuration: one full wave of tiles, then
+    # a remainder of about a third of the slots, cut into K slices
+    m_tail = 128 * ((sms + sms // 3) // 8 + 1)
+    tiles = (m_tail // 128) * 8
+    rest = tiles - sms
+    assert 2 <= sms // rest and rest * min(sms // rest, 5) * 128 * 128 * 4 <= 16 << 20
+    problems = [(1024, 1024, 4096, 2 | k(4), 11, True),
+                (m_tail, 1024, 3000, 2 | g.GEMM_F16_KSPLIT_TAIL, 12, False),
+                (512, 768, 8192, 3 | k(8), 13, True)]
+    ins, refs = [], []
+    for (M, N, K, cfg, seed, relu) in problems:
+        A, B = (x.to(DEV) for x in draw(M, N, K, "normal_scaled", seed))
+        ins.append((A, B, torch.full((M, N), 7.0, dtype=torch.float16, device=DEV)))
+        refs.append(g.gemm_f16(A, B, relu=relu, config=cfg))
+    assert g.check() == g.GEMM_OK
+    for (A, B, C), (M, N, K, cfg, seed, relu) in zip(ins, problems):
+        g.gemm_f16_noalloc(A, B, C, relu=relu, config=cfg)
+    assert g.check() == g.GEMM_OK
+    for (A, B, C), ref, prob in zip(ins, refs, problems):
+        assert torch.equal(C.view(torch.int16), ref.view(torch.int16)), prob
+
+
+def test_automatic_choice_uses_the_scratch(g):
+    # 1024 x 1024 x 16384: configuration 0 cuts K (the table's choice for
+    # few-tile, deep problems); the partials then fill the scratch exactly
+    cfg = g.auto_config(1024, 1024, 16384)
+    A, B = (x.to(DEV) for x in draw(1024, 1024, 16384, "normal_scaled", 14))
+    ref = g.gemm_f16(A, B, relu=True, config=cfg)
+    C = torch.empty_like(ref)
+    g.gemm_f16_noalloc(A, B, C, relu=True, config=0)
+    assert g.check() == g.GEMM_OK
+    assert torch.equal(C.view(torch.int16), ref.view(torch.int16)), hex(cfg)
