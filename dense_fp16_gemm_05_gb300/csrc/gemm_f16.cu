@@ -58,7 +58,10 @@ constexpr ConfigInfo kConfigs[] = {
     {"2sm_256x256_s6", Cfg2x256::SUPER_M, Cfg2x256::BN, 1},
     {"2sm_256x256_s7_direct", Cfg2x256d::SUPER_M, Cfg2x256d::BN, 0},
     {"2sm_256x512_s4", Cfg2x512::SUPER_M, Cfg2x512::BN, 1},
+    {"1sm_128x128_ck_s6", Cfg1x128ck::SUPER_M, Cfg1x128ck::BN, 0},
 };
+// The configuration whose K split runs across a cluster (no workspace).
+constexpr int kClusterKConfig = 6;
 constexpr int kNumConfigs = static_cast<int>(sizeof(kConfigs) / sizeof(kConfigs[0])) - 1;
 
 // ---------------------------------------------------------------- driver entry points
@@ -301,6 +304,7 @@ int config_info(int cfg, int64_t M, int64_t N, bool split, const DeviceInfo &dev
         case 3: return launch_info_config_3(M, N, split, dev, grid_ctas, cluster_size, tiles);
         case 4: return launch_info_config_4(M, N, split, dev, grid_ctas, cluster_size, tiles);
         case 5: return launch_info_config_5(M, N, split, dev, grid_ctas, cluster_size, tiles);
+        case 6: return launch_info_config_6(M, N, split, dev, grid_ctas, cluster_size, tiles);
         default: return GEMM_ERR_INVALID_ARG;
     }
 }
@@ -340,46 +344,26 @@ double wave_eff(int id, int64_t M, int64_t N, bool split, const DeviceInfo &dev)
         case 3: return wave_eff_config_3(M, N, split, dev);
         case 4: return wave_eff_config_4(M, N, split, dev);
         case 5: return wave_eff_config_5(M, N, split, dev);
+        case 6: return wave_eff_config_6(M, N, split, dev);
         default: return 0.0;
     }
 }
 
-// Wave efficiency of configuration `id` with GEMM_F16_KSPLIT_AUTO: whole tiles
-// in rule_k_splits slices, or the plain schedule (tail split allowed) when the
-// rule does not split.
-double ksplit_wave_eff(int id, int64_t M, int64_t N, int64_t K, const DeviceInfo &dev)
+// Cluster size request of a config word for the cluster K split configuration:
+// GEMM_F16_KSPLIT(n) asks for n CTAs per cluster, GEMM_F16_NO_KSPLIT for one,
+// anything else for the size rule (0).
+int ck_request_of(int word)
 {
-    const KSplit kk = k_split_for((K + 63) / 64, rule_k_splits(id, M, N, K, dev));
-    if (kk.count < 2) return wave_eff(id, M, N, true, dev);
-    int grid = 0, cluster = 1, tiles = 0;
-    if (config_info(id, M, N, false, dev, &grid, &cluster, &tiles) != GEMM_OK) return 0.0;
-    const int64_t slots = config_slots(id, dev);
-    const int64_t units = static_cast<int64_t>(tiles) * kk.count;
-    if (slots <= 0 || units <= 0) return 0.0;
-    const int64_t waves = (units + slots - 1) / slots;
-    return static_cast<double>(units) / static_cast<double>(waves * slots);
-}
-
-// Wave efficiency of configuration `id` with GEMM_F16_KSPLIT_TAIL: full waves
-// of whole tiles, then the last wave's tiles in K slices (time in tile units:
-// full waves + ceil(slices of the tail / slots) / slices).
-double tail_wave_eff(int id, int64_t M, int64_t N, int64_t K, const DeviceInfo &dev)
-{
-    int grid = 0, cluster = 1, tiles = 0;
-    if (config_info(id, M, N, false, dev, &grid, &cluster, &tiles) != GEMM_OK) return 0.0;
-    const int64_t slots = config_slots(id, dev);
-    if (slots <= 0 || tiles <= 0) return 0.0;
-    const KPlan kp = plan_k_split(tiles, slots, (K + 63) / 64, 1, true);
-    if (kp.ks.count < 2) return wave_eff(id, M, N, false, dev);
-    const int64_t full_waves = kp.ks_start / slots;
-    const int64_t tail_units = (tiles - kp.ks_start) * kp.ks.count;
-    const double time = static_cast<double>(full_waves) +
-                        static_cast<double>((tail_units + slots - 1) / slots) / static_cast<double>(kp.ks.count);
-    return static_cast<double>(tiles) / (static_cast<double>(slots) * time);
+    const int n = (word & GEMM_F16_KSPLIT_MASK) >> GEMM_F16_KSPLIT_SHIFT;
+    if (n >= 2) return n;
+    if (word & GEMM_F16_NO_KSPLIT) return 1;
+    return 0;
 }
 
 // The automatic choice.  The offline sweep (tune.py) measured every candidate
-// (configuration x tail policy) on a grid of shapes.  For a problem, take the
+// (configuration x tail policy, and the cluster K split's sizes) on a grid of
+// shapes.  None of the candidates allocates memory: a workspace K split is
+// taken only on an explicit request (gemm_f16_ex with the K-split bits).  For a problem, take the
 // nearest measured shape in log2 space (K weighted by half: it changes the
 // per-tile work but not the wave count), scale each candidate's measured
 // throughput by its wave efficiency here over its wave efficiency there, and
@@ -418,14 +402,12 @@ int select_config(int64_t M, int64_t N, int64_t K, bool any_layout, const Device
         const int id = c & GEMM_F16_CONFIG_ID_MASK;
         if (id < 1 || id > kNumConfigs || (any_layout && !kConfigs[id].all_layouts)) continue;
         const bool split = (c & GEMM_F16_NO_SPLIT) == 0;
-        const bool krule = (c & GEMM_F16_KSPLIT_AUTO) != 0;
-        const bool ktail = (c & GEMM_F16_KSPLIT_TAIL) != 0;
-        const double here = krule   ? ksplit_wave_eff(id, M, N, K, dev)
-                            : ktail ? tail_wave_eff(id, M, N, K, dev)
-                                    : wave_eff(id, M, N, split, dev);
-        const double there = krule   ? ksplit_wave_eff(id, t.M, t.N, t.K, dev)
-                             : ktail ? tail_wave_eff(id, t.M, t.N, t.K, dev)
-                                     : wave_eff(id, t.M, t.N, split, dev);
+        const bool ck = id == kClusterKConfig;
+        // The automatic choice allocates nothing: no workspace K split.
+        if (!ck && (c & (GEMM_F16_KSPLIT_AUTO | GEMM_F16_KSPLIT_TAIL | GEMM_F16_KSPLIT_MASK)) != 0) continue;
+        const double here = ck ? ck_wave_eff_config_6(M, N, K, ck_request_of(c), dev) : wave_eff(id, M, N, split, dev);
+        const double there =
+            ck ? ck_wave_eff_config_6(t.M, t.N, t.K, ck_request_of(c), dev) : wave_eff(id, t.M, t.N, split, dev);
         if (here <= 0.0 || there <= 0.0) continue;
         // (ratio first: exactly 1 on a measured shape, so ties keep table order)
         const double predicted = static_cast<double>(t.tflops[i]) * (here / there);
@@ -444,8 +426,7 @@ int select_config(int64_t M, int64_t N, int64_t K, bool any_layout, const Device
 }
 
 // K-split requests of a config word (parse_config's *k_request).
-constexpr int kKsplitNone = 0;     // no K-split bit set
-constexpr int kKsplitNever = -1;   // GEMM_F16_NO_KSPLIT
+constexpr int kKsplitNever = -1;   // GEMM_F16_NO_KSPLIT (0: no K-split bit set)
 constexpr int kKsplitRule = -2;    // GEMM_F16_KSPLIT_AUTO
 constexpr int kKsplitTail = -3;    // GEMM_F16_KSPLIT_TAIL
                                    // n >= 2: GEMM_F16_KSPLIT(n)
@@ -470,14 +451,12 @@ bool parse_config(int config, int *id, bool *allow_split, int *k_request = nullp
     return *id <= kNumConfigs;
 }
 
-// Slice count for a parsed request on configuration `cfg` (id: the id the
-// caller gave, 0 = automatic; picked: the automatic choice's config word).
-int k_splits_for(int k_request, int id, int picked, int cfg, int64_t M, int64_t N, int64_t K,
-                 const DeviceInfo &dev)
+// Workspace slice count for a parsed request on configuration `cfg` (the
+// automatic choice never asks for one).
+int k_splits_for(int k_request, int cfg, int64_t M, int64_t N, int64_t K, const DeviceInfo &dev)
 {
     if (k_request >= 2) return k_request;
-    if (k_request == kKsplitRule || (k_request == kKsplitNone && id == 0 && (picked & GEMM_F16_KSPLIT_AUTO)))
-        return rule_k_splits(cfg, M, N, K, dev);
+    if (k_request == kKsplitRule) return rule_k_splits(cfg, M, N, K, dev);
     return 1;
 }
 
@@ -547,9 +526,22 @@ int run_gemm(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_
     } else {
         a.allow_split = allow_split;
     }
-    a.k_splits = k_splits_for(k_request, id, picked, cfg, M, N, K, dev);
-    a.k_split_tail = k_request == kKsplitTail ||
-                     (k_request == kKsplitNone && id == 0 && (picked & GEMM_F16_KSPLIT_TAIL) != 0);
+    if (cfg == kClusterKConfig) {
+        // The K split runs across the cluster: its size from the config word
+        // (or from the automatic choice's word), no workspace.
+        if (k_request == kKsplitTail)
+            return reject(GEMM_ERR_INVALID_ARG, "the cluster K split configuration has no tail split");
+        a.ck_request = id == 0 ? ck_request_of(picked)
+                       : k_request >= 2 ? k_request
+                       : k_request == kKsplitNever ? 1 : 0;
+        if (a.ck_request != 0 && a.ck_request != 1 && a.ck_request != 2 && a.ck_request != 4 && a.ck_request != 8)
+            return reject(GEMM_ERR_INVALID_ARG, "a cluster K split takes 2, 4 or 8 CTAs per cluster");
+        a.k_splits = 1;
+        a.k_split_tail = false;
+    } else {
+        a.k_splits = k_splits_for(k_request, cfg, M, N, K, dev);
+        a.k_split_tail = k_request == kKsplitTail;
+    }
     if (hook.producer_off) {
         // the timeout self-test never writes C
         a.k_splits = 1;
@@ -564,6 +556,7 @@ int run_gemm(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_
         case 3: st = launch_config_3(a); break;
         case 4: st = launch_config_4(a); break;
         case 5: st = launch_config_5(a); break;
+        case 6: st = launch_config_6(a); break;
         default: return GEMM_ERR_INVALID_ARG;
     }
     if (st == GEMM_ERR_INVALID_ARG)
@@ -782,6 +775,15 @@ extern "C" int gemm_f16_config_layouts(int config)
     return kConfigs[id].all_layouts ? 0xF : 0x1;
 }
 
+extern "C" int gemm_f16_config_cluster_k(int config)
+{
+    int id = 0;
+    bool allow_split = true;
+    if (!parse_config(config, &id, &allow_split))
+        return reject(GEMM_ERR_INVALID_ARG, "unknown configuration id or flag");
+    return id == kClusterKConfig ? 1 : 0;
+}
+
 extern "C" int gemm_f16_auto_config(int64_t M, int64_t N, int64_t K)
 {
     int st = check_sizes(M, N, K, 0);
@@ -790,11 +792,13 @@ extern "C" int gemm_f16_auto_config(int64_t M, int64_t N, int64_t K)
     if ((st = current_device_info(&dev)) != GEMM_OK) return st;
     const int picked = select_config(M, N, K, false, dev);
     const int cfg = picked & GEMM_F16_CONFIG_ID_MASK;
-    const int ks = k_splits_for(kKsplitNone, 0, picked, cfg, M, N, K, dev);
-    const KSplit kk = k_split_for((K + 63) / 64, ks);
-    // The rule resolved for this problem: gemm_f16_ex computes the same with it.
-    const int base = picked & ~GEMM_F16_KSPLIT_AUTO;
-    return kk.count >= 2 ? (base | GEMM_F16_NO_SPLIT | GEMM_F16_KSPLIT(kk.count)) : base;
+    if (cfg == kClusterKConfig) {
+        // The cluster size resolved for this problem.
+        int cluster = 1;
+        ck_launch_info_config_6(M, N, K, ck_request_of(picked), dev, nullptr, &cluster, nullptr);
+        return cfg | (cluster >= 2 ? GEMM_F16_KSPLIT(cluster) : GEMM_F16_NO_KSPLIT);
+    }
+    return picked;
 }
 
 extern "C" int gemm_f16_launch_info(int64_t M, int64_t N, int64_t K, int config, int *grid_ctas,
@@ -814,9 +818,14 @@ extern "C" int gemm_f16_launch_info(int64_t M, int64_t N, int64_t K, int config,
         cfg = picked & GEMM_F16_CONFIG_ID_MASK;
         split = split && (picked & GEMM_F16_NO_SPLIT) == 0;
     }
-    const int k_req = k_splits_for(k_request, id, picked, cfg, M, N, K, dev);
-    const bool tail = k_request == kKsplitTail ||
-                      (k_request == kKsplitNone && id == 0 && (picked & GEMM_F16_KSPLIT_TAIL) != 0);
+    if (cfg == kClusterKConfig) {
+        const int request = id == 0 ? ck_request_of(picked)
+                            : k_request >= 2 ? k_request
+                            : k_request == kKsplitNever ? 1 : 0;
+        return ck_launch_info_config_6(M, N, K, request, dev, grid_ctas, cluster_size, tiles);
+    }
+    const int k_req = k_splits_for(k_request, cfg, M, N, K, dev);
+    const bool tail = k_request == kKsplitTail;
     int grid = 0, cluster = 1, n_tiles = 0;
     if ((st = config_info(cfg, M, N, split && k_req <= 1 && !tail, dev, &grid, &cluster, &n_tiles)) != GEMM_OK)
         return st;

@@ -72,8 +72,10 @@ struct GemmParams {
     int32_t ks_start;       // first tile cut into slices (0: every tile; num_tiles: none)
     float *ws;              // per split tile and slice, a SUPER_M x BN fp32 row-major partial:
                             // ws[((t - ks_start) * k_splits + s) * SUPER_M * BN + r * BN + c]
+    int32_t ck_per;         // cluster K split (configurations with CLUSTER_K): K blocks per CTA of
+                            // the cluster; CTA r of a cluster runs blocks [r * ck_per, +ck_per)
     uint64_t timeout_cycles;
-    __half *C;              // output base (used by the direct-store epilogue)
+    __half *C;              // output base (used by the direct-store epilogues)
     int32_t producer_off;   // test hook: 1 = the producer issues nothing, so the
                             // MMA thread's first wait runs out (see gemm_f16_selftest_timeout)
     unsigned long long *status;   // device status word of this GPU (first timeout record)
@@ -88,6 +90,7 @@ enum WaitSite : uint32_t {
     kSiteDrainLoads = 5,
     kSiteDrainMma = 6,
     kSiteBoxImage = 7,   // the layout diagnostic's wait for its one box (tma_box_image.cu)
+    kSiteClusterPartial = 8,   // cluster K split: waiting for the cluster's partial tiles (or their reads)
 };
 
 constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
@@ -99,12 +102,25 @@ constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
 //   kStages    depth of the shared-memory K ring
 //   kEpiSmem   true: stage C tiles in shared memory and store them with TMA;
 //              false: store C from registers (frees shared memory for a deeper ring)
+//   kClusterK  cluster K split (single-CTA tiles only): the launch forms clusters
+//              of S = 1, 2, 4 or 8 CTAs (a run-time cluster size); all CTAs of a
+//              cluster compute the same output tile, CTA r over the r-th slice of
+//              its K blocks.  Each CTA writes its fp32 partial tile to its own
+//              shared memory; then CTA r adds the S partials of rows
+//              [r * 128/S, (r+1) * 128/S) in rank order, reading the other CTAs'
+//              shared memory through the cluster (distributed shared memory),
+//              applies R and stores fp16 C.  No global workspace, no second
+//              kernel; the result is the same sum as the workspace K split with
+//              the same slices.
 // Every CTA loads its operand boxes from global memory itself (no load is
 // shared across a cluster by multicast).
-template <int kCtaGroup, int kBN, int kStages, bool kEpiSmem = true>
+template <int kCtaGroup, int kBN, int kStages, bool kEpiSmem = true, bool kClusterK = false>
 struct GemmCfg {
     static constexpr int CTA_GROUP = kCtaGroup;
-    static constexpr int CLUSTER = CTA_GROUP;         // CTAs per cluster (the pair, or one CTA)
+    static constexpr int CLUSTER = CTA_GROUP;         // CTAs per cluster (the pair, or one CTA);
+                                                      // with CLUSTER_K the cluster size is a launch choice
+    static constexpr bool CLUSTER_K = kClusterK;
+    static constexpr int MAX_CLUSTER_K = 8;           // largest cluster of a cluster K split
     static constexpr bool EPI_SMEM = kEpiSmem;
     static constexpr int BM = 128;                    // rows of C per CTA = TMEM lanes
     static constexpr int TILE_M = BM * CTA_GROUP;     // rows of C per MMA tile (the MMA's M)
@@ -131,6 +147,11 @@ struct GemmCfg {
     static constexpr int SMEM_A_OFF = 0;
     static constexpr int SMEM_B_OFF = SMEM_A_OFF + STAGES * A_STAGE_BYTES;
     static constexpr int SMEM_C_OFF = SMEM_B_OFF + STAGES * B_STAGE_BYTES;
+    // Cluster K split: once a CTA's single tile is multiplied, its operand ring
+    // holds its fp32 partial tile (BM rows of BN floats) and a receive buffer
+    // of the same size for the other CTAs' row blocks; the 16-byte piece j of
+    // tile row r is stored at piece j ^ (r % 8) of the row.
+    static constexpr int PART_BYTES = kClusterK ? 2 * BM * BN * 4 : 0;
     static constexpr int SMEM_CTL_OFF = SMEM_C_OFF + (kEpiSmem ? 4 * 2 * C_BUF_BYTES : 0);
     // Narrowest split unit: one B box per CTA per MMA.
     static constexpr int MAX_SPLIT_LOG2 = ilog2(BN / (B_BOX_N * CTA_GROUP));
@@ -142,7 +163,9 @@ struct GemmCfg {
     static_assert(BN % (B_BOX_N * CTA_GROUP) == 0 && BN <= 512, "whole B boxes per CTA; at most 512 TMEM columns");
     static_assert(UMMA_N % 16 == 0 && UMMA_N <= 256, "UMMA N: multiple of 16 up to 256");
     static_assert(TMEM_COLS == 128 || TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation is a power of 2");
-    static_assert((2 * STAGES + 5) * 8 + 8 <= SMEM_CTL_BYTES, "control block");
+    static_assert((2 * STAGES + 8) * 8 <= SMEM_CTL_BYTES, "control block");
+    static_assert(!kClusterK || (kCtaGroup == 1 && !kEpiSmem), "cluster K split: single-CTA tiles, direct stores");
+    static_assert(PART_BYTES <= STAGES * (A_STAGE_BYTES + B_STAGE_BYTES), "cluster K buffers fit in the ring");
     static_assert(SMEM_BYTES <= 232448, "shared memory per block on sm_103");
 };
 
@@ -280,6 +303,14 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 // +0 + (-0) = +0, so a sum whose terms are all -0 is +0 (the MMA's first
 // product with accumulate = 0 does not add that +0 itself).  No other value
 // changes.
+__device__ __forceinline__ float4 ld_shared_f32x4(uint32_t addr)
+{
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr)
+                 : "memory");
+    return v;
+}
+
 template <bool kRelu>
 __device__ __forceinline__ float epilogue_value(uint32_t bits)
 {
@@ -293,6 +324,64 @@ __device__ __forceinline__ uint32_t pack_f16x2(uint32_t lo_bits, uint32_t hi_bit
 {
     const __half2 h = __floats2half2_rn(epilogue_value<kRelu>(lo_bits), epilogue_value<kRelu>(hi_bits));
     return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// Cluster K split: receive slot of sender s at the owner of rank o (senders
+// in rank order, the owner itself skipped).
+__device__ __forceinline__ int ck_slot(int s, int o) { return s < o ? s : s - 1; }
+
+// Cluster K split, stage 2: the owner (rank `crank` of a cluster of S) adds
+// its R = 128 / S tile rows over the S senders in rank order, applies R(x),
+// rounds to fp16 and stores them.  Thread t (0..127) takes owned row t % R and
+// the (t / R)-th of S column segments (BN / S columns).  Sender s's rows are in
+// this CTA's partial tile (s == crank) or in receive slot ck_slot(s, crank);
+// tile row r's 16-byte piece j is at piece j ^ (r % 8) of its 4 * BN-byte row.
+template <int S, bool kRelu, int BN>
+__device__ __forceinline__ void ck_reduce_rows(const GemmParams &p, uint32_t part, uint32_t recv, int crank, int mb,
+                                               int col0, int t)
+{
+    constexpr int R = 128 / S;
+    constexpr int kRowBytes = BN * 4;
+    constexpr int SEG = BN / S;               // columns of this thread
+    constexpr int PIECES = SEG / 4;           // fp32 16-byte pieces of this thread
+    static_assert(PIECES % 2 == 0, "whole 16-byte fp16 outputs");
+    const int rr = t % R;
+    const int seg = t / R;
+    const int trow = crank * R + rr;
+    const uint32_t sw = static_cast<uint32_t>(trow & 7);
+    uint32_t src_row[S];
+#pragma unroll
+    for (int s = 0; s < S; ++s)
+        src_row[s] = s == crank ? part + static_cast<uint32_t>(trow * kRowBytes)
+                                : recv + static_cast<uint32_t>((ck_slot(s, crank) * R + rr) * kRowBytes);
+    const int row = mb * 128 + trow;
+    const int cbase = col0 + seg * SEG;
+    if (row >= p.M) return;
+    __half *crow = p.C + static_cast<int64_t>(row) * p.N + cbase;
+#pragma unroll
+    for (int j = 0; j < PIECES; j += 2) {
+        const uint32_t pc = static_cast<uint32_t>(seg * PIECES + j);
+        const uint32_t off_lo = (pc ^ sw) << 4, off_hi = ((pc + 1u) ^ sw) << 4;
+        float4 lo = ld_shared_f32x4(src_row[0] + off_lo), hi = ld_shared_f32x4(src_row[0] + off_hi);
+#pragma unroll
+        for (int s = 1; s < S; ++s) {
+            const float4 a = ld_shared_f32x4(src_row[s] + off_lo);
+            const float4 d = ld_shared_f32x4(src_row[s] + off_hi);
+            lo.x += a.x;
+            lo.y += a.y;
+            lo.z += a.z;
+            lo.w += a.w;
+            hi.x += d.x;
+            hi.y += d.y;
+            hi.z += d.z;
+            hi.w += d.w;
+        }
+        if (cbase + 4 * j < p.N)
+            st_global_v4(crow + 4 * j, pack_f16x2<kRelu>(__float_as_uint(lo.x), __float_as_uint(lo.y)),
+                         pack_f16x2<kRelu>(__float_as_uint(lo.z), __float_as_uint(lo.w)),
+                         pack_f16x2<kRelu>(__float_as_uint(hi.x), __float_as_uint(hi.y)),
+                         pack_f16x2<kRelu>(__float_as_uint(hi.z), __float_as_uint(hi.w)));
+    }
 }
 
 // Operand layouts (the transpose_A / transpose_B of the pages' tile GEMM):
@@ -332,25 +421,33 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     auto tempty_bar = [&](int b) { return ctl + 8u * (2 * Cfg::STAGES + 2 + b); };
     const uint32_t drain_bar = ctl + 8u * (2 * Cfg::STAGES + 4);
     const uint32_t tmem_slot = ctl + 8u * (2 * Cfg::STAGES + 5);
+    // Cluster K split: this CTA's receive buffer holds the other CTAs' row
+    // blocks of the tile (rfull: one arrival with the expected bytes, then the
+    // senders' bulk copies) / every CTA of the cluster has finished its MMAs,
+    // so its operand ring may receive (rready: one arrival per CTA).
+    const uint32_t rfull_bar = ctl + 8u * (2 * Cfg::STAGES + 6);
+    const uint32_t rready_bar = ctl + 8u * (2 * Cfg::STAGES + 7);
     const uint32_t abort_addr = tmem_slot + 4;
     volatile uint32_t *tmem_slot_ptr =
         reinterpret_cast<volatile uint32_t *>(base_ptr + Cfg::SMEM_CTL_OFF + 8 * (2 * Cfg::STAGES + 5));
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t crank = Cfg::CLUSTER > 1 ? cluster_ctarank() : 0u;   // rank in the cluster
+    // CTAs in the cluster: the pair, one, or (cluster K split) the launch's choice
+    const uint32_t ncl = Cfg::CLUSTER_K ? cluster_nctarank() : static_cast<uint32_t>(Cfg::CLUSTER);
+    const uint32_t crank = (Cfg::CLUSTER > 1 || Cfg::CLUSTER_K) ? cluster_ctarank() : 0u;   // rank in the cluster
     const uint32_t rank = kPair ? (crank & 1u) : 0u;                    // rank in the pair; 0 = leader
     const uint32_t leader_rank = 0u;                                      // cluster rank of the pair's leader
     const bool leader = rank == 0;
-    const int cluster_id = static_cast<int>(blockIdx.x) / Cfg::CLUSTER;
-    const int num_clusters = static_cast<int>(gridDim.x) / Cfg::CLUSTER;
+    const int cluster_id = static_cast<int>(blockIdx.x / ncl);
+    const int num_clusters = static_cast<int>(gridDim.x / ncl);
     const uint16_t pair_mask = 0x3u;   // both CTAs of the pair
 
     AbortFlag abort;
     abort.local = reinterpret_cast<volatile int *>(tmem_slot_ptr + 1);
     abort.status = p.status;
     abort.addr = abort_addr;
-    abort.cluster = Cfg::CLUSTER;
+    abort.cluster = ncl;
     abort.rank = crank;
 
     if (threadIdx.x == 0) {
@@ -363,6 +460,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             mbar_init(tempty_bar(b), 4 * Cfg::CTA_GROUP);     // one arrive per epilogue warp
         }
         mbar_init(drain_bar, 1);
+        if constexpr (Cfg::CLUSTER_K) {
+            mbar_init(rfull_bar, 1);
+            mbar_init(rready_bar, ncl);
+        }
         *abort.local = 0;
         fence_mbar_init();
     }
@@ -377,7 +478,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     }
     tc_fence_before_sync();
     __syncthreads();
-    if constexpr (Cfg::CLUSTER > 1) {
+    if (ncl > 1) {
         // Every CTA's barriers are initialised and its TMEM allocated before
         // any CTA of the cluster signals another.
         cluster_arrive();
@@ -395,6 +496,14 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     const uint32_t tmem_base = *tmem_slot_ptr;
     const uint64_t limit = p.timeout_cycles;
     bool aborted = false;
+    // K blocks [kb0, kb1) this CTA runs for unit u (and the workspace slice).
+    auto k_range = [&](int u, int &kb0, int &kb1, int &slice) {
+        unit_k_range(u, p, kb0, kb1, slice);
+        if constexpr (Cfg::CLUSTER_K) {
+            kb0 = static_cast<int>(crank) * p.ck_per;
+            kb1 = min(p.num_k_blocks, kb0 + p.ck_per);
+        }
+    };
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -410,7 +519,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             for (int u = cluster_id; ok && p.producer_off == 0 && u < p.num_units; u += num_clusters) {
                 int mb, col0, shift, kb0, kb1, slice;
                 unit_coords<Cfg::BN>(u, p, mb, col0, shift);
-                unit_k_range(u, p, kb0, kb1, slice);
+                k_range(u, kb0, kb1, slice);
                 const int m0 = mb * Cfg::SUPER_M + static_cast<int>(rank) * Cfg::BM;
                 // Unit width W = BN >> shift, issued as W / umma_n MMAs of N = umma_n.
                 // For MMA h, this CTA supplies umma_n / CTA_GROUP columns (bpm boxes),
@@ -523,7 +632,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 const uint32_t acc_ph = (it / Cfg::ACC_STAGES) & 1;
                 const int shift = (p.k_splits <= 1 && u >= p.split_start) ? p.split_log2 : 0;
                 int kb0, kb1, slice;
-                unit_k_range(u, p, kb0, kb1, slice);
+                k_range(u, kb0, kb1, slice);
                 const int width = Cfg::BN >> shift;
                 const int umma_n = width < Cfg::UMMA_N ? width : Cfg::UMMA_N;
                 const int n_mmas = width / umma_n;
@@ -637,6 +746,104 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             }
         }
         __syncwarp();
+    } else if constexpr (Cfg::CLUSTER_K) {
+        // ------------------------------------------------------------ epilogue, cluster K split (warps 2..5)
+        // One tile per cluster.  CTA o owns rows [o * R, (o+1) * R) of the tile
+        // (R = 128 / ncl).  Once this CTA's MMAs are done, its operand ring is
+        // free and holds two buffers: the fp32 partial tile and a receive buffer
+        // for the other CTAs' row blocks of the owned rows.  Stage 1: the four
+        // warps write the accumulator (TMEM lane = tile row) into the partial
+        // buffer; one thread copies each other owner its R rows (one bulk
+        // shared-memory copy per owner into the owner's receive buffer, slot of
+        // this sender, counted on the owner's rfull barrier) once every owner
+        // has said its ring is free (rready).  Stage 2, once the other ncl - 1
+        // blocks have arrived: the owner adds each of its rows over the senders
+        // in rank order (its own rows from its partial buffer), applies R,
+        // rounds to fp16 and stores C.
+        const int q = warp & 3;
+        const int ew = warp - 2;
+        const bool lead = ew == 0 && lane == 0;   // issues the copies and the cluster signals
+        constexpr uint32_t kEpiBarrier = 1;       // named barrier of the 128 epilogue threads
+        constexpr int kRowBytes = Cfg::BN * 4;
+        const int rows_per_cta = Cfg::BM / static_cast<int>(ncl);
+        const uint32_t block_bytes = static_cast<uint32_t>(rows_per_cta * kRowBytes);
+        const int row_t = q * 32 + lane;          // tile row = TMEM lane of this thread
+        const uint32_t part = sA;                                   // over the operand ring
+        const uint32_t recv = sA + static_cast<uint32_t>(Cfg::BM * kRowBytes);
+        const uint32_t my_row = part + static_cast<uint32_t>(row_t * kRowBytes);
+        const uint32_t rsw = static_cast<uint32_t>(row_t & 7);
+        auto slot = [](int s, int o) { return ck_slot(s, o); };
+        const int u = cluster_id;   // the launch gives every cluster exactly one tile
+        if (u < p.num_units) {
+            int mb, col0_unit, shift, kb0, kb1, slice;
+            unit_coords<Cfg::BN>(u, p, mb, col0_unit, shift);
+            k_range(u, kb0, kb1, slice);
+            int ok = 1;
+            if (lane == 0) ok = wait_phase(tfull_bar(0), 0, abort, limit, kSiteEpilogueTmemFull) ? 1 : 0;
+            if (lead && ok && ncl > 1) {
+                // This CTA's MMAs have read their last operands: its ring may
+                // take the other CTAs' row blocks.
+                mbar_arrive_expect_tx(rfull_bar, (ncl - 1) * block_bytes);
+                for (uint32_t cta = 0; cta < ncl; ++cta) mbar_arrive_cluster(mapa_shared(rready_bar, cta));
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            // one decision for the four warps: each reaches every later barrier, or none
+            if (named_barrier_and(kEpiBarrier, 128, ok != 0)) {
+                griddep_wait();   // before this warp's first store of C
+                tc_fence_after_sync();
+                const uint32_t acc_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+#pragma unroll 1
+                for (int c = 0; c < Cfg::BN / 64; ++c) {
+                    uint32_t r[64];
+                    if (kb1 > kb0) {
+                        tmem_load_32x32b_x64(acc_addr + c * 64, r);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 64; ++j) r[j] = 0u;   // an empty K slice adds +0
+                    }
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const uint32_t piece = static_cast<uint32_t>(c * 16 + j);
+                        st_shared_v4(my_row + ((piece ^ rsw) << 4), r[4 * j], r[4 * j + 1], r[4 * j + 2],
+                                     r[4 * j + 3]);
+                    }
+                }
+                // All TMEM reads of this warp are done.
+                tc_fence_before_sync();
+                fence_proxy_async_smem();   // the partial rows are read by the bulk copies
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty_bar(0));
+                named_barrier_sync(kEpiBarrier, 128);
+                if (lead && ncl > 1) {
+                    if (wait_phase(rready_bar, 0, abort, limit, kSiteClusterPartial)) {
+                        for (int o = 0; o < static_cast<int>(ncl); ++o) {
+                            if (o == static_cast<int>(crank)) continue;
+                            const uint32_t dst =
+                                recv + static_cast<uint32_t>(slot(static_cast<int>(crank), o)) * block_bytes;
+                            bulk_copy_to_cluster(mapa_shared(dst, o), part + static_cast<uint32_t>(o) * block_bytes,
+                                                 block_bytes, mapa_shared(rfull_bar, o));
+                        }
+                        bulk_commit_group();
+                    }
+                }
+                if (ncl > 1) {
+                    if (lane == 0) ok = wait_phase(rfull_bar, 0, abort, limit, kSiteClusterPartial) ? 1 : 0;
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                }
+                if (ok) {
+                    switch (ncl) {
+                        case 1: ck_reduce_rows<1, kRelu, Cfg::BN>(p, part, recv, static_cast<int>(crank), mb, col0_unit, ew * 32 + lane); break;
+                        case 2: ck_reduce_rows<2, kRelu, Cfg::BN>(p, part, recv, static_cast<int>(crank), mb, col0_unit, ew * 32 + lane); break;
+                        case 4: ck_reduce_rows<4, kRelu, Cfg::BN>(p, part, recv, static_cast<int>(crank), mb, col0_unit, ew * 32 + lane); break;
+                        default: ck_reduce_rows<8, kRelu, Cfg::BN>(p, part, recv, static_cast<int>(crank), mb, col0_unit, ew * 32 + lane); break;
+                    }
+                }
+                if (!ok) aborted = true;
+            } else {
+                aborted = true;
+            }
+        }
+        if (lead) bulk_wait_group<0>();   // this CTA's copies have completed before it exits
     } else {
         // ------------------------------------------------------------ epilogue (warps 2..5)
         const int ew = warp - 2;        // owner of smem staging buffers
@@ -649,7 +856,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         for (int u = cluster_id; u < p.num_units; u += num_clusters, ++it) {
             int mb, col0_unit, shift, kb0, kb1, slice;
             unit_coords<Cfg::BN>(u, p, mb, col0_unit, shift);
-            unit_k_range(u, p, kb0, kb1, slice);
+            k_range(u, kb0, kb1, slice);
             const int chunks = (Cfg::BN >> shift) / Cfg::EPI_COLS;
             const int b = it % Cfg::ACC_STAGES;
             const uint32_t acc_ph = (it / Cfg::ACC_STAGES) & 1;
@@ -778,7 +985,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 
     tc_fence_before_sync();
     __syncthreads();
-    if constexpr (Cfg::CLUSTER > 1) {
+    if (ncl > 1) {
         // No CTA of the cluster exits while another may still signal its
         // barriers or read or write its shared memory.
         cluster_arrive();

@@ -46,6 +46,8 @@ struct LaunchArgs {
     int k_splits = 1;          // > 1: split every tile's K loop into (up to) this many slices,
                                // fp32 partials in a stream-ordered workspace, then a reduction
     bool k_split_tail = false; // split only the tiles of a partly filled last wave in K
+    int ck_request = 0;        // cluster K split configurations: 0 = the size rule, 1 = no split,
+                               // 2 / 4 / 8 = that many CTAs per cluster (fewer if K is short)
     bool noalloc = false;      // never allocate: K-slice partials go to the library's fixed
                                // scratch (noalloc_scratch); a split that does not fit it is
                                // rejected before anything is launched
@@ -333,6 +335,188 @@ int launch_one(const LaunchArgs &a)
     return GEMM_OK;
 }
 
+// ---------------------------------------------------------------- cluster K split
+
+// Resident clusters of `size` CTAs (1, 2, 4, 8) of a cluster-K configuration,
+// per device, prepared once like Prepared.
+template <class Cfg, bool kRelu>
+struct PreparedCK {
+    static std::atomic<int> slots[kMaxDevices][4];   // index log2(size); 0: not prepared
+
+    static int64_t get(int dev, int sm_count, int size)
+    {
+        const int li = size >= 8 ? 3 : size >= 4 ? 2 : size >= 2 ? 1 : 0;
+        int v = slots[dev][li].load(std::memory_order_acquire);
+        if (v > 0) return v;
+        auto kern = gemm_f16_relu_sm103a<Cfg, kRelu, false, false>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        v = sm_count / size;
+        cudaLaunchConfig_t lc{};
+        lc.blockDim = dim3(Cfg::THREADS, 1, 1);
+        lc.dynamicSmemBytes = Cfg::SMEM_BYTES;
+        lc.gridDim = dim3(static_cast<unsigned>(size * v), 1, 1);
+        cudaLaunchAttribute attrs[1];
+        attrs[0].id = cudaLaunchAttributeClusterDimension;
+        attrs[0].val.clusterDim.x = static_cast<unsigned>(size);
+        attrs[0].val.clusterDim.y = 1;
+        attrs[0].val.clusterDim.z = 1;
+        lc.attrs = attrs;
+        lc.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, kern, &lc) == cudaSuccess && clusters > 0)
+            v = clusters < v ? clusters : v;
+        else
+            cudaGetLastError();
+        if (v > 0) slots[dev][li].store(v, std::memory_order_release);
+        return v;
+    }
+
+    static void forget(int dev)
+    {
+        for (int i = 0; i < 4; ++i) slots[dev][i].store(0, std::memory_order_release);
+    }
+};
+
+template <class Cfg, bool kRelu>
+std::atomic<int> PreparedCK<Cfg, kRelu>::slots[kMaxDevices][4];
+
+// Cluster size and K blocks per CTA of a cluster K split.
+struct CKPlan {
+    int size = 1;           // CTAs per cluster = K slices per tile
+    int per = 0;            // K blocks per CTA
+    int64_t tiles = 0;      // output tiles (one per cluster at a time)
+    int64_t slots = 0;      // resident clusters of `size` CTAs
+};
+
+// request: 0 = the size rule, 1 = no split, 2 / 4 / 8 = that size.  Every CTA
+// of a cluster gets a non-empty slice: a size whose slices would leave one
+// empty is halved.  The rule takes the largest size (up to 8) whose clusters
+// hold every tile at once and leave each CTA at least two K blocks.
+template <class Cfg>
+CKPlan plan_cluster_k(int64_t M, int64_t N, int64_t K, int request, const DeviceInfo &dev)
+{
+    CKPlan pl;
+    pl.tiles = ((M + Cfg::SUPER_M - 1) / Cfg::SUPER_M) * ((N + Cfg::BN - 1) / Cfg::BN);
+    const int64_t kb = (K + Cfg::BK - 1) / Cfg::BK;
+    auto fits = [&](int size) { return size == 1 || k_split_for(kb, size).count == size; };
+    int size = 1;
+    if (request == 0) {
+        for (int c = 2; c <= Cfg::MAX_CLUSTER_K; c *= 2) {
+            const int64_t slots = PreparedCK<Cfg, true>::get(dev.device, dev.sm_count, c);
+            if (slots >= pl.tiles && kb >= 2 * c && fits(c)) size = c;
+        }
+    } else {
+        size = request;
+        while (size > 1 && !fits(size)) size /= 2;
+    }
+    pl.size = size;
+    pl.per = size > 1 ? k_split_for(kb, size).per : static_cast<int>(kb);
+    pl.slots = PreparedCK<Cfg, true>::get(dev.device, dev.sm_count, size);
+    return pl;
+}
+
+template <class Cfg, bool kRelu>
+int launch_one_ck(const LaunchArgs &a)
+{
+    static_assert(Cfg::CLUSTER_K, "cluster K split configuration");
+    if (a.ck_request != 0 && a.ck_request != 1 && a.ck_request != 2 && a.ck_request != 4 && a.ck_request != 8)
+        return GEMM_ERR_INVALID_ARG;
+    CUtensorMap ta, tb, tc;
+    int st;
+    if ((st = encode_matrix(&ta, a.A, a.M, a.K, Cfg::BK, Cfg::BM)) != GEMM_OK) return st;
+    if ((st = encode_matrix(&tb, a.B, a.K, a.N, Cfg::B_BOX_N, Cfg::BK)) != GEMM_OK) return st;
+    if ((st = encode_matrix(&tc, a.C, a.M, a.N, Cfg::EPI_COLS, 32)) != GEMM_OK) return st;   // unused by the kernel
+    const CKPlan pl = plan_cluster_k<Cfg>(a.M, a.N, a.K, a.ck_request, a.dev);
+    if (pl.slots <= 0) return GEMM_ERR_LAUNCH;
+    if (pl.tiles * pl.size > INT32_MAX / 2) return GEMM_ERR_INVALID_ARG;
+    using Prep = PreparedCK<Cfg, kRelu>;
+    if (Prep::get(a.dev.device, a.dev.sm_count, pl.size) <= 0) return GEMM_ERR_LAUNCH;
+
+    GemmParams p{};
+    p.M = static_cast<int32_t>(a.M);
+    p.N = static_cast<int32_t>(a.N);
+    p.K = static_cast<int32_t>(a.K);
+    p.num_m_blocks = static_cast<int32_t>((a.M + Cfg::SUPER_M - 1) / Cfg::SUPER_M);
+    p.num_n_blocks = static_cast<int32_t>((a.N + Cfg::BN - 1) / Cfg::BN);
+    p.num_k_blocks = static_cast<int32_t>((a.K + Cfg::BK - 1) / Cfg::BK);
+    p.num_tiles = static_cast<int32_t>(pl.tiles);
+    p.num_units = p.num_tiles;
+    p.split_start = p.num_tiles;
+    p.split_log2 = 0;
+    p.k_splits = 1;
+    p.k_per_split = p.num_k_blocks;
+    p.ks_start = p.num_tiles;
+    p.ws = nullptr;
+    p.ck_per = pl.per;
+    p.group_m = group_m_override() ? group_m_override() : 2048 / Cfg::SUPER_M;
+    p.timeout_cycles = a.hook.timeout_cycles ? a.hook.timeout_cycles : timeout_cycles_for(a.K);
+    p.C = static_cast<__half *>(a.C);
+    p.producer_off = a.hook.producer_off;
+    p.status = a.status;
+
+    // One cluster per tile (not persistent): a CTA's operand ring holds its
+    // reduction buffers once its tile is multiplied.
+    const int64_t grid_units = pl.tiles;
+    auto kern = gemm_f16_relu_sm103a<Cfg, kRelu, false, false>;
+    cudaLaunchConfig_t lc{};
+    lc.blockDim = dim3(Cfg::THREADS, 1, 1);
+    lc.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    lc.stream = a.stream;
+    cudaLaunchAttribute attrs[2];
+    attrs[0].id = cudaLaunchAttributeClusterDimension;
+    attrs[0].val.clusterDim.x = static_cast<unsigned>(pl.size);
+    attrs[0].val.clusterDim.y = 1;
+    attrs[0].val.clusterDim.z = 1;
+    attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[1].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attrs;
+    lc.numAttrs = 2;
+    lc.gridDim = dim3(static_cast<unsigned>(grid_units * pl.size), 1, 1);
+    if (cudaLaunchKernelEx(&lc, kern, ta, tb, tc, p) != cudaSuccess) {
+        cudaGetLastError();
+        Prep::forget(a.dev.device);
+        PreparedCK<Cfg, true>::forget(a.dev.device);
+        if (Prep::get(a.dev.device, a.dev.sm_count, pl.size) <= 0 || cudaLaunchKernelEx(&lc, kern, ta, tb, tc, p) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_LAUNCH;
+        }
+    }
+    return GEMM_OK;
+}
+
+// Launch geometry of a cluster K split (no launch).
+template <class Cfg>
+int ck_launch_info(int64_t M, int64_t N, int64_t K, int request, const DeviceInfo &dev, int *grid_ctas,
+                   int *cluster_size, int *tiles)
+{
+    const CKPlan pl = plan_cluster_k<Cfg>(M, N, K, request, dev);
+    const int64_t ctas = pl.tiles * pl.size;   // one cluster per tile
+    if (grid_ctas) *grid_ctas = static_cast<int>(ctas < INT32_MAX ? ctas : INT32_MAX);
+    if (cluster_size) *cluster_size = pl.size;
+    if (tiles) *tiles = static_cast<int>(pl.tiles < INT32_MAX ? pl.tiles : INT32_MAX);
+    return GEMM_OK;
+}
+
+// Share of the GPU's SM time that computes in-range outputs (as
+// config_wave_efficiency): a tile on a cluster of `size` CTAs takes 1/size of
+// its whole K loop, and every SM of the device counts, also those that no
+// cluster occupies.
+template <class Cfg>
+double ck_wave_efficiency(int64_t M, int64_t N, int64_t K, int request, const DeviceInfo &dev)
+{
+    if (M <= 0 || N <= 0 || dev.sm_count <= 0) return 0.0;
+    const CKPlan pl = plan_cluster_k<Cfg>(M, N, K, request, dev);
+    if (pl.slots <= 0) return 0.0;
+    const double waves = static_cast<double>((pl.tiles + pl.slots - 1) / pl.slots);
+    const double area = static_cast<double>(Cfg::SUPER_M) * static_cast<double>(Cfg::BN);
+    return static_cast<double>(M) * static_cast<double>(N) * pl.size /
+           (static_cast<double>(dev.sm_count) * waves * area);
+}
+
 // Dispatch over ReLU and the operand layouts this configuration supports.
 template <class Cfg, bool kAllLayouts>
 int launch_config(const LaunchArgs &a)
@@ -403,7 +587,12 @@ GEMM_DECLARE_CONFIG(2)
 GEMM_DECLARE_CONFIG(3)
 GEMM_DECLARE_CONFIG(4)
 GEMM_DECLARE_CONFIG(5)
+GEMM_DECLARE_CONFIG(6)
 #undef GEMM_DECLARE_CONFIG
+// The cluster K split configuration (6) also answers with its cluster size.
+int ck_launch_info_config_6(int64_t M, int64_t N, int64_t K, int request, const DeviceInfo &dev, int *grid_ctas,
+                            int *cluster_size, int *tiles);
+double ck_wave_eff_config_6(int64_t M, int64_t N, int64_t K, int request, const DeviceInfo &dev);
 
 // The configurations, by id (1-based).
 using Cfg1x256 = GemmCfg<1, 256, 4>;
@@ -411,5 +600,6 @@ using Cfg1x128 = GemmCfg<1, 128, 6>;
 using Cfg2x256 = GemmCfg<2, 256, 6>;
 using Cfg2x256d = GemmCfg<2, 256, 7, /*stage C in smem*/ false>;
 using Cfg2x512 = GemmCfg<2, 512, 4>;
+using Cfg1x128ck = GemmCfg<1, 128, 6, /*stage C in smem*/ false, /*cluster K split*/ true>;
 
 }  // namespace gemm_sm103

@@ -96,6 +96,50 @@ __device__ __forceinline__ void st_shared_cluster_u32(uint32_t addr, uint32_t v)
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
+// Number of CTAs in this CTA's cluster.
+__device__ __forceinline__ uint32_t cluster_nctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
+// from this CTA's shared memory to the shared memory of a CTA of the cluster
+// (dst and bar are shared::cluster addresses in that CTA); the bytes are
+// counted (complete_tx) on `bar`.  A thread that observes the barrier's phase
+// completion sees the copied data.  The source is read asynchronously: wait
+// with bulk_wait_group_read after bulk_commit_group before overwriting it.
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst),
+                 "r"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+// Barrier among the `count` threads (a multiple of 32) that use named barrier `id`.
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t count)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// The same barrier, returning to every participating thread the AND of
+// their `v`: one decision that all of them share.
+__device__ __forceinline__ bool named_barrier_and(uint32_t id, uint32_t count, bool v)
+{
+    uint32_t out;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.and.pred po, %2, %3, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(out)
+        : "r"(v ? 1u : 0u), "r"(id), "r"(count)
+        : "memory");
+    return out != 0;
+}
+
 __device__ __forceinline__ void cluster_arrive()
 {
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");

@@ -113,6 +113,8 @@ def lib() -> ctypes.CDLL:
     L.gemm_fp8_launch_info.restype = ci
     L.gemm_f16_launch_info.argtypes = [i64, i64, i64, ci, pi, pi, pi]
     L.gemm_f16_launch_info.restype = ci
+    L.gemm_f16_config_cluster_k.argtypes = [ci]
+    L.gemm_f16_config_cluster_k.restype = ci
     L.gemm_f16_tma_box_image.argtypes = [vp, i64, i64, i64, i64, i64, vp, vp]
     L.gemm_f16_tma_box_image.restype = ci
     _lib = L
@@ -318,6 +320,19 @@ def tma_box_image(X: torch.Tensor, box_rows: int, x: int, y: int, stream=None) -
     if st != GEMM_OK:
         raise GemmError(st, "gemm_f16_tma_box_image")
     return out
+
+
+def config_cluster_k(config: int) -> bool:
+    """True if the configuration splits K across a cluster (no workspace)."""
+    r = lib().gemm_f16_config_cluster_k(int(config))
+    if r < 0:
+        raise GemmError(r, "gemm_f16_config_cluster_k")
+    return r == 1
+
+
+def workspace_split_configs() -> list[int]:
+    """Fixed configuration ids whose K split uses a workspace."""
+    return [c for c in range(1, num_configs() + 1) if not config_cluster_k(c)]
 
 
 def config_layouts(config: int) -> int:

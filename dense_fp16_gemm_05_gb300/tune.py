@@ -3,9 +3,9 @@
     python -m dense_fp16_gemm_05_gb300.tune [--out PATH] [--rounds 3] [--quick]
 
 Times every fixed configuration, with and without the tail split
-(GEMM_F16_NO_SPLIT) and with the rule-chosen K split (GEMM_F16_KSPLIT_AUTO,
-which splits only when the configuration's tiles do not fill its CTA slots),
-on a grid of problem shapes, and writes the measured
+(GEMM_F16_NO_SPLIT), and the cluster K split configuration at its rule-chosen
+cluster size and at clusters of 2 and 4, on a grid of problem shapes (the
+candidates of the automatic choice; none allocates memory), and writes the measured
 throughputs as a C include (``csrc/gemm_f16_tuned.inc``) that the library
 compiles in.  The tile GEMM lesson of the pages tunes its block sizes with a
 JIT autotuner at run time ("Writing High-Performance Kernels in TileLang, from
@@ -51,10 +51,17 @@ def grid_shapes(quick: bool = False) -> list[tuple[int, int, int]]:
 
 
 def candidates() -> list[int]:
+    """Every schedule the automatic choice may take: each configuration with
+    and without the tail split, and the cluster K split at its rule-chosen
+    size and at clusters of 2 and 4.  None of them allocates memory: the
+    workspace K split stays an explicit request (gemm_f16_ex with the K-split
+    bits), so gemm_f16 itself never allocates."""
     out = []
     for cfg in range(1, g.num_configs() + 1):
-        out += [cfg, cfg | g.GEMM_F16_NO_SPLIT]
-    out += [cfg | g.GEMM_F16_KSPLIT_AUTO for cfg in range(1, g.num_configs() + 1)]
+        if g.config_cluster_k(cfg):
+            out += [cfg, cfg | g.ksplit(2), cfg | g.ksplit(4)]
+        else:
+            out += [cfg, cfg | g.GEMM_F16_NO_SPLIT]
     return out
 
 

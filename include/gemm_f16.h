@@ -154,6 +154,22 @@ int gemm_f16(const void *A, const void *B, void *C,
 #define GEMM_F16_KSPLIT(n) ((n) << GEMM_F16_KSPLIT_SHIFT)
 
 /*
+ * Cluster K split.  One configuration (gemm_f16_config_cluster_k(id) == 1;
+ * "1sm_128x128_ck_s6") splits the K loop of each 128 x 128 output tile over
+ * the CTAs of a cluster instead: CTA r of a cluster of S = 1, 2, 4 or 8 runs
+ * the r-th slice, writes its fp32 partial tile to its own shared memory, and
+ * then adds rows [r * 128/S, (r+1) * 128/S) of all S partials in rank order,
+ * reading the other CTAs' shared memory through the cluster; it applies R,
+ * rounds once to fp16 and stores C.  Nothing is allocated and no second
+ * kernel runs.  The sums are those of the workspace K split with the same
+ * slices (bit for bit).  For this configuration the K-split bits mean:
+ * GEMM_F16_KSPLIT(n), n in {2, 4, 8}: clusters of n CTAs (halved while a
+ * slice would be empty; any other n is GEMM_ERR_INVALID_ARG);
+ * GEMM_F16_NO_KSPLIT: clusters of one CTA; no bit or GEMM_F16_KSPLIT_AUTO: the
+ * size rule (the largest size up to 8 whose clusters hold every tile at once
+ * and leave each CTA at least two 64-element K blocks);
+ * GEMM_F16_KSPLIT_TAIL: GEMM_ERR_INVALID_ARG.  NN layout only.
+ *
  * gemm_f16_ex -- gemm_f16 with an explicit kernel configuration.
  *
  *   config  0: automatic choice (what gemm_f16 uses); 1..gemm_f16_num_configs():
@@ -293,6 +309,11 @@ int attention_fwd_f16(const void *Q, const void *K, const void *V, void *O, int6
  * for each supported (transa, transb); 0xF = all four, 0x1 = only (0,0).
  * GEMM_ERR_INVALID_ARG for an unknown id.  config 0 (automatic) supports all. */
 int gemm_f16_config_layouts(int config);
+
+/* 1 if configuration `config` splits K across the CTAs of a cluster (the
+ * K-split bits then name the cluster size, see gemm_f16_ex), 0 if its K split
+ * uses a workspace, GEMM_ERR_INVALID_ARG for an unknown id. */
+int gemm_f16_config_cluster_k(int config);
 
 /* Number of fixed configurations accepted by gemm_f16_ex (ids 1..n). */
 int gemm_f16_num_configs(void);

@@ -65,6 +65,16 @@ def test_bad_sizes_rejected_before_any_cuda_call(g, M, N, K):
     assert g.gemm_f16_raw(0, 0, 0, M, N, K, 1) == g.GEMM_ERR_INVALID_ARG
 
 
+def test_cluster_k_configuration_is_named_without_cuda(g):
+    ck = [c for c in range(1, g.num_configs() + 1) if g.config_cluster_k(c)]
+    assert len(ck) == 1 and "_ck" in g.config_name(ck[0])
+    assert g.config_layouts(ck[0]) == 0x1
+    assert ck[0] not in g.workspace_split_configs()
+    assert not g.config_cluster_k(0)
+    with pytest.raises(g.GemmError):
+        g.config_cluster_k(g.num_configs() + 1)
+
+
 def test_bad_relu_and_config_rejected(g):
     assert g.gemm_f16_raw(0, 0, 0, 8, 8, 8, 2) == g.GEMM_ERR_INVALID_ARG
     assert g.gemm_f16_raw(0, 0, 0, 8, 8, 8, -1) == g.GEMM_ERR_INVALID_ARG
@@ -174,7 +184,7 @@ def test_tuned_table_is_well_formed(g):
     for c in cands:
         assert 1 <= (c & g.GEMM_F16_CONFIG_ID_MASK) <= g.num_configs()
         assert (c & ~(g.GEMM_F16_CONFIG_ID_MASK | g.GEMM_F16_NO_SPLIT | g.GEMM_F16_KSPLIT_AUTO
-                      | g.GEMM_F16_KSPLIT_TAIL)) == 0
+                      | g.GEMM_F16_KSPLIT_TAIL | g.GEMM_F16_KSPLIT_MASK | g.GEMM_F16_NO_KSPLIT)) == 0
     shapes = [r[:3] for r in rows]
     assert len(set(shapes)) == len(shapes)
     for M, N, K, vals in rows:

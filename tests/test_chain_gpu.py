@@ -40,7 +40,7 @@ def g():
 
 def chain_configs(g):
     k = g.ksplit
-    return [0, 2, 3 | k(4), 5, 1 | k(3), 4, 5 | k(2), 2 | k(2), 0, 5, 3, 1 | k(4)]
+    return [0, 2, 3 | k(4), 5, 1 | k(3), 4, 5 | k(2), 6 | k(4), 2 | k(2), 6, 0, 5, 3, 1 | k(4), 6 | k(2)]
 
 
 @pytest.mark.parametrize("graph", [False, True])
@@ -92,7 +92,7 @@ def test_dependent_chain_without_host_sync(g, graph):
 
 
 def test_mixed_kernels_chain_matches_synchronised_run(g):
-    # GEMM -> K-split GEMM -> ReLU gradient -> attention -> (torch cast) ->
+    # GEMM -> K-split GEMM -> cluster K-split GEMM -> ReLU gradient -> attention -> (torch cast) ->
     # FP8 GEMM -> GEMM, each reading the previous result.  Every kernel is
     # deterministic, so the chain run back to back must give the same bits as
     # the same chain with a device synchronisation after every call.
@@ -115,6 +115,7 @@ def test_mixed_kernels_chain_matches_synchronised_run(g):
             return t
         c1 = step(g.gemm_f16(Ad, Bd, relu=True, config=5))
         c2 = step(g.gemm_f16(c1, B2d, relu=False, config=2 | g.ksplit(4)))
+        c2 = step(g.gemm_f16(c2, Bd, relu=False, config=6 | g.ksplit(4)))   # cluster K split
         dz = step(g.relu_backward(Gd, c2))
         o = step(g.attention_fwd(dz.view(1, 2, 1024, 128), Kd, Vd))
         a8 = o.view(n, n).to(torch.float8_e4m3fn)

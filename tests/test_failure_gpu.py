@@ -21,6 +21,7 @@ pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
 SITE_MMA_FULL = 3
 SITE_EPILOGUE_TMEM_FULL = 4
+SITE_CLUSTER_PARTIAL = 8
 
 
 @pytest.fixture(scope="module")
@@ -34,7 +35,7 @@ def g():
     return gemm_f16
 
 
-@pytest.mark.parametrize("config", [1, 3, 5])
+@pytest.mark.parametrize("config", [1, 3, 5, 6])
 def test_wait_runs_out_and_context_survives(g, config):
     M, N, K = 512, 512, 256
     A, B = draw(M, N, K, "normal", seed=31)
@@ -45,7 +46,7 @@ def test_wait_runs_out_and_context_survives(g, config):
     assert st == g.GEMM_OK
     assert g.check() == g.GEMM_ERR_TIMEOUT
     site = g.last_timeout_record() & 0xFF
-    assert site in (SITE_MMA_FULL, SITE_EPILOGUE_TMEM_FULL), hex(g.last_timeout_record())
+    assert site in (SITE_MMA_FULL, SITE_EPILOGUE_TMEM_FULL, SITE_CLUSTER_PARTIAL), hex(g.last_timeout_record())
     # the aborted kernel stored nothing
     assert torch.all(C == 5.0)
     # the status word was cleared and the context still computes correctly
@@ -63,7 +64,11 @@ def test_launch_geometry(g):
         for (M, N, K) in [(8192, 8192, 8192), (1000, 1000, 1000), (64, 64, 64), (16384, 512, 64)]:
             info = g.launch_info(M, N, K, config)
             assert info["grid_ctas"] % info["cluster_size"] == 0
-            assert 0 < info["grid_ctas"] <= sms
             assert info["tiles"] >= 1
+            if g.config_cluster_k(config):
+                # one cluster per tile
+                assert info["grid_ctas"] == info["tiles"] * info["cluster_size"]
+            else:
+                assert 0 < info["grid_ctas"] <= sms   # persistent grid
     assert g.launch_info(8192, 8192, 8192, 3)["cluster_size"] == 2
     assert g.launch_info(8192, 8192, 8192, 1)["cluster_size"] == 1

@@ -83,7 +83,7 @@ def test_int64_bit_exact(g, relu):
         assert np.array_equal(got.view(np.uint16), ref.view(np.uint16)), cfg
 
 
-@pytest.mark.parametrize("ksplit", [0, 3])
+@pytest.mark.parametrize("ksplit", [0, 4])
 def test_zero_sums_are_plus_zero_without_relu(g, ksplit):
     # Sums that are exactly zero: all terms -0 (a -0 row times a positive
     # column), exact cancellation of +-1 terms, and zeros mixed in.  The
@@ -307,12 +307,22 @@ def test_auto_config_follows_the_tuned_table(g):
     with open(f"{gbuild.CSRC}/gemm_f16_tuned.inc") as f:
         text = f.read()
     cands = [int(x, 16) for x in re.search(r"kTunedCandidates\[[^\]]*\] = \{([^}]*)\}", text).group(1).split(",")]
+    # candidates the automatic choice may take: no workspace K split
+    def allowed(c):
+        return g.config_cluster_k(c) or not (c & (g.GEMM_F16_KSPLIT_AUTO | g.GEMM_F16_KSPLIT_TAIL
+                                                  | g.GEMM_F16_KSPLIT_MASK))
     for m in re.finditer(r"\{(\d+), (\d+), (\d+), \{([^}]*)\}\}", text):
         M, N, K = (int(m.group(i)) for i in (1, 2, 3))
         vals = [float(x.strip().rstrip("f")) for x in m.group(4).split(",")]
-        best = cands[vals.index(max(vals))]
+        best = max((v, -i, c) for i, (v, c) in enumerate(zip(vals, cands)) if allowed(c))[2]
         got = g.auto_config(M, N, K)
-        if best & g.GEMM_F16_KSPLIT_AUTO:
+        if g.config_cluster_k(best):
+            # the cluster size, resolved for this shape (at most the one measured)
+            n = (got & g.GEMM_F16_KSPLIT_MASK) >> g.GEMM_F16_KSPLIT_SHIFT
+            want = (best & g.GEMM_F16_KSPLIT_MASK) >> g.GEMM_F16_KSPLIT_SHIFT
+            assert (got & g.GEMM_F16_CONFIG_ID_MASK) == (best & g.GEMM_F16_CONFIG_ID_MASK), (M, N, K, hex(got))
+            assert n <= (want or 8), (M, N, K, hex(got))
+        elif best & g.GEMM_F16_KSPLIT_AUTO:
             # the rule's slice count, resolved for this shape (whole tiles then)
             n = (got & g.GEMM_F16_KSPLIT_MASK) >> g.GEMM_F16_KSPLIT_SHIFT
             plain = best & ~g.GEMM_F16_KSPLIT_AUTO

@@ -114,13 +114,15 @@ def test_back_to_back_calls_without_sync(g):
         assert torch.equal(C.view(torch.int16), ref.view(torch.int16)), prob
 
 
-def test_automatic_choice_uses_the_scratch(g):
-    # 1024 x 1024 x 16384: configuration 0 cuts K (the table's choice for
-    # few-tile, deep problems); the partials then fill the scratch exactly
-    cfg = g.auto_config(1024, 1024, 16384)
+def test_rule_chosen_split_and_automatic_choice(g):
+    # 1024 x 1024 x 16384 on the 256 x 256 pair configuration with the slice
+    # rule: 16 tiles x 4 slices of 256 x 256 fp32 partials fill the scratch
+    # exactly; configuration 0 (which never takes a workspace split) gives
+    # the bits of gemm_f16
     A, B = (x.to(DEV) for x in draw(1024, 1024, 16384, "normal_scaled", 14))
-    ref = g.gemm_f16(A, B, relu=True, config=cfg)
-    C = torch.empty_like(ref)
-    g.gemm_f16_noalloc(A, B, C, relu=True, config=0)
-    assert g.check() == g.GEMM_OK
-    assert torch.equal(C.view(torch.int16), ref.view(torch.int16)), hex(cfg)
+    for cfg in (3 | g.GEMM_F16_KSPLIT_AUTO, 0):
+        ref = g.gemm_f16(A, B, relu=True, config=cfg)
+        C = torch.empty_like(ref)
+        g.gemm_f16_noalloc(A, B, C, relu=True, config=cfg)
+        assert g.check() == g.GEMM_OK
+        assert torch.equal(C.view(torch.int16), ref.view(torch.int16)), hex(cfg)
