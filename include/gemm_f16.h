@@ -15,14 +15,16 @@
  * Layout.  Leading dimensions are implied: K for A, N for B and N for C (no
  * stride arguments, as in the pages' T.Tensor((M,K)) ... declarations).
  *
- * Ownership.  The caller owns every buffer.  The library allocates nothing per
- * call except the workspace of a GEMM it cuts into K slices (taken from and
- * returned to the stream-ordered allocator on `stream`; gemm_f16_ex_noalloc
- * uses a fixed scratch instead).  Its device state is one status word per GPU
- * (a __device__ variable of the library's module) that the kernels set when
- * a bounded wait expires, the 16 MiB scratch of gemm_f16_ex_noalloc, and the
- * two copy streams per device that the first gemm_f16_from_host call
- * creates.  C must not overlap A or B.
+ * Ownership.  The caller owns every buffer.  gemm_f16 (and every automatic
+ * choice, configuration 0) allocates nothing per call.  Only an explicit
+ * request for a workspace K split (the K-split bits of gemm_f16_ex or
+ * gemm_f16_tx on a configuration whose split uses a workspace) takes that
+ * workspace from the stream-ordered allocator on `stream` and returns it there;
+ * gemm_f16_ex_noalloc uses a fixed scratch instead.  The library's device
+ * state is one status word per GPU (a __device__ variable of the library's
+ * module) that the kernels set when a bounded wait expires, the 16 MiB
+ * scratch of gemm_f16_ex_noalloc, and the two copy streams per device that
+ * the first gemm_f16_from_host call creates.  C must not overlap A or B.
  *
  * Asynchrony.  gemm_f16 and gemm_f16_ex only enqueue work on `stream` (a
  * cudaStream_t; NULL is the legacy default stream) and return without
@@ -51,7 +53,7 @@
 extern "C" {
 #endif
 
-#define GEMM_F16_VERSION 6
+#define GEMM_F16_VERSION 7
 
 /* Return codes.  0 is success; every error is negative. */
 enum gemm_f16_status {
@@ -138,10 +140,9 @@ int gemm_f16(const void *A, const void *B, void *C,
  *   GEMM_F16_NO_KSPLIT    never split K.
  *
  * Configuration 0 takes whatever the offline-measured table chose for the
- * nearest measured shape; its candidates include every configuration with
- * GEMM_F16_KSPLIT_AUTO.  (GEMM_F16_KSPLIT_TAIL is not among them: under the
- * power cap the extra workspace traffic costs more than the idle SMs of a
- * last wave do.)  A fixed configuration id without these bits does not
+ * nearest measured shape among schedules that allocate nothing: whole tiles,
+ * the tail split along N, and the cluster K split below; it never takes a
+ * workspace K split.  A fixed configuration id without these bits does not
  * split K.  If the workspace cannot be allocated the call runs without a K
  * split.  The pages' tile GEMM keeps each tile's K loop in one block; this is
  * a scheduling choice of this library.
@@ -182,22 +183,30 @@ int gemm_f16_ex(const void *A, const void *B, void *C,
                 int64_t M, int64_t N, int64_t K, int relu, int config, void *stream);
 
 /*
- * gemm_f16_ex_noalloc -- gemm_f16_ex that allocates nothing.  When the call
- * splits K (GEMM_F16_KSPLIT(n), GEMM_F16_KSPLIT_AUTO, or a split configuration
- * 0 chose), the fp32 slice partials go to a fixed scratch array of this
- * library on the current device (16 MiB, a file-scope device array) instead of
- * a stream-ordered allocation; without a K split it is gemm_f16_ex.  The pages
+ * gemm_f16_ex_noalloc -- gemm_f16_ex that allocates nothing.  For callers that
+ * may not allocate device memory while they run: a serving process that
+ * reserved its memory budget up front (its own pool holds the GPU's memory,
+ * so a stream-ordered allocation from the default pool can fail or push it
+ * over budget), a plug-in whose host framework forbids allocation during its
+ * execute step, or a latency-bound loop that must not enter the allocator.
+ * When the call splits K through a workspace (GEMM_F16_KSPLIT(n),
+ * GEMM_F16_KSPLIT_AUTO or GEMM_F16_KSPLIT_TAIL on a workspace configuration),
+ * the fp32 slice partials go to a fixed scratch array of this library on the
+ * current device (16 MiB, a file-scope device array that every device using
+ * the library keeps until the process exits) instead of a stream-ordered
+ * allocation; any other call (configuration 0, whose choices never use a
+ * workspace, the cluster K split, no split) is exactly gemm_f16_ex.  The pages
  * have no counterpart: their tile GEMM has no K split and no workspace.
  *
  * Arguments, layouts, ownership and checks as for gemm_f16_ex.  In addition:
  *  - slices x (split tiles) x (tile area) x 4 bytes must fit the 16 MiB (e.g.
  *    1024 x 1024 in 128 x 128 tiles with 4 slices); a larger split is rejected
- *    (GEMM_ERR_INVALID_ARG) before any launch, whether requested or chosen by
- *    configuration 0 (GEMM_F16_NO_KSPLIT never uses the scratch);
+ *    (GEMM_ERR_INVALID_ARG) before anything is launched;
  *  - the scratch's address is looked up once per device, by the first call
- *    that splits K: make that call outside any stream capture;
+ *    that splits K: make that call before any stream capture;
  *  - nothing in the scratch has to start at zero: every element the reduction
- *    reads was written by the GEMM kernel of the same call;
+ *    reads was written by the GEMM kernel of the same call, and the scratch
+ *    keeps whatever the last call left;
  *  - calls that overlap in time on one device (other streams, other threads,
  *    graph replays running concurrently) share the one scratch and race, with
  *    undefined results: serialise them (one stream, or events).
