@@ -372,13 +372,17 @@ int ck_request_of(int word)
 int select_config(int64_t M, int64_t N, int64_t K, bool any_layout, const DeviceInfo &dev)
 {
 #if GEMM_F16_HAVE_TUNED
+    // The last choices are kept per thread (callers often repeat a few shapes).
     struct Last {
         int64_t M = -1, N = -1, K = -1;
         int device = -1, any_layout = -1, choice = 0;
     };
-    thread_local Last last;
-    if (last.M == M && last.N == N && last.K == K && last.device == dev.device && last.any_layout == any_layout)
-        return last.choice;
+    constexpr int kCached = 64;
+    thread_local Last cache[kCached];
+    thread_local int next_slot = 0;
+    for (const Last &c : cache)
+        if (c.M == M && c.N == N && c.K == K && c.device == dev.device && c.any_layout == (any_layout ? 1 : 0))
+            return c.choice;
     const double lm = std::log2(static_cast<double>(M > 0 ? M : 1));
     const double ln = std::log2(static_cast<double>(N > 0 ? N : 1));
     const double lk = std::log2(static_cast<double>(K > 0 ? K : 1));
@@ -417,7 +421,8 @@ int select_config(int64_t M, int64_t N, int64_t K, bool any_layout, const Device
         }
     }
     if (choice != 0) {
-        last = Last{M, N, K, dev.device, any_layout ? 1 : 0, choice};
+        cache[next_slot] = Last{M, N, K, dev.device, any_layout ? 1 : 0, choice};
+        next_slot = (next_slot + 1) % kCached;
         return choice;
     }
 #endif

@@ -191,6 +191,7 @@ std::atomic<int> Prepared<Cfg, kRelu, kTA, kTB>::slots[kMaxDevices];
 struct Schedule {
     int64_t tiles = 0, units = 0, split_start = 0, grid_units = 0;
     int shift = 0;
+    double tail_cost = 0.0;   // modelled time of the last (partly filled) wave, in whole-tile times
 };
 
 template <class Cfg>
@@ -203,18 +204,26 @@ Schedule make_schedule(int64_t M, int64_t N, int64_t slots, bool allow_split)
     if (slots <= 0) return sc;
     const int64_t full = (sc.tiles / slots) * slots;
     const int64_t rest = sc.tiles - full;
-    // Tail time of split shift s: ceil(rest * 2^s / slots) / 2^s tile times
-    // (ties go to the coarser split).
+    // Tail time of split shift s: ceil(rest * 2^s / slots) / 2^s tile times,
+    // times the cost of narrow units: a unit narrower than 256 columns (CTA
+    // pair) or 128 (one CTA) reuses each operand byte for fewer MMAs and runs
+    // narrower, slower MMAs; each halving below that width is charged 1.5x
+    // (measured: 256 x 128 units of the 256 x 512 pair kernel ran a 4096^3
+    // tail at a third of the whole tiles' rate per output).  Ties go to the
+    // coarser split.
+    constexpr int kFullReuseWidth = Cfg::CTA_GROUP == 2 ? 256 : 128;
     int shift = 0;
     double best = 1e30;
     for (int s = 0; allow_split && rest > 0 && s <= Cfg::MAX_SPLIT_LOG2; ++s) {
         const int64_t waves = ((rest << s) + slots - 1) / slots;
-        const double t = static_cast<double>(waves) / static_cast<double>(1 << s);
+        double t = static_cast<double>(waves) / static_cast<double>(1 << s);
+        for (int w = Cfg::BN >> s; w < kFullReuseWidth; w *= 2) t *= 1.5;
         if (t < best - 1e-9) {
             best = t;
             shift = s;
         }
     }
+    sc.tail_cost = rest > 0 ? (allow_split ? best : 1.0) : 0.0;
     if (shift > 0) {
         sc.shift = shift;
         sc.split_start = full;
@@ -563,14 +572,8 @@ double config_wave_efficiency(int64_t M, int64_t N, bool allow_split, const Devi
     const int64_t slots = Prepared<Cfg, true, false, false>::get(dev.device, dev.sm_count);
     if (slots <= 0 || M <= 0 || N <= 0) return 0.0;
     const Schedule sc = make_schedule<Cfg>(M, N, slots, allow_split);
-    double t;
-    if (sc.shift == 0) {
-        t = static_cast<double>((sc.tiles + slots - 1) / slots);
-    } else {
-        const int64_t tail_units = sc.units - sc.split_start;
-        t = static_cast<double>(sc.split_start / slots) +
-            static_cast<double>((tail_units + slots - 1) / slots) / static_cast<double>(1 << sc.shift);
-    }
+    // full waves of whole tiles, then the modelled tail (narrow units charged)
+    const double t = static_cast<double>(sc.tiles / slots) + sc.tail_cost;
     const double area = static_cast<double>(Cfg::SUPER_M) * static_cast<double>(Cfg::BN);
     return static_cast<double>(M) * static_cast<double>(N) / (static_cast<double>(slots) * t * area);
 }

@@ -249,6 +249,30 @@ def test_from_host_row_panels(g, M):
     assert not np.any(Ch.numpy() == np.float16(9.0))
 
 
+@pytest.mark.parametrize("M,N,K", [(2500, 5000, 1000), (8192, 8192, 512), (700, 3000, 264)])
+def test_from_host_ragged_shapes_bit_exact(g, M, N, K):
+    # larger, ragged shapes through the host-buffer call: every element of C
+    # comes down (no sentinel left), bit for bit on integer operands
+    A, B = draw(M, N, K, "integer", seed=M + N)
+    Ah, Bh = A.pin_memory(), B.pin_memory()
+    Ch = torch.full((M, N), 9.5, dtype=torch.float16).pin_memory()
+    Ad = torch.empty_like(A, device=DEV)
+    Bd = torch.empty_like(B, device=DEV)
+    Cd = torch.empty((M, N), dtype=torch.float16, device=DEV)
+    g.gemm_f16_from_host(Ah, Bh, Ch, Ad, Bd, Cd, relu=False)
+    torch.cuda.synchronize()
+    assert g.check() == g.GEMM_OK
+    got = Ch.numpy()
+    assert not np.any(got.view(np.uint16) == np.float16(9.5).view(np.uint16))   # every block came down
+    # integer operands: every partial sum is exact in fp32, one rounding to
+    # fp16 as in the oracle, so the comparison is bit for bit
+    rows = sorted(set(sample_rows(M, seed=N)) | {1023, 1024, 1279, 1280, 2047, 2048} & set(range(M)))
+    ref = oracle.gemm_f16(A, B, relu=False, rows=rows)
+    assert np.array_equal(got[rows].view(np.uint16), ref.view(np.uint16)), (M, N, K)
+    # the device result equals the host copy
+    assert np.array_equal(Cd.cpu().numpy().view(np.uint16), got.view(np.uint16))
+
+
 # ---------------------------------------------------------------- argument errors (nothing launched)
 
 def test_rejects_bad_buffers(g):
