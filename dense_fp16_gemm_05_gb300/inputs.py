@@ -160,6 +160,47 @@ def draw_fp8_block_scaled(M: int, N: int, K: int, values: str, seed: int, block:
     raise ValueError(f"unknown value recipe {values!r}")
 
 
+def _quantize_blocks_pow2(x: torch.Tensor, rows_per_block: int, block: int) -> tuple[torch.Tensor, torch.Tensor]:
+    """As _quantize_blocks with each scale rounded up to a power of two
+    (2^ceil(log2(amax / 448))), returned as its E8M0 byte (exponent + 127)."""
+    R, K = x.shape
+    RB, KB = -(-R // rows_per_block), -(-K // block)
+    pad = torch.zeros(RB * rows_per_block, KB * block, dtype=torch.float32)
+    pad[:R, :K] = x
+    blocks = pad.view(RB, rows_per_block, KB, block)
+    amax = blocks.abs().amax(dim=(1, 3))
+    e = torch.where(amax > 0, torch.ceil(torch.log2(amax / 448.0)), torch.zeros_like(amax)).to(torch.int32)
+    scale = torch.ldexp(torch.ones_like(amax), e.to(torch.float32))
+    q = (blocks / scale[:, None, :, None]).clamp(-448.0, 448.0)
+    codes = q.reshape(RB * rows_per_block, KB * block)[:R, :K].contiguous().to(torch.float8_e4m3fn)
+    return codes.view(torch.uint8), (e + 127).to(torch.uint8)
+
+
+def draw_mxfp8_block_scaled(M: int, N: int, K: int, values: str, seed: int):
+    """CPU tensors (A codes (M,K) uint8, SA (M,KB) E8M0 bytes, W codes (N,K)
+    uint8, SW (NB,KB) E8M0 bytes) for the power-of-two-scale FP8 GEMM, blocks
+    of 128: the "normal" recipe of draw_fp8_block_scaled with every scale
+    rounded up to a power of two, or small integers with exponents -3..3."""
+    g = torch.Generator().manual_seed(int(seed))
+    block = FP8_BLOCK
+    KB, NB = -(-K // block), -(-N // block)
+    if values == "normal":
+        a = torch.randn(M, K, generator=g, dtype=torch.float32)
+        w = torch.randn(N, K, generator=g, dtype=torch.float32) * (1.0 / math.sqrt(max(K, 1)))
+        A, SA = _quantize_blocks_pow2(a, 1, block)
+        W, SW = _quantize_blocks_pow2(w, block, block)
+        return A, SA, W, SW
+    if values == "integer":
+        a = torch.randint(-4, 5, (M, K), generator=g, dtype=torch.int32).to(torch.float32)
+        w = torch.randint(-4, 5, (N, K), generator=g, dtype=torch.int32).to(torch.float32)
+        SA = (torch.randint(-3, 4, (M, KB), generator=g, dtype=torch.int32) + 127).to(torch.uint8)
+        SW = (torch.randint(-3, 4, (NB, KB), generator=g, dtype=torch.int32) + 127).to(torch.uint8)
+        A = a.to(torch.float8_e4m3fn).view(torch.uint8)
+        W = w.to(torch.float8_e4m3fn).view(torch.uint8)
+        return A, SA, W, SW
+    raise ValueError(f"unknown value recipe {values!r}")
+
+
 FP8_WORKLOADS: dict[str, Fp8Workload] = {
     "fp8_int_256": Fp8Workload("fp8_int_256", 256, 256, 384, True, "integer", 21),
     "fp8_ragged_1000": Fp8Workload("fp8_ragged_1000", 1000, 1000, 1040, True, "normal", 22),

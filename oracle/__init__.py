@@ -228,6 +228,25 @@ def gemm_fp8_block_scaled(A, SA, W, SW, relu: bool, block: int = 128, rows=None)
     return c.view(np.float16)
 
 
+def e8m0_to_f32(codes) -> np.ndarray:
+    """Decodes E8M0 scale bytes (the OCP microscaling formats' scale type: an
+    8-bit biased exponent and nothing else) to float32: code c < 255 is
+    2^(c - 127), code 255 is NaN.  Every value is exact in float32 (2^-127 is a
+    subnormal)."""
+    c = np.asarray(codes, dtype=np.int64)
+    out = np.ldexp(np.float32(1.0), (c - 127).astype(np.int32)).astype(np.float32)
+    return np.where(c == 255, np.float32(np.nan), out).astype(np.float32)
+
+
+def gemm_mxfp8_block_scaled(A, SA, W, SW, relu: bool, rows=None) -> np.ndarray:
+    """The FP8 block-scaled GEMM with power-of-two scales given as E8M0 bytes:
+    C = R(sum_b 2^(SA[i,b]-127) 2^(SW[n/128,b]-127) (A_b @ W_b^T)) as float16.
+    The scales are decoded exactly and the product is the one of
+    gemm_fp8_block_scaled (blocks of 128)."""
+    sa, sw = _as_u8(SA), _as_u8(SW)
+    return gemm_fp8_block_scaled(A, e8m0_to_f32(sa), W, e8m0_to_f32(sw), relu=relu, block=128, rows=rows)
+
+
 # ---------------------------------------------------------------------------
 # Attention forward (the FlashAttention skeleton of the TileLang-MUSA lesson,
 # section 5; the plain definition is written out in gemm_oracle.c above

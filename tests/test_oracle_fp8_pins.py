@@ -225,3 +225,83 @@ def test_fp8_input_recipes(oracle_mod):
     # every block reaches the top code magnitude (scale = block max / 448)
     blk = np.abs(w[:128, :128])
     assert blk.max() == 448.0
+
+
+# --------------------------------------------------------------------------
+# Power-of-two scales given as E8M0 bytes (the block-scaled MMA's scale type)
+# --------------------------------------------------------------------------
+
+def _mx_golden():
+    with open(os.path.join(HERE, "golden", "mxfp8_cases.json")) as f:
+        return json.load(f)
+
+
+@pytest.mark.parametrize("entry", _mx_golden()["e8m0"], ids=lambda e: str(e["code"]))
+def test_e8m0_named_values(oracle_mod, entry):
+    got = oracle_mod.e8m0_to_f32(np.array([entry["code"]], dtype=np.uint8))[0]
+    if entry["value"] == "nan":
+        assert np.isnan(got)
+    else:
+        assert got == np.float32(entry["value"]) and got.dtype == np.float32
+
+
+def test_e8m0_codes_are_consecutive_powers_of_two(oracle_mod):
+    # each code doubles the one below it, from 2^-127 at code 0 (exact values)
+    v = oracle_mod.e8m0_to_f32(np.arange(255, dtype=np.uint8)).astype(np.float64)
+    assert np.array_equal(v[1:] / v[:-1], np.full(254, 2.0))
+    assert v[0] == 2.0 ** -127 and v[127] == 1.0
+
+
+def _runs_to_codes(runs):
+    return np.array([[c for c, n in row for _ in range(n)] for row in runs], dtype=np.uint8)
+
+
+@pytest.mark.parametrize("case", _mx_golden()["cases"], ids=lambda c: c["name"])
+def test_mx_hand_cases(oracle_mod, case):
+    A, W = _runs_to_codes(case["A_runs"]), _runs_to_codes(case["W_runs"])
+    assert A.shape == (case["M"], case["K"]) and W.shape == (case["N"], case["K"])
+    SA, SW = np.array(case["SA"], dtype=np.uint8), np.array(case["SW"], dtype=np.uint8)
+    got = oracle_mod.gemm_mxfp8_block_scaled(A, SA, W, SW, relu=bool(case["relu"]))
+    assert np.array_equal(got.view(np.uint16), np.array(case["C_bits"], dtype=np.uint16))
+
+
+@pytest.mark.parametrize("relu", [True, False])
+def test_mx_integer_operands_exact(oracle_mod, relu):
+    # E8M0 exponents around the bias: the exact rational result, bit for bit
+    rng = np.random.default_rng(21)
+    M, N, K = 4, 200, 300
+    a, w, _, _ = int_problem(rng, M, N, K, 128)
+    ea = rng.integers(124, 131, (M, 3)).astype(np.uint8)
+    ew = rng.integers(124, 131, (2, 3)).astype(np.uint8)
+    sa = np.ldexp(1.0, ea.astype(np.int64) - 127).astype(np.float32)
+    sw = np.ldexp(1.0, ew.astype(np.int64) - 127).astype(np.float32)
+    got = oracle_mod.gemm_mxfp8_block_scaled(e4m3_codes(a), ea, e4m3_codes(w), ew, relu=relu)
+    assert np.array_equal(got.view(np.uint16), exact_result(a, sa, w, sw, 128, relu))
+
+
+def test_mx_pins_catch_an_off_by_one_bias(oracle_mod):
+    # a decoder with bias 128 (or 126) would halve (double) every scale: the
+    # first hand case then comes out 384 (1536) instead of 768
+    case = _mx_golden()["cases"][0]
+    A, W = _runs_to_codes(case["A_runs"]), _runs_to_codes(case["W_runs"])
+    SA, SW = np.array(case["SA"], dtype=np.uint8), np.array(case["SW"], dtype=np.uint8)
+    for bias in (126, 128):
+        sa = np.ldexp(1.0, SA.astype(np.int64) - bias).astype(np.float32)
+        sw = np.ldexp(1.0, SW.astype(np.int64) - bias).astype(np.float32)
+        wrong = oracle_mod.gemm_fp8_block_scaled(A, sa, W, sw, relu=True)
+        assert not np.array_equal(wrong.view(np.uint16), np.array(case["C_bits"], dtype=np.uint16))
+
+
+def test_mx_input_recipes(oracle_mod):
+    from dense_fp16_gemm_05_gb300.inputs import draw_mxfp8_block_scaled
+    A, SA, W, SW = draw_mxfp8_block_scaled(70, 150, 260, "normal", 3)
+    assert SA.dtype == torch.uint8 and SA.shape == (70, 3) and SW.shape == (2, 3)
+    w = oracle_mod.e4m3_to_f64(W.numpy())
+    assert np.isfinite(w).all() and np.abs(w).max() <= 448
+    # a power-of-two scale rounded up: each block's largest code is in (224, 448]
+    blk = np.abs(w[:128, :128])
+    assert 224 < blk.max() <= 448
+    A, SA, W, SW = draw_mxfp8_block_scaled(70, 150, 260, "integer", 2)
+    a = oracle_mod.e4m3_to_f64(A.numpy())
+    assert np.array_equal(a, np.round(a)) and np.abs(a).max() <= 4
+    assert SA.numpy().min() >= 124 and SA.numpy().max() <= 130
