@@ -713,6 +713,56 @@ extern "C" int gemm_fp8_block_scaled(const void *A, const float *SA, const void 
     return launch_fp8(a);
 }
 
+extern "C" int gemm_mxfp8_block_scaled(const void *A, const uint8_t *SA, const void *W, const uint8_t *SW, void *C,
+                                       int64_t M, int64_t N, int64_t K, int relu, void *stream)
+{
+    int st = check_sizes(M, N, K, relu);
+    if (st != GEMM_OK) return st;
+    if (M == 0 || N == 0) return GEMM_OK;
+    DeviceInfo dev;
+    if ((st = current_device_info(&dev)) != GEMM_OK) return st;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const uint64_t c_bytes = static_cast<uint64_t>(M) * static_cast<uint64_t>(N) * 2u;
+    if ((st = check_device_buffer(C, c_bytes, dev.device)) != GEMM_OK) return st;
+    if (K == 0) {
+        // Empty sum in every block: every output is R(+0) = +0.
+        if (cudaMemsetAsync(C, 0, c_bytes, s) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_CUDA;
+        }
+        return GEMM_OK;
+    }
+    if ((K % 16) != 0)
+        return reject(GEMM_ERR_ALIGNMENT, "K is not a multiple of 16 (the E4M3 row pitch of A and W is K bytes)");
+    if ((N % 8) != 0) return reject(GEMM_ERR_ALIGNMENT, "N is not a multiple of 8 (the fp16 row pitch of C)");
+    const uint64_t KB = static_cast<uint64_t>((K + 127) / 128), NB = static_cast<uint64_t>((N + 127) / 128);
+    const uint64_t a_bytes = static_cast<uint64_t>(M) * static_cast<uint64_t>(K);
+    const uint64_t w_bytes = static_cast<uint64_t>(N) * static_cast<uint64_t>(K);
+    const uint64_t sa_bytes = static_cast<uint64_t>(M) * KB, sw_bytes = NB * KB;
+    if ((st = check_device_buffer(A, a_bytes, dev.device)) != GEMM_OK) return st;
+    if ((st = check_device_buffer(W, w_bytes, dev.device)) != GEMM_OK) return st;
+    if ((st = check_device_buffer(SA, sa_bytes, dev.device, 1)) != GEMM_OK) return st;
+    if ((st = check_device_buffer(SW, sw_bytes, dev.device, 1)) != GEMM_OK) return st;
+    if (ranges_overlap(C, c_bytes, A, a_bytes) || ranges_overlap(C, c_bytes, W, w_bytes) ||
+        ranges_overlap(C, c_bytes, SA, sa_bytes) || ranges_overlap(C, c_bytes, SW, sw_bytes))
+        return reject(GEMM_ERR_INVALID_ARG, "C overlaps an input");
+    MxLaunchArgs a;
+    a.A = A;
+    a.SA = SA;
+    a.W = W;
+    a.SW = SW;
+    a.C = C;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.relu = relu;
+    a.dev = dev;
+    a.stream = s;
+    a.status = status_word(dev.device);
+    if (a.status == nullptr) return GEMM_ERR_CUDA;
+    return launch_mxfp8(a);
+}
+
 extern "C" int gemm_fp8_launch_info(int64_t M, int64_t N, int64_t K, int *grid_ctas, int *tiles)
 {
     int st = check_sizes(M, N, K, 0);

@@ -108,6 +108,8 @@ def lib() -> ctypes.CDLL:
     L.attention_fwd_f16.restype = ci
     L.gemm_fp8_block_scaled.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ci, vp]
     L.gemm_fp8_block_scaled.restype = ci
+    L.gemm_mxfp8_block_scaled.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ci, vp]
+    L.gemm_mxfp8_block_scaled.restype = ci
     pi = ctypes.POINTER(ctypes.c_int)
     L.gemm_fp8_launch_info.argtypes = [i64, i64, i64, pi, pi]
     L.gemm_fp8_launch_info.restype = ci
@@ -450,6 +452,35 @@ def gemm_fp8_block_scaled(A: torch.Tensor, SA: torch.Tensor, W: torch.Tensor, SW
                                      M, N, K, int(bool(relu)), _stream_handle(stream, A.device))
     if st != GEMM_OK:
         raise GemmError(st, "gemm_fp8_block_scaled")
+    return C
+
+
+def gemm_mxfp8_block_scaled(A: torch.Tensor, SA: torch.Tensor, W: torch.Tensor, SW: torch.Tensor,
+                            C: torch.Tensor | None = None, relu: bool = True, stream=None) -> torch.Tensor:
+    """FP8 block-scaled GEMM with power-of-two scales: SA (M, ceil(K/128)) and
+    SW (ceil(N/128), ceil(K/128)) uint8 E8M0 exponents; otherwise as
+    gemm_fp8_block_scaled (see gemm_f16.h)."""
+    _check_fp8(A, "A")
+    _check_fp8(W, "W")
+    M, K = A.shape
+    N, K2 = W.shape
+    if K != K2:
+        raise ValueError(f"A {tuple(A.shape)} and W {tuple(W.shape)} disagree on K")
+    KB, NB = -(-K // 128), -(-N // 128)
+    for t, name, shape in ((SA, "SA", (M, KB)), (SW, "SW", (NB, KB))):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.uint8 or tuple(t.shape) != shape or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous uint8 tensor of shape {shape}")
+    if C is None:
+        C = torch.empty((M, N), dtype=torch.float16, device=A.device)
+    _check_operand(C, "C")
+    if tuple(C.shape) != (M, N):
+        raise ValueError(f"C must be {(M, N)}, got {tuple(C.shape)}")
+    L = lib()
+    with _device_scope(A.device):
+        st = L.gemm_mxfp8_block_scaled(A.data_ptr(), SA.data_ptr(), W.data_ptr(), SW.data_ptr(), C.data_ptr(),
+                                       M, N, K, int(bool(relu)), _stream_handle(stream, A.device))
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_mxfp8_block_scaled")
     return C
 
 

@@ -7,7 +7,7 @@
 the workload (dA = dZ @ B^T in the NT layout, dB = A^T @ dZ in the TN layout)
 or the ReLU-gradient mask over an (M,N) gradient; --op fp8 runs the FP8
 block-scaled GEMM on the workload's sizes (E4M3 operands quantized per
-128-block, fp32 scales); --op attn runs the attention forward on an attention
+128-block, fp32 scales), --op mxfp8 the same with power-of-two scales; --op attn runs the attention forward on an attention
 workload (--workload attn_4096_d128, ...).
 
 A minimal program around the library (no oracle, no other kernels besides the
@@ -23,7 +23,7 @@ import torch
 
 from . import gemm_f16 as g
 from .inputs import (ATTN_WORKLOADS, WORKLOADS, Workload, draw_attention_workload, draw_fp8_block_scaled,
-                     draw_workload)
+                     draw_mxfp8_block_scaled, draw_workload)
 
 
 def main(argv=None):
@@ -32,7 +32,7 @@ def main(argv=None):
     p.add_argument("--reps", type=int, default=4)
     p.add_argument("--config", type=int, default=0)
     p.add_argument("--relu", type=int, default=None, help="override the workload's ReLU flag")
-    p.add_argument("--op", default="gemm", choices=["gemm", "dA_nt", "dB_tn", "relu_backward", "fp8", "attn"])
+    p.add_argument("--op", default="gemm", choices=["gemm", "dA_nt", "dB_tn", "relu_backward", "fp8", "mxfp8", "attn"])
     args = p.parse_args(argv)
     if args.op == "attn":
         return run_attention(ATTN_WORKLOADS[args.workload], args.reps, torch.device("cuda", 0))
@@ -43,8 +43,8 @@ def main(argv=None):
         w = Workload(args.workload, M, N, K, True, "normal_scaled", 0)
     relu = w.relu if args.relu is None else bool(args.relu)
     dev = torch.device("cuda", 0)
-    if args.op == "fp8":
-        return run_fp8(w, relu, args.reps, dev)
+    if args.op in ("fp8", "mxfp8"):
+        return run_fp8(w, relu, args.reps, dev, pow2=args.op == "mxfp8")
     A_cpu, B_cpu = draw_workload(w)
     A, B = A_cpu.to(dev), B_cpu.to(dev)
     C = torch.empty((w.M, w.N), dtype=torch.float16, device=dev)
@@ -87,21 +87,23 @@ def main(argv=None):
     print(json.dumps(out))
 
 
-def run_fp8(w, relu, reps, dev):
-    A8, SA, W8, SW = (t.to(dev) for t in draw_fp8_block_scaled(w.M, w.N, w.K, "normal", w.seed))
+def run_fp8(w, relu, reps, dev, pow2=False):
+    draw = draw_mxfp8_block_scaled if pow2 else draw_fp8_block_scaled
+    fn = g.gemm_mxfp8_block_scaled if pow2 else g.gemm_fp8_block_scaled
+    A8, SA, W8, SW = (t.to(dev) for t in draw(w.M, w.N, w.K, "normal", w.seed))
     C = torch.empty((w.M, w.N), dtype=torch.float16, device=dev)
     times = []
     for _ in range(reps):
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s.record()
-        g.gemm_fp8_block_scaled(A8, SA, W8, SW, C=C, relu=relu)
+        fn(A8, SA, W8, SW, C=C, relu=relu)
         e.record()
         e.synchronize()
         times.append(s.elapsed_time(e))
     st = g.check()
     if st != g.GEMM_OK:
         raise SystemExit(f"device status {st}: {g.strerror(st)}")
-    print(json.dumps({"workload": w.name, "op": "fp8", "M": w.M, "N": w.N, "K": w.K, "relu": relu, "ms": times,
+    print(json.dumps({"workload": w.name, "op": "mxfp8" if pow2 else "fp8", "M": w.M, "N": w.N, "K": w.K, "relu": relu, "ms": times,
                       "best_tflops": w.flops / (min(times) * 1e-3) / 1e12}))
 
 

@@ -286,6 +286,29 @@ int gemm_f16_relu_backward(const void *dC, const void *C, void *dZ, int64_t n, v
 int gemm_fp8_block_scaled(const void *A, const float *SA, const void *W, const float *SW, void *C,
                           int64_t M, int64_t N, int64_t K, int relu, void *stream);
 
+/*
+ * gemm_mxfp8_block_scaled -- the FP8 block-scaled GEMM of gemm_fp8_block_scaled
+ * with every scale a power of two, given as an E8M0 byte (the scale type of
+ * the OCP microscaling formats: value 2^(byte - 127), byte 0xFF is NaN):
+ *
+ *   C[i,j] = R( sum_b 2^(SA[i,b]-127) * 2^(SW[j/128,b]-127) * sum_{k in block b} A[i,k] * W[j,k] )
+ *
+ * Same blocks of 128, layouts and checks as gemm_fp8_block_scaled, except
+ *
+ *   SA  (M, ceil(K/128)) uint8 E8M0, row-major: one exponent per row of A per K block
+ *   SW  (ceil(N/128), ceil(K/128)) uint8 E8M0, row-major: one per 128 x 128 block of W
+ *
+ * (no alignment requirement on SA and SW).  Restricting the scales to powers of
+ * two lets the tensor core apply them inside the MMA (the block-scaled MMA
+ * multiplies each 32-element product group by its two scales), so every K
+ * block accumulates into one fp32 accumulator in tensor memory.  Quantizers
+ * that round each block's scale up to a power of two produce such scales.
+ * The sums are exact where the fp32 one of gemm_fp8_block_scaled is (small
+ * integer operands); otherwise the two may differ in the last bits.
+ */
+int gemm_mxfp8_block_scaled(const void *A, const uint8_t *SA, const void *W, const uint8_t *SW, void *C,
+                            int64_t M, int64_t N, int64_t K, int relu, void *stream);
+
 /* Launch geometry of gemm_fp8_block_scaled for this problem on the current
  * device: persistent grid in CTAs (CTA pairs over 256 x 256 output tiles) and
  * the number of tiles.  Either pointer may be NULL.  Launches nothing. */
