@@ -13,26 +13,39 @@
 // K blocks accumulate into one fp32 accumulator in TMEM, as in the fp16
 // kernel, and the promotion work of the fp32-scale kernel disappears.
 //
-// Layout of the scale factors in TMEM (established with a layout probe of
-// the instruction on this GPU): the scale of A row m is read from lane m,
-// column sfa + m / 32; the scale of B column n (of one MMA's N) from lane
-// 32 * q + n % 32, column sfb + n / 32, by the lanes of quarter q, so it is
-// written to all four lane quarters; byte 0 of the 32-bit word (scale id 0).
-// Every K block of 128 is four MMAs of K = 32 that share one scale, so each
-// word repeats its byte.
+// Scale factors in TMEM: the MMA reads one 32-bit word per row of A (at the
+// row's lane) and per group of 32 columns of B, and takes the byte that the
+// instruction descriptor's scale ids select.  Four consecutive K blocks share
+// one word (byte i = K block 4g + i), so one store serves four blocks and the
+// MMAs of block kb select byte kb % 4.  Every K block of 128 is four MMAs of
+// K = 32 with the same scales.  The scale of A row m is stored in every
+// column of its lane's A range, so whichever column the MMA reads for a row
+// it finds the row's word.  For the B scales, each CTA of the pair supplies
+// the words for the accumulator rows in its own TMEM, for all N = 256
+// columns of the MMA: column group n / 32 at column sfb + n / 32, the same
+// word in every lane.  Columns [0, 128) of the tile lie in W block 2 nb and
+// [128, 256) in block 2 nb + 1, so both CTAs write block 2 nb's word into
+// columns 0..3 of the B range and block 2 nb + 1's into 4..7.  (Established
+// on this GPU by decoding which exponent each output element received, with
+// A, W and the scales chosen so that every element names its byte.)
 //
-// Roles per CTA (320 threads, one CTA per SM, persistent grid over 128 x 256
-// output tiles in grouped raster order; the tile's accumulator is 256 TMEM
-// columns, computed as two N = 128 halves):
-//   warp 0, one lane   TMA producer: A box 128 (K) x 128 rows, W box 128 (K)
-//                      x 256 rows per stage
-//   warp 1, one lane   MMA issuer; allocates the 512 TMEM columns (the
-//                      accumulator and a ring of scale-factor slots)
-//   warps 2..5         epilogue: TMEM -> ReLU -> fp16 -> swizzled smem -> TMA
-//                      store, handing each half of the accumulator back as soon
-//                      as it is read (the next tile's MMAs start on half 0)
-//   warps 6..9         scale writers: per K block, read the block's scale
-//                      bytes and store them into a TMEM slot (tcgen05.st)
+// Roles per CTA (320 threads, one CTA per SM, a cluster = one CTA pair, a
+// persistent grid over 256 x 256 output tiles in grouped raster order; each
+// CTA holds 128 rows of the tile's accumulator, 256 TMEM columns):
+//   warp 0, one lane   TMA producer: an A box 128 (K) x 128 rows and a W box
+//                      128 (K) x 128 rows per K block (each CTA supplies 128
+//                      of the tile's 256 columns), completing on the pair
+//                      leader's "full" barrier
+//   warp 1, one lane   (leader CTA only) MMA issuer, tcgen05.mma.cta_group::2
+//                      M = 256, N = 256; warp 1 also allocates the 512 TMEM
+//                      columns (the accumulator and a ring of scale slots)
+//   warps 2..5         epilogue: reads the whole accumulator out of TMEM
+//                      (double-buffered loads, ReLU, fp16, into a swizzled
+//                      staging tile in shared memory) and hands TMEM back
+//                      before the TMA stores, so the next tile's MMAs wait
+//                      only for the reads
+//   warps 6..9         scale writers: per four K blocks, read the scale bytes
+//                      and store the packed words into a TMEM slot
 // Ragged edges: TMA zero-fills operand elements outside A or W; rows and
 // columns outside C are not stored.  Every wait is bounded; on expiry the
 // site is recorded in the device status word and all roles leave.
@@ -50,14 +63,14 @@ namespace gemm_sm103 {
 
 // D[tmem] (+)= (A[smem] x scale_A) * (B[smem] x scale_B), E4M3 operands,
 // E8M0 scales from TMEM (one per row of A and per column of B for the
-// instruction's K = 32), fp32 accumulator, one CTA.
-__device__ __forceinline__ void mma_mxf8_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
+// instruction's K = 32), fp32 accumulator, CTA pair (M = 256).
+__device__ __forceinline__ void mma_mxf8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
 {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
+        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
             d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
         : "memory");
@@ -90,46 +103,62 @@ __host__ __device__ constexpr uint32_t idesc_mxf8_e4m3(int M, int N)
     return (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// The descriptor with both scale ids set to `id` (byte `id` of the scale words).
+__device__ __forceinline__ uint32_t idesc_with_sf_id(uint32_t idesc, uint32_t id)
+{
+    return idesc | (id << 4) | (id << 29);
+}
+
+// Stores four consecutive 32-bit columns of the warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_store_x4(uint32_t taddr, uint32_t v0, uint32_t v1, uint32_t v2, uint32_t v3)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v0), "r"(v1),
+                 "r"(v2), "r"(v3)
+                 : "memory");
+}
+
 // ---------------------------------------------------------------- configuration
 
 struct MxCfg {
-    static constexpr int BM = 128;             // rows of C per tile (TMEM lanes)
-    static constexpr int BN = 256;             // columns of C per tile
-    static constexpr int HALF_N = 128;         // columns per MMA (one half of the accumulator)
+    static constexpr int BM = 128;             // rows of C per CTA (TMEM lanes)
+    static constexpr int TILE_M = 256;         // rows per pair tile (the MMA's M)
+    static constexpr int BN = 256;             // columns of C per tile (the MMA's N)
+    static constexpr int BN_CTA = BN / 2;      // rows of W each CTA loads
     static constexpr int BK = 128;             // E4M3 elements per K block = one 128-byte swizzle row
     static constexpr int SCALE_BLOCK = 128;
     static constexpr int UMMA_K = 32;
-    static constexpr int STAGES = 4;           // operand ring
-    static constexpr int SF_STAGES = 8;        // scale-factor slots in TMEM (>= STAGES: a slot is
-                                               // held as long as its operands)
+    static constexpr int SF_PACK = 4;          // K blocks per scale word (one byte each)
+    static constexpr int STAGES = 5;           // operand ring
+    static constexpr int SF_SLOTS = 4;         // scale slots in TMEM, SF_PACK K blocks each
     static constexpr int THREADS = 320;
-    static constexpr int A_STAGE_BYTES = BM * BK;     // 16 KiB
-    static constexpr int W_STAGE_BYTES = BN * BK;     // 32 KiB
+    static constexpr int A_STAGE_BYTES = BM * BK;       // 16 KiB
+    static constexpr int W_STAGE_BYTES = BN_CTA * BK;   // 16 KiB
     static constexpr int STAGE_TX_BYTES = A_STAGE_BYTES + W_STAGE_BYTES;
-    static constexpr int ACC_COLS = BN;               // one accumulator of two halves
-    static constexpr int SF_COL0 = ACC_COLS;          // first scale-factor slot
-    static constexpr int SF_SLOT_COLS = 16;           // A: 4 columns, B: 8 columns (2 halves x 4)
+    static constexpr int ACC_COLS = BN;                 // one accumulator
+    static constexpr int SF_COL0 = ACC_COLS;            // first scale slot
+    static constexpr int SF_SLOT_COLS = 16;             // A: columns 0-3; B: 8-15
+    static constexpr int SFB_COL = 8;
     static constexpr int TMEM_COLS = 512;
     static constexpr int EPI_COLS = 64;
-    static constexpr int C_BUF_BYTES = 32 * EPI_COLS * 2;
+    static constexpr int EPI_CHUNKS = BN / EPI_COLS;    // 4
+    static constexpr int C_BUF_BYTES = 32 * EPI_COLS * 2;   // one warp's 32 rows of one chunk
     static constexpr int SMEM_A_OFF = 0;
     static constexpr int SMEM_W_OFF = STAGES * A_STAGE_BYTES;
     static constexpr int SMEM_C_OFF = SMEM_W_OFF + STAGES * W_STAGE_BYTES;
-    static constexpr int SMEM_CTL_OFF = SMEM_C_OFF + 4 * 2 * C_BUF_BYTES;
+    static constexpr int SMEM_CTL_OFF = SMEM_C_OFF + 4 * EPI_CHUNKS * C_BUF_BYTES;   // the whole tile staged
     static constexpr int SMEM_CTL_BYTES = 256;
     static constexpr int SMEM_BYTES = 1024 + SMEM_CTL_OFF + SMEM_CTL_BYTES;
-    static constexpr uint32_t IDESC = idesc_mxf8_e4m3(BM, HALF_N);
+    static constexpr uint32_t IDESC = idesc_mxf8_e4m3(TILE_M, BN);
 
-    static_assert(BK == SCALE_BLOCK && 2 * HALF_N == BN && HALF_N == SCALE_BLOCK, "one scale per K block and half");
-    static_assert(SF_STAGES >= STAGES, "a scale slot lives as long as its operand slot");
-    static_assert(SF_COL0 + SF_STAGES * SF_SLOT_COLS <= TMEM_COLS, "TMEM columns");
-    static_assert((2 * STAGES + 2 * SF_STAGES + 5) * 8 <= SMEM_CTL_BYTES, "control block");
+    static_assert(BK == SCALE_BLOCK && 2 * SCALE_BLOCK == BN, "one scale per K block and W block");
+    static_assert(SF_COL0 + SF_SLOTS * SF_SLOT_COLS <= TMEM_COLS, "TMEM columns");
+    static_assert((2 * STAGES + 2 * SF_SLOTS + 4) * 8 + 8 <= SMEM_CTL_BYTES, "control block");
     static_assert(SMEM_BYTES <= 232448, "shared memory per block on sm_103");
 };
 
 struct MxParams {
     int32_t M, N, K;
-    int32_t num_m_blocks;   // ceil(M / 128)
+    int32_t num_m_blocks;   // ceil(M / 256)
     int32_t num_n_blocks;   // ceil(N / 256)
     int32_t num_k_blocks;   // ceil(K / 128) = KB, the columns of SA and SW
     int32_t num_w_blocks;   // ceil(N / 128), the rows of SW
@@ -167,40 +196,43 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
     const uint32_t sW = base + Cfg::SMEM_W_OFF;
     const uint32_t sC = base + Cfg::SMEM_C_OFF;
     const uint32_t ctl = base + Cfg::SMEM_CTL_OFF;
-    constexpr int S = Cfg::STAGES, SF = Cfg::SF_STAGES;
+    constexpr int S = Cfg::STAGES, SF = Cfg::SF_SLOTS, P = Cfg::SF_PACK;
     auto full_bar = [&](int s) { return ctl + 8u * s; };
     auto empty_bar = [&](int s) { return ctl + 8u * (S + s); };
     auto sfull_bar = [&](int j) { return ctl + 8u * (2 * S + j); };
     auto sempty_bar = [&](int j) { return ctl + 8u * (2 * S + SF + j); };
     const uint32_t tfull_bar = ctl + 8u * (2 * S + 2 * SF);
-    auto tempty_bar = [&](int h) { return ctl + 8u * (2 * S + 2 * SF + 1 + h); };
-    const uint32_t drain_bar = ctl + 8u * (2 * S + 2 * SF + 3);
-    const uint32_t tmem_slot = ctl + 8u * (2 * S + 2 * SF + 4);
+    const uint32_t tempty_bar = ctl + 8u * (2 * S + 2 * SF + 1);
+    const uint32_t drain_bar = ctl + 8u * (2 * S + 2 * SF + 2);
+    const uint32_t tmem_slot = ctl + 8u * (2 * S + 2 * SF + 3);
     const uint32_t abort_addr = tmem_slot + 4;
     volatile uint32_t *tmem_slot_ptr =
-        reinterpret_cast<volatile uint32_t *>(base_ptr + Cfg::SMEM_CTL_OFF + 8 * (2 * S + 2 * SF + 4));
+        reinterpret_cast<volatile uint32_t *>(base_ptr + Cfg::SMEM_CTL_OFF + 8 * (2 * S + 2 * SF + 3));
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();   // 0: the pair leader, which issues the MMAs
+    const bool leader = rank == 0;
+    constexpr uint16_t kPairMask = 0x3u;
 
     AbortFlag abort;
     abort.local = reinterpret_cast<volatile int *>(tmem_slot_ptr + 1);
     abort.status = p.status;
     abort.addr = abort_addr;
-    abort.cluster = 1;
-    abort.rank = 0;
+    abort.cluster = 2;
+    abort.rank = rank;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(full_bar(s), 1);    // the producer's arrive.expect_tx
-            mbar_init(empty_bar(s), 1);   // one MMA commit
+            mbar_init(full_bar(s), 2);    // each CTA's arrive.expect_tx (used on the leader)
+            mbar_init(empty_bar(s), 1);   // one MMA commit, sent to both CTAs
         }
         for (int j = 0; j < SF; ++j) {
-            mbar_init(sfull_bar(j), 4);   // one arrive per scale-writer warp
-            mbar_init(sempty_bar(j), 1);  // one MMA commit
+            mbar_init(sfull_bar(j), 8);   // one arrive per scale-writer warp of both CTAs
+            mbar_init(sempty_bar(j), 1);  // one MMA commit, sent to both CTAs
         }
-        mbar_init(tfull_bar, 1);
-        for (int h = 0; h < 2; ++h) mbar_init(tempty_bar(h), 4);   // one arrive per epilogue warp
+        mbar_init(tfull_bar, 1);          // one MMA commit, sent to both CTAs
+        mbar_init(tempty_bar, 8);         // one arrive per epilogue warp of both CTAs
         mbar_init(drain_bar, 1);
         *abort.local = 0;
         fence_mbar_init();
@@ -211,11 +243,15 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
         prefetch_tensormap(&tmap_c);
     }
     if (warp == 1) {
-        tmem_alloc<1>(tmem_slot, Cfg::TMEM_COLS);
-        tmem_relinquish<1>();
+        tmem_alloc<2>(tmem_slot, Cfg::TMEM_COLS);
+        tmem_relinquish<2>();
     }
     tc_fence_before_sync();
     __syncthreads();
+    // Both CTAs' barriers are initialised and their TMEM allocated before
+    // either signals the other.
+    cluster_arrive();
+    cluster_wait();
     tc_fence_after_sync();
     // The set-up above may overlap the previous kernel of the stream; each
     // role waits for it (griddep_wait) before its first global access.
@@ -223,7 +259,7 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
     const uint32_t tmem_base = *tmem_slot_ptr;
     const uint64_t limit = p.timeout_cycles;
     const int KB = p.num_k_blocks;
-    const int first = static_cast<int>(blockIdx.x), stride = static_cast<int>(gridDim.x);
+    const int first = static_cast<int>(blockIdx.x >> 1), stride = static_cast<int>(gridDim.x >> 1);
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -232,10 +268,12 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
             uint32_t ph = 0;
             uint32_t issued_mask = 0, issued_parity = 0;
             bool ok = true, dep_waited = false;
+            const uint32_t full_base = leader ? full_bar(0) : mapa_shared(full_bar(0), 0);
             for (int t = first; ok && t < p.num_tiles; t += stride) {
                 int mb, nb;
                 mx_tile_coords(t, p, mb, nb);
-                const int m0 = mb * Cfg::BM, n0 = nb * Cfg::BN;
+                const int m0 = mb * Cfg::TILE_M + static_cast<int>(rank) * Cfg::BM;
+                const int n0 = nb * Cfg::BN + static_cast<int>(rank) * Cfg::BN_CTA;
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!wait_phase(empty_bar(s), ph ^ 1u, abort, limit, kSiteProducerEmpty)) {
                         ok = false;
@@ -245,11 +283,14 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
                         griddep_wait();
                         dep_waited = true;
                     }
-                    const uint32_t fb = full_bar(s);
-                    mbar_arrive_expect_tx(fb, Cfg::STAGE_TX_BYTES);
+                    // Both CTAs' bytes are counted on the leader's barrier; each
+                    // announces its own.
+                    const uint32_t fb = full_base + 8u * s;
+                    if (leader) mbar_arrive_expect_tx(fb, Cfg::STAGE_TX_BYTES);
+                    else mbar_arrive_expect_tx_cluster(fb, Cfg::STAGE_TX_BYTES);
                     const int k0 = kb * Cfg::BK;
-                    tma_load_2d(sA + s * Cfg::A_STAGE_BYTES, &tmap_a, fb, k0, m0);
-                    tma_load_2d(sW + s * Cfg::W_STAGE_BYTES, &tmap_w, fb, k0, n0);
+                    tma_load_2d_pair(sA + s * Cfg::A_STAGE_BYTES, &tmap_a, fb, k0, m0);
+                    tma_load_2d_pair(sW + s * Cfg::W_STAGE_BYTES, &tmap_w, fb, k0, n0);
                     issued_mask |= 1u << s;
                     issued_parity = (issued_parity & ~(1u << s)) | (ph << s);
                     if (++s == S) {
@@ -259,107 +300,84 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
                 }
             }
             if (!ok) {
-                // Let the loads in flight land before the CTA exits.
-                for (int i = 0; i < S; ++i)
-                    if (issued_mask & (1u << i))
-                        wait_phase_drain(full_bar(i), (issued_parity >> i) & 1u, limit, kSiteDrainLoads, p.status);
+                if (leader) {
+                    // Let the loads in flight land before the CTA exits.
+                    for (int i = 0; i < S; ++i)
+                        if (issued_mask & (1u << i))
+                            wait_phase_drain(full_bar(i), (issued_parity >> i) & 1u, limit, kSiteDrainLoads,
+                                             p.status);
+                } else {
+                    // This CTA's loads complete on the leader's barrier, which it
+                    // cannot probe: give them a bounded time (~1e6 cycles) to land.
+                    const long long t0 = clock64();
+                    while (clock64() - t0 < 1000000) {
+                    }
+                }
             }
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // ------------------------------------------------------------ MMA issuer (leader CTA)
+        if (lane == 0 && leader) {
             int s = 0, j = 0;
             uint32_t ph = 0, sph = 0, acc_it = 0;
             bool ok = true, issued_any = false;
             // K-major SW128 operands: 8-row groups 1024 B apart; a K step of 32
-            // one-byte elements is +32 B inside the swizzle row; W half h starts
-            // 128 rows (16 KiB) further.
+            // one-byte elements is +32 B inside the swizzle row.
             const uint64_t a_desc0 = smem_desc_sw128(sA, 16, 1024);
             const uint64_t w_desc0 = smem_desc_sw128(sW, 16, 1024);
-            auto issue = [&](int st, int slot, int h_lo, int h_hi, bool first_block) {
-                const uint64_t a_st = a_desc0 + static_cast<uint64_t>((st * Cfg::A_STAGE_BYTES) >> 4);
-                const uint64_t w_st = w_desc0 + static_cast<uint64_t>((st * Cfg::W_STAGE_BYTES) >> 4);
-                const uint32_t sf = tmem_base + Cfg::SF_COL0 + static_cast<uint32_t>(slot * Cfg::SF_SLOT_COLS);
-#pragma unroll
-                for (int ks = 0; ks < Cfg::BK / Cfg::UMMA_K; ++ks) {
-                    const uint64_t step = static_cast<uint64_t>((ks * Cfg::UMMA_K) >> 4);
-                    for (int h = h_lo; h < h_hi; ++h) {
-                        const uint64_t w_h = w_st + static_cast<uint64_t>((h * Cfg::HALF_N * 128) >> 4);
-                        mma_mxf8_ss(tmem_base + static_cast<uint32_t>(h * Cfg::HALF_N), a_st + step, w_h + step,
-                                    Cfg::IDESC, sf, sf + 4u + static_cast<uint32_t>(4 * h),
-                                    (ks != 0 || !first_block) ? 1u : 0u);
-                    }
-                }
-            };
-            auto release = [&](int st, int slot) {
-                mma_commit(empty_bar(st));
-                mma_commit(sempty_bar(slot));
-            };
-            auto wait_block = [&](int st, uint32_t sph_, int slot, uint32_t ph_) {
-                return wait_phase(full_bar(st), ph_, abort, limit, kSiteMmaFull) &&
-                       wait_phase(sfull_bar(slot), sph_, abort, limit, kSiteMmaFull);
-            };
-            auto advance = [&]() {
-                if (++s == S) {
-                    s = 0;
-                    ph ^= 1u;
-                }
-                if (++j == SF) {
-                    j = 0;
-                    sph ^= 1u;
-                }
-            };
             for (int t = first; ok && t < p.num_tiles; t += stride, ++acc_it) {
-                const uint32_t acc_ph = acc_it & 1u;
-                // Half 0 as soon as the previous tile's epilogue has read it: the
-                // first ring-full of K blocks on half 0, then the same blocks on
-                // half 1 once it is free too (same per-column order of sums).
-                if (!wait_phase(tempty_bar(0), acc_ph ^ 1u, abort, limit, kSiteMmaTmemEmpty)) {
+                // The previous tile's accumulator has been read by both CTAs.
+                if (!wait_phase(tempty_bar, (acc_it & 1u) ^ 1u, abort, limit, kSiteMmaTmemEmpty)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
-                const int npre = KB < S ? KB : S;
-                int pre_s[S], pre_j[S];
-                for (int i = 0; i < npre; ++i) {
-                    if (!wait_block(s, sph, j, ph)) {
+                for (int kb = 0; kb < KB; ++kb) {
+                    const int in_word = kb % P;
+                    if (in_word == 0) {
+                        // The next scale slot (this and the next P - 1 K blocks).
+                        if (!wait_phase(sfull_bar(j), sph, abort, limit, kSiteMmaFull)) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                    if (!wait_phase(full_bar(s), ph, abort, limit, kSiteMmaFull)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
-                    pre_s[i] = s;
-                    pre_j[i] = j;
-                    issue(s, j, 0, 1, i == 0);
+                    const uint64_t a_st = a_desc0 + static_cast<uint64_t>((s * Cfg::A_STAGE_BYTES) >> 4);
+                    const uint64_t w_st = w_desc0 + static_cast<uint64_t>((s * Cfg::W_STAGE_BYTES) >> 4);
+                    const uint32_t sf = tmem_base + Cfg::SF_COL0 + static_cast<uint32_t>(j * Cfg::SF_SLOT_COLS);
+                    const uint32_t idesc = idesc_with_sf_id(Cfg::IDESC, static_cast<uint32_t>(in_word));
+#pragma unroll
+                    for (int ks = 0; ks < Cfg::BK / Cfg::UMMA_K; ++ks) {
+                        const uint64_t step = static_cast<uint64_t>((ks * Cfg::UMMA_K) >> 4);
+                        mma_mxf8_pair(tmem_base, a_st + step, w_st + step, idesc, sf, sf + Cfg::SFB_COL,
+                                      (kb != 0 || ks != 0) ? 1u : 0u);
+                    }
                     issued_any = true;
-                    advance();
-                }
-                if (!ok) break;
-                if (!wait_phase(tempty_bar(1), acc_ph ^ 1u, abort, limit, kSiteMmaTmemEmpty)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after_sync();
-                for (int i = 0; i < npre; ++i) {
-                    issue(pre_s[i], pre_j[i], 1, 2, i == 0);
-                    release(pre_s[i], pre_j[i]);
-                }
-                for (int kb = npre; kb < KB; ++kb) {
-                    if (!wait_block(s, sph, j, ph)) {
-                        ok = false;
-                        break;
+                    // Operand slot s is free in both CTAs once these MMAs have read it.
+                    mma_commit_pair_mc(empty_bar(s), kPairMask);
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1u;
                     }
-                    tc_fence_after_sync();
-                    issue(s, j, 0, 2, false);
-                    release(s, j);
-                    advance();
+                    if (in_word == P - 1 || kb == KB - 1) {
+                        mma_commit_pair_mc(sempty_bar(j), kPairMask);
+                        if (++j == SF) {
+                            j = 0;
+                            sph ^= 1u;
+                        }
+                    }
                 }
                 if (!ok) break;
-                mma_commit(tfull_bar);   // the tile's accumulator is complete
+                mma_commit_pair_mc(tfull_bar, kPairMask);   // the tile's accumulator is complete in both CTAs
             }
             if (!ok && issued_any) {
                 // Wait for this thread's MMAs before the TMEM is freed.
-                mma_commit(drain_bar);
+                mma_commit_pair_mc(drain_bar, static_cast<uint16_t>(1u << rank));
                 wait_phase_drain(drain_bar, 0, limit, kSiteDrainMma, p.status);
             }
         }
@@ -370,95 +388,124 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
         const int q = warp & 3;        // TMEM lane quarter this warp may access
         const uint32_t row_off = static_cast<uint32_t>(lane) * 128u;
         const uint32_t sw = static_cast<uint32_t>(lane & 7);
-        constexpr int kChunks = Cfg::BN / Cfg::EPI_COLS;   // 4: chunks 0-1 are half 0, 2-3 half 1
-        uint32_t chunk = 0, acc_it = 0;
+        const uint32_t tempty_leader = leader ? tempty_bar : mapa_shared(tempty_bar, 0);
+        const uint32_t cbuf0 = sC + static_cast<uint32_t>(ew * Cfg::EPI_CHUNKS * Cfg::C_BUF_BYTES);
+        // Chunk c of this warp's 32 rows, 64 fp32 columns -> ReLU -> fp16 into
+        // its staging buffer (16-byte piece jj of a row at piece jj ^ (row % 8):
+        // the layout a SWIZZLE_128B tensor-map store expects).
+        auto stage = [&](const uint32_t (&r)[64], int c) {
+            const uint32_t cbuf = cbuf0 + static_cast<uint32_t>(c * Cfg::C_BUF_BYTES);
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+                const uint32_t w0 = pack_f16x2<kRelu>(r[8 * jj + 0], r[8 * jj + 1]);
+                const uint32_t w1 = pack_f16x2<kRelu>(r[8 * jj + 2], r[8 * jj + 3]);
+                const uint32_t w2 = pack_f16x2<kRelu>(r[8 * jj + 4], r[8 * jj + 5]);
+                const uint32_t w3 = pack_f16x2<kRelu>(r[8 * jj + 6], r[8 * jj + 7]);
+                st_shared_v4(cbuf + row_off + ((static_cast<uint32_t>(jj) ^ sw) << 4), w0, w1, w2, w3);
+            }
+        };
+        uint32_t acc_it = 0;
         for (int t = first; t < p.num_tiles; t += stride, ++acc_it) {
             int mb, nb;
             mx_tile_coords(t, p, mb, nb);
             int ok = 1;
-            if (lane == 0) ok = wait_phase(tfull_bar, acc_it & 1u, abort, limit, kSiteEpilogueTmemFull) ? 1 : 0;
+            if (lane == 0) {
+                ok = wait_phase(tfull_bar, acc_it & 1u, abort, limit, kSiteEpilogueTmemFull) ? 1 : 0;
+                // The previous tile's stores have read the staging buffers.
+                bulk_wait_group_read<0>();
+            }
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             if (acc_it == 0) griddep_wait();   // before this warp's first store of C
             tc_fence_after_sync();
-            const int row0 = mb * Cfg::BM + q * 32;
+            const int row0 = mb * Cfg::TILE_M + static_cast<int>(rank) * Cfg::BM + q * 32;
             const uint32_t acc_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+            // Double-buffered reads of the four chunks; TMEM goes back to the
+            // MMA issuer as soon as the last read has completed.
+            uint32_t ra[64], rb[64];
+            tmem_load_32x32b_x64_async(acc_addr, ra);
+            tmem_wait_ld_x64(ra);
+            tmem_load_32x32b_x64_async(acc_addr + 1 * Cfg::EPI_COLS, rb);
+            stage(ra, 0);
+            tmem_wait_ld_x64(rb);
+            tmem_load_32x32b_x64_async(acc_addr + 2 * Cfg::EPI_COLS, ra);
+            stage(rb, 1);
+            tmem_wait_ld_x64(ra);
+            tmem_load_32x32b_x64_async(acc_addr + 3 * Cfg::EPI_COLS, rb);
+            stage(ra, 2);
+            tmem_wait_ld_x64(rb);
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) {
+                if (leader) mbar_arrive(tempty_bar);
+                else mbar_arrive_cluster(tempty_leader);
+            }
+            stage(rb, 3);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                if (row0 < p.M) {
 #pragma unroll 1
-            for (int c = 0; c < kChunks; ++c) {
-                uint32_t r[64];
-                tmem_load_32x32b_x64(acc_addr + c * Cfg::EPI_COLS, r);
-                if (c == 1 || c == 3) {
-                    // This warp has read half c / 2 of the accumulator.
-                    tc_fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(tempty_bar(c / 2));
+                    for (int c = 0; c < Cfg::EPI_CHUNKS; ++c) {
+                        const int col0 = nb * Cfg::BN + c * Cfg::EPI_COLS;
+                        if (col0 < p.N)
+                            tma_store_2d(&tmap_c, cbuf0 + static_cast<uint32_t>(c * Cfg::C_BUF_BYTES), col0, row0);
+                    }
                 }
-                const int col0 = nb * Cfg::BN + c * Cfg::EPI_COLS;
-                const bool in_range = row0 < p.M && col0 < p.N;
-                const uint32_t cbuf = sC + (ew * 2 + (chunk & 1u)) * Cfg::C_BUF_BYTES;
-                ++chunk;
-                if (lane == 0) bulk_wait_group_read<1>();   // the store that used cbuf has read it
-                __syncwarp();
-#pragma unroll
-                for (int jj = 0; jj < 8; ++jj) {
-                    const uint32_t w0 = pack_f16x2<kRelu>(r[8 * jj + 0], r[8 * jj + 1]);
-                    const uint32_t w1 = pack_f16x2<kRelu>(r[8 * jj + 2], r[8 * jj + 3]);
-                    const uint32_t w2 = pack_f16x2<kRelu>(r[8 * jj + 4], r[8 * jj + 5]);
-                    const uint32_t w3 = pack_f16x2<kRelu>(r[8 * jj + 6], r[8 * jj + 7]);
-                    // 16-byte piece jj of this row goes to piece jj ^ (row % 8): the
-                    // layout a SWIZZLE_128B tensor-map store expects.
-                    st_shared_v4(cbuf + row_off + ((static_cast<uint32_t>(jj) ^ sw) << 4), w0, w1, w2, w3);
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    if (in_range) tma_store_2d(&tmap_c, cbuf, col0, row0);
-                    bulk_commit_group();   // one group per chunk, empty or not
-                }
+                bulk_commit_group();
             }
         }
         if (lane == 0) bulk_wait_group<0>();
     } else {
         // ------------------------------------------------------------ scale writers (warps 6..9)
-        // Per K block: this warp's 32 rows of A scales into column q of the
-        // slot (row m at lane m, column m / 32) and the two W block scales of
-        // the tile's column halves into columns 4..11 (four columns per half,
-        // the same word in every lane).
+        // Per P K blocks, in each CTA of the pair: this warp's 32 rows of A
+        // scale words (row m at lane m) into columns 0..3 of the slot, and the
+        // W block scale words into columns 8..15 (block 2 nb in 8..11, block
+        // 2 nb + 1 in 12..15), the same word in every lane.
         const int q = warp & 3;
+        const uint32_t sfull0 = leader ? sfull_bar(0) : mapa_shared(sfull_bar(0), 0);
         int j = 0;
         uint32_t sph = 0;
-        bool dep_waited = false;
+        griddep_wait();   // the scales may come from the previous kernel
         for (int t = first; t < p.num_tiles; t += stride) {
             int mb, nb;
             mx_tile_coords(t, p, mb, nb);
-            const int row = mb * Cfg::BM + q * 32 + lane;
+            const int row = mb * Cfg::TILE_M + static_cast<int>(rank) * Cfg::BM + q * 32 + lane;
             const int wb = nb * (Cfg::BN / Cfg::SCALE_BLOCK);
+            const bool w0_in = wb < p.num_w_blocks, w1_in = wb + 1 < p.num_w_blocks;
             const uint8_t *sa = p.SA + static_cast<int64_t>(row < p.M ? row : 0) * KB;
-            const uint8_t *sw0 = p.SW + static_cast<int64_t>(wb < p.num_w_blocks ? wb : 0) * KB;
-            const uint8_t *sw1 = p.SW + static_cast<int64_t>(wb + 1 < p.num_w_blocks ? wb + 1 : 0) * KB;
+            const uint8_t *sw0 = p.SW + static_cast<int64_t>(w0_in ? wb : 0) * KB;
+            const uint8_t *sw1 = p.SW + static_cast<int64_t>(w1_in ? wb + 1 : 0) * KB;
             int ok = 1;
-            for (int kb = 0; kb < KB; ++kb) {
+            for (int kg = 0; kg < KB; kg += P) {
+                // Byte i of each word: K block kg + i.  Rows or W blocks outside
+                // the problem multiply zero operands: 2^0.
+                uint32_t wa = 0, w0 = 0, w1 = 0;
+#pragma unroll
+                for (int i = 0; i < P; ++i) {
+                    const int kb = kg + i;
+                    const uint32_t ea = (kb < KB && row < p.M) ? __ldg(sa + kb) : 127u;
+                    const uint32_t e0 = (kb < KB && w0_in) ? __ldg(sw0 + kb) : 127u;
+                    const uint32_t e1 = (kb < KB && w1_in) ? __ldg(sw1 + kb) : 127u;
+                    wa |= ea << (8 * i);
+                    w0 |= e0 << (8 * i);
+                    w1 |= e1 << (8 * i);
+                }
                 if (lane == 0) ok = wait_phase(sempty_bar(j), sph ^ 1u, abort, limit, kSiteMmaTmemEmpty) ? 1 : 0;
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) break;
-                if (!dep_waited) {
-                    griddep_wait();   // the scales may come from the previous kernel
-                    dep_waited = true;
-                }
                 tc_fence_after_sync();
-                // Rows or W blocks outside the problem multiply zero operands: 2^0.
-                const uint32_t ea = row < p.M ? __ldg(sa + kb) : 127u;
-                const uint32_t e0 = wb < p.num_w_blocks ? __ldg(sw0 + kb) : 127u;
-                const uint32_t e1 = wb + 1 < p.num_w_blocks ? __ldg(sw1 + kb) : 127u;
                 const uint32_t slot = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + Cfg::SF_COL0 +
                                       static_cast<uint32_t>(j * Cfg::SF_SLOT_COLS);
-                const uint32_t wa = ea * 0x01010101u, w0 = e0 * 0x01010101u, w1 = e1 * 0x01010101u;
-                tmem_store_x1(slot + static_cast<uint32_t>(q), wa);
-                tmem_store_x8(slot + 4u, w0, w0, w0, w0, w1, w1, w1, w1);
+                tmem_store_x4(slot, wa, wa, wa, wa);
+                tmem_store_x8(slot + Cfg::SFB_COL, w0, w0, w0, w0, w1, w1, w1, w1);
                 tmem_wait_st();
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(sfull_bar(j));
+                if (lane == 0) {
+                    if (leader) mbar_arrive(sfull_bar(j));
+                    else mbar_arrive_cluster(sfull0 + 8u * static_cast<uint32_t>(j));
+                }
                 if (++j == SF) {
                     j = 0;
                     sph ^= 1u;
@@ -470,10 +517,14 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
 
     tc_fence_before_sync();
     __syncthreads();
+    // Neither CTA exits while the other may still signal its barriers or its
+    // MMAs may still use this CTA's shared or tensor memory.
+    cluster_arrive();
+    cluster_wait();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after_sync();
-        tmem_dealloc<1>(tmem_base, Cfg::TMEM_COLS);
+        tmem_dealloc<2>(tmem_base, Cfg::TMEM_COLS);
     }
 }
 
