@@ -196,10 +196,11 @@ struct AbortFlag {
 // become visible through the barrier's transaction count, and TMEM hand-offs
 // are ordered by the tcgen05 fences around the waits.
 // kSleepNs > 0 adds a short sleep to each slow-path probe (fewer issue slots
-// spent on polling).  No wait uses it: a 256 ns sleep in the epilogue's wait
-// for a finished accumulator delayed the hand-back of TMEM to the next tile
-// and measured 1.6 % slower (the try_wait probe already suspends the thread
-// for a while when the phase is not complete).
+// spent on polling).  The fp16 GEMM's waits do not use it: a 256 ns sleep in
+// the epilogue's wait for a finished accumulator delayed the hand-back of TMEM
+// to the next tile and measured 1.6 % slower (the try_wait probe already
+// suspends the thread for a while when the phase is not complete).  Roles that
+// run far ahead of the MMAs (the scale writers of the E8M0 FP8 kernel) use it.
 template <int kSleepNs = 0>
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const AbortFlag &abort, uint64_t limit,
                                            uint32_t site)

@@ -129,7 +129,8 @@ struct MxCfg {
     static constexpr int UMMA_K = 32;
     static constexpr int SF_PACK = 4;          // K blocks per scale word (one byte each)
     static constexpr int STAGES = 5;           // operand ring
-    static constexpr int SF_SLOTS = 4;         // scale slots in TMEM, SF_PACK K blocks each
+    static constexpr int SF_SLOTS = 8;         // scale slots in TMEM, SF_PACK K blocks each
+    static constexpr int SF_BATCH = 4;         // scale words a writer loads ahead, per batch
     static constexpr int THREADS = 320;
     static constexpr int A_STAGE_BYTES = BM * BK;       // 16 KiB
     static constexpr int W_STAGE_BYTES = BN_CTA * BK;   // 16 KiB
@@ -477,38 +478,66 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
             const uint8_t *sw0 = p.SW + static_cast<int64_t>(w0_in ? wb : 0) * KB;
             const uint8_t *sw1 = p.SW + static_cast<int64_t>(w1_in ? wb + 1 : 0) * KB;
             int ok = 1;
-            for (int kg = 0; kg < KB; kg += P) {
-                // Byte i of each word: K block kg + i.  Rows or W blocks outside
-                // the problem multiply zero operands: 2^0.
-                uint32_t wa = 0, w0 = 0, w1 = 0;
+            // Byte i of each word: K block 4 g + i.  Rows or W blocks outside
+            // the problem multiply zero operands: 2^0.  The bytes of the next
+            // batch of words are loaded while this batch is stored, so a
+            // load's latency (about one word's worth of MMAs at this size) is
+            // never waited for.
+            constexpr int D = Cfg::SF_BATCH;
+            auto load_batch = [&](int kg0, uint32_t (&wa)[D], uint32_t (&w0)[D], uint32_t (&w1)[D]) {
 #pragma unroll
-                for (int i = 0; i < P; ++i) {
-                    const int kb = kg + i;
-                    const uint32_t ea = (kb < KB && row < p.M) ? __ldg(sa + kb) : 127u;
-                    const uint32_t e0 = (kb < KB && w0_in) ? __ldg(sw0 + kb) : 127u;
-                    const uint32_t e1 = (kb < KB && w1_in) ? __ldg(sw1 + kb) : 127u;
-                    wa |= ea << (8 * i);
-                    w0 |= e0 << (8 * i);
-                    w1 |= e1 << (8 * i);
+                for (int g = 0; g < D; ++g) {
+                    wa[g] = w0[g] = w1[g] = 0;
+#pragma unroll
+                    for (int i = 0; i < P; ++i) {
+                        const int kb = kg0 + g * P + i;
+                        const uint32_t ea = (kb < KB && row < p.M) ? __ldg(sa + kb) : 127u;
+                        const uint32_t e0 = (kb < KB && w0_in) ? __ldg(sw0 + kb) : 127u;
+                        const uint32_t e1 = (kb < KB && w1_in) ? __ldg(sw1 + kb) : 127u;
+                        wa[g] |= ea << (8 * i);
+                        w0[g] |= e0 << (8 * i);
+                        w1[g] |= e1 << (8 * i);
+                    }
                 }
-                if (lane == 0) ok = wait_phase(sempty_bar(j), sph ^ 1u, abort, limit, kSiteMmaTmemEmpty) ? 1 : 0;
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) break;
-                tc_fence_after_sync();
-                const uint32_t slot = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + Cfg::SF_COL0 +
-                                      static_cast<uint32_t>(j * Cfg::SF_SLOT_COLS);
-                tmem_store_x4(slot, wa, wa, wa, wa);
-                tmem_store_x8(slot + Cfg::SFB_COL, w0, w0, w0, w0, w1, w1, w1, w1);
-                tmem_wait_st();
-                tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) {
-                    if (leader) mbar_arrive(sfull_bar(j));
-                    else mbar_arrive_cluster(sfull0 + 8u * static_cast<uint32_t>(j));
+            };
+            uint32_t ca[D], c0[D], c1[D];
+            load_batch(0, ca, c0, c1);
+            for (int kg0 = 0; ok && kg0 < KB; kg0 += D * P) {
+                uint32_t na[D], n0[D], n1[D];
+                load_batch(kg0 + D * P, na, n0, n1);
+#pragma unroll
+                for (int g = 0; g < D; ++g) {
+                    if (kg0 + g * P >= KB) break;
+                    // The writers run up to SF_SLOTS words ahead of the MMAs: their
+                    // waits sleep between probes, leaving issue slots and barrier
+                    // traffic to the roles on the critical path (measured 1.5 %
+                    // faster than polling without a pause).
+                    if (lane == 0)
+                        ok = wait_phase<1000>(sempty_bar(j), sph ^ 1u, abort, limit, kSiteMmaTmemEmpty) ? 1 : 0;
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                    const uint32_t slot = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + Cfg::SF_COL0 +
+                                          static_cast<uint32_t>(j * Cfg::SF_SLOT_COLS);
+                    tmem_store_x4(slot, ca[g], ca[g], ca[g], ca[g]);
+                    tmem_store_x8(slot + Cfg::SFB_COL, c0[g], c0[g], c0[g], c0[g], c1[g], c1[g], c1[g], c1[g]);
+                    tmem_wait_st();
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (leader) mbar_arrive(sfull_bar(j));
+                        else mbar_arrive_cluster(sfull0 + 8u * static_cast<uint32_t>(j));
+                    }
+                    if (++j == SF) {
+                        j = 0;
+                        sph ^= 1u;
+                    }
                 }
-                if (++j == SF) {
-                    j = 0;
-                    sph ^= 1u;
+#pragma unroll
+                for (int g = 0; g < D; ++g) {
+                    ca[g] = na[g];
+                    c0[g] = n0[g];
+                    c1[g] = n1[g];
                 }
             }
             if (!ok) break;
