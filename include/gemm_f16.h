@@ -388,6 +388,12 @@ int gemm_f16_launch_info(int64_t M, int64_t N, int64_t K, int config, int *grid_
  * Returns after enqueueing.  Errors as gemm_f16, plus GEMM_ERR_INVALID_ARG for
  * a NULL host pointer and GEMM_ERR_CUDA when a copy, event or stream cannot be
  * created or enqueued (work enqueued before that point still runs).
+ * Calls on one stream run one after the other (each overwrites its device
+ * buffers).  Calls on different streams with different device buffers may
+ * overlap: a caller streaming independent problems through two streams and
+ * two buffer sets gets one call's uploads started as soon as the previous
+ * call's uploads are done (the uploads of all calls share one copy stream,
+ * in call order).
  */
 int gemm_f16_from_host(const void *A_host, const void *B_host, void *C_host,
                        void *A_dev, void *B_dev, void *C_dev,

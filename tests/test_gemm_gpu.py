@@ -273,6 +273,33 @@ def test_from_host_ragged_shapes_bit_exact(g, M, N, K):
     assert np.array_equal(Cd.cpu().numpy().view(np.uint16), got.view(np.uint16))
 
 
+def test_from_host_two_streams_in_flight(g):
+    # The pattern of a caller streaming independent problems: steps alternate
+    # between two streams, each with its own device buffers and host result,
+    # and nothing is synchronised until the end, so one step's uploads run
+    # while the previous step's GEMMs and downloads finish.  Every step's
+    # result must be its own problem's, bit for bit (integer operands).
+    M, N, K = 2304, 1024, 768
+    steps = 4
+    probs = [draw(M, N, K, "integer", seed=900 + i) for i in range(steps)]
+    hosts = [(A.pin_memory(), B.pin_memory(), torch.full((M, N), 9.5, dtype=torch.float16).pin_memory())
+             for A, B in probs]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    devs = [(torch.empty((M, K), dtype=torch.float16, device=DEV), torch.empty((K, N), dtype=torch.float16, device=DEV),
+             torch.empty((M, N), dtype=torch.float16, device=DEV)) for _ in range(2)]
+    for i in range(steps):
+        Ah, Bh, Ch = hosts[i]
+        Ad, Bd, Cd = devs[i % 2]
+        g.gemm_f16_from_host(Ah, Bh, Ch, Ad, Bd, Cd, relu=bool(i % 2), stream=streams[i % 2])
+    for s in streams:
+        s.synchronize()
+        assert g.check(stream=s) == g.GEMM_OK
+    for i, (A, B) in enumerate(probs):
+        rows = sorted(set(sample_rows(M, seed=i)) | {0, 1023, 1024, 2303})
+        ref = oracle.gemm_f16(A, B, relu=bool(i % 2), rows=rows)
+        assert np.array_equal(hosts[i][2].numpy()[rows].view(np.uint16), ref.view(np.uint16)), i
+
+
 # ---------------------------------------------------------------- argument errors (nothing launched)
 
 def test_rejects_bad_buffers(g):
