@@ -601,13 +601,13 @@ def run_ours(args):
             "entry": "gemm_mxfp8_block_scaled", "launches": reps8}
         del A8, SA8, W8, SW8, C8
 
-    # ---- attention forward (the next-row extension): 4096 tokens, 32 heads,
-    # batch 4, dim 128, fp16, non-causal and causal
+    # ---- attention forward (the next-row extension): 4096 tokens, batch 4,
+    # 32 heads of dim 128 and 64 heads of dim 64, fp16, non-causal and causal
     attention = None
     if not args.no_secondary:
         from dense_fp16_gemm_05_gb300.inputs import ATTN_WORKLOADS, draw_attention_workload
         attention = {}
-        for name in ("attn_4096_d128", "attn_4096_d128_causal"):
+        for name in ("attn_4096_d128", "attn_4096_d128_causal", "attn_4096_d64", "attn_4096_d64_causal"):
             wa = ATTN_WORKLOADS[name]
             Qa, Ka, Va = (t.to(dev) for t in draw_attention_workload(wa))
             Oa = torch.empty_like(Qa)

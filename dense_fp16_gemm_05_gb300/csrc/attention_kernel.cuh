@@ -10,19 +10,26 @@
 // score matrix is never stored.
 //
 // One CTA per (pair of query blocks, head, batch): two query tiles of 128
-// rows that share every K/V block; 320 threads:
-//   warp 0, one lane   TMA: the two Q tiles once (3-D tensor maps: rows of
+// rows that share every K/V block; 384 threads in three warpgroups (two of
+// softmax warps, one of control warps), launched at 168 registers a thread
+// (three warps share each SM sub-partition's register file); the control
+// warpgroup then hands registers to the softmax warpgroups (setmaxnreg: 88
+// and 200), so the 128 scores a softmax thread holds stay in registers and
+// nothing spills:
+//   warps 0..7         softmax (below)
+//   warp 8, one lane   TMA: the two Q tiles once (3-D tensor maps: rows of
 //                      another head are never read, rows past seq read as
 //                      zero), then K and V blocks through rings of KV_STAGES
 //                      slots, each loaded once for both tiles
-//   warp 1, one lane   MMA issuer (and TMEM owner): per tile t,
+//   warp 9, one lane   MMA issuer (and TMEM owner): per tile t,
 //                      S^t_j = Q^t K_j^T (both from shared memory) into the
 //                      tile's 128-column TMEM score buffer and
 //                      O^t += P^t_j V_j into its TMEM output accumulator.  The
 //                      stream alternates tiles (O^0 += P^0_j V_j, S^0_{j+1},
 //                      O^1 += P^1_j V_j, S^1_{j+1}), so the tensor core works
 //                      on one tile while the other tile's softmax runs
-//   warps 2..9         softmax, four warps per tile, one thread per query row
+//   warps 10, 11       idle (they complete the control warpgroup)
+//   warps 0..7         softmax, four warps per tile, one thread per query row
 //                      (TMEM lane) and all 128 keys of a block: masked
 //                      scores, row maximum, p = 2^(s*c - m) with
 //                      c = sm_scale * log2(e), row sum, P in fp16 written back
@@ -173,6 +180,18 @@ __device__ __forceinline__ float max3(float a, float b, float c)
     return d;
 }
 
+// Per-warpgroup register budget (every warp of the warpgroup executes it).
+template <int kRegs>
+__device__ __forceinline__ void setmaxnreg_inc()
+{
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <int kRegs>
+__device__ __forceinline__ void setmaxnreg_dec()
+{
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+
 // D[tmem] (+)= A[tmem] * B[smem], fp16 inputs, fp32 accumulator: the A
 // operand is read from tensor memory (one row per lane, K packed two fp16 per
 // 32-bit column).
@@ -195,8 +214,13 @@ struct AttnCfg {
     static constexpr int BQ = 128;                // query rows per tile (TMEM lanes)
     static constexpr int BKV = 128;               // keys per block
     static constexpr int TILE_WARPS = 4;          // softmax warps per tile: one per TMEM lane quarter
-    static constexpr int SOFTMAX_WARPS = TILES * TILE_WARPS;
-    static constexpr int THREADS = 64 + 32 * SOFTMAX_WARPS;
+    static constexpr int SOFTMAX_WARPS = TILES * TILE_WARPS;   // warps 0 .. 7
+    static constexpr int TMA_WARP = SOFTMAX_WARPS;              // 8
+    static constexpr int MMA_WARP = SOFTMAX_WARPS + 1;          // 9
+    static constexpr int THREADS = 32 * (SOFTMAX_WARPS + 4);    // a whole control warpgroup
+    static constexpr int LAUNCH_REGS = 168;   // 65536 / 384, rounded down to a multiple of 8
+    static constexpr int CONTROL_REGS = 88;   // below this the MMA issuer's loop spills
+    static constexpr int SOFTMAX_REGS = 200;
     static constexpr int ATOMS = kDim / 64;       // 128-byte swizzle atoms along dim
     static constexpr int TILE_BYTES = 128 * kDim * 2;   // Q, K or V tile of 128 rows
     static constexpr int ATOM_BYTES = 128 * 128;        // 128 rows x 128 bytes
@@ -215,6 +239,11 @@ struct AttnCfg {
     static constexpr uint32_t IDESC_O = idesc_f16_f32(BQ, kDim, false, true);   // P K-major, V MN-major
 
     static_assert(kDim == 64 || kDim == 128, "head dimension 64 or 128");
+    static_assert(SOFTMAX_WARPS == 8 && THREADS == 384, "two softmax warpgroups and one control warpgroup");
+    // setmaxnreg can only hand out what the launch reserved: the new budgets
+    // must sum to no more than THREADS x LAUNCH_REGS.
+    static_assert(32 * SOFTMAX_WARPS * SOFTMAX_REGS + 128 * CONTROL_REGS <= THREADS * LAUNCH_REGS,
+                  "register budgets exceed the launch's");
     static_assert(TMEM_O_COL + TILES * 128 <= TMEM_COLS, "TMEM columns");
     static_assert(SMEM_BYTES <= 232448, "shared memory per block on sm_103");
     static_assert((10 + 4 * KV_STAGES) * 8 <= SMEM_CTL_BYTES, "control block");
@@ -305,12 +334,12 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
         *abort.local = 0;
         fence_mbar_init();
     }
-    if (warp == 0 && lane == 0) {
+    if (warp == Cfg::TMA_WARP && lane == 0) {
         prefetch_tensormap(&tmap_q);
         prefetch_tensormap(&tmap_k);
         prefetch_tensormap(&tmap_v);
     }
-    if (warp == 1) {
+    if (warp == Cfg::MMA_WARP) {
         tmem_alloc<1>(tmem_slot, Cfg::TMEM_COLS);
         tmem_relinquish<1>();
     }
@@ -323,9 +352,12 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
     griddep_launch_dependents();
     const uint32_t tmem_base = *tmem_slot_ptr;
     const uint64_t limit = p.timeout_cycles;
+    // Each role sets its warpgroup's register budget first thing in its own
+    // branch (the compiler allocates each branch's registers within it).
 
-    if (warp == 0) {
+    if (warp == Cfg::TMA_WARP) {
         // ------------------------------------------------------------ TMA producer
+        setmaxnreg_dec<Cfg::CONTROL_REGS>();
         if (lane == 0) {
             bool ok = true;
             mbar_arrive_expect_tx(q_full, Cfg::TILES * Cfg::TILE_BYTES);
@@ -366,8 +398,9 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
             }
         }
         __syncwarp();
-    } else if (warp == 1) {
+    } else if (warp == Cfg::MMA_WARP) {
         // ------------------------------------------------------------ MMA issuer
+        setmaxnreg_dec<Cfg::CONTROL_REGS>();
         if (lane == 0) {
             bool ok = wait_phase(q_full, 0, abort, limit, kSiteMmaFull);
             bool issued_any = false;
@@ -440,10 +473,11 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
             }
         }
         __syncwarp();
-    } else {
-        // ------------------------------------------------------------ softmax (warps 2..9)
+    } else if (warp < Cfg::SOFTMAX_WARPS) {
+        // ------------------------------------------------------------ softmax (warps 0..7)
+        setmaxnreg_inc<Cfg::SOFTMAX_REGS>();
         // One thread per query row (TMEM lane) and all 128 keys of a block.
-        const int t = (warp - 2) / Cfg::TILE_WARPS;   // query tile
+        const int t = warp / Cfg::TILE_WARPS;        // query tile
         const int q = warp & 3;                      // TMEM lane quarter
         const int row_local = q * 32 + lane;
         const int row = (2 * grp + t) * Cfg::BQ + row_local;
@@ -571,9 +605,14 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
         }
     }
 
+    else {
+        // ------------------------------------------------------------ idle (warps 10, 11)
+        setmaxnreg_dec<Cfg::CONTROL_REGS>();
+    }
+
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == Cfg::MMA_WARP) {
         __syncwarp();
         tc_fence_after_sync();
         tmem_dealloc<1>(tmem_base, Cfg::TMEM_COLS);

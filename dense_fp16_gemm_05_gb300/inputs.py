@@ -257,4 +257,6 @@ ATTN_WORKLOADS: dict[str, AttnWorkload] = {
     "attn_causal_ragged_d128": AttnWorkload("attn_causal_ragged_d128", 2, 3, 300, 128, True, 42),
     "attn_4096_d128": AttnWorkload("attn_4096_d128", 4, 32, 4096, 128, False, 43),
     "attn_4096_d128_causal": AttnWorkload("attn_4096_d128_causal", 4, 32, 4096, 128, True, 44),
+    "attn_4096_d64": AttnWorkload("attn_4096_d64", 4, 64, 4096, 64, False, 45),
+    "attn_4096_d64_causal": AttnWorkload("attn_4096_d64_causal", 4, 64, 4096, 64, True, 46),
 }
