@@ -17,7 +17,9 @@
 // row's lane) and per group of 32 columns of B, and takes the byte that the
 // instruction descriptor's scale ids select.  Four consecutive K blocks share
 // one word (byte i = K block 4g + i), so one store serves four blocks and the
-// MMAs of block kb select byte kb % 4.  Every K block of 128 is four MMAs of
+// MMAs of block kb select byte kb % 4; a TMEM slot holds four such words (16
+// K blocks per hand-off between the scale writers and the MMA issuer; one word
+// per slot measured 1.5 % slower).  Every K block of 128 is four MMAs of
 // K = 32 with the same scales.  The scale of A row m is stored in every
 // column of its lane's A range, so whichever column the MMA reads for a row
 // it finds the row's word.  For the B scales, each CTA of the pair supplies
@@ -44,7 +46,7 @@
 //                      staging tile in shared memory) and hands TMEM back
 //                      before the TMA stores, so the next tile's MMAs wait
 //                      only for the reads
-//   warps 6..9         scale writers: per four K blocks, read the scale bytes
+//   warps 6..9         scale writers: per 16 K blocks, read the scale bytes
 //                      and store the packed words into a TMEM slot
 // Ragged edges: TMA zero-fills operand elements outside A or W; rows and
 // columns outside C are not stored.  Every wait is bounded; on expiry the
@@ -129,7 +131,9 @@ struct MxCfg {
     static constexpr int UMMA_K = 32;
     static constexpr int SF_PACK = 4;          // K blocks per scale word (one byte each)
     static constexpr int STAGES = 5;           // operand ring
-    static constexpr int SF_SLOTS = 8;         // scale slots in TMEM, SF_PACK K blocks each
+    static constexpr int SF_WORDS = 4;         // scale words per TMEM slot (SF_PACK K blocks each)
+    static constexpr int SF_KB = SF_PACK * SF_WORDS;   // K blocks per slot (one hand-off)
+    static constexpr int SF_SLOTS = SF_WORDS == 4 ? 4 : 8;   // scale slots in TMEM
     static constexpr int SF_BATCH = 4;         // scale words a writer loads ahead, per batch
     static constexpr int THREADS = 320;
     static constexpr int A_STAGE_BYTES = BM * BK;       // 16 KiB
@@ -137,8 +141,10 @@ struct MxCfg {
     static constexpr int STAGE_TX_BYTES = A_STAGE_BYTES + W_STAGE_BYTES;
     static constexpr int ACC_COLS = BN;                 // one accumulator
     static constexpr int SF_COL0 = ACC_COLS;            // first scale slot
-    static constexpr int SF_SLOT_COLS = 16;             // A: columns 0-3; B: 8-15
-    static constexpr int SFB_COL = 8;
+    // Slot layout: A word w in columns 4w .. 4w+3, B words w from column
+    // SFB_COL + 8w (8 columns each); slots start on multiples of 16 columns.
+    static constexpr int SFB_COL = SF_WORDS == 1 ? 8 : 4 * SF_WORDS;
+    static constexpr int SF_SLOT_COLS = SF_WORDS == 1 ? 16 : (SF_WORDS == 2 ? 32 : 64);
     static constexpr int TMEM_COLS = 512;
     static constexpr int EPI_COLS = 64;
     static constexpr int EPI_CHUNKS = BN / EPI_COLS;    // 4
@@ -153,6 +159,7 @@ struct MxCfg {
 
     static_assert(BK == SCALE_BLOCK && 2 * SCALE_BLOCK == BN, "one scale per K block and W block");
     static_assert(SF_COL0 + SF_SLOTS * SF_SLOT_COLS <= TMEM_COLS, "TMEM columns");
+    static_assert(SFB_COL + 8 * SF_WORDS <= SF_SLOT_COLS && SF_BATCH % SF_WORDS == 0, "scale slot layout");
     static_assert((2 * STAGES + 2 * SF_SLOTS + 4) * 8 + 8 <= SMEM_CTL_BYTES, "control block");
     static_assert(SMEM_BYTES <= 232448, "shared memory per block on sm_103");
 };
@@ -335,8 +342,9 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
                 }
                 tc_fence_after_sync();
                 for (int kb = 0; kb < KB; ++kb) {
-                    const int in_word = kb % P;
-                    if (in_word == 0) {
+                    const int in_slot = kb % Cfg::SF_KB;
+                    const int word = in_slot / P, in_word = in_slot % P;
+                    if (in_slot == 0) {
                         // The next scale slot (this and the next P - 1 K blocks).
                         if (!wait_phase(sfull_bar(j), sph, abort, limit, kSiteMmaFull)) {
                             ok = false;
@@ -351,11 +359,13 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
                     const uint64_t a_st = a_desc0 + static_cast<uint64_t>((s * Cfg::A_STAGE_BYTES) >> 4);
                     const uint64_t w_st = w_desc0 + static_cast<uint64_t>((s * Cfg::W_STAGE_BYTES) >> 4);
                     const uint32_t sf = tmem_base + Cfg::SF_COL0 + static_cast<uint32_t>(j * Cfg::SF_SLOT_COLS);
+                    const uint32_t sfa = sf + static_cast<uint32_t>(4 * word);
+                    const uint32_t sfb = sf + static_cast<uint32_t>(Cfg::SFB_COL + 8 * word);
                     const uint32_t idesc = idesc_with_sf_id(Cfg::IDESC, static_cast<uint32_t>(in_word));
 #pragma unroll
                     for (int ks = 0; ks < Cfg::BK / Cfg::UMMA_K; ++ks) {
                         const uint64_t step = static_cast<uint64_t>((ks * Cfg::UMMA_K) >> 4);
-                        mma_mxf8_pair(tmem_base, a_st + step, w_st + step, idesc, sf, sf + Cfg::SFB_COL,
+                        mma_mxf8_pair(tmem_base, a_st + step, w_st + step, idesc, sfa, sfb,
                                       (kb != 0 || ks != 0) ? 1u : 0u);
                     }
                     issued_any = true;
@@ -365,7 +375,7 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
                         s = 0;
                         ph ^= 1u;
                     }
-                    if (in_word == P - 1 || kb == KB - 1) {
+                    if (in_slot == Cfg::SF_KB - 1 || kb == KB - 1) {
                         mma_commit_pair_mc(sempty_bar(j), kPairMask);
                         if (++j == SF) {
                             j = 0;
@@ -459,10 +469,11 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
         if (lane == 0) bulk_wait_group<0>();
     } else {
         // ------------------------------------------------------------ scale writers (warps 6..9)
-        // Per P K blocks, in each CTA of the pair: this warp's 32 rows of A
-        // scale words (row m at lane m) into columns 0..3 of the slot, and the
-        // W block scale words into columns 8..15 (block 2 nb in 8..11, block
-        // 2 nb + 1 in 12..15), the same word in every lane.
+        // Per slot (SF_WORDS words of P K blocks), in each CTA of the pair: for
+        // word w, this warp's 32 rows of A scale words (row m at lane m) into
+        // columns 4w .. 4w+3 of the slot, and the W block scale words into
+        // columns SFB_COL + 8w .. SFB_COL + 8w + 7 (block 2 nb in the first
+        // four, block 2 nb + 1 in the next four), the same word in every lane.
         const int q = warp & 3;
         const uint32_t sfull0 = leader ? sfull_bar(0) : mapa_shared(sfull_bar(0), 0);
         int j = 0;
@@ -506,8 +517,8 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
                 uint32_t na[D], n0[D], n1[D];
                 load_batch(kg0 + D * P, na, n0, n1);
 #pragma unroll
-                for (int g = 0; g < D; ++g) {
-                    if (kg0 + g * P >= KB) break;
+                for (int sl = 0; sl < D / Cfg::SF_WORDS; ++sl) {
+                    if (kg0 + sl * Cfg::SF_KB >= KB) break;
                     // The writers run up to SF_SLOTS words ahead of the MMAs: their
                     // waits sleep between probes, leaving issue slots and barrier
                     // traffic to the roles on the critical path (measured 1.5 %
@@ -519,8 +530,13 @@ __global__ void __launch_bounds__(MxCfg::THREADS, 1)
                     tc_fence_after_sync();
                     const uint32_t slot = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + Cfg::SF_COL0 +
                                           static_cast<uint32_t>(j * Cfg::SF_SLOT_COLS);
-                    tmem_store_x4(slot, ca[g], ca[g], ca[g], ca[g]);
-                    tmem_store_x8(slot + Cfg::SFB_COL, c0[g], c0[g], c0[g], c0[g], c1[g], c1[g], c1[g], c1[g]);
+#pragma unroll
+                    for (int w = 0; w < Cfg::SF_WORDS; ++w) {
+                        const int g = sl * Cfg::SF_WORDS + w;
+                        tmem_store_x4(slot + static_cast<uint32_t>(4 * w), ca[g], ca[g], ca[g], ca[g]);
+                        tmem_store_x8(slot + static_cast<uint32_t>(Cfg::SFB_COL + 8 * w), c0[g], c0[g], c0[g], c0[g],
+                                      c1[g], c1[g], c1[g], c1[g]);
+                    }
                     tmem_wait_st();
                     tc_fence_before_sync();
                     __syncwarp();
