@@ -59,7 +59,7 @@ def test_workloads_full(g, name, causal):
     assert_close(run(g, Q, K, V, causal, w.sm_scale), ref, f"{name} causal={causal}")
 
 
-@pytest.mark.parametrize("name", ["attn_4096_d128", "attn_4096_d128_causal"])
+@pytest.mark.parametrize("name", ["attn_4096_d128", "attn_4096_d128_causal", "attn_4096_d64", "attn_4096_d64_causal"])
 def test_4096_sampled_rows(g, name):
     w = ATTN_WORKLOADS[name]
     Q, K, V = draw_attention_workload(w)
