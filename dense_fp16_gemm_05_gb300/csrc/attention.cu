@@ -54,9 +54,12 @@ int launch_dim(const AttnLaunchArgs &a)
     p.O = static_cast<__half *>(a.O);
     p.status = a.status;
     if (!AttnPrepared<kDim>::get(a.dev.device)) return GEMM_ERR_LAUNCH;
-    // One CTA per pair of query blocks (its two tiles), per head and batch.
-    const dim3 grid(static_cast<unsigned>((p.num_q_blocks + Cfg::TILES - 1) / Cfg::TILES),
-                    static_cast<unsigned>(a.heads), static_cast<unsigned>(a.batch));
+    // A persistent grid: one CTA per SM (the kernel's shared memory and TMEM
+    // admit one), each walking every G-th super-item (with the causal mask two
+    // pairs of query blocks of one head and batch, else one; see the kernel).
+    const int64_t n_grp = (p.num_q_blocks + Cfg::TILES - 1) / Cfg::TILES;
+    const int64_t supers = (a.causal ? (n_grp + 1) / 2 : n_grp) * a.heads * a.batch;
+    const dim3 grid(static_cast<unsigned>(supers < a.dev.sm_count ? supers : a.dev.sm_count), 1, 1);
     cudaLaunchConfig_t lc{};
     lc.gridDim = grid;
     lc.blockDim = dim3(Cfg::THREADS, 1, 1);

@@ -9,11 +9,16 @@
 // streamed in blocks of 128 with a running row maximum and row sum, so the
 // score matrix is never stored.
 //
-// One CTA per (pair of query blocks, head, batch): two query tiles of 128
-// rows that share every K/V block; 384 threads in three warpgroups (two of
+// A persistent grid (one CTA per SM) walks the work items (pair of query
+// blocks, head, batch), heavier causal pairs first, each CTA taking every
+// G-th item; per item two query tiles of 128 rows share every K/V block.
+// The next item's Q is loaded once the current item's last score MMAs are
+// complete and its first score MMAs follow the current item's last products
+// in the tensor core's stream, so an item's start overlaps the previous
+// item's last softmax and output stores.  384 threads in three warpgroups (two of
 // softmax warps, one of control warps), launched at 168 registers a thread
 // (three warps share each SM sub-partition's register file); the control
-// warpgroup then hands registers to the softmax warpgroups (setmaxnreg: 88
+// warpgroup then hands registers to the softmax warpgroups (setmaxnreg: 104
 // and 200), so the 128 scores a softmax thread holds stay in registers and
 // nothing spills:
 //   warps 0..7         softmax (below)
@@ -219,7 +224,7 @@ struct AttnCfg {
     static constexpr int MMA_WARP = SOFTMAX_WARPS + 1;          // 9
     static constexpr int THREADS = 32 * (SOFTMAX_WARPS + 4);    // a whole control warpgroup
     static constexpr int LAUNCH_REGS = 168;   // 65536 / 384, rounded down to a multiple of 8
-    static constexpr int CONTROL_REGS = 88;   // below this the MMA issuer's loop spills
+    static constexpr int CONTROL_REGS = 104;  // below this the MMA issuer's loop spills
     static constexpr int SOFTMAX_REGS = 200;
     static constexpr int ATOMS = kDim / 64;       // 128-byte swizzle atoms along dim
     static constexpr int TILE_BYTES = 128 * kDim * 2;   // Q, K or V tile of 128 rows
@@ -275,7 +280,10 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
     const uint32_t ctl = base + Cfg::SMEM_CTL_OFF;
     // Barriers (8 bytes each): q_full; k_full, k_empty, v_full, v_empty
     // [KV_STAGES] (the K and V rings); per tile s_full, p_full, o_ready;
-    // drain; then the TMEM address slot and the abort flag.
+    // drain; q_empty; then the TMEM address slot and the abort flag.  Their
+    // phases run over all items of the CTA: the K/V ring by the CTA's running
+    // count of key blocks, s_full / p_full / o_ready by each tile's running
+    // count of blocks, q_full / q_empty by the item count.
     //
     // Order of the MMA stream: S^0_0, S^1_0, then per block j and tile t:
     // O^t += P^t_j V_j, S^t_{j+1}.  Tile t's score buffer is rewritten by
@@ -292,23 +300,48 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
     auto p_full = [&](int t) { return ctl + 8u * (3 + 4 * S + t); };
     auto o_ready = [&](int t) { return ctl + 8u * (5 + 4 * S + t); };
     const uint32_t drain = ctl + 8u * (7 + 4 * S);
-    const uint32_t tmem_slot = ctl + 8u * (8 + 4 * S);
+    const uint32_t q_empty = ctl + 8u * (8 + 4 * S);   // the item's score MMAs (readers of Q) are complete
+    const uint32_t tmem_slot = ctl + 8u * (9 + 4 * S);
     const uint32_t abort_addr = tmem_slot + 4;
     volatile uint32_t *tmem_slot_ptr =
-        reinterpret_cast<volatile uint32_t *>(base_ptr + Cfg::SMEM_CTL_OFF + 8 * (8 + 4 * S));
+        reinterpret_cast<volatile uint32_t *>(base_ptr + Cfg::SMEM_CTL_OFF + 8 * (9 + 4 * S));
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // Heavier (causal) query-block pairs first: index reversed.  Tile t
-    // covers query block 2 * grp + t.
-    const int grp = static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x);
-    const int head = static_cast<int>(blockIdx.y);
-    const int bh = static_cast<int>(blockIdx.z) * p.heads + head;
+    // Work items: an item is a pair of query blocks grp (tile t covers query
+    // block 2 * grp + t) of one head-batch index bh.  With the causal mask the
+    // items are grouped two by two into super-items of one head, the heaviest
+    // pair with the lightest, the next heaviest with the next lightest, ...,
+    // so that every super-item has the same number of key blocks; without it
+    // every item has the same work and a super-item is one item.  Super-items
+    // are numbered head by head, and CTA c takes super-items c, c + G, ... (G
+    // CTAs): at any time the CTAs work on a few heads at once, whose K and V
+    // the L2 then serves to all of them.  item_of(k) decodes this CTA's k-th
+    // item: 1 = an item, 0 = none at this k (the middle pair of an odd count),
+    // -1 = no more.
+    const int n_grp = (p.num_q_blocks + Cfg::TILES - 1) / Cfg::TILES;
+    const int sup_shift = p.causal ? 1 : 0;   // log2 of the items per super-item
+    const int n_sub = p.causal ? (n_grp + 1) / 2 : n_grp;
+    const int num_super = n_sub * p.batch * p.heads;
+    const int first = static_cast<int>(blockIdx.x), stride = static_cast<int>(gridDim.x);
     const int kv_blocks_all = (p.seq + Cfg::BKV - 1) / Cfg::BKV;
     // Key blocks of each tile (tile 1 never needs fewer than tile 0; both >= 1).
-    auto tile_blocks = [&](int t) { return p.causal ? min(2 * grp + t + 1, kv_blocks_all) : kv_blocks_all; };
-    const int nb0 = tile_blocks(0);
-    const int nb1 = tile_blocks(1);
+    auto item_of = [&](int k, int &grp, int &bh, int &nb0, int &nb1) -> int {
+        const int sup = first + (k >> sup_shift) * stride;
+        if (sup >= num_super) return -1;
+        bh = sup / n_sub;
+        const int kp = sup - bh * n_sub;
+        if (!p.causal) {
+            grp = kp;
+            nb0 = nb1 = kv_blocks_all;
+            return 1;
+        }
+        grp = (k & 1) ? kp : n_grp - 1 - kp;
+        if ((k & 1) && grp == n_grp - 1 - kp) return 0;
+        nb0 = min(2 * grp + 1, kv_blocks_all);
+        nb1 = min(2 * grp + 2, kv_blocks_all);
+        return 1;
+    };
 
     AbortFlag abort;
     abort.local = reinterpret_cast<volatile int *>(tmem_slot_ptr + 1);
@@ -331,6 +364,7 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
             mbar_init(o_ready(t), 1);
         }
         mbar_init(drain, 1);
+        mbar_init(q_empty, 1);
         *abort.local = 0;
         fence_mbar_init();
     }
@@ -360,34 +394,49 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
         setmaxnreg_dec<Cfg::CONTROL_REGS>();
         if (lane == 0) {
             bool ok = true;
-            mbar_arrive_expect_tx(q_full, Cfg::TILES * Cfg::TILE_BYTES);
-            for (int t = 0; t < Cfg::TILES; ++t) {
-#pragma unroll
-                for (int a = 0; a < Cfg::ATOMS; ++a)
-                    tma_load_3d(sQ + t * Cfg::TILE_BYTES + a * Cfg::ATOM_BYTES, &tmap_q, q_full, a * 64,
-                                (2 * grp + t) * Cfg::BQ, bh);
-            }
-            for (int j = 0; ok && j < nb1; ++j) {
-                const int slot = j % S;
-                const uint32_t ph = (j / S) & 1u;
-                if (!wait_phase(k_empty(slot), ph ^ 1u, abort, limit, kSiteProducerEmpty)) {
+            int kvc = 0;   // key blocks loaded by this CTA so far (the K/V rings' position)
+            int it = 0;
+            for (int k = 0; ok; ++k) {
+                int grp, bh, nb0, nb1;
+                const int have = item_of(k, grp, bh, nb0, nb1);
+                if (have < 0) break;
+                if (have == 0) continue;
+                (void)nb0;
+                // The previous item's score MMAs, the readers of Q, are complete.
+                if (it > 0 && !wait_phase(q_empty, (it - 1) & 1u, abort, limit, kSiteProducerEmpty)) {
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(k_full(slot), Cfg::TILE_BYTES);
+                mbar_arrive_expect_tx(q_full, Cfg::TILES * Cfg::TILE_BYTES);
+                for (int t = 0; t < Cfg::TILES; ++t) {
 #pragma unroll
-                for (int a = 0; a < Cfg::ATOMS; ++a)
-                    tma_load_3d(sK + slot * Cfg::TILE_BYTES + a * Cfg::ATOM_BYTES, &tmap_k, k_full(slot), a * 64,
-                                j * Cfg::BKV, bh);
-                if (!wait_phase(v_empty(slot), ph ^ 1u, abort, limit, kSiteProducerEmpty)) {
-                    ok = false;
-                    break;
+                    for (int a = 0; a < Cfg::ATOMS; ++a)
+                        tma_load_3d(sQ + t * Cfg::TILE_BYTES + a * Cfg::ATOM_BYTES, &tmap_q, q_full, a * 64,
+                                    (2 * grp + t) * Cfg::BQ, bh);
                 }
-                mbar_arrive_expect_tx(v_full(slot), Cfg::TILE_BYTES);
+                for (int j = 0; j < nb1; ++j, ++kvc) {
+                    const int slot = kvc % S;
+                    const uint32_t ph = (kvc / S) & 1u;
+                    if (!wait_phase(k_empty(slot), ph ^ 1u, abort, limit, kSiteProducerEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(k_full(slot), Cfg::TILE_BYTES);
 #pragma unroll
-                for (int a = 0; a < Cfg::ATOMS; ++a)
-                    tma_load_3d(sV + slot * Cfg::TILE_BYTES + a * Cfg::ATOM_BYTES, &tmap_v, v_full(slot), a * 64,
-                                j * Cfg::BKV, bh);
+                    for (int a = 0; a < Cfg::ATOMS; ++a)
+                        tma_load_3d(sK + slot * Cfg::TILE_BYTES + a * Cfg::ATOM_BYTES, &tmap_k, k_full(slot),
+                                    a * 64, j * Cfg::BKV, bh);
+                    if (!wait_phase(v_empty(slot), ph ^ 1u, abort, limit, kSiteProducerEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(v_full(slot), Cfg::TILE_BYTES);
+#pragma unroll
+                    for (int a = 0; a < Cfg::ATOMS; ++a)
+                        tma_load_3d(sV + slot * Cfg::TILE_BYTES + a * Cfg::ATOM_BYTES, &tmap_v, v_full(slot),
+                                    a * 64, j * Cfg::BKV, bh);
+                }
+                ++it;
             }
             if (!ok) {
                 // Let every load this thread issued land before the CTA exits
@@ -402,8 +451,10 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
         // ------------------------------------------------------------ MMA issuer
         setmaxnreg_dec<Cfg::CONTROL_REGS>();
         if (lane == 0) {
-            bool ok = wait_phase(q_full, 0, abort, limit, kSiteMmaFull);
+            bool ok = true;
             bool issued_any = false;
+            int kvb = 0;          // key blocks of this CTA's earlier items (the K/V rings' position)
+            int bc[2] = {0, 0};   // each tile's blocks in this CTA's earlier items
             const uint64_t q_desc0 = smem_desc_sw128(sQ, 16, 1024);
             const uint64_t k_desc0 = smem_desc_sw128(sK, 16, 1024);
             const uint64_t v_desc0 = smem_desc_sw128(sV, Cfg::ATOM_BYTES, 1024);
@@ -415,8 +466,8 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
             // S^t_j = Q^t K_j^T into tile t's score buffer; the second user of
             // a K slot (tile 1) releases it.
             auto issue_s = [&](int t, int j) -> bool {
-                const int ks = j % S;
-                if (!wait_phase(k_full(ks), (j / S) & 1u, abort, limit, kSiteMmaFull)) return false;
+                const int ks = (kvb + j) % S;
+                if (!wait_phase(k_full(ks), ((kvb + j) / S) & 1u, abort, limit, kSiteMmaFull)) return false;
                 const uint32_t s_tmem = tmem_base + Cfg::TMEM_S_COL + t * Cfg::BKV;
                 const uint64_t q_desc = q_desc0 + static_cast<uint64_t>((t * Cfg::TILE_BYTES) >> 4);
                 const uint64_t k_desc = k_desc0 + static_cast<uint64_t>((ks * Cfg::TILE_BYTES) >> 4);
@@ -432,9 +483,9 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
             // O^t += P^t_j V_j (P in TMEM, over the scores it came from); the
             // second user of a V slot (tile 1) releases it.
             auto issue_pv = [&](int t, int j) -> bool {
-                const int vs = j % S;
-                if (!wait_phase(v_full(vs), (j / S) & 1u, abort, limit, kSiteMmaFull) ||
-                    !wait_phase(p_full(t), j & 1u, abort, limit, kSiteMmaTmemEmpty))
+                const int vs = (kvb + j) % S;
+                if (!wait_phase(v_full(vs), ((kvb + j) / S) & 1u, abort, limit, kSiteMmaFull) ||
+                    !wait_phase(p_full(t), (bc[t] + j) & 1u, abort, limit, kSiteMmaTmemEmpty))
                     return false;
                 tc_fence_after_sync();
                 const uint32_t p_tmem = tmem_base + Cfg::TMEM_S_COL + t * Cfg::BKV;
@@ -451,18 +502,45 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
                 mma_commit(o_ready(t));
                 return true;
             };
-            if (ok) ok = issue_s(0, 0) && issue_s(1, 0);
-            for (int j = 0; ok && j < nb1; ++j) {
-                if (j < nb0) {
-                    if (!issue_pv(0, j) || (j + 1 < nb0 && !issue_s(0, j + 1))) {
-                        ok = false;
-                        break;
-                    }
-                }
-                if (!issue_pv(1, j) || (j + 1 < nb1 && !issue_s(1, j + 1))) {
+            int it = 0;
+            for (int k = 0; ok; ++k) {
+                int grp, bh, nb0, nb1;
+                const int have = item_of(k, grp, bh, nb0, nb1);
+                if (have < 0) break;
+                if (have == 0) continue;
+                (void)grp;
+                (void)bh;
+                // This item's Q is in shared memory.  Its first score MMAs follow
+                // the previous item's last products in the stream: tile t's
+                // score buffer holds that item's last P until then, and each
+                // tile's output is overwritten (accumulate = 0 at block 0) only
+                // once the softmax warps, done with the previous item's output,
+                // have handed over this item's first P.
+                if (!wait_phase(q_full, it & 1u, abort, limit, kSiteMmaFull)) {
                     ok = false;
                     break;
                 }
+                ok = issue_s(0, 0) && issue_s(1, 0);
+                // The item's last score MMA is S^1_{nb1-1}; once it completes, Q
+                // may be overwritten with the next item's.
+                if (ok && nb1 == 1) mma_commit(q_empty);
+                for (int j = 0; ok && j < nb1; ++j) {
+                    if (j < nb0) {
+                        if (!issue_pv(0, j) || (j + 1 < nb0 && !issue_s(0, j + 1))) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                    if (!issue_pv(1, j) || (j + 1 < nb1 && !issue_s(1, j + 1))) {
+                        ok = false;
+                        break;
+                    }
+                    if (j + 2 == nb1) mma_commit(q_empty);
+                }
+                kvb += nb1;
+                bc[0] += nb0;
+                bc[1] += nb1;
+                ++it;
             }
             if (!ok) {
                 if (issued_any) {
@@ -480,128 +558,138 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
         const int t = warp / Cfg::TILE_WARPS;        // query tile
         const int q = warp & 3;                      // TMEM lane quarter
         const int row_local = q * 32 + lane;
-        const int row = (2 * grp + t) * Cfg::BQ + row_local;
-        const int nblk = t == 0 ? nb0 : nb1;
         const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
         const uint32_t s_base = tmem_base + lane_addr + Cfg::TMEM_S_COL + t * Cfg::BKV;
         const uint32_t o_addr = tmem_base + lane_addr + Cfg::TMEM_O_COL + t * 128;
         constexpr int NK = Cfg::BKV;   // keys per block
-        float m_ref = -INFINITY;       // reference maximum (log2 units, scaled scores)
-        float l = 0.0f;                // row sum of weights relative to m_ref
         bool ok = true;
-        for (int j = 0; j < nblk; ++j) {
-            const bool got = wait_phase(s_full(t), j & 1u, abort, limit, kSiteEpilogueTmemFull);
-            if (!__all_sync(0xffffffffu, got)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after_sync();
-            // The row's 128 raw scores of block j; the scale (positive) is
-            // applied inside the exponent's argument.
-            float x[NK];
-            {
-                uint32_t r[4][32];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) attn_tmem_ld32_nowait(s_base + c * 32, r[c]);
-                attn_tmem_wait_ld();
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(r[c][i]);
-            }
-            const int key0 = j * Cfg::BKV;
-            const int last_key = p.causal ? min(row, p.seq - 1) : p.seq - 1;
-            if (key0 + NK - 1 > last_key) {
-#pragma unroll
-                for (int i = 0; i < NK; ++i)
-                    if (key0 + i > last_key) x[i] = -INFINITY;
-            }
-            // Maximum as eight independent chains of three-input maxima.
-            float m8[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                m8[k] = max3(x[16 * k], x[16 * k + 1], x[16 * k + 2]);
-#pragma unroll
-                for (int i = 3; i < 15; i += 2) m8[k] = max3(m8[k], x[16 * k + i], x[16 * k + i + 1]);
-                m8[k] = fmaxf(m8[k], x[16 * k + 15]);
-            }
-            const float mx = max3(max3(m8[0], m8[1], m8[2]), max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7])) *
-                             p.scale_log2;
-            // Move the reference only when the block's maximum exceeds it by
-            // more than 8 (weights then stay <= 2^8).
-            float alpha = 1.0f;
-            if (mx > m_ref + 8.0f) {
-                alpha = ex2_approx(m_ref - mx);   // 0 on the first block (m_ref = -inf)
-                l *= alpha;
-                m_ref = mx;
-            }
-            const bool rescale = j > 0 && __any_sync(0xffffffffu, alpha != 1.0f);
-            // P (fp16 pairs) into TMEM over the scores of this block: keys
-            // 32c .. 32c+31 are columns 16c .. 16c+15 of the buffer, scores
-            // this thread has already read into registers.
-            float lsum0 = 0.0f, lsum1 = 0.0f;
-            const float neg_m = -m_ref;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t w[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float a0, a1;   // s * c - m for the pair, one packed instruction
-                    fma2_bcast(a0, a1, x[32 * c + 2 * i], x[32 * c + 2 * i + 1], p.scale_log2, neg_m);
-                    const float p0 = ex2_approx(a0);
-                    const float p1 = ex2_approx(a1);
-                    add2(lsum0, lsum1, p0, p1);
-                    const __half2 v = __floats2half2_rn(p0, p1);
-                    w[i] = *reinterpret_cast<const uint32_t *>(&v);
+        int bc = 0;   // this tile's blocks in the CTA's earlier items (the barriers' phases)
+        for (int k = 0; ok; ++k) {
+            int grp, bh, nb0, nb1;
+            const int have = item_of(k, grp, bh, nb0, nb1);
+            if (have < 0) break;
+            if (have == 0) continue;
+            const int row = (2 * grp + t) * Cfg::BQ + row_local;
+            const int nblk = t == 0 ? nb0 : nb1;
+            float m_ref = -INFINITY;       // reference maximum (log2 units, scaled scores)
+            float l = 0.0f;                // row sum of weights relative to m_ref
+            for (int j = 0; j < nblk; ++j) {
+                const bool got = wait_phase(s_full(t), (bc + j) & 1u, abort, limit, kSiteEpilogueTmemFull);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
                 }
-                attn_tmem_st16_nowait(s_base + c * 16, w);
-            }
-            l += lsum0 + lsum1;
-            if (rescale) {
-                // The output holds exactly blocks 0 .. j-1 (see the MMA order
-                // above): rescale the row's dim columns.
-#pragma unroll
-                for (int c = 0; c < kDim / 32; ++c) {
-                    uint32_t r[32];
-                    attn_tmem_ld32(o_addr + c * 32, r);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                    attn_tmem_st32(o_addr + c * 32, r);
-                }
-            }
-            attn_tmem_wait_st();
-            tc_fence_before_sync();   // P (and a rescaled O) in TMEM before the MMA is told
-            __syncwarp();
-            if (lane == 0) mbar_arrive(p_full(t));
-        }
-        if (ok) {
-            // The MMAs of the tile's last block (one phase per block; those of
-            // the block before completed before its scores did).
-            const int jl = nblk - 1;
-            const bool got_o = wait_phase(o_ready(t), jl & 1u, abort, limit, kSiteEpilogueTmemFull);
-            if (__all_sync(0xffffffffu, got_o)) {
                 tc_fence_after_sync();
-                const float inv_l = 1.0f / l;
-                __half *orow = p.O + (static_cast<int64_t>(bh) * p.seq + row) * kDim;
-#pragma unroll
-                for (int c = 0; c < kDim / 32; ++c) {
-                    uint32_t r[32];
-                    attn_tmem_ld32(o_addr + c * 32, r);
-                    if (row < p.seq) {
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            uint32_t w[4];
-#pragma unroll
-                            for (int h = 0; h < 4; ++h) {
-                                const __half2 hv = __floats2half2_rn(__uint_as_float(r[8 * v + 2 * h]) * inv_l,
-                                                                     __uint_as_float(r[8 * v + 2 * h + 1]) * inv_l);
-                                w[h] = *reinterpret_cast<const uint32_t *>(&hv);
+                // The row's 128 raw scores of block j; the scale (positive) is
+                // applied inside the exponent's argument.
+                float x[NK];
+                {
+                    uint32_t r[4][32];
+    #pragma unroll
+                    for (int c = 0; c < 4; ++c) attn_tmem_ld32_nowait(s_base + c * 32, r[c]);
+                    attn_tmem_wait_ld();
+    #pragma unroll
+                    for (int c = 0; c < 4; ++c)
+    #pragma unroll
+                        for (int i = 0; i < 32; ++i) x[c * 32 + i] = __uint_as_float(r[c][i]);
+                }
+                const int key0 = j * Cfg::BKV;
+                const int last_key = p.causal ? min(row, p.seq - 1) : p.seq - 1;
+                if (key0 + NK - 1 > last_key) {
+    #pragma unroll
+                    for (int i = 0; i < NK; ++i)
+                        if (key0 + i > last_key) x[i] = -INFINITY;
+                }
+                // Maximum as eight independent chains of three-input maxima.
+                float m8[8];
+    #pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    m8[k] = max3(x[16 * k], x[16 * k + 1], x[16 * k + 2]);
+    #pragma unroll
+                    for (int i = 3; i < 15; i += 2) m8[k] = max3(m8[k], x[16 * k + i], x[16 * k + i + 1]);
+                    m8[k] = fmaxf(m8[k], x[16 * k + 15]);
+                }
+                const float mx = max3(max3(m8[0], m8[1], m8[2]), max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7])) *
+                                 p.scale_log2;
+                // Move the reference only when the block's maximum exceeds it by
+                // more than 8 (weights then stay <= 2^8).
+                float alpha = 1.0f;
+                if (mx > m_ref + 8.0f) {
+                    alpha = ex2_approx(m_ref - mx);   // 0 on the first block (m_ref = -inf)
+                    l *= alpha;
+                    m_ref = mx;
+                }
+                const bool rescale = j > 0 && __any_sync(0xffffffffu, alpha != 1.0f);
+                // P (fp16 pairs) into TMEM over the scores of this block: keys
+                // 32c .. 32c+31 are columns 16c .. 16c+15 of the buffer, scores
+                // this thread has already read into registers.
+                float lsum0 = 0.0f, lsum1 = 0.0f;
+                const float neg_m = -m_ref;
+    #pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t pw[16];
+    #pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        float a0, a1;   // s * c - m for the pair, one packed instruction
+                        fma2_bcast(a0, a1, x[32 * c + 2 * i], x[32 * c + 2 * i + 1], p.scale_log2, neg_m);
+                        const float p0 = ex2_approx(a0);
+                        const float p1 = ex2_approx(a1);
+                        add2(lsum0, lsum1, p0, p1);
+                        const __half2 v = __floats2half2_rn(p0, p1);
+                        pw[i] = *reinterpret_cast<const uint32_t *>(&v);
+                    }
+                    attn_tmem_st16_nowait(s_base + c * 16, pw);
+                }
+                l += lsum0 + lsum1;
+                if (rescale) {
+                    // The output holds exactly blocks 0 .. j-1 (see the MMA order
+                    // above): rescale the row's dim columns.
+    #pragma unroll
+                    for (int c = 0; c < kDim / 32; ++c) {
+                        uint32_t r[32];
+                        attn_tmem_ld32(o_addr + c * 32, r);
+    #pragma unroll
+                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                        attn_tmem_st32(o_addr + c * 32, r);
+                    }
+                }
+                attn_tmem_wait_st();
+                tc_fence_before_sync();   // P (and a rescaled O) in TMEM before the MMA is told
+                __syncwarp();
+                if (lane == 0) mbar_arrive(p_full(t));
+            }
+            if (ok) {
+                // The MMAs of the tile's last block (one phase per block; those of
+                // the block before completed before its scores did).
+                const int jl = bc + nblk - 1;
+                const bool got_o = wait_phase(o_ready(t), jl & 1u, abort, limit, kSiteEpilogueTmemFull);
+                if (!__all_sync(0xffffffffu, got_o)) {
+                    ok = false;
+                } else {
+                    tc_fence_after_sync();
+                    const float inv_l = 1.0f / l;
+                    __half *orow = p.O + (static_cast<int64_t>(bh) * p.seq + row) * kDim;
+    #pragma unroll
+                    for (int c = 0; c < kDim / 32; ++c) {
+                        uint32_t r[32];
+                        attn_tmem_ld32(o_addr + c * 32, r);
+                        if (row < p.seq) {
+    #pragma unroll
+                            for (int v = 0; v < 4; ++v) {
+                                uint32_t wv[4];
+    #pragma unroll
+                                for (int h = 0; h < 4; ++h) {
+                                    const __half2 hv = __floats2half2_rn(__uint_as_float(r[8 * v + 2 * h]) * inv_l,
+                                                                         __uint_as_float(r[8 * v + 2 * h + 1]) * inv_l);
+                                    wv[h] = *reinterpret_cast<const uint32_t *>(&hv);
+                                }
+                                st_global_v4(orow + c * 32 + v * 8, wv[0], wv[1], wv[2], wv[3]);
                             }
-                            st_global_v4(orow + c * 32 + v * 8, w[0], w[1], w[2], w[3]);
                         }
                     }
                 }
             }
+            bc += nblk;
         }
     }
 

@@ -82,6 +82,17 @@ def test_edge_lengths(g, seq, dim, causal):
     assert_close(run(g, Q, K, V, causal, sm), ref, f"seq {seq} dim {dim} causal {causal}")
 
 
+@pytest.mark.parametrize("seq", [640, 1152])
+@pytest.mark.parametrize("causal", [False, True])
+def test_many_items_per_cta(g, seq, causal):
+    # 3 x 40 heads: more work items than CTAs, so every CTA walks several;
+    # with the causal mask an odd count of query-block pairs (3 and 5) leaves
+    # a middle pair with no partner in its head
+    Q, K, V = draw_attention(3, 40, seq, 64, seed=seq + int(causal))
+    ref = oracle.attention_fwd(Q, K, V, sm_scale=0.125, causal=causal)
+    assert_close(run(g, Q, K, V, causal, 0.125), ref, f"3x40 heads seq {seq} causal {causal}")
+
+
 def test_zero_queries_average_the_values(g):
     Q = torch.zeros((1, 4, 300, 128), dtype=torch.float16)
     _, K, V = draw_attention(1, 4, 300, 128, seed=77)
