@@ -10,8 +10,9 @@
 // score matrix is never stored.
 //
 // A persistent grid (one CTA per SM) walks the work items (pair of query
-// blocks, head, batch), heavier causal pairs first, each CTA taking every
-// G-th item; per item two query tiles of 128 rows share every K/V block.
+// blocks, head, batch) head by head, causal items paired heaviest with
+// lightest so that each CTA's share has the same work (see item_of below);
+// per item two query tiles of 128 rows share every K/V block.
 // The next item's Q is loaded once the current item's last score MMAs are
 // complete and its first score MMAs follow the current item's last products
 // in the tensor core's stream, so an item's start overlaps the previous
