@@ -615,14 +615,18 @@ def run_ours(args):
             wa = ATTN_WORKLOADS[name]
             Qa, Ka, Va = (t.to(dev) for t in draw_attention_workload(wa))
             Oa = torch.empty_like(Qa)
+            # causal: the work queue, zero before the first launch; each launch
+            # leaves it zero, so one serves all launches on this stream
+            with torch.cuda.stream(stream):
+                qa = torch.zeros(2, dtype=torch.int32, device=dev)
             for _ in range(3):
-                g.attention_fwd(Qa, Ka, Va, O=Oa, causal=wa.causal, stream=stream)
+                g.attention_fwd(Qa, Ka, Va, O=Oa, causal=wa.causal, stream=stream, queue=qa)
             torch.cuda.synchronize()
             sa, ea = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             reps_a = max(10, args.steps // 2)
             sa.record(stream)
             for _ in range(reps_a):
-                g.attention_fwd(Qa, Ka, Va, O=Oa, causal=wa.causal, stream=stream)
+                g.attention_fwd(Qa, Ka, Va, O=Oa, causal=wa.causal, stream=stream, queue=qa)
             ea.record(stream)
             ea.synchronize()
             msa = sa.elapsed_time(ea) / reps_a
@@ -634,8 +638,9 @@ def run_ours(args):
                                "roofline": {"bound": "tensor", "achieved": tfa, "peak": peak, "unit": "TFLOP/s",
                                             "frac": tfa / peak,
                                             "peak_source": f"{peak_src} bf16 matmul burst (fp16 rate)"},
-                               "flops_counted": "4 batch heads seq^2 dim (halved when causal)", "launches": reps_a}
-            del Qa, Ka, Va, Oa
+                               "flops_counted": "4 batch heads seq^2 dim (halved when causal)", "launches": reps_a,
+                               "schedule": "work queue" if wa.causal else "fixed shares"}
+            del Qa, Ka, Va, Oa, qa
 
     # ---- every configuration of the benchmark description (the shape sweep
     # and the named sizes) and a seconds-long loop of the headline workload

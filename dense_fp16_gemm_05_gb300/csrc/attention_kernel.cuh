@@ -11,7 +11,8 @@
 //
 // A persistent grid (one CTA per SM) walks the work items (pair of query
 // blocks, head, batch) head by head, causal items paired heaviest with
-// lightest so that each CTA's share has the same work (see item_of below);
+// lightest so that each CTA's share has the same work, or from a work queue
+// (see static_item and queue_item below);
 // per item two query tiles of 128 rows share every K/V block.
 // The next item's Q is loaded once the current item's last score MMAs are
 // complete and its first score MMAs follow the current item's last products
@@ -252,7 +253,7 @@ struct AttnCfg {
                   "register budgets exceed the launch's");
     static_assert(TMEM_O_COL + TILES * 128 <= TMEM_COLS, "TMEM columns");
     static_assert(SMEM_BYTES <= 232448, "shared memory per block on sm_103");
-    static_assert((10 + 4 * KV_STAGES) * 8 <= SMEM_CTL_BYTES, "control block");
+    static_assert((14 + 4 * KV_STAGES) * 8 <= SMEM_CTL_BYTES, "control block");
 };
 
 struct AttnParams {
@@ -263,6 +264,12 @@ struct AttnParams {
     uint64_t timeout_cycles;
     __half *O;
     unsigned long long *status;
+    // Causal only, may be null: {next ticket, CTAs done}, zero at launch and
+    // left zero at exit; with it the CTAs take work items from a shared
+    // queue (heaviest first within groups of chunk_heads heads) instead of
+    // the fixed assignment.
+    unsigned int *queue;
+    int32_t chunk_heads;
 };
 
 template <int kDim>
@@ -281,10 +288,15 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
     const uint32_t ctl = base + Cfg::SMEM_CTL_OFF;
     // Barriers (8 bytes each): q_full; k_full, k_empty, v_full, v_empty
     // [KV_STAGES] (the K and V rings); per tile s_full, p_full, o_ready;
-    // drain; q_empty; then the TMEM address slot and the abort flag.  Their
-    // phases run over all items of the CTA: the K/V ring by the CTA's running
-    // count of key blocks, s_full / p_full / o_ready by each tile's running
-    // count of blocks, q_full / q_empty by the item count.
+    // drain; q_empty; then the TMEM address slot and the abort flag;
+    // item_full[2]; the item ring[2] (query-block pair and head-batch index
+    // of the CTA's item k in entry k % 2, written by the producer before it
+    // arrives on item_full[k % 2]).  Their phases run over all items of the
+    // CTA: the K/V ring by the CTA's running count of key blocks, s_full /
+    // p_full / o_ready by each tile's running count of blocks, q_full /
+    // q_empty / item_full by the item count.  The producer publishes item
+    // k + 2 only after item k + 1's score MMAs are complete (q_empty), when
+    // both tiles' softmax warps are past reading entry k.
     //
     // Order of the MMA stream: S^0_0, S^1_0, then per block j and tile t:
     // O^t += P^t_j V_j, S^t_{j+1}.  Tile t's score buffer is rewritten by
@@ -306,42 +318,63 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
     const uint32_t abort_addr = tmem_slot + 4;
     volatile uint32_t *tmem_slot_ptr =
         reinterpret_cast<volatile uint32_t *>(base_ptr + Cfg::SMEM_CTL_OFF + 8 * (9 + 4 * S));
+    auto item_full = [&](int i) { return ctl + 8u * (10 + 4 * S + i); };
+    volatile int *ring = reinterpret_cast<volatile int *>(base_ptr + Cfg::SMEM_CTL_OFF + 8 * (12 + 4 * S));
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     // Work items: an item is a pair of query blocks grp (tile t covers query
-    // block 2 * grp + t) of one head-batch index bh.  With the causal mask the
-    // items are grouped two by two into super-items of one head, the heaviest
-    // pair with the lightest, the next heaviest with the next lightest, ...,
-    // so that every super-item has the same number of key blocks; without it
-    // every item has the same work and a super-item is one item.  Super-items
-    // are numbered head by head, and CTA c takes super-items c, c + G, ... (G
-    // CTAs): at any time the CTAs work on a few heads at once, whose K and V
-    // the L2 then serves to all of them.  item_of(k) decodes this CTA's k-th
-    // item: 1 = an item, 0 = none at this k (the middle pair of an odd count),
-    // -1 = no more.
+    // block 2 * grp + t) of one head-batch index bh.
+    //
+    // Fixed assignment: with the causal mask the items are grouped two by two
+    // into super-items of one head, the heaviest pair with the lightest, the
+    // next heaviest with the next lightest, ..., so that every super-item has
+    // the same number of key blocks; without it every item has the same work
+    // and a super-item is one item.  Super-items are numbered head by head,
+    // and CTA c takes super-items c, c + G, ... (G CTAs): at any time the CTAs
+    // work on a few heads at once, whose K and V the L2 then serves to all of
+    // them.  static_item(k) decodes this CTA's k-th item: 1 = an item, 0 =
+    // none at this k (the middle pair of an odd count), -1 = no more.
+    //
+    // Work queue (causal, p.queue given): items are numbered in groups of
+    // chunk_heads heads, heaviest pairs first within a group, so that the
+    // light items come last in each group and the CTAs finish together; CTA c
+    // starts with item c and then takes item G + the next ticket.
     const int n_grp = (p.num_q_blocks + Cfg::TILES - 1) / Cfg::TILES;
+    const int hb_count = p.batch * p.heads;
+    const bool use_queue = p.causal && p.queue != nullptr;
+    const int num_items = n_grp * hb_count;
     const int sup_shift = p.causal ? 1 : 0;   // log2 of the items per super-item
     const int n_sub = p.causal ? (n_grp + 1) / 2 : n_grp;
-    const int num_super = n_sub * p.batch * p.heads;
+    const int num_super = n_sub * hb_count;
     const int first = static_cast<int>(blockIdx.x), stride = static_cast<int>(gridDim.x);
     const int kv_blocks_all = (p.seq + Cfg::BKV - 1) / Cfg::BKV;
-    // Key blocks of each tile (tile 1 never needs fewer than tile 0; both >= 1).
-    auto item_of = [&](int k, int &grp, int &bh, int &nb0, int &nb1) -> int {
+    auto static_item = [&](int k, int &grp, int &bh) -> int {
         const int sup = first + (k >> sup_shift) * stride;
         if (sup >= num_super) return -1;
         bh = sup / n_sub;
         const int kp = sup - bh * n_sub;
         if (!p.causal) {
             grp = kp;
-            nb0 = nb1 = kv_blocks_all;
             return 1;
         }
         grp = (k & 1) ? kp : n_grp - 1 - kp;
         if ((k & 1) && grp == n_grp - 1 - kp) return 0;
-        nb0 = min(2 * grp + 1, kv_blocks_all);
-        nb1 = min(2 * grp + 2, kv_blocks_all);
         return 1;
+    };
+    auto queue_item = [&](int w, int &grp, int &bh) {
+        const int per_chunk = p.chunk_heads * n_grp;
+        const int c = w / per_chunk;
+        const int h0 = c * p.chunk_heads;
+        const int ych = min(p.chunk_heads, hb_count - h0);
+        const int r = w - c * per_chunk;
+        grp = n_grp - 1 - r / ych;
+        bh = h0 + (r - (r / ych) * ych);
+    };
+    // Key blocks of each tile (tile 1 never needs fewer than tile 0; both >= 1).
+    auto tile_blocks = [&](int grp, int &nb0, int &nb1) {
+        nb0 = p.causal ? min(2 * grp + 1, kv_blocks_all) : kv_blocks_all;
+        nb1 = p.causal ? min(2 * grp + 2, kv_blocks_all) : kv_blocks_all;
     };
 
     AbortFlag abort;
@@ -366,6 +399,8 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
         }
         mbar_init(drain, 1);
         mbar_init(q_empty, 1);
+        mbar_init(item_full(0), 1);
+        mbar_init(item_full(1), 1);
         *abort.local = 0;
         fence_mbar_init();
     }
@@ -396,18 +431,30 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
         if (lane == 0) {
             bool ok = true;
             int kvc = 0;   // key blocks loaded by this CTA so far (the K/V rings' position)
-            int it = 0;
-            for (int k = 0; ok; ++k) {
-                int grp, bh, nb0, nb1;
-                const int have = item_of(k, grp, bh, nb0, nb1);
-                if (have < 0) break;
-                if (have == 0) continue;
-                (void)nb0;
-                // The previous item's score MMAs, the readers of Q, are complete.
+            int ks = 0;    // position in the fixed assignment
+            for (int it = 0; ok; ++it) {
+                int grp = -1, bh = 0;
+                if (use_queue) {
+                    const int w = it == 0 ? first : stride + static_cast<int>(atomicAdd(p.queue, 1u));
+                    if (w < num_items) queue_item(w, grp, bh);
+                } else {
+                    int have;
+                    while ((have = static_item(ks++, grp, bh)) == 0) {
+                    }
+                    if (have < 0) grp = -1;
+                }
+                // Item it - 1's score MMAs, the readers of Q, are complete (and
+                // every consumer is past ring entry it - 2).
                 if (it > 0 && !wait_phase(q_empty, (it - 1) & 1u, abort, limit, kSiteProducerEmpty)) {
                     ok = false;
                     break;
                 }
+                ring[2 * (it & 1)] = grp;   // grp < 0: no more items
+                ring[2 * (it & 1) + 1] = bh;
+                mbar_arrive(item_full(it & 1));
+                if (grp < 0) break;
+                int nb0, nb1;
+                tile_blocks(grp, nb0, nb1);
                 mbar_arrive_expect_tx(q_full, Cfg::TILES * Cfg::TILE_BYTES);
                 for (int t = 0; t < Cfg::TILES; ++t) {
 #pragma unroll
@@ -437,7 +484,14 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
                         tma_load_3d(sV + slot * Cfg::TILE_BYTES + a * Cfg::ATOM_BYTES, &tmap_v, v_full(slot),
                                     a * 64, j * Cfg::BKV, bh);
                 }
-                ++it;
+            }
+            if (use_queue) {
+                // Every CTA stops taking tickets before it counts itself done;
+                // the last one to count leaves the queue zero for the next launch.
+                if (atomicAdd(p.queue + 1, 1u) == gridDim.x - 1u) {
+                    atomicExch(p.queue, 0u);
+                    atomicExch(p.queue + 1, 0u);
+                }
             }
             if (!ok) {
                 // Let every load this thread issued land before the CTA exits
@@ -503,14 +557,15 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
                 mma_commit(o_ready(t));
                 return true;
             };
-            int it = 0;
-            for (int k = 0; ok; ++k) {
-                int grp, bh, nb0, nb1;
-                const int have = item_of(k, grp, bh, nb0, nb1);
-                if (have < 0) break;
-                if (have == 0) continue;
-                (void)grp;
-                (void)bh;
+            for (int it = 0; ok; ++it) {
+                if (!wait_phase(item_full(it & 1), (it >> 1) & 1u, abort, limit, kSiteMmaFull)) {
+                    ok = false;
+                    break;
+                }
+                const int grp = ring[2 * (it & 1)];
+                if (grp < 0) break;
+                int nb0, nb1;
+                tile_blocks(grp, nb0, nb1);
                 // This item's Q is in shared memory.  Its first score MMAs follow
                 // the previous item's last products in the stream: tile t's
                 // score buffer holds that item's last P until then, and each
@@ -541,7 +596,6 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
                 kvb += nb1;
                 bc[0] += nb0;
                 bc[1] += nb1;
-                ++it;
             }
             if (!ok) {
                 if (issued_any) {
@@ -565,11 +619,17 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
         constexpr int NK = Cfg::BKV;   // keys per block
         bool ok = true;
         int bc = 0;   // this tile's blocks in the CTA's earlier items (the barriers' phases)
-        for (int k = 0; ok; ++k) {
-            int grp, bh, nb0, nb1;
-            const int have = item_of(k, grp, bh, nb0, nb1);
-            if (have < 0) break;
-            if (have == 0) continue;
+        for (int it = 0; ok; ++it) {
+            const bool got_item = wait_phase(item_full(it & 1), (it >> 1) & 1u, abort, limit, kSiteEpilogueTmemFull);
+            if (!__all_sync(0xffffffffu, got_item)) {
+                ok = false;
+                break;
+            }
+            const int grp = ring[2 * (it & 1)];
+            const int bh = ring[2 * (it & 1) + 1];
+            if (grp < 0) break;
+            int nb0, nb1;
+            tile_blocks(grp, nb0, nb1);
             const int row = (2 * grp + t) * Cfg::BQ + row_local;
             const int nblk = t == 0 ? nb0 : nb1;
             float m_ref = -INFINITY;       // reference maximum (log2 units, scaled scores)

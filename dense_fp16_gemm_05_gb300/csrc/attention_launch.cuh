@@ -15,6 +15,7 @@ struct AttnLaunchArgs {
     DeviceInfo dev;
     cudaStream_t stream = nullptr;
     unsigned long long *status = nullptr;
+    unsigned int *queue = nullptr;   // caller's work queue (two zero words), or null
 };
 
 // (batch * heads, seq, dim) fp16 tensor as a 3-D tensor map with boxes of

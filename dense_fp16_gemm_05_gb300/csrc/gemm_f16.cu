@@ -775,6 +775,13 @@ extern "C" int gemm_fp8_launch_info(int64_t M, int64_t N, int64_t K, int *grid_c
 extern "C" int attention_fwd_f16(const void *Q, const void *K, const void *V, void *O, int64_t batch,
                                  int64_t heads, int64_t seq, int64_t dim, float sm_scale, int causal, void *stream)
 {
+    return attention_fwd_f16_queue(Q, K, V, O, batch, heads, seq, dim, sm_scale, causal, nullptr, stream);
+}
+
+extern "C" int attention_fwd_f16_queue(const void *Q, const void *K, const void *V, void *O, int64_t batch,
+                                       int64_t heads, int64_t seq, int64_t dim, float sm_scale, int causal,
+                                       unsigned int *queue, void *stream)
+{
     if (batch < 0 || heads < 0 || seq < 0) return reject(GEMM_ERR_INVALID_ARG, "a size is negative");
     if (dim != 64 && dim != 128) return reject(GEMM_ERR_INVALID_ARG, "dim is not 64 or 128");
     if (causal != 0 && causal != 1) return reject(GEMM_ERR_INVALID_ARG, "causal is not 0 or 1");
@@ -793,6 +800,13 @@ extern "C" int attention_fwd_f16(const void *Q, const void *K, const void *V, vo
     if ((st = check_device_buffer(O, bytes, dev.device)) != GEMM_OK) return st;
     if (ranges_overlap(O, bytes, Q, bytes) || ranges_overlap(O, bytes, K, bytes) || ranges_overlap(O, bytes, V, bytes))
         return reject(GEMM_ERR_INVALID_ARG, "O overlaps Q, K or V");
+    if (causal && queue != nullptr) {
+        const uint64_t qb = 2 * sizeof(unsigned int);
+        if ((st = check_device_buffer(queue, qb, dev.device, 4)) != GEMM_OK) return st;
+        if (ranges_overlap(queue, qb, O, bytes) || ranges_overlap(queue, qb, Q, bytes) ||
+            ranges_overlap(queue, qb, K, bytes) || ranges_overlap(queue, qb, V, bytes))
+            return reject(GEMM_ERR_INVALID_ARG, "queue overlaps Q, K, V or O");
+    }
     AttnLaunchArgs a;
     a.Q = Q;
     a.K = K;
@@ -808,6 +822,7 @@ extern "C" int attention_fwd_f16(const void *Q, const void *K, const void *V, vo
     a.stream = static_cast<cudaStream_t>(stream);
     a.status = status_word(dev.device);
     if (a.status == nullptr) return GEMM_ERR_CUDA;
+    a.queue = causal ? queue : nullptr;
     return launch_attention(a);
 }
 

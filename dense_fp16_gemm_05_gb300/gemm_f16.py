@@ -106,6 +106,8 @@ def lib() -> ctypes.CDLL:
     L.gemm_f16_selftest_timeout.restype = ci
     L.attention_fwd_f16.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_float, ci, vp]
     L.attention_fwd_f16.restype = ci
+    L.attention_fwd_f16_queue.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_float, ci, vp, vp]
+    L.attention_fwd_f16_queue.restype = ci
     L.gemm_fp8_block_scaled.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ci, vp]
     L.gemm_fp8_block_scaled.restype = ci
     L.gemm_mxfp8_block_scaled.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, ci, vp]
@@ -492,13 +494,29 @@ def fp8_launch_info(M: int, N: int, K: int) -> dict:
     return {"grid_ctas": g.value, "tiles": t.value}
 
 
+def _launch_stream(stream, device) -> torch.cuda.Stream:
+    if stream is None:
+        return torch.cuda.current_stream(device)
+    if isinstance(stream, torch.cuda.Stream):
+        return stream
+    return torch.cuda.ExternalStream(int(stream), device=device)
+
+
 def attention_fwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, O: torch.Tensor | None = None,
-                  sm_scale: float | None = None, causal: bool = False, stream=None) -> torch.Tensor:
+                  sm_scale: float | None = None, causal: bool = False, stream=None,
+                  queue: torch.Tensor | bool | None = None) -> torch.Tensor:
     """O = softmax(sm_scale Q K^T [causal]) V per (batch, head).
 
     Q, K, V (and O): contiguous float16 CUDA tensors of one shape
     (batch, heads, seq, dim), dim 64 or 128; sm_scale defaults to
     1/sqrt(dim).  O is allocated when not given.  Asynchronous on ``stream``.
+
+    ``queue`` (causal only): the work queue of attention_fwd_f16_queue, a
+    2-element int32 CUDA tensor that is zero when the launch starts and that
+    the kernel leaves zero; one queue serves launches that run one after
+    another, launches that may overlap need one each.  None: a fresh zeroed
+    queue is made on the launch stream for this call.  False: no queue (the
+    fixed shares of attention_fwd_f16).  Results are the same bits either way.
     """
     for t, n in ((Q, "Q"), (K, "K"), (V, "V")):
         if not isinstance(t, torch.Tensor) or t.dtype != torch.float16 or t.dim() != 4 or not t.is_contiguous():
@@ -512,10 +530,19 @@ def attention_fwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, O: torch.Te
         O = torch.empty_like(Q)
     if O.dtype != torch.float16 or O.shape != Q.shape or not O.is_contiguous():
         raise ValueError("O must be a contiguous float16 tensor shaped like Q")
+    q_ptr = None
+    if causal and queue is not False and Q.numel() > 0:
+        if queue is None or queue is True:
+            with torch.cuda.stream(_launch_stream(stream, Q.device)):
+                queue = torch.zeros(2, dtype=torch.int32, device=Q.device)
+        if (not isinstance(queue, torch.Tensor) or queue.dtype != torch.int32 or queue.numel() < 2
+                or not queue.is_contiguous() or queue.device != Q.device):
+            raise ValueError("queue must be a contiguous int32 tensor of >= 2 elements on Q's device")
+        q_ptr = queue.data_ptr()
     L = lib()
     with _device_scope(Q.device):
-        st = L.attention_fwd_f16(Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), B, H, S, D,
-                                 float(sm_scale), int(bool(causal)), _stream_handle(stream, Q.device))
+        st = L.attention_fwd_f16_queue(Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), B, H, S, D,
+                                       float(sm_scale), int(bool(causal)), q_ptr, _stream_handle(stream, Q.device))
     if st != GEMM_OK:
-        raise GemmError(st, "attention_fwd_f16")
+        raise GemmError(st, "attention_fwd_f16_queue")
     return O

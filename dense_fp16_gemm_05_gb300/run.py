@@ -8,7 +8,9 @@ the workload (dA = dZ @ B^T in the NT layout, dB = A^T @ dZ in the TN layout)
 or the ReLU-gradient mask over an (M,N) gradient; --op fp8 runs the FP8
 block-scaled GEMM on the workload's sizes (E4M3 operands quantized per
 128-block, fp32 scales), --op mxfp8 the same with power-of-two scales; --op attn runs the attention forward on an attention
-workload (--workload attn_4096_d128, ...).
+workload (--workload attn_4096_d128, ...); causal attention takes work items
+from one work queue made before the first launch (--attn-queue fixed: the
+fixed shares instead).
 
 A minimal program around the library (no oracle, no other kernels besides the
 input upload), suited as the target of a profiler capture: every GPU kernel it
@@ -33,9 +35,10 @@ def main(argv=None):
     p.add_argument("--config", type=int, default=0)
     p.add_argument("--relu", type=int, default=None, help="override the workload's ReLU flag")
     p.add_argument("--op", default="gemm", choices=["gemm", "dA_nt", "dB_tn", "relu_backward", "fp8", "mxfp8", "attn"])
+    p.add_argument("--attn-queue", default="reuse", choices=["reuse", "fixed"])
     args = p.parse_args(argv)
     if args.op == "attn":
-        return run_attention(ATTN_WORKLOADS[args.workload], args.reps, torch.device("cuda", 0))
+        return run_attention(ATTN_WORKLOADS[args.workload], args.reps, torch.device("cuda", 0), args.attn_queue)
     if args.workload in WORKLOADS:
         w = WORKLOADS[args.workload]
     else:
@@ -107,21 +110,23 @@ def run_fp8(w, relu, reps, dev, pow2=False):
                       "best_tflops": w.flops / (min(times) * 1e-3) / 1e12}))
 
 
-def run_attention(w, reps, dev):
+def run_attention(w, reps, dev, queue_mode="reuse"):
     Q, K, V = (t.to(dev) for t in draw_attention_workload(w))
     O = torch.empty_like(Q)
+    # the kernel leaves the queue zero, so one serves every launch below
+    queue = torch.zeros(2, dtype=torch.int32, device=dev) if queue_mode == "reuse" else False
     times = []
     for _ in range(reps):
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s.record()
-        g.attention_fwd(Q, K, V, O=O, sm_scale=w.sm_scale, causal=w.causal)
+        g.attention_fwd(Q, K, V, O=O, sm_scale=w.sm_scale, causal=w.causal, queue=queue)
         e.record()
         e.synchronize()
         times.append(s.elapsed_time(e))
     st = g.check()
     if st != g.GEMM_OK:
         raise SystemExit(f"device status {st}: {g.strerror(st)}")
-    print(json.dumps({"workload": w.name, "op": "attn", "causal": w.causal, "ms": times,
+    print(json.dumps({"workload": w.name, "op": "attn", "causal": w.causal, "queue": queue_mode, "ms": times,
                       "best_tflops": w.flops / (min(times) * 1e-3) / 1e12}))
 
 

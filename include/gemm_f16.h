@@ -337,6 +337,27 @@ int gemm_fp8_launch_info(int64_t M, int64_t N, int64_t K, int *grid_ctas, int *t
 int attention_fwd_f16(const void *Q, const void *K, const void *V, void *O, int64_t batch, int64_t heads,
                       int64_t seq, int64_t dim, float sm_scale, int causal, void *stream);
 
+/*
+ * attention_fwd_f16_queue -- attention_fwd_f16 with a work queue for the
+ * causal case.  Same operation, arguments, checks and results (bit for bit:
+ * the queue changes which SM computes a query block, not how).  With the
+ * causal mask the query blocks have unequal work; attention_fwd_f16 gives
+ * every SM a fixed share, this entry lets the SMs take the next block pair
+ * from a queue, so they finish together.
+ *
+ * `queue`: device pointer to two 32-bit words, 4-byte aligned, on the current
+ * device, owned by the caller, zero when the launch starts; the kernel leaves
+ * them zero when it completes, so one queue serves any number of launches
+ * that run one after another (on one stream).  Two launches that may run at
+ * the same time (other streams, graphs) need separate queues: a shared one
+ * gives wrong results.  NULL: the fixed shares of attention_fwd_f16.  Not
+ * used when causal = 0 (every block pair has the same work).  Non-zero words
+ * at launch make the launch skip work items (results undefined; no error).
+ */
+int attention_fwd_f16_queue(const void *Q, const void *K, const void *V, void *O, int64_t batch, int64_t heads,
+                            int64_t seq, int64_t dim, float sm_scale, int causal, unsigned int *queue,
+                            void *stream);
+
 /* Operand layouts a configuration supports: bit (transa * 2 + transb) is set
  * for each supported (transa, transb); 0xF = all four, 0x1 = only (0,0).
  * GEMM_ERR_INVALID_ARG for an unknown id.  config 0 (automatic) supports all. */

@@ -206,3 +206,7 @@ def test_attention_arguments_rejected_before_cuda(g):
     assert L.attention_fwd_f16(None, None, None, None, 1, 1, 64, 64, 0.1, 2, None) == g.GEMM_ERR_INVALID_ARG
     assert L.attention_fwd_f16(None, None, None, None, 1, 1, 64, 64, float("inf"), 0, None) == g.GEMM_ERR_INVALID_ARG
     assert L.attention_fwd_f16(None, None, None, None, 0, 1, 64, 64, 0.1, 0, None) == g.GEMM_OK
+    Lq = L.attention_fwd_f16_queue
+    assert Lq(None, None, None, None, 1, 1, 64, 96, 0.1, 1, None, None) == g.GEMM_ERR_INVALID_ARG
+    assert Lq(None, None, None, None, 1, 1, 64, 64, 0.1, 2, None, None) == g.GEMM_ERR_INVALID_ARG
+    assert Lq(None, None, None, None, 0, 1, 64, 64, 0.1, 1, None, None) == g.GEMM_OK

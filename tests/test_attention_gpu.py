@@ -83,14 +83,67 @@ def test_edge_lengths(g, seq, dim, causal):
 
 
 @pytest.mark.parametrize("seq", [640, 1152])
-@pytest.mark.parametrize("causal", [False, True])
-def test_many_items_per_cta(g, seq, causal):
+@pytest.mark.parametrize("causal,queue", [(False, None), (True, None), (True, False)])
+def test_many_items_per_cta(g, seq, causal, queue):
     # 3 x 40 heads: more work items than CTAs, so every CTA walks several;
     # with the causal mask an odd count of query-block pairs (3 and 5) leaves
-    # a middle pair with no partner in its head
+    # a middle pair with no partner in its head (fixed shares), and the work
+    # queue hands out 120 x 3 or 120 x 5 items
     Q, K, V = draw_attention(3, 40, seq, 64, seed=seq + int(causal))
     ref = oracle.attention_fwd(Q, K, V, sm_scale=0.125, causal=causal)
-    assert_close(run(g, Q, K, V, causal, 0.125), ref, f"3x40 heads seq {seq} causal {causal}")
+    O = g.attention_fwd(Q.to(DEV), K.to(DEV), V.to(DEV), sm_scale=0.125, causal=causal, queue=queue)
+    assert g.check() == g.GEMM_OK
+    assert_close(O.cpu().numpy(), ref, f"3x40 heads seq {seq} causal {causal} queue {queue}")
+
+
+def _fixed_and_queued(g, shape, seed, qt):
+    Q, K, V = (t.to(DEV) for t in draw_attention(*shape, seed=seed))
+    fixed = g.attention_fwd(Q, K, V, causal=True, queue=False)
+    queued = g.attention_fwd(Q, K, V, causal=True, queue=qt)
+    return fixed, queued
+
+
+@pytest.mark.parametrize("shape", [(3, 40, 1152, 64), (1, 24, 2048, 128), (4, 32, 4096, 128)])
+def test_queue_gives_the_fixed_shares_bits_and_ends_zero(g, shape):
+    # the queue changes which SM computes a pair of query blocks, not how
+    qt = torch.zeros(2, dtype=torch.int32, device=DEV)
+    fixed, queued = _fixed_and_queued(g, shape, 300 + shape[2], qt)
+    assert g.check() == g.GEMM_OK
+    assert torch.equal(fixed, queued), f"{shape}: queue and fixed shares differ"
+    assert qt.cpu().tolist() == [0, 0]
+
+
+def test_one_queue_for_back_to_back_launches(g):
+    # three launches of different sizes share one queue on one stream with no
+    # synchronisation between them; each leaves it zero for the next
+    qt = torch.zeros(2, dtype=torch.int32, device=DEV)
+    shapes = [(2, 8, 4096, 128), (3, 40, 640, 64), (1, 4, 129, 128)]
+    inputs = [tuple(t.to(DEV) for t in draw_attention(*sh, seed=400 + i)) for i, sh in enumerate(shapes)]
+    queued = [g.attention_fwd(Q, K, V, causal=True, queue=qt) for Q, K, V in inputs]
+    fixed = [g.attention_fwd(Q, K, V, causal=True, queue=False) for Q, K, V in inputs]
+    assert g.check() == g.GEMM_OK
+    for sh, a, b in zip(shapes, queued, fixed):
+        assert torch.equal(a, b), f"{sh}: queue and fixed shares differ"
+    assert qt.cpu().tolist() == [0, 0]
+
+
+def test_queue_arguments_rejected(g):
+    Q, K, V = (t.to(DEV) for t in draw_attention(1, 2, 256, 64, seed=5))
+    O = torch.empty_like(Q)
+    L = g.lib()
+    qt = torch.zeros(4, dtype=torch.int32, device=DEV)
+    args = (Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), 1, 2, 256, 64, 0.125, 1)
+    assert L.attention_fwd_f16_queue(*args, qt.data_ptr() + 2, None) == g.GEMM_ERR_ALIGNMENT
+    assert L.attention_fwd_f16_queue(*args, O.data_ptr() + 64, None) == g.GEMM_ERR_INVALID_ARG   # inside O
+    assert L.attention_fwd_f16_queue(*args, K.data_ptr(), None) == g.GEMM_ERR_INVALID_ARG        # inside K
+    # not causal: the queue is not used, so not checked
+    nc = args[:-1] + (0,)
+    assert L.attention_fwd_f16_queue(*nc, qt.data_ptr() + 2, None) == g.GEMM_OK
+    assert g.check() == g.GEMM_OK
+    with pytest.raises(ValueError):
+        g.attention_fwd(Q, K, V, causal=True, queue=torch.zeros(2, dtype=torch.int64, device=DEV))
+    with pytest.raises(ValueError):
+        g.attention_fwd(Q, K, V, causal=True, queue=torch.zeros(1, dtype=torch.int32, device=DEV))
 
 
 def test_zero_queries_average_the_values(g):
