@@ -127,6 +127,30 @@ def test_one_queue_for_back_to_back_launches(g):
     assert qt.cpu().tolist() == [0, 0]
 
 
+@pytest.mark.parametrize("explicit_queue", [True, False])
+def test_queue_inside_a_cuda_graph(g, explicit_queue):
+    # captured once and replayed three times: an explicit queue is left zero
+    # by every replay; the binding's own queue is zeroed by a captured fill
+    Q, K, V = (t.to(DEV) for t in draw_attention(2, 24, 1536, 128, seed=77))
+    expect = g.attention_fwd(Q, K, V, causal=True, queue=False)
+    O = torch.empty_like(Q)
+    qt = torch.zeros(2, dtype=torch.int32, device=DEV) if explicit_queue else None
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    cg = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(cg, stream=s):
+        g.attention_fwd(Q, K, V, O=O, causal=True, queue=qt)
+    for _ in range(3):
+        O.fill_(float("nan"))
+        cg.replay()
+        torch.cuda.synchronize()
+        assert g.check() == g.GEMM_OK
+        assert torch.equal(O, expect)
+    if explicit_queue:
+        assert qt.cpu().tolist() == [0, 0]
+
+
 def test_queue_arguments_rejected(g):
     Q, K, V = (t.to(DEV) for t in draw_attention(1, 2, 256, 64, seed=5))
     O = torch.empty_like(Q)
