@@ -293,8 +293,8 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
     // of the CTA's item k in entry k % 2, written by the producer before it
     // arrives on item_full[k % 2]).  Their phases run over all items of the
     // CTA: the K/V ring by the CTA's running count of key blocks, s_full /
-    // p_full / o_ready by each tile's running count of blocks, q_full /
-    // q_empty / item_full by the item count.  The producer publishes item
+    // p_full by each tile's running count of blocks, q_full / q_empty /
+    // item_full / o_ready by the item count.  The producer publishes item
     // k + 2 only after item k + 1's score MMAs are complete (q_empty), when
     // both tiles' softmax warps are past reading entry k.
     //
@@ -519,10 +519,12 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
                 return static_cast<uint64_t>(((t >> 2) * Cfg::ATOM_BYTES + (t & 3) * 32) >> 4);
             };
             // S^t_j = Q^t K_j^T into tile t's score buffer; the second user of
-            // a K slot (tile 1) releases it.
-            auto issue_s = [&](int t, int j) -> bool {
+            // a K slot (tile 1) releases it.  Tile 1 waits for the K block only
+            // when tile 0 does not use it (tile 0, issued before, has seen it
+            // arrive, and the slot is not refilled before tile 1 releases it).
+            auto issue_s = [&](int t, int j, bool seen) -> bool {
                 const int ks = (kvb + j) % S;
-                if (!wait_phase(k_full(ks), ((kvb + j) / S) & 1u, abort, limit, kSiteMmaFull)) return false;
+                if (!seen && !wait_phase(k_full(ks), ((kvb + j) / S) & 1u, abort, limit, kSiteMmaFull)) return false;
                 const uint32_t s_tmem = tmem_base + Cfg::TMEM_S_COL + t * Cfg::BKV;
                 const uint64_t q_desc = q_desc0 + static_cast<uint64_t>((t * Cfg::TILE_BYTES) >> 4);
                 const uint64_t k_desc = k_desc0 + static_cast<uint64_t>((ks * Cfg::TILE_BYTES) >> 4);
@@ -536,10 +538,12 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
                 return true;
             };
             // O^t += P^t_j V_j (P in TMEM, over the scores it came from); the
-            // second user of a V slot (tile 1) releases it.
-            auto issue_pv = [&](int t, int j) -> bool {
+            // second user of a V slot (tile 1) releases it (the V block waited
+            // for as the K block above).  o_ready(t) is signalled after the
+            // tile's last product of the item only (last).
+            auto issue_pv = [&](int t, int j, bool seen, bool last) -> bool {
                 const int vs = (kvb + j) % S;
-                if (!wait_phase(v_full(vs), ((kvb + j) / S) & 1u, abort, limit, kSiteMmaFull) ||
+                if ((!seen && !wait_phase(v_full(vs), ((kvb + j) / S) & 1u, abort, limit, kSiteMmaFull)) ||
                     !wait_phase(p_full(t), (bc[t] + j) & 1u, abort, limit, kSiteMmaTmemEmpty))
                     return false;
                 tc_fence_after_sync();
@@ -554,7 +558,7 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
                     mma_f16_ts(o_tmem, p_tmem + k * 8, vb, Cfg::IDESC_O, (j > 0 || k > 0) ? 1u : 0u);
                 }
                 if (t == 1) mma_commit(v_empty(vs));
-                mma_commit(o_ready(t));
+                if (last) mma_commit(o_ready(t));
                 return true;
             };
             for (int it = 0; ok; ++it) {
@@ -576,18 +580,18 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
                     ok = false;
                     break;
                 }
-                ok = issue_s(0, 0) && issue_s(1, 0);
+                ok = issue_s(0, 0, false) && issue_s(1, 0, true);
                 // The item's last score MMA is S^1_{nb1-1}; once it completes, Q
                 // may be overwritten with the next item's.
                 if (ok && nb1 == 1) mma_commit(q_empty);
                 for (int j = 0; ok && j < nb1; ++j) {
                     if (j < nb0) {
-                        if (!issue_pv(0, j) || (j + 1 < nb0 && !issue_s(0, j + 1))) {
+                        if (!issue_pv(0, j, false, j + 1 == nb0) || (j + 1 < nb0 && !issue_s(0, j + 1, false))) {
                             ok = false;
                             break;
                         }
                     }
-                    if (!issue_pv(1, j) || (j + 1 < nb1 && !issue_s(1, j + 1))) {
+                    if (!issue_pv(1, j, j < nb0, j + 1 == nb1) || (j + 1 < nb1 && !issue_s(1, j + 1, j + 1 < nb0))) {
                         ok = false;
                         break;
                     }
@@ -720,10 +724,9 @@ __global__ void __launch_bounds__(AttnCfg<kDim>::THREADS, 1)
                 if (lane == 0) mbar_arrive(p_full(t));
             }
             if (ok) {
-                // The MMAs of the tile's last block (one phase per block; those of
-                // the block before completed before its scores did).
-                const int jl = bc + nblk - 1;
-                const bool got_o = wait_phase(o_ready(t), jl & 1u, abort, limit, kSiteEpilogueTmemFull);
+                // The MMAs of the tile's last block (one phase per item: signalled
+                // after the tile's last product; those before completed before it).
+                const bool got_o = wait_phase(o_ready(t), it & 1u, abort, limit, kSiteEpilogueTmemFull);
                 if (!__all_sync(0xffffffffu, got_o)) {
                     ok = false;
                 } else {
