@@ -231,7 +231,9 @@ struct AttnCfg {
     static constexpr int ATOMS = kDim / 64;       // 128-byte swizzle atoms along dim
     static constexpr int TILE_BYTES = 128 * kDim * 2;   // Q, K or V tile of 128 rows
     static constexpr int ATOM_BYTES = 128 * 128;        // 128 rows x 128 bytes
-    static constexpr int KV_STAGES = kDim == 64 ? 4 : 2;   // K and V ring depth (what shared memory holds)
+    // K and V ring depth: dim 128, what shared memory holds; dim 64, measured
+    // (2, 3, 4 and 6 slots: 923, 925, 911 and 906 TFLOP/s at 4 x 64 x 4096).
+    static constexpr int KV_STAGES = kDim == 64 ? 3 : 2;
     static constexpr int SMEM_Q_OFF = 0;                   // TILES query tiles
     static constexpr int SMEM_K_OFF = SMEM_Q_OFF + TILES * TILE_BYTES;
     static constexpr int SMEM_V_OFF = SMEM_K_OFF + KV_STAGES * TILE_BYTES;
