@@ -127,6 +127,26 @@ def test_one_queue_for_back_to_back_launches(g):
     assert qt.cpu().tolist() == [0, 0]
 
 
+def test_concurrent_streams_each_with_its_own_queue(g):
+    # two causal launches in flight on two streams, each with the binding's
+    # own fresh queue (made on its launch stream)
+    shapes = [(2, 16, 2048, 128), (3, 20, 1536, 64)]
+    inputs = [tuple(t.to(DEV) for t in draw_attention(*sh, seed=500 + i)) for i, sh in enumerate(shapes)]
+    expect = [g.attention_fwd(Q, K, V, causal=True, queue=False) for Q, K, V in inputs]
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = []
+    for _ in range(3):
+        for st, (Q, K, V) in zip(streams, inputs):
+            st.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(st):
+                outs.append(g.attention_fwd(Q, K, V, causal=True))
+    torch.cuda.synchronize()
+    assert g.check() == g.GEMM_OK
+    for i, o in enumerate(outs):
+        assert torch.equal(o, expect[i % 2]), f"launch {i}"
+
+
 @pytest.mark.parametrize("explicit_queue", [True, False])
 def test_queue_inside_a_cuda_graph(g, explicit_queue):
     # captured once and replayed three times: an explicit queue is left zero
