@@ -198,6 +198,29 @@ def test_zero_queries_average_the_values(g):
     assert np.abs(got - mean).max() <= ATOL
 
 
+@pytest.mark.parametrize("queue", [None, False])
+def test_causal_first_row_is_the_first_value_row(g, queue):
+    # with the causal mask row 0 sees key 0 alone: weight 1, so O[.., 0, :]
+    # is V[.., 0, :] exactly, for every head, at the bench's size
+    w = ATTN_WORKLOADS["attn_4096_d128_causal"]
+    Q, K, V = (t.to(DEV) for t in draw_attention_workload(w))
+    O = g.attention_fwd(Q, K, V, sm_scale=w.sm_scale, causal=True, queue=queue)
+    assert g.check() == g.GEMM_OK
+    assert torch.equal(O[:, :, 0, :], V[:, :, 0, :])
+
+
+@pytest.mark.parametrize("dim", [64, 128])
+def test_causal_zero_queries_give_prefix_means(g, dim):
+    # zero queries: equal scores, so row i averages V[0..i]
+    B, H, S = 2, 3, 1000
+    Q = torch.zeros((B, H, S, dim), dtype=torch.float16)
+    _, K, V = draw_attention(B, H, S, dim, seed=90 + dim)
+    got = run(g, Q, K, V, True).astype(np.float64)
+    v = V.double().numpy()
+    mean = np.cumsum(v, axis=2) / np.arange(1, S + 1).reshape(1, 1, S, 1)
+    assert np.abs(got - mean).max() <= ATOL
+
+
 def test_large_scores_do_not_overflow(g):
     # scores up to ~ 3e4: the running maximum keeps every exponent <= 8
     Q, K, V = draw_attention(1, 2, 256, 64, seed=78)
